@@ -1,0 +1,387 @@
+#!/usr/bin/env python3
+"""GDN chunked-prefill forward benchmark (tokens/s and % of roofline).
+
+One step = one full forward pass (gate -> inverse -> [correction + scan] ->
+fused) over the layer workload B=4, T=8192, H=32, dk=dv=128 (bf16 q/k/v, fp32
+gates), inputs resident in HBM.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the checker the CUDA path is
+pinned to) on a bounded sample of the same workload, on the host cores.
+With N > 1 (torchrun) every rank runs its own replica: the path shards over
+independent (sequence, head) units and has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunked-prefill fwd tokens/s & % roofline (B=4,T=8192,H=32,d=128)"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 512 << 20          # > 129 MB L2
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_work(cfg):
+    """Bytes and FLOPs the path must move / issue (per-token-head figures times
+    token-heads, plus the states)."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    th = cfg.total_tokens * cfg.H
+    per_th_bytes = (2 * cfg.dk + cfg.dv) * e + cfg.dv * e + 8
+    state = cfg.num_seqs * cfg.H * cfg.dk * cfg.dv * 4
+    nbytes = th * per_th_bytes + state * (2 if cfg.s0_std is not None else 1)
+    flops = th * (6 * cfg.dk * cfg.dv + 4 * 64 * (cfg.dk + cfg.dv))
+    return nbytes, flops, per_th_bytes
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + CLOCK_QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reference_arm(args, cfg):
+    """The fp64 oracle on the host cores, on a bounded sample of the workload."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from chunked_prefill_gdn_gb300.inputs import make_inputs
+    inp = make_inputs(cfg.scaled(B=1), "cpu")      # one sequence of the layer batch
+    heads = list(range(args.ref_heads))
+    step_times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.gdn_reference(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, None,
+                             scale=inp["scale"], heads=heads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            step_times.append(dt)
+    per = statistics.mean(step_times)
+    token_heads = cfg.T * len(heads)
+    value = token_heads / per / cfg.H                  # tokens/s of the full-width layer
+    sample = "1 of %d sequences x %d of %d heads (all %d tokens, all %d value rows) per step" % (
+        cfg.B, len(heads), cfg.H, cfg.T, cfg.dv)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "GDN fwd layer B=4 T=8192 H=32 dk=dv=128 (%s)" % cfg.name,
+                   "global_batch": cfg.B, "seq_len": cfg.T, "heads": cfg.H, "head_dim": cfg.dk,
+                   "parallelism": "host cores (OpenMP)", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.oracle_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(cfg, budget_s):
+    """Oracle throughput on the host cores for a bounded sample (tokens/s of the
+    full-width layer)."""
+    import oracle
+    from chunked_prefill_gdn_gb300.inputs import make_inputs
+    inp = make_inputs(cfg.scaled(B=1), "cpu")
+    heads = [0]
+    t0 = time.perf_counter()
+    oracle.gdn_reference(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, None, scale=inp["scale"],
+                         heads=heads)
+    t1 = time.perf_counter() - t0
+    nh = max(1, min(cfg.H, int(budget_s / max(t1, 1e-3))))
+    heads = list(range(nh))
+    t0 = time.perf_counter()
+    oracle.gdn_reference(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, None, scale=inp["scale"],
+                         heads=heads)
+    dt = time.perf_counter() - t0
+    value = cfg.T * nh / dt / cfg.H
+    return {"value": value, "unit": "tokens/s", "cores": oracle.oracle_threads(), "kind": "oracle",
+            "sample": "1 of %d sequences x %d of %d heads, all %d tokens and %d value rows, %.1f s" % (
+                cfg.B, nh, cfg.H, cfg.T, cfg.dv, dt)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=1, help="workload index (1 = the layer shape)")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "simt"])
+    ap.add_argument("--cp", default="auto", choices=["auto", "off", "force"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-heads", type=int, default=2, help="heads per reference-arm step")
+    args = ap.parse_args()
+
+    from chunked_prefill_gdn_gb300.inputs import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        reference_arm(args, cfg)
+        return
+
+    import torch
+    import chunked_prefill_gdn_gb300 as gdn
+    from chunked_prefill_gdn_gb300 import build as lib_build
+    from chunked_prefill_gdn_gb300.inputs import make_inputs
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist = None
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        lib_build.build()
+    if dist is not None:
+        dist.barrier()
+    gdn.load_library()
+
+    kernel = {"auto": gdn.KERNEL_AUTO, "tc": gdn.KERNEL_TC, "simt": gdn.KERNEL_SIMT}[args.kernel]
+    cp = {"auto": gdn.CP_AUTO, "off": gdn.CP_OFF, "force": gdn.CP_FORCE}[args.cp]
+    opts = gdn.default_options(kernel=kernel, cp_mode=cp)
+    inp = make_inputs(cfg, dev)
+    q, k, v, g, beta = inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"]
+    s0, cu, scale = inp["initial_state"], inp["cu_seqlens"], inp["scale"]
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cfg.num_seqs
+    dtc = gdn.BF16 if q.dtype == torch.bfloat16 else gdn.F32
+    plan = gdn.gdn_plan_query(B, T, H, dk, dv, N, cu is not None, dtc, opts)
+    out = torch.empty(B, T, H, dv, dtype=q.dtype, device=dev)
+    fs = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    wsp = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev_fb = torch.cuda.Event(enable_timing=True)
+    ev_fe = torch.cuda.Event(enable_timing=True)
+    ev_fb.record(stream)
+    ev_fe.record(stream)
+    opts.prof_begin = ev_fb.cuda_event
+    opts.prof_end = ev_fe.cuda_event
+
+    def step():
+        gdn.chunk_fwd(q, k, v, g, beta, s0, cu, scale, opts=opts, out=out, final_state=fs, workspace=wsp,
+                      stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    st = gdn.gdn_chunk_fwd_check(ctypes_ptr(wsp), ctypes_ptr_stream(stream))
+    if st != 0:
+        raise SystemExit("device check failed: %s" % gdn.gdn_status_string(st))
+    torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    fused_ms = []
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)                       # untimed: evict the previous step from L2
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+            ev_fe.synchronize()
+            fused_ms.append(ev_fb.elapsed_time(ev_fe))
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens = cfg.total_tokens
+    value = tokens * ws / (ms_per_step * 1e-3)
+
+    peaks, peak_src = load_peaks()
+    nbytes, flops, per_th = algorithmic_work(cfg)
+    fused_avg_ms = statistics.mean(fused_ms)
+    achieved = nbytes / (fused_avg_ms * 1e-3) / 1e9
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    roof_ms = max(t_hbm, t_tc) * 1e3
+    traffic = None
+    prof_json = os.path.join(ROOT, "profiles", "fused_pass_layer_traffic.json")
+    kname = "tc" if plan.kernel == gdn.KERNEL_TC else "simt"
+    try:
+        with open(prof_json) as f:
+            pj = json.load(f)
+        if pj.get("kernel") == kname and pj.get("source_sha") == kernel_source_sha(kname):
+            traffic = pj.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    launches_per_step = 5 + (2 if plan.cp_enabled else 0)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": "GDN fwd layer B=%d T=%d H=%d dk=dv=%d (%s)" % (B, T, H, dk, cfg.name),
+                   "global_batch": B * ws, "seq_len": T, "heads": H, "head_dim": dk,
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "l2": "flushed between timed steps (512 MB write) and inputs (805 MB) exceed L2",
+                   "fused_kernel": kname, "cp": bool(plan.cp_enabled)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "fused output pass (%s)" % kname, "kernel_ms": fused_avg_ms,
+                     "alg_bytes_per_launch": nbytes, "peak_source": peak_src},
+        "path_roofline": {"roofline_ms": roof_ms, "t_hbm_ms": t_hbm * 1e3, "t_tensor_ms": t_tc * 1e3,
+                          "measured_ms": ms_per_step, "frac": roof_ms / ms_per_step,
+                          "alg_bytes": nbytes, "alg_flops": flops, "peak_source": peak_src},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_e2e:
+        result["e2e"] = e2e_measure(gdn, torch, inp, cfg, opts, dev, args)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(cfg, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def ctypes_ptr(t):
+    import ctypes
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def ctypes_ptr_stream(s):
+    import ctypes
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def kernel_source_sha(kname):
+    import hashlib
+    path = os.path.join(ROOT, "chunked_prefill_gdn_gb300", "csrc", "fused_tc.cu" if kname == "tc" else "fused_simt.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def e2e_measure(gdn, torch, inp, cfg, opts, dev, args):
+    """Same metric through gdn_chunk_fwd_host: pinned host inputs copied in,
+    the pass, o and final_state copied out, all inside the timed region."""
+    import ctypes
+    host = {k: (v.cpu().pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    B, T, H, dk = host["q"].shape
+    dv = host["v"].shape[-1]
+    N = cfg.num_seqs
+    o = torch.empty(B, T, H, dv, dtype=host["q"].dtype, pin_memory=True)
+    fs = torch.empty(N, H, dk, dv, dtype=torch.float32, pin_memory=True)
+    dtc = gdn.BF16 if host["q"].dtype == torch.bfloat16 else gdn.F32
+    e2e_opts = gdn.default_options(kernel=opts.kernel, cp_mode=opts.cp_mode)
+    nbuf = gdn.gdn_chunk_fwd_host_buffer_size(B, T, H, dk, dv, N, host["cu_seqlens"] is not None,
+                                              host["initial_state"] is not None, dtc, e2e_opts)
+    buf = torch.empty(nbuf, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def once():
+        gdn.chunk_fwd_host(host["q"], host["k"], host["v"], host["g"], host["beta"], host["initial_state"],
+                           host["cu_seqlens"], host["scale"], opts=e2e_opts, out=o, final_state=fs,
+                           device_buffer=buf, stream=stream, device=dev)
+
+    for _ in range(2):
+        once()
+    steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        once()
+    dt = (time.perf_counter() - t0) / steps
+    el = host["q"].element_size()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v", "g", "beta"))
+    if host["initial_state"] is not None:
+        h2d += host["initial_state"].numel() * 4
+    if host["cu_seqlens"] is not None:
+        h2d += host["cu_seqlens"].numel() * 4
+    d2h = o.numel() * el + fs.numel() * 4
+    return {"value": cfg.total_tokens / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps,
+            "api": "gdn_chunk_fwd_host (pinned host buffers, synchronous per step)"}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,285 @@
+"""GB300 (sm_103a) Gated Delta Network chunked-prefill forward pass.
+
+A thin ctypes binding over the C ABI in include/gdn.h: every function here only
+marshals arguments; all of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: when the library is missing or cannot load, every
+call raises.
+
+    o, final_state = chunk_fwd(q, k, v, g, beta, initial_state=None,
+                               cu_seqlens=None, scale=None)
+
+q, k [B,T,H,dk] and v [B,T,H,dv] in bf16 or fp32, g and beta [B,T,H] fp32,
+initial_state [N,H,dk,dv] fp32, cu_seqlens int32 [N+1] (then B = 1), all on
+the same CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "GdnOptions", "GdnPlanInfo", "GdnWorkspaceLayout", "WORK_ITEM_DTYPE",
+    "load_library", "library_path", "default_options",
+    "gdn_default_options", "gdn_plan_query", "gdn_chunk_fwd_workspace_size", "gdn_workspace_query",
+    "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
+    "gdn_status_string", "gdn_version", "chunk_fwd", "chunk_fwd_host", "workspace_for", "GdnError",
+    "CP_AUTO", "CP_OFF", "CP_FORCE", "KERNEL_AUTO", "KERNEL_TC", "KERNEL_SIMT", "BF16", "F32",
+    "STAGE_PREP", "STAGE_INVERSE", "STAGE_CORRECTION", "STAGE_FUSED",
+]
+
+BF16, F32 = 0, 1
+CP_AUTO, CP_OFF, CP_FORCE = 0, 1, 2
+KERNEL_AUTO, KERNEL_TC, KERNEL_SIMT = 0, 1, 2
+STAGE_PREP, STAGE_INVERSE, STAGE_CORRECTION, STAGE_FUSED = 1, 2, 4, 8
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE",
+          4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_CHECK", 6: "GDN_ERR_TIMEOUT"}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__("%s%s" % (STATUS.get(status, "status %d" % status), (" in " + where) if where else ""))
+
+
+class GdnOptions(ctypes.Structure):
+    _fields_ = [("cp_mode", ctypes.c_int32), ("kernel", ctypes.c_int32),
+                ("chunks_per_segment", ctypes.c_int32), ("sliding", ctypes.c_int32),
+                ("sw_eps", ctypes.c_float), ("sm_count", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("debug_checks", ctypes.c_int32),
+                ("prof_begin", ctypes.c_void_p), ("prof_end", ctypes.c_void_p),
+                ("reserved", ctypes.c_int32 * 4)]
+
+
+class GdnPlanInfo(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("cp_enabled", ctypes.c_int32),
+                ("chunks_per_segment", ctypes.c_int32), ("max_chunks", ctypes.c_int32),
+                ("max_items", ctypes.c_int32), ("max_cp_slots", ctypes.c_int32),
+                ("sm_count", ctypes.c_int32), ("grid_fused", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class GdnWorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("error_word", "gate_cumsum", "chunk_totals", "head_flags",
+                                              "tprime", "chunk_table", "num_chunks", "items", "num_items",
+                                              "total")]
+
+
+# field order of gdn_work_item (eight int32)
+WORK_ITEM_DTYPE = ("seq", "head", "c_begin", "c_end", "c_start", "flags", "slot", "pad")
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = False):
+    """Load the CUDA library (raises when it is absent and not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError("GDN CUDA library not built: %s (run __graft_entry__.build() or "
+                               "python chunked_prefill_gdn_gb300/build.py)" % path)
+        _build.build()
+    lib = ctypes.CDLL(path)
+    vp, sz, i32, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+    opt = ctypes.POINTER(GdnOptions)
+    lib.gdn_default_options.argtypes = [opt]
+    lib.gdn_default_options.restype = None
+    lib.gdn_plan_query.argtypes = [i32] * 7 + [i32, opt, ctypes.POINTER(GdnPlanInfo)]
+    lib.gdn_plan_query.restype = i32
+    lib.gdn_chunk_fwd_workspace_size.argtypes = [i32] * 7 + [i32, opt]
+    lib.gdn_chunk_fwd_workspace_size.restype = sz
+    lib.gdn_workspace_query.argtypes = [i32] * 7 + [i32, opt, ctypes.POINTER(GdnWorkspaceLayout)]
+    lib.gdn_workspace_query.restype = i32
+    fwd_args = [vp, vp, vp, vp, vp, vp, vp, i32, f32, i32, i32, i32, i32, i32, i32, vp, vp, vp, sz, opt, vp]
+    lib.gdn_chunk_fwd.argtypes = fwd_args
+    lib.gdn_chunk_fwd.restype = i32
+    lib.gdn_chunk_fwd_check.argtypes = [vp, vp]
+    lib.gdn_chunk_fwd_check.restype = i32
+    lib.gdn_chunk_fwd_host_buffer_size.argtypes = [i32] * 8 + [i32, opt]
+    lib.gdn_chunk_fwd_host_buffer_size.restype = sz
+    lib.gdn_chunk_fwd_host.argtypes = fwd_args
+    lib.gdn_chunk_fwd_host.restype = i32
+    lib.gdn_status_string.argtypes = [i32]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_version.argtypes = []
+    lib.gdn_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def default_options(**kw) -> GdnOptions:
+    o = GdnOptions()
+    load_library().gdn_default_options(ctypes.byref(o))
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+# ----------------------------------------------------------- raw C-ABI names
+
+def gdn_default_options(opts: GdnOptions) -> None:
+    load_library().gdn_default_options(ctypes.byref(opts))
+
+
+def gdn_plan_query(B, T, H, dk, dv, n_seqs, varlen, dtype, opts=None) -> GdnPlanInfo:
+    info = GdnPlanInfo()
+    st = load_library().gdn_plan_query(B, T, H, dk, dv, n_seqs, int(varlen), dtype,
+                                       ctypes.byref(opts) if opts is not None else None, ctypes.byref(info))
+    if st != 0:
+        raise GdnError(st, "gdn_plan_query")
+    return info
+
+
+def gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, n_seqs, varlen, dtype, opts=None) -> int:
+    return int(load_library().gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, n_seqs, int(varlen), dtype,
+                                                            ctypes.byref(opts) if opts is not None else None))
+
+
+def gdn_workspace_query(B, T, H, dk, dv, n_seqs, varlen, dtype, opts=None) -> GdnWorkspaceLayout:
+    lay = GdnWorkspaceLayout()
+    st = load_library().gdn_workspace_query(B, T, H, dk, dv, n_seqs, int(varlen), dtype,
+                                            ctypes.byref(opts) if opts is not None else None, ctypes.byref(lay))
+    if st != 0:
+        raise GdnError(st, "gdn_workspace_query")
+    return lay
+
+
+def gdn_chunk_fwd(*args) -> int:
+    return int(load_library().gdn_chunk_fwd(*args))
+
+
+def gdn_chunk_fwd_check(workspace_ptr, stream_ptr) -> int:
+    return int(load_library().gdn_chunk_fwd_check(workspace_ptr, stream_ptr))
+
+
+def gdn_chunk_fwd_host_buffer_size(B, T, H, dk, dv, n_seqs, varlen, has_initial_state, dtype, opts=None) -> int:
+    return int(load_library().gdn_chunk_fwd_host_buffer_size(
+        B, T, H, dk, dv, n_seqs, int(varlen), int(has_initial_state), dtype,
+        ctypes.byref(opts) if opts is not None else None))
+
+
+def gdn_chunk_fwd_host(*args) -> int:
+    return int(load_library().gdn_chunk_fwd_host(*args))
+
+
+def gdn_status_string(status: int) -> str:
+    return load_library().gdn_status_string(status).decode()
+
+
+def gdn_version() -> str:
+    return load_library().gdn_version().decode()
+
+
+# ---------------------------------------------------------------- tensor API
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _shape(q, v, cu_seqlens):
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, dk]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("cu_seqlens needs B == 1")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    return B, T, H, dk, dv, N
+
+
+def workspace_for(q, v, cu_seqlens=None, opts: Optional[GdnOptions] = None) -> torch.Tensor:
+    B, T, H, dk, dv, N = _shape(q, v, cu_seqlens)
+    n = gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, N, cu_seqlens is not None, _dtype_code(q), opts)
+    if n == 0:
+        raise GdnError(1, "gdn_chunk_fwd_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
+              opts: Optional[GdnOptions] = None, out=None, final_state=None, workspace=None,
+              stream: Optional[torch.cuda.Stream] = None, check: bool = False):
+    """GDN chunked-prefill forward on the GPU; returns (o, final_state)."""
+    B, T, H, dk, dv, N = _shape(q, v, cu_seqlens)
+    dt = _dtype_code(q)
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype != q.dtype:
+            raise TypeError("%s must have q's dtype" % name)
+    tensors = dict(q=q, k=k, v=v, g=g, beta=beta)
+    for name, t in tensors.items():
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    if initial_state is not None and (initial_state.dtype != torch.float32 or not initial_state.is_contiguous()):
+        raise TypeError("initial_state must be contiguous float32")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if out is None:
+        out = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+    if final_state is None:
+        final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = workspace_for(q, v, cu_seqlens, opts)
+    stream = stream if stream is not None else torch.cuda.current_stream(q.device)
+    st = gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
+                       N, float(scale) if scale is not None else 0.0, B, T, H, dk, dv, dt,
+                       _ptr(out), _ptr(final_state), _ptr(workspace), workspace.numel(),
+                       ctypes.byref(opts) if opts is not None else None, ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise GdnError(st, "gdn_chunk_fwd")
+    if check:
+        st = gdn_chunk_fwd_check(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise GdnError(st, "device check")
+    return out, final_state
+
+
+def chunk_fwd_host(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
+                   opts: Optional[GdnOptions] = None, out=None, final_state=None, device_buffer=None,
+                   stream: Optional[torch.cuda.Stream] = None, device=None):
+    """The same pass for CPU (ideally pinned) tensors through gdn_chunk_fwd_host:
+    the library copies inputs in, runs, copies results out and syncs."""
+    B, T, H, dk, dv, N = _shape(q, v, cu_seqlens)
+    dt = _dtype_code(q)
+    for name, t in dict(q=q, k=k, v=v, g=g, beta=beta).items():
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous host tensor" % name)
+    device = torch.device(device or "cuda")
+    if out is None:
+        out = torch.empty(B, T, H, dv, dtype=q.dtype, pin_memory=True)
+    if final_state is None:
+        final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, pin_memory=True)
+    if device_buffer is None:
+        n = gdn_chunk_fwd_host_buffer_size(B, T, H, dk, dv, N, cu_seqlens is not None,
+                                           initial_state is not None, dt, opts)
+        device_buffer = torch.empty(n, dtype=torch.uint8, device=device)
+    stream = stream if stream is not None else torch.cuda.current_stream(device)
+    st = gdn_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
+                            N, float(scale) if scale is not None else 0.0, B, T, H, dk, dv, dt,
+                            _ptr(out), _ptr(final_state), _ptr(device_buffer), device_buffer.numel(),
+                            ctypes.byref(opts) if opts is not None else None, ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise GdnError(st, "gdn_chunk_fwd_host")
+    return out, final_state

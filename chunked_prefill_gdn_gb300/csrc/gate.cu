@@ -1,0 +1,327 @@
+// Sequence preparation, the gate kernel and the device-side work planner.
+//
+// Gate kernel (FlashQLA talk "Qwen系列模型线性注意力高性能优化实践": the Gamma
+// paragraph keeps the in-chunk gate product in log space, the SFU paragraph
+// writes Gamma_{st} = exp(G_s - G_t); the sliding-window paragraph launches a
+// light kernel that scans each head's gate to find the heads whose alpha is not
+// identically 1): chunk-local inclusive cumsum G of g, per-chunk totals, and a
+// per-(sequence, head) flag "some g != 0".
+//
+// Planner (compute-for-memory, auto-CP and sliding-window paragraphs): splits
+// each (sequence, head) unit into segments of at most L chunks, orders the work
+// longest sequence first, and gives each later segment either a look-back
+// restart (flagged heads) or correction-matrix work plus a scan (alpha == 1
+// heads).  It runs on the device so no cu_seqlens or gate data crosses to the
+// host.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+// ---------------------------------------------------------------------------
+// Sequence preparation: validate cu_seqlens, build the per-sequence table and
+// the chunk table, zero the counters and head flags.  One CTA.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) seqprep_kernel(Problem p, Workspace w) {
+    __shared__ int s_bad;
+    __shared__ int s_carry;
+    __shared__ int s_warp[32];
+    const int tid = threadIdx.x;
+    const int N = p.N;
+    if (tid == 0) {
+        s_bad = 0;
+        s_carry = 0;
+        *w.err = 0;
+        *w.num_chunks = 0;
+    }
+    if (tid < 8) w.counters[tid] = 0;
+    if (tid < 4) w.num_items[tid] = 0;
+    for (int i = tid; i < N * p.H; i += blockDim.x) w.flags[i] = 0;
+    __syncthreads();
+    if (p.varlen) {
+        for (int n = tid; n <= N; n += blockDim.x) {
+            int a = p.cu[n];
+            bool bad = (n == 0 && a != 0) || (n == N && a != p.total_T) || a < 0 || a > p.total_T;
+            if (n < N && p.cu[n + 1] < a) bad = true;
+            if (bad) s_bad = 1;
+        }
+        __syncthreads();
+        if (s_bad) {
+            if (tid == 0) report_error(w.err, GDN_ERR_DEVICE_CHECK);
+            return;
+        }
+    }
+    // exclusive scan of chunk counts over sequences, 1024 at a time
+    for (int base = 0; base < N; base += blockDim.x) {
+        int n = base + tid;
+        int t0 = 0, len = 0, nc = 0;
+        if (n < N) {
+            t0 = p.varlen ? p.cu[n] : n * p.T;
+            len = p.varlen ? p.cu[n + 1] - t0 : p.T;
+            nc = (len + kChunk - 1) / kChunk;
+        }
+        // block inclusive scan of nc
+        int x = nc;
+        const int lane = tid & 31, wid = tid >> 5;
+        for (int off = 1; off < 32; off <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) s_warp[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int y = s_warp[lane];
+            for (int off = 1; off < 32; off <<= 1) {
+                int z = __shfl_up_sync(0xffffffffu, y, off);
+                if (lane >= off) y += z;
+            }
+            s_warp[lane] = y;
+        }
+        __syncthreads();
+        int incl = x + (wid > 0 ? s_warp[wid - 1] : 0);
+        int carry = s_carry;
+        if (n < N) w.seqinfo[n] = make_int4(t0, len, carry + incl - nc, nc);
+        __syncthreads();
+        if (tid == blockDim.x - 1) s_carry = carry + incl;
+        __syncthreads();
+    }
+    const int total = s_carry;
+    if (total > w.max_chunks) {  // cannot happen for consistent sizes; never overrun the table
+        if (tid == 0) report_error(w.err, GDN_ERR_DEVICE_CHECK);
+        return;
+    }
+    __syncthreads();
+    // chunk table: binary search the sequence of every chunk
+    for (int c = tid; c < total; c += blockDim.x) {
+        int lo = 0, hi = N - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (w.seqinfo[mid].z <= c) lo = mid; else hi = mid - 1;
+        }
+        // skip empty sequences that share the same first chunk
+        while (lo + 1 < N && w.seqinfo[lo + 1].z <= c) ++lo;
+        int4 si = w.seqinfo[lo];
+        int ci = c - si.z;
+        int t0 = si.x + ci * kChunk;
+        int len = min(kChunk, si.x + si.y - t0);
+        w.chunks[c] = make_int4(lo, t0, len, ci);
+    }
+    if (tid == 0) *w.num_chunks = total;
+}
+
+// ---------------------------------------------------------------------------
+// Gate: one CTA per (chunk, group of 64 heads).
+// ---------------------------------------------------------------------------
+constexpr int kGateHeads = 64;
+
+__global__ void __launch_bounds__(256) gate_kernel(Problem p, Workspace w) {
+    __shared__ float tile[kChunk][kGateHeads + 1];
+    __shared__ int s_nz[kGateHeads];
+    const int cid = blockIdx.x;
+    if (cid >= *w.num_chunks) return;
+    const int4 ci = w.chunks[cid];
+    const int t0 = ci.y, len = ci.z;
+    const int h0 = blockIdx.y * kGateHeads;
+    const int nh = min(kGateHeads, p.H - h0);
+    for (int idx = threadIdx.x; idx < kChunk * nh; idx += blockDim.x) {
+        int r = idx / nh, hh = idx % nh;
+        tile[r][hh] = r < len ? p.g[(size_t)(t0 + r) * p.H + h0 + hh] : 0.f;
+    }
+    __syncthreads();
+    for (int hh = threadIdx.x; hh < nh; hh += blockDim.x) {
+        float acc = 0.f;
+        int nz = 0;
+        for (int r = 0; r < len; ++r) {
+            float x = tile[r][hh];
+            nz |= (x != 0.f);
+            acc += x;
+            tile[r][hh] = acc;
+        }
+        // rows past the end keep the last cumsum (they never contribute)
+        for (int r = len; r < kChunk; ++r) tile[r][hh] = acc;
+        w.totals[(size_t)(h0 + hh) * w.max_chunks + cid] = acc;
+        s_nz[hh] = nz;
+    }
+    __syncthreads();
+    for (int hh = threadIdx.x; hh < nh; hh += blockDim.x)
+        if (s_nz[hh]) w.flags[ci.x * p.H + h0 + hh] = 1;
+    for (int idx = threadIdx.x; idx < kChunk * nh; idx += blockDim.x) {
+        int hh = idx / kChunk, r = idx % kChunk;
+        if (r < len) w.G[(size_t)(h0 + hh) * p.total_T + t0 + r] = tile[r][hh];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Planner: one CTA builds the work lists.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int block_exclusive_scan(int x, int *s_warp, int *s_total) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nw = (blockDim.x + 31) >> 5;
+    int incl = x;
+    for (int off = 1; off < 32; off <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) s_warp[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int y = lane < nw ? s_warp[lane] : 0;
+        for (int off = 1; off < 32; off <<= 1) {
+            int z = __shfl_up_sync(0xffffffffu, y, off);
+            if (lane >= off) y += z;
+        }
+        s_warp[lane] = y;
+        if (lane == 31) *s_total = y;
+    }
+    __syncthreads();
+    int excl = incl - x + (wid > 0 ? s_warp[wid - 1] : 0);
+    __syncthreads();
+    return excl;
+}
+
+// Look-back window for the segment starting at chunk c_begin of a unit: the
+// least number of whole chunks whose summed gate is <= ln_eps, or the whole
+// prefix.  Returns -1 when more than max_walk chunks would be needed (the unit
+// then takes the exact correction-matrix path instead).
+__device__ int lookback_window(const Workspace &w, int h, int chunk0, int c_begin, float ln_eps,
+                               int max_walk) {
+    float acc = 0.f;
+    int wnd = 0;
+    while (wnd < c_begin) {
+        if (wnd >= max_walk) return -1;
+        acc += w.totals[(size_t)h * w.max_chunks + chunk0 + c_begin - 1 - wnd];
+        ++wnd;
+        if (acc <= ln_eps) break;
+    }
+    return wnd;
+}
+
+constexpr int kMaxLookbackChunks = 256;
+
+__global__ void __launch_bounds__(1024) plan_kernel(Problem p, Workspace w, PlanParams pp) {
+    __shared__ int s_warp[32];
+    __shared__ int s_tot[4];
+    __shared__ int s_base[4];
+    const int tid = threadIdx.x;
+    if (*w.err != 0) return;
+    const int N = p.N, H = p.H;
+    // 1. order sequences longest first (rank by counting; natural order when N is large)
+    if (N <= 8192) {
+        for (int n = tid; n < N; n += blockDim.x) {
+            int mine = w.seqinfo[n].w;
+            int rank = 0;
+            for (int m = 0; m < N; ++m) {
+                int o = w.seqinfo[m].w;
+                rank += (o > mine) || (o == mine && m < n);
+            }
+            w.seq_order[rank] = n;
+        }
+    } else {
+        for (int n = tid; n < N; n += blockDim.x) w.seq_order[n] = n;
+    }
+    if (tid < 4) s_base[tid] = 0;
+    __syncthreads();
+    const int units = N * H;
+    const int max_walk = min(pp.L, kMaxLookbackChunks);
+    for (int ubase = 0; ubase < units; ubase += blockDim.x) {
+        const int u = ubase + tid;
+        int seq = 0, h = 0, nc = 0, NS = 0, Lu = 1, chunk0 = 0;
+        bool mpath = false;
+        if (u < units) {
+            seq = w.seq_order[u / H];
+            h = u % H;
+            nc = w.seqinfo[seq].w;
+            chunk0 = w.seqinfo[seq].z;
+            // an empty sequence still gets one (empty) item: it writes final = initial
+            NS = (pp.cp_enabled && nc > pp.L) ? (nc + pp.L - 1) / pp.L : 1;
+            Lu = max(1, (nc + NS - 1) / NS);
+            NS = nc > 0 ? (nc + Lu - 1) / Lu : 1;
+            const bool flagged = w.flags[seq * H + h] != 0;
+            if (NS > 1) {
+                mpath = !(flagged && pp.sliding);
+                for (int j = 1; j < NS && !mpath; ++j)
+                    if (lookback_window(w, h, chunk0, j * Lu, pp.ln_eps, max_walk) < 0) mpath = true;
+            }
+        }
+        const int c2 = NS, c1 = mpath ? 2 * NS - 3 : 0, cs = mpath ? NS - 1 : 0, cu = mpath ? 1 : 0;
+        const int o2 = s_base[0] + block_exclusive_scan(c2, s_warp, &s_tot[0]);
+        const int o1 = s_base[1] + block_exclusive_scan(c1, s_warp, &s_tot[1]);
+        const int os = s_base[2] + block_exclusive_scan(cs, s_warp, &s_tot[2]);
+        const int ou = s_base[3] + block_exclusive_scan(cu, s_warp, &s_tot[3]);
+        const bool fits = o2 + c2 <= w.max_items && o1 + c1 <= w.max_items1 &&
+                          os + cs <= w.max_cp_slots && ou + cu <= w.max_cp_slots;
+        if (u < units && !fits) report_error(w.err, GDN_ERR_DEVICE_CHECK);
+        if (u < units && fits) {
+            for (int j = 0; j < NS; ++j) {
+                gdn_work_item it;
+                it.seq = seq;
+                it.head = h;
+                it.c_begin = j * Lu;
+                it.c_end = min(nc, (j + 1) * Lu);
+                it.c_start = it.c_begin;
+                it.slot = -1;
+                it.pad = 0;
+                int f = GDN_ITEM_OUTPUT | (j == NS - 1 ? GDN_ITEM_WRITE_FINAL : 0);
+                if (j == 0) {
+                    f |= GDN_ITEM_FROM_INITIAL;
+                } else if (mpath) {
+                    f |= GDN_ITEM_FROM_SLOT;
+                    it.slot = os + j - 1;
+                } else {
+                    it.c_start = it.c_begin - lookback_window(w, h, chunk0, it.c_begin, pp.ln_eps, max_walk);
+                    f |= it.c_start == 0 ? GDN_ITEM_FROM_INITIAL : GDN_ITEM_FROM_ZERO;
+                }
+                it.flags = f;
+                w.items2[o2 + j] = it;
+            }
+            if (mpath) {
+                int k1 = o1;
+                for (int j = 0; j < NS - 1; ++j) {
+                    gdn_work_item it;
+                    it.seq = seq;
+                    it.head = h;
+                    it.c_begin = it.c_start = j * Lu;
+                    it.c_end = min(nc, (j + 1) * Lu);
+                    it.slot = os + j;
+                    it.pad = 0;
+                    if (j == 0) {
+                        it.flags = GDN_ITEM_FROM_INITIAL | GDN_ITEM_WRITE_SLOT;
+                        w.items1[k1++] = it;
+                    } else {
+                        it.flags = GDN_ITEM_FROM_ZERO | GDN_ITEM_WRITE_SLOT;
+                        w.items1[k1++] = it;
+                        it.flags = GDN_ITEM_FROM_IDENTITY | GDN_ITEM_WRITE_M;
+                        w.items1[k1++] = it;
+                    }
+                }
+                w.scan_units[ou] = make_int4(seq, h, NS, os);
+            }
+        }
+        __syncthreads();
+        if (tid < 4) s_base[tid] += s_tot[tid];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        bool ok = s_base[0] <= w.max_items && s_base[1] <= w.max_items1 && s_base[2] <= w.max_cp_slots;
+        w.num_items[0] = ok ? s_base[0] : 0;
+        w.num_items[1] = ok ? s_base[1] : 0;
+        w.num_items[2] = ok ? s_base[3] : 0;
+    }
+}
+
+cudaError_t launch_seqprep(const Problem &p, const Workspace &w, cudaStream_t s) {
+    seqprep_kernel<<<1, 1024, 0, s>>>(p, w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gate(const Problem &p, const Workspace &w, cudaStream_t s) {
+    dim3 grid(w.max_chunks, (p.H + kGateHeads - 1) / kGateHeads);
+    gate_kernel<<<grid, 256, 0, s>>>(p, w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &pp, cudaStream_t s) {
+    plan_kernel<<<1, 1024, 0, s>>>(p, w, pp);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

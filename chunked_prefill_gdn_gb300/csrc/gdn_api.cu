@@ -1,0 +1,440 @@
+// C ABI of the library: argument checks, the host planner, the workspace
+// layout and the launch sequence
+//   sequence prep -> gate -> device planner -> per-chunk inverse
+//   -> [correction pass -> segment scan] -> fused pass
+// all on the caller's stream, with no host synchronisation.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "gdn_internal.cuh"
+
+using namespace gdn;
+
+namespace {
+
+constexpr int kDefaultSMs = 152;        // GB300
+constexpr int kMinSegmentChunks = 8;
+// Cost-model constants of the auto-CP planner, in units of one chunk step of the
+// fused kernel (the talk's one-wave model T = lambda1 L + lambda2 N / L, made
+// wave-aware): a scan step, the expected look-back of a split segment, and the
+// share of split heads expected to need the correction pass.
+constexpr double kScanStepChunks = 0.5;
+constexpr double kLookbackChunks = 4.0;
+constexpr double kCorrectionShare = 0.5;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool valid_head_dim(int d) { return d == 32 || d == 64 || d == 128; }
+
+int device_sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return kDefaultSMs;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = kDefaultSMs;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+struct HostPlan {
+    int kernel;
+    int cp;
+    int L;
+    int sms;
+    int grid;
+    int N;
+    long long total_T;
+    Layout lay;
+};
+
+void default_options(gdn_options *o) {
+    memset(o, 0, sizeof(*o));
+    o->cp_mode = GDN_CP_AUTO;
+    o->kernel = GDN_KERNEL_AUTO;
+    o->chunks_per_segment = 0;
+    o->sliding = 1;
+    o->sw_eps = 5.9604645e-08f;  // 2^-24
+    o->sm_count = 0;
+}
+
+// Segments per unit for B equal sequences of nc chunks: minimise the waves of
+// the persistent grid times the longest segment, plus the scan and the expected
+// correction pass.  One segment unless splitting wins by 10%.
+int choose_segments(int units, int nc, int sms) {
+    auto cost = [&](int ns) {
+        const int L = (nc + ns - 1) / ns;
+        const double waves = ceil((double)units * ns / sms);
+        double c = waves * (L + (ns > 1 ? kLookbackChunks : 0.0));
+        if (ns > 1) {
+            const double w1 = ceil(kCorrectionShare * 2.0 * units * (ns - 1) / sms);
+            c += kCorrectionShare * w1 * L + kScanStepChunks * (ns - 2);
+        }
+        return c;
+    };
+    int best = 1;
+    double best_cost = cost(1);
+    const int max_ns = std::max(1, std::min(nc / kMinSegmentChunks, 4 * sms));
+    for (int ns = 2; ns <= max_ns; ++ns) {
+        const double c = cost(ns);
+        if (c < best_cost) {
+            best_cost = c;
+            best = ns;
+        }
+    }
+    return best_cost < 0.9 * cost(1) ? best : 1;
+}
+
+gdn_status make_plan(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, int dtype,
+                     const gdn_options *opts_in, int sms_query, HostPlan *hp) {
+    gdn_options opts;
+    if (opts_in) opts = *opts_in; else default_options(&opts);
+    if (B < 1 || T < 0 || H < 1 || H > 4096) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_F32) return GDN_ERR_INVALID_ARG;
+    if (!valid_head_dim(dk) || !valid_head_dim(dv)) return GDN_ERR_UNSUPPORTED;
+    if (varlen && (B != 1 || n_seqs < 1)) return GDN_ERR_INVALID_ARG;
+    if (opts.cp_mode < GDN_CP_AUTO || opts.cp_mode > GDN_CP_FORCE) return GDN_ERR_INVALID_ARG;
+    if (opts.kernel < GDN_KERNEL_AUTO || opts.kernel > GDN_KERNEL_SIMT) return GDN_ERR_INVALID_ARG;
+    const int N = varlen ? n_seqs : B;
+    const long long total_T = varlen ? (long long)T : (long long)B * T;
+    const long long nc_seq = ((long long)T + kChunk - 1) / kChunk;
+    const long long max_chunks_ll = varlen ? total_T / kChunk + N : (long long)B * nc_seq;
+    if (total_T * H * kChunk >= (1LL << 40) || max_chunks_ll >= (1LL << 30) || (long long)N * H >= (1LL << 30))
+        return GDN_ERR_UNSUPPORTED;
+    const int max_chunks = (int)max_chunks_ll;
+    const int sms = opts.sm_count > 0 ? opts.sm_count : sms_query;
+
+    int kernel = GDN_KERNEL_SIMT;
+    const bool tc_ok = fused_tc_supported(dtype, dk, dv);
+    if (opts.kernel == GDN_KERNEL_TC && !tc_ok) return GDN_ERR_UNSUPPORTED;
+    if (opts.kernel != GDN_KERNEL_SIMT && tc_ok) kernel = GDN_KERNEL_TC;
+
+    int cp = 0;
+    int L = std::max(1, max_chunks);
+    const int units = N * H;
+    if (opts.cp_mode == GDN_CP_FORCE) {
+        cp = 1;
+        L = opts.chunks_per_segment > 0
+                ? opts.chunks_per_segment
+                : std::max(1, (int)(((long long)max_chunks * H + sms - 1) / sms));
+    } else if (opts.cp_mode == GDN_CP_AUTO) {
+        if (opts.chunks_per_segment > 0) {
+            cp = 1;
+            L = opts.chunks_per_segment;
+        } else if (!varlen) {
+            const int ns = nc_seq > 0 ? choose_segments(units, (int)nc_seq, sms) : 1;
+            if (ns > 1) {
+                cp = 1;
+                L = (int)((nc_seq + ns - 1) / ns);
+            }
+        } else {
+            cp = 1;
+            L = std::max(kMinSegmentChunks, (int)(((long long)max_chunks * H + sms - 1) / sms));
+        }
+    }
+    const int segs_bound = cp ? (int)(((long long)max_chunks + L - 1) / L) : 0;
+    Layout &lay = hp->lay;
+    lay.max_chunks = max_chunks;
+    lay.max_items = H * (N + segs_bound);
+    lay.max_items1 = cp ? 2 * H * segs_bound : 0;
+    lay.max_cp_slots = cp ? H * segs_bound : 0;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    lay.err = take(256);                      // error word, counters and counts share one block
+    lay.counters = lay.err + 16;
+    lay.num_chunks = lay.err + 48;
+    lay.num_items = lay.err + 64;
+    lay.seqinfo = take((size_t)N * 16);
+    lay.chunks = take((size_t)max_chunks * 16);
+    lay.flags = take((size_t)N * H * 4);
+    lay.G = take((size_t)H * total_T * 4);
+    lay.totals = take((size_t)H * max_chunks * 4);
+    lay.tprime = take((size_t)H * total_T * kChunk * (dtype == GDN_BF16 ? 2 : 4));
+    lay.items2 = take((size_t)lay.max_items * sizeof(gdn_work_item));
+    lay.items1 = take((size_t)lay.max_items1 * sizeof(gdn_work_item));
+    lay.scan_units = take((size_t)lay.max_cp_slots * 16);
+    lay.seq_order = take((size_t)N * 4);
+    lay.cp_s = take((size_t)lay.max_cp_slots * dk * dv * 4);
+    lay.cp_m = take((size_t)lay.max_cp_slots * dk * dk * 4);
+    lay.total = off;
+    hp->kernel = kernel;
+    hp->cp = cp;
+    hp->L = L;
+    hp->sms = sms;
+    hp->grid = sms;
+    hp->N = N;
+    hp->total_T = total_T;
+    return GDN_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+void gdn_default_options(gdn_options *opts) {
+    if (opts) default_options(opts);
+}
+
+gdn_status gdn_plan_query(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, gdn_dtype dtype,
+                          const gdn_options *opts, gdn_plan_info *out) {
+    if (!out) return GDN_ERR_INVALID_ARG;
+    HostPlan hp;
+    const int sms = (opts && opts->sm_count > 0) ? opts->sm_count : device_sm_count();
+    gdn_status st = make_plan(B, T, H, dk, dv, n_seqs, varlen, dtype, opts, sms, &hp);
+    if (st != GDN_OK) return st;
+    out->kernel = hp.kernel;
+    out->cp_enabled = hp.cp;
+    out->chunks_per_segment = hp.L;
+    out->max_chunks = hp.lay.max_chunks;
+    out->max_items = hp.lay.max_items;
+    out->max_cp_slots = hp.lay.max_cp_slots;
+    out->sm_count = hp.sms;
+    out->grid_fused = hp.grid;
+    out->workspace_bytes = hp.lay.total;
+    return GDN_OK;
+}
+
+size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, gdn_dtype dtype,
+                                    const gdn_options *opts) {
+    gdn_plan_info info;
+    if (gdn_plan_query(B, T, H, dk, dv, n_seqs, varlen, dtype, opts, &info) != GDN_OK) return 0;
+    return info.workspace_bytes;
+}
+
+gdn_status gdn_workspace_query(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, gdn_dtype dtype,
+                               const gdn_options *opts, gdn_workspace_layout *out) {
+    if (!out) return GDN_ERR_INVALID_ARG;
+    HostPlan hp;
+    const int sms = (opts && opts->sm_count > 0) ? opts->sm_count : device_sm_count();
+    gdn_status st = make_plan(B, T, H, dk, dv, n_seqs, varlen, dtype, opts, sms, &hp);
+    if (st != GDN_OK) return st;
+    out->error_word = hp.lay.err;
+    out->gate_cumsum = hp.lay.G;
+    out->chunk_totals = hp.lay.totals;
+    out->head_flags = hp.lay.flags;
+    out->tprime = hp.lay.tprime;
+    out->chunk_table = hp.lay.chunks;
+    out->num_chunks = hp.lay.num_chunks;
+    out->items = hp.lay.items2;
+    out->num_items = hp.lay.num_items;
+    out->total = hp.lay.total;
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                         const float *initial_state, const int32_t *cu_seqlens, int n_seqs, float scale,
+                         int B, int T, int H, int dk, int dv, gdn_dtype dtype, void *o, float *final_state,
+                         void *workspace, size_t workspace_bytes, const gdn_options *opts_in,
+                         gdn_stream_t stream_in) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_in);
+    gdn_options opts;
+    if (opts_in) opts = *opts_in; else default_options(&opts);
+    const int varlen = cu_seqlens != nullptr;
+    HostPlan hp;
+    const int sms = opts.sm_count > 0 ? opts.sm_count : device_sm_count();
+    gdn_status st = make_plan(B, T, H, dk, dv, n_seqs, varlen, dtype, &opts, sms, &hp);
+    if (st != GDN_OK) return st;
+    if (!workspace || !final_state) return GDN_ERR_INVALID_ARG;
+    if (hp.total_T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, beta, initial_state, o, final_state, workspace};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    if (workspace_bytes < hp.lay.total) return GDN_ERR_WORKSPACE;
+    if (!(opts.sw_eps > 0.f && opts.sw_eps < 1.f)) opts.sw_eps = 5.9604645e-08f;
+
+    Problem p;
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.s0 = initial_state; p.cu = cu_seqlens;
+    p.o = o; p.sf = final_state;
+    p.B = B; p.T = T; p.H = H; p.dk = dk; p.dv = dv; p.N = hp.N; p.total_T = (int)hp.total_T;
+    p.varlen = varlen; p.dtype = dtype;
+    p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)dk);
+
+    char *base = static_cast<char *>(workspace);
+    const Layout &L = hp.lay;
+    Workspace w;
+    w.err = reinterpret_cast<int *>(base + L.err);
+    w.counters = reinterpret_cast<int *>(base + L.counters);
+    w.num_chunks = reinterpret_cast<int *>(base + L.num_chunks);
+    w.num_items = reinterpret_cast<int *>(base + L.num_items);
+    w.seqinfo = reinterpret_cast<int4 *>(base + L.seqinfo);
+    w.chunks = reinterpret_cast<int4 *>(base + L.chunks);
+    w.flags = reinterpret_cast<int *>(base + L.flags);
+    w.G = reinterpret_cast<float *>(base + L.G);
+    w.totals = reinterpret_cast<float *>(base + L.totals);
+    w.tprime = base + L.tprime;
+    w.items2 = reinterpret_cast<gdn_work_item *>(base + L.items2);
+    w.items1 = reinterpret_cast<gdn_work_item *>(base + L.items1);
+    w.scan_units = reinterpret_cast<int4 *>(base + L.scan_units);
+    w.seq_order = reinterpret_cast<int *>(base + L.seq_order);
+    w.cp_s = reinterpret_cast<float *>(base + L.cp_s);
+    w.cp_m = reinterpret_cast<float *>(base + L.cp_m);
+    w.max_chunks = L.max_chunks;
+    w.max_items = L.max_items;
+    w.max_items1 = L.max_items1;
+    w.max_cp_slots = L.max_cp_slots;
+
+    PlanParams pp;
+    pp.L = hp.L;
+    pp.cp_enabled = hp.cp;
+    pp.sliding = opts.sliding ? 1 : 0;
+    pp.ln_eps = logf(opts.sw_eps);
+
+    const int stages = opts.stages ? opts.stages : (GDN_STAGE_PREP | GDN_STAGE_INVERSE | GDN_STAGE_CORRECTION |
+                                                    GDN_STAGE_FUSED);
+    cudaGetLastError();  // clear a stale error so it is not blamed on these launches
+    if (stages & GDN_STAGE_PREP) {
+        if (launch_seqprep(p, w, stream) != cudaSuccess) return GDN_ERR_CUDA;
+        if (L.max_chunks > 0 && launch_gate(p, w, stream) != cudaSuccess) return GDN_ERR_CUDA;
+        if (launch_plan(p, w, pp, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    if ((stages & GDN_STAGE_INVERSE) && L.max_chunks > 0) {
+        if (launch_inverse(p, w, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    const bool tc = hp.kernel == GDN_KERNEL_TC;
+    if (hp.cp && (stages & GDN_STAGE_CORRECTION)) {
+        cudaError_t e = tc ? launch_fused_tc(p, w, 1, hp.grid, stream) : launch_fused_simt(p, w, 1, hp.grid, stream);
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+        if (launch_scan(p, w, stream) != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    if (stages & GDN_STAGE_FUSED) {
+        if (opts.prof_begin &&
+            cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts.prof_begin), stream) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        cudaError_t e = tc ? launch_fused_tc(p, w, 2, hp.grid, stream) : launch_fused_simt(p, w, 2, hp.grid, stream);
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+        if (opts.prof_end && cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts.prof_end), stream) != cudaSuccess)
+            return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_fwd_check(const void *workspace, gdn_stream_t stream) {
+    if (!workspace) return GDN_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+    if (word == 0) return GDN_OK;
+    if (word == GDN_ERR_TIMEOUT) return GDN_ERR_TIMEOUT;
+    return GDN_ERR_DEVICE_CHECK;
+}
+
+namespace {
+struct HostLayout {
+    size_t q, k, v, g, beta, s0, cu, o, sf, ws, total;
+};
+
+bool host_layout(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, int has_s0, int dtype,
+                 const gdn_options *opts, HostLayout *hl, size_t *ws_bytes) {
+    gdn_plan_info info;
+    if (gdn_plan_query(B, T, H, dk, dv, n_seqs, varlen, (gdn_dtype)dtype, opts, &info) != GDN_OK) return false;
+    const size_t e = dtype == GDN_BF16 ? 2 : 4;
+    const size_t ntok = varlen ? (size_t)T : (size_t)B * T;
+    const size_t N = varlen ? (size_t)n_seqs : (size_t)B;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    hl->q = take(ntok * H * dk * e);
+    hl->k = take(ntok * H * dk * e);
+    hl->v = take(ntok * H * dv * e);
+    hl->g = take(ntok * H * 4);
+    hl->beta = take(ntok * H * 4);
+    hl->s0 = take(has_s0 ? N * H * dk * dv * 4 : 0);
+    hl->cu = take(varlen ? (N + 1) * 4 : 0);
+    hl->o = take(ntok * H * dv * e);
+    hl->sf = take(N * H * dk * dv * 4);
+    hl->ws = take(info.workspace_bytes);
+    hl->total = off;
+    *ws_bytes = info.workspace_bytes;
+    return true;
+}
+}  // namespace
+
+size_t gdn_chunk_fwd_host_buffer_size(int B, int T, int H, int dk, int dv, int n_seqs, int varlen,
+                                      int has_initial_state, gdn_dtype dtype, const gdn_options *opts) {
+    HostLayout hl;
+    size_t ws = 0;
+    if (!host_layout(B, T, H, dk, dv, n_seqs, varlen, has_initial_state, dtype, opts, &hl, &ws)) return 0;
+    return hl.total;
+}
+
+gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                              const float *initial_state, const int32_t *cu_seqlens, int n_seqs, float scale,
+                              int B, int T, int H, int dk, int dv, gdn_dtype dtype, void *o, float *final_state,
+                              void *device_buffer, size_t device_buffer_bytes, const gdn_options *opts,
+                              gdn_stream_t stream_in) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_in);
+    const int varlen = cu_seqlens != nullptr;
+    HostLayout hl;
+    size_t ws_bytes = 0;
+    if (!host_layout(B, T, H, dk, dv, n_seqs, varlen, initial_state != nullptr, dtype, opts, &hl, &ws_bytes))
+        return GDN_ERR_INVALID_ARG;
+    if (!device_buffer || !final_state) return GDN_ERR_INVALID_ARG;
+    if (device_buffer_bytes < hl.total) return GDN_ERR_WORKSPACE;
+    const size_t e = dtype == GDN_BF16 ? 2 : 4;
+    const size_t ntok = varlen ? (size_t)T : (size_t)B * T;
+    const size_t N = varlen ? (size_t)n_seqs : (size_t)B;
+    if (ntok > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+    char *d = static_cast<char *>(device_buffer);
+    struct Copy { void *dst; const void *src; size_t n; };
+    const Copy in[] = {
+        {d + hl.q, q, ntok * H * dk * e}, {d + hl.k, k, ntok * H * dk * e}, {d + hl.v, v, ntok * H * dv * e},
+        {d + hl.g, g, ntok * H * 4}, {d + hl.beta, beta, ntok * H * 4},
+        {d + hl.s0, initial_state, initial_state ? N * H * dk * dv * 4 : 0},
+        {d + hl.cu, cu_seqlens, varlen ? (N + 1) * 4 : 0},
+    };
+    cudaGetLastError();
+    for (const Copy &c : in)
+        if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return GDN_ERR_CUDA;
+    gdn_status st = gdn_chunk_fwd(d + hl.q, d + hl.k, d + hl.v, reinterpret_cast<float *>(d + hl.g),
+                                  reinterpret_cast<float *>(d + hl.beta),
+                                  initial_state ? reinterpret_cast<float *>(d + hl.s0) : nullptr,
+                                  varlen ? reinterpret_cast<int32_t *>(d + hl.cu) : nullptr, n_seqs, scale, B, T, H,
+                                  dk, dv, dtype, d + hl.o, reinterpret_cast<float *>(d + hl.sf), d + hl.ws, ws_bytes,
+                                  opts, stream_in);
+    if (st != GDN_OK) return st;
+    if (ntok && cudaMemcpyAsync(o, d + hl.o, ntok * H * dv * e, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (cudaMemcpyAsync(final_state, d + hl.sf, N * H * dk * dv * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    return gdn_chunk_fwd_check(d + hl.ws, stream_in);
+}
+
+const char *gdn_status_string(gdn_status s) {
+    switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_DEVICE_CHECK: return "GDN_ERR_DEVICE_CHECK";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+const char *gdn_version(void) { return "gdn-gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+// Internal declarations shared by the CUDA translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;  // C, the chunk length (WY paragraph of the FlashQLA talk)
+
+// Problem description as the kernels see it (device pointers).
+struct Problem {
+    const void *q, *k, *v;
+    const float *g, *beta, *s0;
+    const int32_t *cu;      // device cu_seqlens or nullptr (batched)
+    void *o;
+    float *sf;
+    int B, T, H, dk, dv, N, total_T, varlen, dtype;
+    float scale;
+};
+
+// Device pointers into the caller's workspace.
+struct Workspace {
+    int *err;               // error word (a gdn_status)
+    int *counters;          // [8] work-queue counters, zeroed by the sequence-prep kernel
+    int *num_chunks;        // [1]
+    int *num_items;         // [4]: pass-2 items, pass-1 items, scan units, -
+    int4 *seqinfo;          // [N]: (first token, length, first chunk, chunks)
+    int4 *chunks;           // [max_chunks]: (seq, first token, length, chunk index in seq)
+    int *flags;             // [N*H]
+    float *G;               // [H, total_T]
+    float *totals;          // [H, max_chunks]
+    void *tprime;           // [H, total_T, C] bf16 (bf16 inputs) or fp32 (fp32 inputs)
+    gdn_work_item *items2;  // [max_items]
+    gdn_work_item *items1;  // [max_items1]
+    int4 *scan_units;       // [max_cp_slots]: (seq, head, segments, first slot)
+    int *seq_order;         // [N]: sequences, longest first
+    float *cp_s;            // [max_cp_slots, dk, dv]
+    float *cp_m;            // [max_cp_slots, dk, dk]
+    int max_chunks, max_items, max_items1, max_cp_slots;
+};
+
+struct PlanParams {
+    int L;            // chunks per segment (huge when CP is off)
+    int cp_enabled;
+    int sliding;
+    float ln_eps;
+};
+
+// Host-side layout of the workspace for one problem.
+struct Layout {
+    size_t err, counters, num_chunks, num_items, seqinfo, chunks, flags, G, totals, tprime,
+        items2, items1, scan_units, seq_order, cp_s, cp_m, total;
+    int max_chunks, max_items, max_items1, max_cp_slots;
+};
+
+// Launchers (each returns cudaGetLastError() of its launch).
+cudaError_t launch_seqprep(const Problem &p, const Workspace &w, cudaStream_t s);
+cudaError_t launch_gate(const Problem &p, const Workspace &w, cudaStream_t s);
+cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &pp, cudaStream_t s);
+cudaError_t launch_inverse(const Problem &p, const Workspace &w, cudaStream_t s);
+cudaError_t launch_scan(const Problem &p, const Workspace &w, cudaStream_t s);
+// pass 1 (state-only correction items) or pass 2 (output items) on the CUDA-core kernel
+cudaError_t launch_fused_simt(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s);
+// the tcgen05 kernel; returns cudaErrorNotSupported when this build/device cannot run it
+cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s);
+bool fused_tc_supported(int dtype, int dk, int dv);
+int fused_simt_smem_bytes(int dk, int dv);
+
+// Called once per CTA of a persistent pass after it found the queue empty: the
+// last CTA to leave resets the item counter and the exit counter to zero.
+__device__ __forceinline__ void finish_queue(int *item_counter, int *exit_counter) {
+    __threadfence();
+    const int done = atomicAdd(exit_counter, 1) + 1;
+    if (done == (int)gridDim.x) {
+        atomicExch(item_counter, 0);
+        atomicExch(exit_counter, 0);
+        __threadfence();
+    }
+}
+
+// Records `code` in the error word unless one is already recorded.
+__device__ __forceinline__ void report_error(int *err, int code) { atomicCAS(err, 0, code); }
+
+__device__ __forceinline__ float load_elem(const void *base, size_t idx, int dtype) {
+    if (dtype == GDN_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[idx]);
+    return reinterpret_cast<const float *>(base)[idx];
+}
+
+__device__ __forceinline__ void store_elem(void *base, size_t idx, int dtype, float x) {
+    if (dtype == GDN_BF16)
+        reinterpret_cast<__nv_bfloat16 *>(base)[idx] = __float2bfloat16_rn(x);
+    else
+        reinterpret_cast<float *>(base)[idx] = x;
+}
+
+}  // namespace gdn

@@ -1,0 +1,232 @@
+/*
+ * gdn.h — C ABI of the GB300 (sm_103a) Gated Delta Network chunked-prefill
+ * forward pass.
+ *
+ * The operation (FlashQLA talk "Qwen系列模型线性注意力高性能优化实践", the
+ * recurrent-form and GDN paragraphs): for every sequence n and head h, with the
+ * state S in R^{dv x dk},
+ *
+ *     S_t = S_{t-1} alpha_t (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *     o_t = scale * S_t q_t,            alpha_t = exp(g_t),
+ *
+ * computed chunk by chunk (C = 64 tokens) in the WY form (same talk, WY and
+ * four-step paragraphs): a gate kernel (chunk-local log-space cumsum, head
+ * flags), a per-chunk kernel that inverts I + diag(beta) strictlower(K K^T)
+ * without any exponentials (Gamma-extraction paragraph), optional intra-card
+ * sequence parallelism (difference, compute-for-memory, auto-CP and
+ * sliding-window paragraphs), and one fused kernel that forms U, runs the
+ * chunk-to-chunk state recurrence and writes o.
+ *
+ * Layouts (all row-major, C order):
+ *   q, k           [B, T, H, dk]   dtype (bf16 or fp32)
+ *   v, o           [B, T, H, dv]   dtype
+ *   g, beta        [B, T, H]       fp32 (g = log alpha <= 0, beta in [0, 1])
+ *   initial_state,
+ *   final_state    [N, H, dk, dv]  fp32; element [n][h][j][i] is S[i][j]
+ *                                  (key index j outer, value index i inner)
+ *   cu_seqlens     [N + 1]         int32, device memory; with it the batch is
+ *                                  packed (B = 1, T = total tokens) and
+ *                                  sequence n is tokens cu[n] .. cu[n+1]-1
+ *
+ * Ownership: the caller allocates every buffer (inputs, outputs, workspace)
+ * and keeps them alive until the work on `stream` completes.  The library
+ * allocates no device or host memory, keeps no state between calls besides a
+ * per-device cache of device attributes and driver entry points, and never
+ * synchronises the stream inside gdn_chunk_fwd.
+ *
+ * Errors: every call returns a gdn_status and never aborts.  Argument errors
+ * are found on the host before any launch.  Errors found on the device (a
+ * malformed cu_seqlens, a bounded wait that ran out) are written to an error
+ * word inside the workspace; gdn_chunk_fwd_check() reads it.
+ *
+ * Preconditions that are not checked: q and k rows are L2-normalised (the
+ * sliding-window bound relies on it), g <= 0, 0 <= beta <= 1, all inputs
+ * finite, and no two calls share a workspace concurrently.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer */
+    GDN_ERR_UNSUPPORTED = 2,   /* shape/dtype/device this build does not handle */
+    GDN_ERR_WORKSPACE = 3,     /* workspace smaller than gdn_chunk_fwd_workspace_size() */
+    GDN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    GDN_ERR_DEVICE_CHECK = 5,  /* the device found bad input (e.g. cu_seqlens) */
+    GDN_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out */
+} gdn_status;
+
+typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
+
+/* Intra-card sequence parallelism (auto-CP paragraph): AUTO lets the planner
+ * decide; OFF runs every (sequence, head) as one unit and is bitwise
+ * deterministic; FORCE always splits sequences into segments. */
+typedef enum { GDN_CP_AUTO = 0, GDN_CP_OFF = 1, GDN_CP_FORCE = 2 } gdn_cp_mode;
+
+/* Which fused kernel runs: AUTO picks the tcgen05 kernel when it supports the
+ * shape (bf16, dk = dv = 128) and the CUDA-core kernel otherwise. */
+typedef enum { GDN_KERNEL_AUTO = 0, GDN_KERNEL_TC = 1, GDN_KERNEL_SIMT = 2 } gdn_kernel;
+
+typedef struct {
+    int32_t cp_mode;            /* gdn_cp_mode */
+    int32_t kernel;             /* gdn_kernel */
+    int32_t chunks_per_segment; /* > 0 forces the segment length L (chunks) when CP is on */
+    int32_t sliding;            /* 1 (default): heads with alpha != 1 restart from a
+                                   look-back window; 0: every split head uses
+                                   correction matrices */
+    float sw_eps;               /* look-back tolerance: the window is long enough that
+                                   prod(alpha) over it <= sw_eps (default 2^-24) */
+    int32_t sm_count;           /* 0: query the device; > 0: plan for this many SMs */
+    int32_t stages;             /* 0: the whole path; else a GDN_STAGE_* mask (stages not
+                                   selected are skipped and their workspace outputs must
+                                   already be there from an earlier call on the same
+                                   problem and workspace) */
+    int32_t debug_checks;       /* reserved, 0 */
+    void *prof_begin;           /* optional cudaEvent_t, recorded on `stream` right before
+                                   the fused output pass is launched */
+    void *prof_end;             /* optional cudaEvent_t, recorded right after it */
+    int32_t reserved[4];
+} gdn_options;
+
+enum {
+    GDN_STAGE_PREP = 1,         /* sequence tables, gate kernel, device planner */
+    GDN_STAGE_INVERSE = 2,      /* per-chunk inverse T' */
+    GDN_STAGE_CORRECTION = 4,   /* correction pass and segment scan (when CP is on) */
+    GDN_STAGE_FUSED = 8         /* fused output pass */
+};
+
+/* What the host planner decided for a problem (host-only, no GPU needed). */
+typedef struct {
+    int32_t kernel;             /* gdn_kernel actually used (TC or SIMT) */
+    int32_t cp_enabled;         /* 1 when sequences may be split into segments */
+    int32_t chunks_per_segment; /* segment length L in chunks */
+    int32_t max_chunks;         /* upper bound on chunks over all sequences */
+    int32_t max_items;          /* capacity of the fused-kernel work list */
+    int32_t max_cp_slots;       /* capacity of the correction-matrix buffers */
+    int32_t sm_count;           /* SMs the plan was made for */
+    int32_t grid_fused;         /* CTAs of the persistent fused kernel */
+    size_t workspace_bytes;     /* bytes gdn_chunk_fwd needs */
+} gdn_plan_info;
+
+/* Byte offsets of the intermediate tensors inside the workspace, so tests and
+ * tools can inspect them after a call (read them only after the stream syncs). */
+typedef struct {
+    size_t error_word;     /* int32: 0 or a gdn_status found on the device */
+    size_t gate_cumsum;    /* fp32 [H, total_T]: chunk-local inclusive cumsum of g */
+    size_t chunk_totals;   /* fp32 [H, max_chunks]: sum of g per chunk (chunks in sequence order) */
+    size_t head_flags;     /* int32 [N, H]: 1 when some g != 0 (alpha not identically 1) */
+    size_t tprime;         /* [H, total_T, 64] T' rows by token; bf16 for bf16 inputs, fp32 for fp32 */
+    size_t chunk_table;    /* int32x4 [max_chunks]: (seq, first token, length, chunk index in seq) */
+    size_t num_chunks;     /* int32: chunks actually present */
+    size_t items;          /* int32x8 [max_items]: fused-kernel work items (see gdn_work_item) */
+    size_t num_items;      /* int32: [0] pass-2 items, [1] pass-1 items, [2] scan units */
+    size_t total;
+} gdn_workspace_layout;
+
+/* One unit of fused-kernel work as the planner writes it. */
+typedef struct {
+    int32_t seq, head;
+    int32_t c_begin, c_end;   /* chunks [c_begin, c_end) of the sequence produce output */
+    int32_t c_start;          /* first chunk run (c_start <= c_begin); chunks before
+                                 c_begin only advance the state (look-back) */
+    int32_t flags;            /* GDN_ITEM_* bits */
+    int32_t slot;             /* correction-buffer slot (CP) or -1 */
+    int32_t pad;
+} gdn_work_item;
+
+enum {
+    GDN_ITEM_OUTPUT = 1,        /* write o for chunks [c_begin, c_end) */
+    GDN_ITEM_FROM_INITIAL = 2,  /* start from initial_state (or zero when it is NULL) */
+    GDN_ITEM_FROM_ZERO = 4,     /* start from S = 0 */
+    GDN_ITEM_FROM_IDENTITY = 8, /* start from S = I and use zero values (correction matrix) */
+    GDN_ITEM_FROM_SLOT = 16,    /* start from the scanned segment start in `slot` */
+    GDN_ITEM_WRITE_FINAL = 32,  /* write final_state */
+    GDN_ITEM_WRITE_SLOT = 64,   /* write the end state to the S* buffer `slot` */
+    GDN_ITEM_WRITE_M = 128      /* write the end state to the M buffer `slot` */
+};
+
+/* Fill *opts with the defaults (AUTO everywhere, sliding on, sw_eps 2^-24). */
+void gdn_default_options(gdn_options *opts);
+
+/* Host-only planning: which kernel, whether CP is on, the segment length and
+ * the workspace size.  `total_T` is B*T for batched input or the packed token
+ * count with cu_seqlens (then B must be 1 and n_seqs = N).  opts may be NULL. */
+gdn_status gdn_plan_query(int B, int T, int H, int dk, int dv, int n_seqs, int varlen,
+                          gdn_dtype dtype, const gdn_options *opts, gdn_plan_info *out);
+
+/* Bytes of device workspace gdn_chunk_fwd needs for this problem (0 on bad
+ * arguments).  `varlen` is 1 when cu_seqlens will be passed. */
+size_t gdn_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int n_seqs, int varlen,
+                                    gdn_dtype dtype, const gdn_options *opts);
+
+/* Offsets of the intermediates inside the workspace for this problem. */
+gdn_status gdn_workspace_query(int B, int T, int H, int dk, int dv, int n_seqs, int varlen,
+                               gdn_dtype dtype, const gdn_options *opts, gdn_workspace_layout *out);
+
+/*
+ * The forward pass.  All pointers are device pointers (initial_state and
+ * cu_seqlens may be NULL).  With cu_seqlens == NULL the batch is B sequences of
+ * T tokens (n_seqs is ignored); otherwise B must be 1, T is the total token
+ * count and n_seqs = N.  scale <= 0 selects dk^-0.5.  dk, dv in {32, 64, 128}.
+ * q, k, v, o, g, beta, states and workspace must be 16-byte aligned.
+ * The workspace must hold gdn_chunk_fwd_workspace_size() bytes; it needs no
+ * initialisation.  Everything is enqueued on `stream`; nothing syncs.
+ */
+gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *g, const float *beta,
+                         const float *initial_state,
+                         const int32_t *cu_seqlens, int n_seqs,
+                         float scale,
+                         int B, int T, int H, int dk, int dv, gdn_dtype dtype,
+                         void *o, float *final_state,
+                         void *workspace, size_t workspace_bytes,
+                         const gdn_options *opts, gdn_stream_t stream);
+
+/* Synchronises `stream`, then reads the device error word of `workspace`:
+ * GDN_OK, GDN_ERR_DEVICE_CHECK (bad cu_seqlens) or GDN_ERR_TIMEOUT. */
+gdn_status gdn_chunk_fwd_check(const void *workspace, gdn_stream_t stream);
+
+/* Device bytes gdn_chunk_fwd_host needs as its staging buffer (inputs, outputs
+ * and workspace together). */
+size_t gdn_chunk_fwd_host_buffer_size(int B, int T, int H, int dk, int dv, int n_seqs, int varlen,
+                                      int has_initial_state, gdn_dtype dtype, const gdn_options *opts);
+
+/*
+ * The same forward pass for inputs and outputs in HOST memory (pinned memory
+ * makes the copies asynchronous).  The call copies the inputs into
+ * `device_buffer` (gdn_chunk_fwd_host_buffer_size() bytes, caller-owned), runs
+ * gdn_chunk_fwd on `stream`, copies o and final_state back, synchronises the
+ * stream and returns the device error status as gdn_chunk_fwd_check does.
+ * cu_seqlens is a host array here.
+ */
+gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v,
+                              const float *g, const float *beta,
+                              const float *initial_state,
+                              const int32_t *cu_seqlens, int n_seqs,
+                              float scale,
+                              int B, int T, int H, int dk, int dv, gdn_dtype dtype,
+                              void *o, float *final_state,
+                              void *device_buffer, size_t device_buffer_bytes,
+                              const gdn_options *opts, gdn_stream_t stream);
+
+/* Human-readable name of a status. */
+const char *gdn_status_string(gdn_status status);
+
+/* Library version string. */
+const char *gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

@@ -1,0 +1,118 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads, exports
+every function include/gdn.h declares, plans sensibly and rejects bad
+arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_prefill_gdn_gb300 as gdn
+from chunked_prefill_gdn_gb300 import build as gdn_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gdn_build.build()
+    return gdn.load_library()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(gdn_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "gdn_chunk_fwd" in names and len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in gdn.gdn_version()
+    assert gdn.gdn_status_string(0) == "GDN_OK"
+    assert gdn.gdn_status_string(5) == "GDN_ERR_DEVICE_CHECK"
+
+
+def test_option_struct_layout(lib):
+    assert ctypes.sizeof(gdn.GdnOptions) == 64
+    o = gdn.default_options()
+    assert o.cp_mode == gdn.CP_AUTO and o.sliding == 1 and abs(o.sw_eps - 2 ** -24) < 1e-12
+
+
+def plan(*a, **kw):
+    opts = gdn.default_options(**kw) if kw else None
+    return gdn.gdn_plan_query(*a, opts=opts)
+
+
+def test_plan_layer_shape_runs_without_cp(lib):
+    p = plan(4, 8192, 32, 128, 128, 4, 0, gdn.BF16, sm_count=152)
+    assert p.cp_enabled == 0 and p.max_chunks == 512 and p.max_items == 128
+
+
+def test_plan_few_long_sequences_split(lib):
+    p = plan(1, 131072, 8, 128, 128, 1, 0, gdn.BF16, sm_count=152)
+    assert p.cp_enabled == 1
+    segs = -(-2048 // p.chunks_per_segment)
+    assert 8 * segs <= 152 * 2 and segs >= 10
+    assert p.max_cp_slots >= 8 * (segs - 1)
+
+
+def test_plan_cp_modes(lib):
+    off = plan(1, 131072, 8, 128, 128, 1, 0, gdn.BF16, sm_count=152, cp_mode=gdn.CP_OFF)
+    assert off.cp_enabled == 0 and off.max_cp_slots == 0
+    force = plan(4, 8192, 32, 128, 128, 4, 0, gdn.BF16, sm_count=152, cp_mode=gdn.CP_FORCE,
+                 chunks_per_segment=16)
+    assert force.cp_enabled == 1 and force.chunks_per_segment == 16
+    assert force.max_items >= 4 * 32 * 8
+
+
+def test_plan_varlen_capacity_bounds(lib):
+    p = plan(1, 262144, 16, 128, 128, 64, 1, gdn.BF16, sm_count=152)
+    assert p.max_chunks == 262144 // 64 + 64
+    L = p.chunks_per_segment
+    assert p.max_items >= 16 * 64 and p.max_cp_slots == 16 * (-(-p.max_chunks // L))
+
+
+def test_plan_rejects_bad_shapes(lib):
+    with pytest.raises(gdn.GdnError):
+        plan(1, 100, 2, 48, 64, 1, 0, gdn.BF16)       # unsupported head size
+    with pytest.raises(gdn.GdnError):
+        plan(2, 100, 2, 64, 64, 2, 1, gdn.BF16)       # varlen needs B == 1
+    with pytest.raises(gdn.GdnError):
+        plan(1, 100, 0, 64, 64, 1, 0, gdn.BF16)
+
+
+def test_workspace_size_grows_with_tokens(lib):
+    a = gdn.gdn_chunk_fwd_workspace_size(1, 1000, 4, 128, 128, 1, 0, gdn.BF16)
+    b = gdn.gdn_chunk_fwd_workspace_size(1, 2000, 4, 128, 128, 1, 0, gdn.BF16)
+    assert 0 < a < b
+    assert gdn.gdn_chunk_fwd_workspace_size(1, 10, 4, 48, 128, 1, 0, gdn.BF16) == 0
+
+
+def test_host_argument_errors_before_launch(lib):
+    """Null or misaligned pointers and a short workspace are rejected on the
+    host; these calls never reach the GPU."""
+    fake = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    args = dict(q=fake, k=fake, v=fake, g=fake, b=fake)
+    ws = gdn.gdn_chunk_fwd_workspace_size(1, 256, 2, 32, 32, 1, 0, gdn.F32)
+
+    def call(q=fake, o=fake, sf=fake, wsp=fake, wsb=ws):
+        return gdn.gdn_chunk_fwd(q, fake, fake, fake, fake, None, None, 1, 0.0, 1, 256, 2, 32, 32, gdn.F32,
+                                 o, sf, wsp, wsb, None, None)
+    assert call(q=None) == 1
+    assert call(q=mis) == 1
+    assert call(sf=None) == 1
+    assert call(wsb=ws - 1) == 3
+    assert gdn.gdn_chunk_fwd(fake, fake, fake, fake, fake, None, None, 1, 0.0, 1, 256, 2, 48, 32, gdn.F32,
+                             fake, fake, fake, ws, None, None) == 2

@@ -1,0 +1,236 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle
+on the same seeded inputs.  Bar: relative L2 <= 5e-3 and max-abs <= 2e-2 on o
+and final_state.
+
+Reduced cases keep each workload's distributions but shrink it so the oracle
+finishes in seconds while still spanning many chunks, a ragged last chunk and
+several segments; the full-size cases run the workload in the bench's launch
+configuration and check sampled (sequence, head, value-row) slices, which the
+oracle computes exactly because state rows evolve independently.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import chunked, gate
+import chunked_prefill_gdn_gb300 as gdn
+from chunked_prefill_gdn_gb300.inputs import CONFIGS, make_inputs
+
+from gpu_helpers import (assert_close, full_reference, gpu_run, gpu_sampled, sampled_reference, seq_bounds,
+                         to_device)
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = {"auto": gdn.KERNEL_AUTO, "simt": gdn.KERNEL_SIMT}
+
+
+def opts_for(kernel="auto", **kw):
+    return gdn.default_options(kernel=KERNELS[kernel], **kw)
+
+
+REDUCED = {
+    "tiny": CONFIGS[0],
+    "layer_ragged": CONFIGS[1].scaled(B=2, T=1000, H=4),
+    "long_cp": CONFIGS[2].scaled(T=4133, H=4, zero_gate_heads=(0, 1)),
+    "varlen": CONFIGS[3].scaled(T=6000, H=4, n_seqs=9),
+    "mix_cp": CONFIGS[4].scaled(T=5000, H=5, zero_gate_heads=(0, 1)),
+}
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+@pytest.mark.parametrize("name", sorted(REDUCED))
+@pytest.mark.parametrize("cp", ["off", "force"])
+def test_reduced_parity(name, cp, kernel):
+    cfg = REDUCED[name]
+    inp = to_device(make_inputs(cfg, "cpu"))
+    o_ref, sf_ref = full_reference(inp)
+    kw = dict(cp_mode=gdn.CP_OFF) if cp == "off" else dict(cp_mode=gdn.CP_FORCE, chunks_per_segment=5)
+    o, sf = gpu_run(inp, opts_for(kernel, **kw))
+    B, T, H, dv = o.shape
+    assert_close("o", oracle.to_f64(o).reshape(B * T, H, dv), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
+def test_cp_forced_without_sliding():
+    """Every split head through correction matrices and the scan."""
+    inp = to_device(make_inputs(REDUCED["mix_cp"], "cpu"))
+    o_ref, sf_ref = full_reference(inp)
+    o, sf = gpu_run(inp, opts_for(cp_mode=gdn.CP_FORCE, chunks_per_segment=7, sliding=0))
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 129])
+def test_short_and_ragged_lengths(T):
+    inp = to_device(make_inputs(CONFIGS[1].scaled(B=3, T=T, H=2, s0_std=0.02), "cpu"))
+    o_ref, sf_ref = full_reference(inp)
+    o, sf = gpu_run(inp)
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
+def test_varlen_with_empty_and_tiny_sequences():
+    lens = [0, 1, 64, 0, 200, 3, 0]
+    cfg = CONFIGS[1].scaled(B=1, T=sum(lens), H=3, s0_std=0.02)
+    inp = make_inputs(cfg, "cpu")
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    inp["cu_seqlens"] = cu
+    inp["initial_state"] = 0.02 * torch.randn(len(lens), 3, 128, 128, generator=torch.Generator().manual_seed(5))
+    inp = to_device(inp)
+    o_ref, sf_ref = full_reference(inp)
+    o, sf = gpu_run(inp)
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+    # empty sequences hand their initial state straight through
+    for n in (0, 3, 6):
+        assert torch.equal(sf[n], inp["initial_state"][n])
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_head_sizes_fp32(d):
+    cfg = CONFIGS[0].scaled(T=300, H=3, dk=d, dv=d, s0_std=0.1)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    o_ref, sf_ref = full_reference(inp)
+    o, sf = gpu_run(inp, opts_for(cp_mode=gdn.CP_FORCE, chunks_per_segment=2))
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
+def test_unequal_head_sizes():
+    cfg = CONFIGS[1].scaled(B=2, T=150, H=2, dk=128, dv=64, s0_std=0.02)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    o_ref, sf_ref = full_reference(inp)
+    o, sf = gpu_run(inp, opts_for(cp_mode=gdn.CP_FORCE, chunks_per_segment=1, sliding=0))
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
+def test_resume_two_calls_equal_one():
+    inp = to_device(make_inputs(CONFIGS[1].scaled(B=1, T=700, H=2), "cpu"))
+    o, sf = gpu_run(inp)
+    cut = 320
+    a = dict(inp, q=inp["q"][:, :cut].contiguous(), k=inp["k"][:, :cut].contiguous(), v=inp["v"][:, :cut].contiguous(),
+             g=inp["g"][:, :cut].contiguous(), beta=inp["beta"][:, :cut].contiguous())
+    oa, sfa = gpu_run(a)
+    b = dict(inp, q=inp["q"][:, cut:].contiguous(), k=inp["k"][:, cut:].contiguous(), v=inp["v"][:, cut:].contiguous(),
+             g=inp["g"][:, cut:].contiguous(), beta=inp["beta"][:, cut:].contiguous(), initial_state=sfa)
+    ob, sfb = gpu_run(b)
+    assert_close("o", oracle.to_f64(torch.cat([oa, ob], 1)), oracle.to_f64(o), 2e-3, 1e-2)
+    assert_close("final_state", oracle.to_f64(sfb), oracle.to_f64(sf), 2e-3, 1e-2)
+
+
+def test_cp_off_is_deterministic():
+    inp = to_device(make_inputs(CONFIGS[1].scaled(B=2, T=500, H=4), "cpu"))
+    o1, s1 = gpu_run(inp, opts_for(cp_mode=gdn.CP_OFF))
+    o2, s2 = gpu_run(inp, opts_for(cp_mode=gdn.CP_OFF))
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+# ----------------------------------------------------------- intermediates
+
+def _workspace_views(inp, ws, opts=None):
+    q, v = inp["q"], inp["v"]
+    B, T, H, dk = q.shape
+    cu = inp.get("cu_seqlens")
+    N = B if cu is None else cu.numel() - 1
+    dt = gdn.BF16 if q.dtype == torch.bfloat16 else gdn.F32
+    lay = gdn.gdn_workspace_query(B, T, H, dk, v.shape[-1], N, cu is not None, dt, opts)
+    total_T = B * T
+    info = gdn.gdn_plan_query(B, T, H, dk, v.shape[-1], N, cu is not None, dt, opts)
+
+    def view(off, n, dtype):
+        esz = torch.tensor([], dtype=dtype).element_size()
+        return ws[off:off + n * esz].view(dtype)
+
+    return dict(
+        G=view(lay.gate_cumsum, H * total_T, torch.float32).view(H, total_T),
+        flags=view(lay.head_flags, N * H, torch.int32).view(N, H),
+        tprime=view(lay.tprime, H * total_T * 64, q.dtype).view(H, total_T, 64),
+        totals=view(lay.chunk_totals, H * info.max_chunks, torch.float32).view(H, info.max_chunks),
+        num_chunks=int(view(lay.num_chunks, 1, torch.int32).item()),
+        items=view(lay.items, 8 * info.max_items, torch.int32).view(info.max_items, 8),
+        num_items=view(lay.num_items, 4, torch.int32).tolist(),
+    )
+
+
+def test_gate_and_inverse_intermediates():
+    cfg = CONFIGS[3].scaled(T=3000, H=3, n_seqs=5, zero_gate_heads=(1,))
+    inp = to_device(make_inputs(cfg, "cpu"))
+    ws = gdn.workspace_for(inp["q"], inp["v"], inp["cu_seqlens"])
+    gpu_run(inp, workspace=ws)
+    views = _workspace_views(inp, ws)
+    cu = seq_bounds(inp)
+    g = oracle.to_f64(inp["g"]).reshape(-1, 3)
+    # chunk-local cumsum of the gate
+    G_ref = gate.chunk_local_cumsum(g, cu, 64)
+    assert np.abs(oracle.to_f64(views["G"]).T - G_ref).max() < 1e-4
+    # chunk totals and head flags
+    tot_ref = gate.chunk_totals(g, cu, 64)
+    nck = views["num_chunks"]
+    assert nck == len(gate.chunk_table(cu, 64))
+    assert np.abs(oracle.to_f64(views["totals"][:, :nck]).T - tot_ref).max() < 1e-4
+    assert views["flags"].cpu().numpy().tolist() == gate.head_flags(g, cu).tolist()
+    # T' rows against the fp64 inverse (bf16 storage)
+    Tp_ref = chunked.inverse_rows(oracle.to_f64(inp["k"]).reshape(-1, 3, 128), oracle.to_f64(inp["beta"]).reshape(-1, 3),
+                                  cu, 64)
+    Tp = oracle.to_f64(views["tprime"]).transpose(1, 0, 2)
+    assert np.abs(Tp - Tp_ref).max() < 2e-2
+    assert np.linalg.norm(Tp - Tp_ref) / np.linalg.norm(Tp_ref) < 4e-3
+
+
+def test_bad_cu_seqlens_is_reported_not_faulted():
+    cfg = CONFIGS[3].scaled(T=1000, H=2, n_seqs=4)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    bad = inp["cu_seqlens"].clone()
+    bad[2] = bad[1] - 5            # decreasing
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, bad, inp["scale"], check=True)
+    assert e.value.status == 5
+    bad = inp["cu_seqlens"].clone()
+    bad[-1] = 999                  # does not cover the tokens
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, bad, inp["scale"], check=True)
+    assert e.value.status == 5
+    # the context is still usable afterwards
+    o, sf = gpu_run(inp)
+    assert torch.isfinite(o.float()).all()
+
+
+def test_host_buffer_entry_point():
+    inp = make_inputs(CONFIGS[3].scaled(T=2500, H=2, n_seqs=3, s0_std=0.02), "cpu")
+    pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    o, sf = gdn.chunk_fwd_host(pinned["q"], pinned["k"], pinned["v"], pinned["g"], pinned["beta"],
+                               pinned["initial_state"], pinned["cu_seqlens"], inp["scale"])
+    o_ref, sf_ref = full_reference(inp)
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
+# ---------------------------------------------- full sizes, sampled outputs
+
+FULL_SAMPLES = {
+    0: dict(seqs=[0], heads=[0, 1], rows=None),
+    1: dict(seqs=[0, 3], heads=[0, 17, 31], rows=[0, 5, 64, 127]),
+    2: dict(seqs=[0], heads=[0, 2, 3, 7], rows=[1, 100]),
+    3: dict(seqs=None, heads=[0, 9, 15], rows=[3, 90]),
+    4: dict(seqs=[0], heads=[0, 4, 5, 15], rows=[7]),
+}
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
+def test_full_size_sampled(idx):
+    cfg = CONFIGS[idx]
+    inp = make_inputs(cfg, "cuda")
+    o, sf = gpu_run(inp)
+    spec = FULL_SAMPLES[idx]
+    seqs = spec["seqs"]
+    if seqs is None:   # varlen: the longest and two short sequences
+        cu = seq_bounds(inp)
+        lens = np.diff(cu)
+        order = np.argsort(-lens)
+        seqs = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
+    o_ref, sf_ref, tidx = sampled_reference(inp, seqs, spec["heads"], spec["rows"])
+    o_s, sf_s = gpu_sampled(o, sf, inp, seqs, spec["heads"], spec["rows"], tidx)
+    assert_close("o", o_s, o_ref)
+    assert_close("final_state", sf_s, sf_ref)
