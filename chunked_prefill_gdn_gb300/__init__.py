@@ -27,7 +27,7 @@ __all__ = [
     "load_library", "library_path", "default_options",
     "gdn_default_options", "gdn_plan_query", "gdn_chunk_fwd_workspace_size", "gdn_workspace_query",
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
-    "gdn_status_string", "gdn_version", "chunk_fwd", "chunk_fwd_host", "workspace_for", "GdnError",
+    "gdn_status_string", "gdn_version", "gdn_last_error_detail", "chunk_fwd", "chunk_fwd_host", "workspace_for", "GdnError",
     "CP_AUTO", "CP_OFF", "CP_FORCE", "KERNEL_AUTO", "KERNEL_TC", "KERNEL_SIMT", "BF16", "F32",
     "STAGE_PREP", "STAGE_INVERSE", "STAGE_CORRECTION", "STAGE_FUSED",
 ]
@@ -43,7 +43,11 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
 class GdnError(RuntimeError):
     def __init__(self, status: int, where: str = ""):
         self.status = status
-        super().__init__("%s%s" % (STATUS.get(status, "status %d" % status), (" in " + where) if where else ""))
+        detail = ""
+        if status == 4 and _lib is not None:
+            detail = _lib.gdn_last_error_detail().decode()
+        super().__init__("%s%s%s" % (STATUS.get(status, "status %d" % status), (" in " + where) if where else "",
+                                     (" (" + detail + ")") if detail else ""))
 
 
 class GdnOptions(ctypes.Structure):
@@ -114,6 +118,8 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_version.argtypes = []
     lib.gdn_version.restype = ctypes.c_char_p
+    lib.gdn_last_error_detail.argtypes = []
+    lib.gdn_last_error_detail.restype = ctypes.c_char_p
     _lib = lib
     return lib
 
@@ -179,6 +185,10 @@ def gdn_status_string(status: int) -> str:
 
 def gdn_version() -> str:
     return load_library().gdn_version().decode()
+
+
+def gdn_last_error_detail() -> str:
+    return load_library().gdn_last_error_detail().decode()
 
 
 # ---------------------------------------------------------------- tensor API

@@ -186,7 +186,24 @@ gdn_status make_plan(int B, int T, int H, int dk, int dv, int n_seqs, int varlen
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+thread_local char g_error_detail[256] = "";
+
+gdn_status cuda_fail(const char *where, cudaError_t e) {
+    gdn::set_error_detail(where, e);
+    return GDN_ERR_CUDA;
+}
+
 }  // namespace
+
+namespace gdn {
+void set_error_detail(const char *where, cudaError_t e, int driver_result) {
+    if (driver_result)
+        snprintf(g_error_detail, sizeof(g_error_detail), "%s: %s (driver result %d)", where, cudaGetErrorName(e),
+                 driver_result);
+    else
+        snprintf(g_error_detail, sizeof(g_error_detail), "%s: %s", where, cudaGetErrorName(e));
+}
+}  // namespace gdn
 
 extern "C" {
 
@@ -302,36 +319,41 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
                                                     GDN_STAGE_FUSED);
     cudaGetLastError();  // clear a stale error so it is not blamed on these launches
     if (stages & GDN_STAGE_PREP) {
-        if (launch_seqprep(p, w, stream) != cudaSuccess) return GDN_ERR_CUDA;
-        if (L.max_chunks > 0 && launch_gate(p, w, stream) != cudaSuccess) return GDN_ERR_CUDA;
-        if (launch_plan(p, w, pp, stream) != cudaSuccess) return GDN_ERR_CUDA;
+        cudaError_t e = launch_seqprep(p, w, stream);
+        if (e != cudaSuccess) return cuda_fail("launch seqprep", e);
+        if (L.max_chunks > 0 && (e = launch_gate(p, w, stream)) != cudaSuccess) return cuda_fail("launch gate", e);
+        if ((e = launch_plan(p, w, pp, stream)) != cudaSuccess) return cuda_fail("launch plan", e);
     }
     if ((stages & GDN_STAGE_INVERSE) && L.max_chunks > 0) {
-        if (launch_inverse(p, w, stream) != cudaSuccess) return GDN_ERR_CUDA;
+        cudaError_t e = launch_inverse(p, w, stream);
+        if (e != cudaSuccess) return cuda_fail("launch inverse", e);
     }
     const bool tc = hp.kernel == GDN_KERNEL_TC;
     if (hp.cp && (stages & GDN_STAGE_CORRECTION)) {
         cudaError_t e = tc ? launch_fused_tc(p, w, 1, hp.grid, stream) : launch_fused_simt(p, w, 1, hp.grid, stream);
-        if (e != cudaSuccess) return GDN_ERR_CUDA;
-        if (launch_scan(p, w, stream) != cudaSuccess) return GDN_ERR_CUDA;
+        if (e != cudaSuccess) return cuda_fail(tc ? "launch fused_tc pass 1" : "launch fused_simt pass 1", e);
+        if ((e = launch_scan(p, w, stream)) != cudaSuccess) return cuda_fail("launch scan", e);
     }
     if (stages & GDN_STAGE_FUSED) {
+        cudaError_t e;
         if (opts.prof_begin &&
-            cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts.prof_begin), stream) != cudaSuccess)
-            return GDN_ERR_CUDA;
-        cudaError_t e = tc ? launch_fused_tc(p, w, 2, hp.grid, stream) : launch_fused_simt(p, w, 2, hp.grid, stream);
-        if (e != cudaSuccess) return GDN_ERR_CUDA;
-        if (opts.prof_end && cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts.prof_end), stream) != cudaSuccess)
-            return GDN_ERR_CUDA;
+            (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts.prof_begin), stream)) != cudaSuccess)
+            return cuda_fail("record prof_begin", e);
+        e = tc ? launch_fused_tc(p, w, 2, hp.grid, stream) : launch_fused_simt(p, w, 2, hp.grid, stream);
+        if (e != cudaSuccess) return cuda_fail(tc ? "launch fused_tc pass 2" : "launch fused_simt pass 2", e);
+        if (opts.prof_end && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts.prof_end), stream)) != cudaSuccess)
+            return cuda_fail("record prof_end", e);
     }
     return GDN_OK;
 }
 
 gdn_status gdn_chunk_fwd_check(const void *workspace, gdn_stream_t stream) {
     if (!workspace) return GDN_ERR_INVALID_ARG;
-    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("stream synchronize", e);
     int word = 0;
-    if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+    if ((e = cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail("read error word", e);
     if (word == 0) return GDN_OK;
     if (word == GDN_ERR_TIMEOUT) return GDN_ERR_TIMEOUT;
     return GDN_ERR_DEVICE_CHECK;
@@ -436,5 +458,7 @@ const char *gdn_status_string(gdn_status s) {
 }
 
 const char *gdn_version(void) { return "gdn-gb300 0.1 (sm_103a)"; }
+
+const char *gdn_last_error_detail(void) { return g_error_detail; }
 
 }  // extern "C"

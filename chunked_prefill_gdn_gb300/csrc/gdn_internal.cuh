@@ -57,6 +57,9 @@ struct Layout {
     int max_chunks, max_items, max_items1, max_cp_slots;
 };
 
+// Records the CUDA error behind a GDN_ERR_CUDA for gdn_last_error_detail().
+void set_error_detail(const char *where, cudaError_t e, int driver_result = 0);
+
 // Launchers (each returns cudaGetLastError() of its launch).
 cudaError_t launch_seqprep(const Problem &p, const Workspace &w, cudaStream_t s);
 cudaError_t launch_gate(const Problem &p, const Workspace &w, cudaStream_t s);

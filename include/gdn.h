@@ -219,6 +219,11 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v,
                               void *device_buffer, size_t device_buffer_bytes,
                               const gdn_options *opts, gdn_stream_t stream);
 
+/* The CUDA error (and, for tensor-map encoding, the driver result) behind the
+ * most recent GDN_ERR_CUDA returned on the calling host thread, as text such
+ * as "launch fused_tc: cudaErrorInvalidValue"; "" when there was none. */
+const char *gdn_last_error_detail(void);
+
 /* Human-readable name of a status. */
 const char *gdn_status_string(gdn_status status);
 

@@ -234,3 +234,16 @@ def test_full_size_sampled(idx):
     o_s, sf_s = gpu_sampled(o, sf, inp, seqs, spec["heads"], spec["rows"], tidx)
     assert_close("o", o_s, o_ref)
     assert_close("final_state", sf_s, sf_ref)
+
+
+def test_tcgen05_kernel_matches_cuda_core_kernel():
+    """The tcgen05 kernel and the CUDA-core kernel follow the same chunked
+    algebra; on a layer-shaped case they agree far inside the oracle bar."""
+    cfg = CONFIGS[1].scaled(B=2, T=777, H=3, s0_std=0.02)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    info = gdn.gdn_plan_query(2, 777, 3, 128, 128, 2, 0, gdn.BF16, opts_for("auto"))
+    assert info.kernel == gdn.KERNEL_TC
+    o_tc, s_tc = gpu_run(inp, opts_for("auto", cp_mode=gdn.CP_FORCE, chunks_per_segment=3))
+    o_si, s_si = gpu_run(inp, opts_for("simt", cp_mode=gdn.CP_FORCE, chunks_per_segment=3))
+    assert_close("o", oracle.to_f64(o_tc), oracle.to_f64(o_si), 4e-3, 2e-2)
+    assert_close("final_state", oracle.to_f64(s_tc), oracle.to_f64(s_si), 4e-3, 2e-2)
