@@ -152,26 +152,34 @@ def reference_arm(args, cfg):
 
 
 def cpu_baseline(cfg, budget_s):
-    """Oracle throughput on the host cores for a bounded sample (tokens/s of the
-    full-width layer)."""
+    """Oracle throughput on the host cores (tokens/s of the full-width layer) on a
+    bounded sample: whole (sequence, head) units of the workload, added until the
+    estimated run time reaches budget_s; the whole workload is the upper bound."""
     import oracle
     from chunked_prefill_gdn_gb300.inputs import make_inputs
     inp = make_inputs(cfg.scaled(B=1), "cpu")
-    heads = [0]
     t0 = time.perf_counter()
     oracle.gdn_reference(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, None, scale=inp["scale"],
-                         heads=heads)
-    t1 = time.perf_counter() - t0
-    nh = max(1, min(cfg.H, int(budget_s / max(t1, 1e-3))))
-    heads = list(range(nh))
-    t0 = time.perf_counter()
-    oracle.gdn_reference(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, None, scale=inp["scale"],
-                         heads=heads)
-    dt = time.perf_counter() - t0
-    value = cfg.T * nh / dt / cfg.H
+                         heads=[0])
+    per_unit = max(time.perf_counter() - t0, 1e-4)       # one head of one sequence
+    units = int(min(cfg.B * cfg.H, max(1, budget_s / per_unit)))
+    nseq = min(cfg.B, -(-units // cfg.H))
+    done = 0
+    elapsed = 0.0
+    for b in range(nseq):
+        heads = list(range(min(cfg.H, units - done)))
+        if not heads:
+            break
+        seq_inp = inp if b == 0 else make_inputs(cfg.scaled(B=1, seed=cfg.seed + 1000 + b), "cpu")
+        t0 = time.perf_counter()
+        oracle.gdn_reference(seq_inp["q"], seq_inp["k"], seq_inp["v"], seq_inp["g"], seq_inp["beta"], None, None,
+                             scale=seq_inp["scale"], heads=heads)
+        elapsed += time.perf_counter() - t0
+        done += len(heads)
+    value = cfg.T * done / elapsed / cfg.H
     return {"value": value, "unit": "tokens/s", "cores": oracle.oracle_threads(), "kind": "oracle",
-            "sample": "1 of %d sequences x %d of %d heads, all %d tokens and %d value rows, %.1f s" % (
-                cfg.B, nh, cfg.H, cfg.T, cfg.dv, dt)}
+            "sample": "%d (sequence, head) units of %d (T=%d each, all %d value rows), %.1f s" % (
+                done, cfg.B * cfg.H, cfg.T, cfg.dv, elapsed)}
 
 
 def main():
@@ -187,10 +195,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-heads", type=int, default=2, help="heads per reference-arm step")
+    ap.add_argument("--override", action="append", default=[],
+                    help="workload field override, e.g. B=1 (profiling runs on smaller cases)")
     args = ap.parse_args()
 
     from chunked_prefill_gdn_gb300.inputs import CONFIGS
     cfg = CONFIGS[args.config]
+    if args.override:
+        kw = {}
+        for item in args.override:
+            key, val = item.split("=", 1)
+            kw[key] = type(getattr(cfg, key))(val) if getattr(cfg, key) is not None else int(val)
+        cfg = cfg.scaled(**kw)
     if args.impl == "reference":
         reference_arm(args, cfg)
         return

@@ -5,23 +5,34 @@
 // Everything is written transposed so that the state's value index i (dv =
 // 128) runs along the 128 TMEM lanes and every MMA has M = 128.  Per chunk,
 // with S the state at chunk start (dv x dk, fp32 in TMEM), G the chunk-local
-// gate cumsum, gamma = exp(G), Gamma_ri = exp(G_r - G_m):
+// gate cumsum, gamma = exp(G), G* the middle of the chunk's gate range and
 //
-//   MMA1  P^T   = S [K;Q]^T                      (A = bf16(S) from TMEM, N = 128)
-//   E2    V'^T  = diag-beta (V^T - P_K^T D_gamma)   forward merge ("V - S first")
-//   MMA2  U^T   = V'^T T^T,   T = Gamma ⊙ T'     (T' from the inverse kernel)
-//   E3    Ut^T  = U^T diag(gamma_C / gamma)
-//   MMA3  S    += Ut^T K      (S pre-scaled by gamma_C in E1)
-//   P0    Q K^T                                   (for the output, off the chain)
-//   MMA4  D4^T  = U^T (Gamma ⊙ tril(Q K^T))^T
-//   O     o     = scale (D_gamma P_Q + D4)
+//   Gamma_rm = exp(G_r - G_m) = a_r b_m,  a_r = exp(G_r - G*), b_m = exp(G* - G_m),
+//
+// the gated inverse T = Gamma ⊙ T' = D_a T' D_b (Gamma-extraction paragraph),
+// so the inverse kernel's T' feeds the MMAs without an element-wise pass:
+//
+//   MMA1   P    = S [K;Q]^T                    A = bf16(S) (TMEM), N = 128
+//   MMA2a  U'   = V^T (T' D_c1)^T              A = the V tile (smem, MN-major)
+//   E2     W2   = -c2 P_K                       (forward merge: "V - S first")
+//   MMA2b  U'  += W2 T'^T                       and U = D_a U'
+//   E3     Ut   = e U',  W4 = f U'              e = exp(G_C - G*), f = exp(-G*)
+//   MMA3   S   += Ut K           (S pre-scaled by gamma_C in E1)
+//   P0     Q K^T                                (off the chain)
+//   MMA4   P_Q += W4 tril(Q K^T)^T              since a_r / gamma_r = exp(-G*)
+//   O      o    = scale gamma_r P_Q
+//
+// with c1 = b beta and c2 = b beta gamma.  f U' = U_m / gamma_m, so a chunk
+// whose gate cumsum falls below -80 (where that could overflow) takes the exact
+// form instead: a = b = 1, T = Gamma ⊙ T' element by element, and the output
+// term goes to its own TMEM columns (o = scale (gamma P_Q + D4)).
 //
 // W, U and the per-chunk states never reach HBM.  Warp roles: warps 0-7 are
 // the epilogue (warps w and w+4 share TMEM lane quadrant w % 4 and split the
-// columns), warp 8 feeds q/k/v/T' tiles by TMA into a two-stage ring, warp 9
-// allocates TMEM and issues the MMAs.  Every wait is bounded: on timeout the
-// kernel records GDN_ERR_TIMEOUT, waits for its own copies in flight, frees
-// TMEM and returns.
+// columns), warp 8 feeds q/k/v/T' tiles by TMA into a three-stage ring and
+// computes the per-row gate coefficients, warp 9 allocates TMEM and issues the
+// MMAs.  Every wait is bounded: on timeout the kernel records GDN_ERR_TIMEOUT,
+// waits for its own copies in flight, frees TMEM and returns.
 #include <string.h>
 
 #include <mutex>
@@ -45,27 +56,44 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr uint32_t kKQBytes = 32768;  // [dk half][K rows 0-63 | Q rows 64-127][128 B]
 constexpr uint32_t kVBytes = 16384;   // [dv half][64 rows][128 B]
-constexpr uint32_t kTPBytes = 8192;   // [64 rows][128 B]: T', then T = Gamma ⊙ T'
-constexpr uint32_t kStageBytes = kKQBytes + kVBytes + kTPBytes;
-constexpr uint32_t kOffQM = 2 * kStageBytes;        // Gamma ⊙ tril(Q K^T), [64][128 B]
+constexpr uint32_t kTPBytes = 8192;   // [64 rows][128 B]: T' (exact form: Gamma ⊙ T')
+constexpr uint32_t kT1Bytes = 8192;   // [64 rows][128 B]: T' D_c1
+constexpr uint32_t kOffV = kKQBytes;
+constexpr uint32_t kOffTP = kKQBytes + kVBytes;
+constexpr uint32_t kOffT1 = kOffTP + kTPBytes;
+constexpr uint32_t kStageBytes = kOffT1 + kT1Bytes;
+constexpr uint32_t kTxBytes = kKQBytes + kVBytes + kTPBytes;  // bytes TMA brings per stage
+constexpr int kStages = 3;
+constexpr uint32_t kOffQM = kStages * kStageBytes;  // tril(Q K^T), [64][128 B]
 constexpr uint32_t kOffO = kOffQM + 8192;           // output tile [dv half][64][128 B]
 constexpr uint32_t kOffSmall = kOffO + 16384;
-constexpr uint32_t kTxBytes = kStageBytes;
 
 // TMEM columns (512 allocated)
-constexpr uint32_t kColS32 = 0;    // fp32 state, 128 cols
-constexpr uint32_t kColS16 = 128;  // bf16 state (MMA1 A operand), 64 cols
-constexpr uint32_t kColP = 192;    // MMA1 out: P_K^T cols 0-63 (V'^T bf16 at +16..+47), P_Q^T cols 64-127
-constexpr uint32_t kColU = 320;    // MMA2 out: U^T fp32 64 cols (Ut^T bf16 at +16..+47)
-constexpr uint32_t kColU16 = 384;  // U^T bf16 (MMA4 A operand), 32 cols
-constexpr uint32_t kColD0 = 416;   // Q K^T (P0 out, lanes 64-127), then D4 (MMA4 out), 64 cols
+constexpr uint32_t kColS32 = 0;    // fp32 state
+constexpr uint32_t kColS16 = 128;  // bf16 state (MMA1 A operand)
+constexpr uint32_t kColP = 192;    // two P buffers of 128 columns (chunk parity):
+                                   //   +0..63 P_K (W2, then W4, bf16 at +16..+47), +64..127 P_Q (+ output)
+                                   //   the other buffer's +0..63 takes Q K^T (and the exact-form D4)
+constexpr uint32_t kColU = 448;    // U' fp32 (Ut bf16 at +16..+47)
+
+// Per-chunk gate coefficients (written by the producer warp with the tiles).
+struct Coef {
+    float G[64];     // chunk-local cumsum (rows past the end repeat the last)
+    float gam[64];   // gamma_r
+    float so[64];    // scale * gamma_r (output)
+    float c1[64];    // b_r beta_r           (multiplies V)
+    float c2[64];    // b_r beta_r gamma_r   (multiplies P_K)
+    float e[64];     // a_r gamma_C / gamma_r   (Ut = e U')
+    float f[64];     // exp(-G*) (1 in the exact form)   (W4 = f U')
+    float gC;        // gamma_C
+    int exact;       // 1: Gamma is applied element by element
+    int pad[2];
+};
 
 struct Small {
-    float G[2][64];
-    float B[2][64];
-    float coef[2][5][64];  // gamma, beta*gamma, gamma_C/gamma, Gamma row factor, Gamma column factor
-    uint64_t full[2], empty[2];
-    uint64_t e1, e2, e3, oepi, coefb, ofree, otile;
+    Coef coef[kStages];
+    uint64_t full[kStages], empty[kStages];
+    uint64_t e1, e2, e3, oepi, pre, ofree, otile;
     uint64_t m1, m2, m3, m4, p0, fin;
     uint32_t tmem_base;
     int abort;
@@ -101,97 +129,181 @@ __device__ __forceinline__ bool ewait(const Ctx &cx, uint64_t *bar, uint32_t par
     return __all_sync(0xffffffffu, r);
 }
 
+// Stage ring: chunk n uses stage n % kStages; its use index is n / kStages.
+__device__ __forceinline__ int stage_of(uint32_t n) { return static_cast<int>(n % kStages); }
+__device__ __forceinline__ uint32_t use_parity(uint32_t n) { return (n / kStages) & 1u; }
+
 // ---------------------------------------------------------------- producer
 __device__ void producer_role(const Ctx &cx, const TcMaps &maps, int lane) {
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
     Small &sm = *cx.sm;
-    uint32_t n = 0;
-    uint32_t arms0 = 0, arms1 = 0;
-    bool ok = true;
-    for (int k = blockIdx.x; k < cx.n_items && ok; k += gridDim.x) {
-        const gdn_work_item it = cx.items[k];
-        const int4 si = w.seqinfo[it.seq];
-        const int h = it.head;
-        for (int c = it.c_start; c < it.c_end; ++c, ++n) {
-            const int s = n & 1;
-            if (n >= 2 && !wait_or_abort(cx, &sm.empty[s], ((n >> 1) - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            const int4 ci = w.chunks[si.z + c];
-            const int t0 = ci.y, len = ci.z;
-            for (int rr = lane; rr < 64; rr += 32) {
-                const int rc = rr < len ? rr : len - 1;
-                sm.G[s][rr] = w.G[(size_t)h * p.total_T + t0 + rc];
-                sm.B[s][rr] = rr < len ? p.beta[(size_t)(t0 + rr) * p.H + h] : 0.f;
-            }
-            uint8_t *st = cx.smem + s * kStageBytes;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&sm.full[s], kTxBytes);
-                tma_load_3d(st + 0, &maps.k, &sm.full[s], 0, h, t0);
-                tma_load_3d(st + 8192, &maps.q, &sm.full[s], 0, h, t0);
-                tma_load_3d(st + 16384, &maps.k, &sm.full[s], 64, h, t0);
-                tma_load_3d(st + 24576, &maps.q, &sm.full[s], 64, h, t0);
-                tma_load_3d(st + kKQBytes, &maps.v, &sm.full[s], 0, h, t0);
-                tma_load_3d(st + kKQBytes + 8192, &maps.v, &sm.full[s], 64, h, t0);
-                tma_load_2d(st + kKQBytes + kVBytes, &maps.tp, &sm.full[s], 0, h * p.total_T + t0);
-            } else {
-                mbar_arrive(&sm.full[s]);
-            }
-            if (s) ++arms1; else ++arms0;
+    // cursor over this CTA's chunks, items in order, empty items skipped
+    int k = blockIdx.x, c = 0, cend = 0, chunk0 = 0, head = 0;
+    bool started = false;
+    auto advance = [&]() -> bool {
+        if (started && c + 1 < cend) {
+            ++c;
+            return true;
         }
+        if (started) k += gridDim.x;
+        started = true;
+        for (; k < cx.n_items; k += gridDim.x) {
+            const gdn_work_item it = cx.items[k];
+            if (it.c_start < it.c_end) {
+                c = it.c_start;
+                cend = it.c_end;
+                chunk0 = w.seqinfo[it.seq].z;
+                head = it.head;
+                return true;
+            }
+        }
+        return false;
+    };
+    // the gate values of the next chunk are fetched one step ahead, so their
+    // latency overlaps the wait for a free stage
+    float pg0 = 0.f, pg1 = 0.f, pb0 = 0.f, pb1 = 0.f;
+    int ph = 0, pt0 = 0, plen = 1;
+    auto fetch = [&]() {
+        const int4 ci = w.chunks[chunk0 + c];
+        pt0 = ci.y;
+        plen = ci.z;
+        ph = head;
+        const size_t gb = (size_t)ph * p.total_T + pt0;
+        pg0 = w.G[gb + min(lane, plen - 1)];
+        pg1 = w.G[gb + min(lane + 32, plen - 1)];
+        pb0 = lane < plen ? p.beta[(size_t)(pt0 + lane) * p.H + ph] : 0.f;
+        pb1 = lane + 32 < plen ? p.beta[(size_t)(pt0 + lane + 32) * p.H + ph] : 0.f;
+    };
+    bool more = advance();
+    if (more) fetch();
+    uint32_t n = 0;
+    while (more) {
+        const float g0 = pg0, g1 = pg1, b0 = pb0, b1 = pb1;
+        const int h = ph, t0 = pt0;
+        more = advance();
+        if (more) fetch();
+        const int s = stage_of(n);
+        if (n >= kStages && !wait_or_abort(cx, &sm.empty[s], ((n / kStages) - 1) & 1)) break;
+        {
+            const float Gfirst = __shfl_sync(0xffffffffu, g0, 0);
+            const float Glast = __shfl_sync(0xffffffffu, g1, 31);  // row 63 repeats row len-1
+            // W4 = f U' equals U_m / gamma_m, so the factored form needs gamma_m > e^-80
+            // everywhere in the chunk; past that the exact form is used
+            const bool exact = Glast < -80.f;
+            const float Gs = 0.5f * (Gfirst + Glast);
+            Coef &cf = sm.coef[s];
+            const float gg[2] = {g0, g1}, bb[2] = {b0, b1};
+            const float fN = __expf(-Gs), eN = __expf(Glast - Gs);
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int r = lane + 32 * q2;
+                const float G = gg[q2];
+                const float gam = __expf(G);
+                const float b = exact ? 1.f : __expf(Gs - G);
+                cf.G[r] = G;
+                cf.gam[r] = gam;
+                cf.so[r] = p.scale * gam;
+                cf.c1[r] = b * bb[q2];
+                cf.c2[r] = b * bb[q2] * gam;
+                cf.e[r] = exact ? __expf(Glast - G) : eN;
+                cf.f[r] = exact ? 1.f : fN;
+            }
+            if (lane == 0) {
+                cf.gC = __expf(Glast);
+                cf.exact = exact;
+            }
+        }
+        uint8_t *st = cx.smem + s * kStageBytes;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.full[s], kTxBytes);
+            tma_load_3d(st + 0, &maps.k, &sm.full[s], 0, h, t0);
+            tma_load_3d(st + 8192, &maps.q, &sm.full[s], 0, h, t0);
+            tma_load_3d(st + 16384, &maps.k, &sm.full[s], 64, h, t0);
+            tma_load_3d(st + 24576, &maps.q, &sm.full[s], 64, h, t0);
+            tma_load_3d(st + kOffV, &maps.v, &sm.full[s], 0, h, t0);
+            tma_load_3d(st + kOffV + 8192, &maps.v, &sm.full[s], 64, h, t0);
+            tma_load_2d(st + kOffTP, &maps.tp, &sm.full[s], 0, h * p.total_T + t0);
+        } else {
+            mbar_arrive(&sm.full[s]);
+        }
+        ++n;
     }
     // never leave a copy in flight into shared memory that is about to be released
     if (lane == 0) {
         int dummy = 0;
-        if (arms0) mbar_wait(&sm.full[0], (arms0 - 1) & 1, &dummy, kTimeoutNs);
-        if (arms1) mbar_wait(&sm.full[1], (arms1 - 1) & 1, &dummy, kTimeoutNs);
+        for (int s = 0; s < kStages; ++s) {
+            const uint32_t arms = n > (uint32_t)s ? (n - 1 - s) / kStages + 1 : 0;
+            if (arms) mbar_wait(&sm.full[s], (arms - 1) & 1, &dummy, kTimeoutNs);
+        }
     }
 }
 
 // --------------------------------------------------------------------- MMA
 __device__ void mma_role(const Ctx &cx) {
-    const Workspace &w = *cx.w;
     Small &sm = *cx.sm;
     const uint32_t t = cx.tbase;
     const uint32_t smem0 = smem_u32(cx.smem);
-    constexpr uint32_t I1 = idesc_bf16_f32(128, 128, 0, 0);  // P^T = S16 x [K;Q]^T
-    constexpr uint32_t I0 = idesc_bf16_f32(128, 64, 0, 0);   // [K;Q] K^T
-    constexpr uint32_t I2 = idesc_bf16_f32(128, 64, 0, 0);   // U^T = V'^T T^T
-    constexpr uint32_t I3 = idesc_bf16_f32(128, 128, 0, 1);  // S += Ut^T K   (K as MN-major B)
-    constexpr uint32_t I4 = idesc_bf16_f32(128, 64, 0, 0);   // D4^T = U^T Qm^T
+    constexpr uint32_t I1 = idesc_bf16_f32(128, 128, 0, 0);   // P = S16 [K;Q]^T
+    constexpr uint32_t I0 = idesc_bf16_f32(128, 64, 0, 0);    // [K;Q] K^T
+    constexpr uint32_t I2a = idesc_bf16_f32(128, 64, 1, 0);   // U' = V^T (T' D_c1)^T, V^T MN-major
+    constexpr uint32_t I2b = idesc_bf16_f32(128, 64, 0, 0);   // U' += W2 T'^T
+    constexpr uint32_t I3 = idesc_bf16_f32(128, 128, 0, 1);   // S += Ut K   (K as MN-major B)
+    constexpr uint32_t I4 = idesc_bf16_f32(128, 64, 0, 0);    // P_Q (or D4) += W4 Qm^T
     uint32_t n = 0;
-    bool ok = true;
+    bool ok = true, prev_exact = false;
     for (int k = blockIdx.x; k < cx.n_items && ok; k += gridDim.x) {
         const gdn_work_item it = cx.items[k];
         for (int c = it.c_start; c < it.c_end; ++c, ++n) {
-            const int s = n & 1;
+            const int s = stage_of(n);
             const uint32_t par = n & 1;
             const bool out = (it.flags & GDN_ITEM_OUTPUT) && c >= it.c_begin;
-            const uint32_t kq = smem0 + s * kStageBytes;
-            const uint32_t tp = kq + kKQBytes + kVBytes;
-            if (!wait_or_abort(cx, &sm.full[s], (n >> 1) & 1) || !wait_or_abort(cx, &sm.e1, par)) {
+            const uint32_t st = smem0 + s * kStageBytes;
+            const uint32_t pc = t + kColP + (n & 1) * 128;        // this chunk's P buffer
+            const uint32_t po = t + kColP + ((n + 1) & 1) * 128;  // the other one
+            if (!wait_or_abort(cx, &sm.full[s], use_parity(n)) || !wait_or_abort(cx, &sm.e1, par)) {
+                ok = false;
+                break;
+            }
+            // the exact form keeps the previous output in the buffer MMA1 is about to write
+            if (prev_exact && !wait_or_abort(cx, &sm.oepi, (n - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            const bool exact = cx.sm->coef[s].exact;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t b = smem_desc_sw128(st + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                mma_ts(pc, t + kColS16 + 8 * kk, b, I1, kk > 0);
+            }
+            tc_commit(&sm.m1);
+            // V term of U' as soon as T' D_c1 is ready (U' is free once MMA3 of the last chunk is done)
+            if (!wait_or_abort(cx, &sm.pre, par)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            // (correction-matrix items run with zero values: no V term)
+            const bool zero_v = it.flags & GDN_ITEM_FROM_IDENTITY;
+            if (!zero_v) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t b = smem_desc_sw128(kq + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                mma_ts(t + kColP, t + kColS16 + 8 * kk, b, I1, kk > 0);
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t a = smem_desc_sw128(st + kOffV + kk * 2048, 8192, 1024);
+                    const uint64_t b = smem_desc_sw128(st + kOffT1 + kk * 32, 16, 1024);
+                    mma_ss(t + kColU, a, b, I2a, kk > 0);
+                }
             }
-            tc_commit(&sm.m1);
-            if (n > 0 && !wait_or_abort(cx, &sm.oepi, (n - 1) & 1)) {
+            // Q K^T into the other buffer's first half, once MMA4 of the last chunk stopped reading it
+            if (n > 0 && !wait_or_abort(cx, &sm.m4, (n - 1) & 1)) {
                 ok = false;
                 break;
             }
             if (out) {
-                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t a = smem_desc_sw128(kq + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                    mma_ss(t + kColD0, a, a, I0, kk > 0);
+                    const uint64_t a = smem_desc_sw128(st + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                    mma_ss(po, a, a, I0, kk > 0);
                 }
             }
             tc_commit(&sm.p0);
@@ -202,8 +314,8 @@ __device__ void mma_role(const Ctx &cx) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t b = smem_desc_sw128(tp + kk * 32, 16, 1024);
-                mma_ts(t + kColU, t + kColP + 16 + 8 * kk, b, I2, kk > 0);
+                const uint64_t b = smem_desc_sw128(st + kOffTP + kk * 32, 16, 1024);
+                mma_ts(t + kColU, pc + 16 + 8 * kk, b, I2b, (kk > 0 || !zero_v) ? 1u : 0u);
             }
             tc_commit(&sm.m2);
             if (!wait_or_abort(cx, &sm.e3, par)) {
@@ -213,7 +325,7 @@ __device__ void mma_role(const Ctx &cx) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t b = smem_desc_sw128(kq + kk * 2048, 16384, 1024);
+                const uint64_t b = smem_desc_sw128(st + kk * 2048, 16384, 1024);
                 mma_ts(t + kColS32, t + kColU + 16 + 8 * kk, b, I3, 1);
             }
             tc_commit(&sm.m3);
@@ -222,14 +334,17 @@ __device__ void mma_role(const Ctx &cx) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t b = smem_desc_sw128(qm + kk * 32, 16, 1024);
-                    mma_ts(t + kColD0, t + kColU16 + 8 * kk, b, I4, kk > 0);
+                    if (exact)
+                        mma_ts(po, pc + 16 + 8 * kk, b, I4, kk > 0);
+                    else
+                        mma_ts(pc + 64, pc + 16 + 8 * kk, b, I4, 1);
                 }
             }
             tc_commit(&sm.m4);
             tc_commit(&sm.empty[s]);
+            prev_exact = out && exact;
         }
     }
-    (void)w;
     // all issued MMAs must finish before TMEM is released
     tc_commit(&sm.fin);
     int dummy = 0;
@@ -241,11 +356,6 @@ struct EpiThread {
     int q, ch, i, et, lane;
     uint32_t lane_base;  // TMEM lane field of this warp's quadrant
 };
-
-__device__ __forceinline__ float gamma_rm(const float *G, const float *ga, const float *gb, bool exact, int r,
-                                          int m) {
-    return exact ? __expf(G[r] - G[m]) : ga[r] * gb[m];
-}
 
 __device__ __forceinline__ void load_tile32(const Ctx &cx, const EpiThread &e, uint32_t col, float *x) {
     uint32_t r[32];
@@ -312,8 +422,58 @@ __device__ __forceinline__ void store_state32(const Ctx &cx, const EpiThread &e,
     tmem_st32(cx.tbase + e.lane_base + kColS32 + 64 * e.ch + 32 * hh, sc);
 }
 
-__device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
+// Output of one finished chunk.  Usual form: o = scale gamma_r P_Q (P_Q already
+// holds the intra-chunk term); exact form: o = scale (gamma_r P_Q + D4).  Full
+// chunks go through the swizzled smem tile and a TMA store; a ragged last
+// chunk is stored row by row.
+__device__ bool output_chunk(const Ctx &cx, const EpiThread &e, const Coef &cf, bool exact, uint32_t pq_col,
+                             uint32_t d4_col, int t0, int len, int h, uint32_t &ocount) {
     const Problem &p = *cx.p;
+    Small &sm = *cx.sm;
+    uint8_t *o_tile = cx.smem + kOffO;
+    float x[32];
+    load_tile32(cx, e, pq_col, x);
+    const int r0 = 32 * e.ch;
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr) x[rr] *= cf.so[r0 + rr];
+    if (exact) {
+        float d4[32];
+        load_tile32(cx, e, d4_col, d4);
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) x[rr] = fmaf(p.scale, d4[rr], x[rr]);
+    }
+    const int i = e.i;
+    if (len == 64) {
+        if (e.et == 0) {
+            bulk_wait_group_read_all();
+            mbar_arrive(&sm.ofree);
+        }
+        if (!ewait(cx, &sm.ofree, ocount & 1)) return false;
+        const int half = i >> 6, col = i & 63;
+        uint8_t *base = o_tile + half * 8192 + (col & 7) * 2;
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr)
+            *reinterpret_cast<__nv_bfloat16 *>(base + sw128_offset(r0 + rr, col >> 3)) = __float2bfloat16_rn(x[rr]);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.otile);
+        if (e.et == 0) {
+            if (!wait_or_abort(cx, &sm.otile, ocount & 1)) return false;
+            tma_store_3d(&cx.maps->o, o_tile, 0, h, t0);
+            tma_store_3d(&cx.maps->o, o_tile + 8192, 64, h, t0);
+            bulk_commit_group();
+        }
+        ++ocount;
+    } else {
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.o);
+        for (int rr = 0; rr < 32; ++rr) {
+            const int r = r0 + rr;
+            if (r < len) o[((size_t)(t0 + r) * p.H + h) * kD + i] = __float2bfloat16_rn(x[rr]);
+        }
+    }
+    return true;
+}
+
+__device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
     const Workspace &w = *cx.w;
     Small &sm = *cx.sm;
     EpiThread e;
@@ -325,21 +485,20 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
     e.lane_base = static_cast<uint32_t>(32 * e.q) << 16;
     const int ch = e.ch, i = e.i;
     uint8_t *qm_tile = cx.smem + kOffQM;
-    uint8_t *o_tile = cx.smem + kOffO;
 
     uint32_t n = 0, ocount = 0;
-    int pv_out = 0, pv_t0 = 0, pv_len = 0, pv_h = 0;
+    // the previous chunk, whose output is written one step later
+    int pv_out = 0, pv_t0 = 0, pv_len = 0, pv_h = 0, pv_s = 0, pv_exact = 0;
+    uint32_t pv_pcol = 0, pv_ocol = 0;
     // the item whose end state sits in TMEM and has not been written yet
     bool pending = false;
     gdn_work_item prev_item;
     prev_item.flags = 0;
-    float pq[32];
     bool ok = true;
 
     for (int k = blockIdx.x; k < cx.n_items && ok; k += gridDim.x) {
         const gdn_work_item it = cx.items[k];
         const int4 si = w.seqinfo[it.seq];
-        const bool ident = it.flags & GDN_ITEM_FROM_IDENTITY;
         if (it.c_start >= it.c_end) {
             // an empty sequence: its end state is its start state
             if (pending) {
@@ -357,70 +516,49 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
             continue;
         }
         for (int c = it.c_start; c < it.c_end; ++c, ++n) {
-            const int s = n & 1;
+            const int s = stage_of(n);
             const uint32_t par = n & 1;
             const int4 ci = w.chunks[si.z + c];
             const int t0 = ci.y, len = ci.z;
             const bool out = (it.flags & GDN_ITEM_OUTPUT) && c >= it.c_begin;
             uint8_t *st = cx.smem + s * kStageBytes;
-            const uint8_t *vt = st + kKQBytes;
-            uint8_t *tpt = st + kKQBytes + kVBytes;
-            if (!ewait(cx, &sm.full[s], (n >> 1) & 1)) { ok = false; break; }
+            const uint32_t pcol = kColP + (n & 1) * 128, ocol = kColP + ((n + 1) & 1) * 128;
+            const Coef &cf = sm.coef[s];
+            if (!ewait(cx, &sm.full[s], use_parity(n))) { ok = false; break; }
+            const bool exact = cf.exact;
 
-            // ---- per-chunk coefficients
-            const float *G = sm.G[s];
-            if (e.et < 64) {
-                const int r = e.et;
-                const float Gr = G[r], Gc = G[63];
-                const float Gref = 0.5f * (G[0] + Gc);
-                const float gam = __expf(Gr);
-                sm.coef[s][0][r] = gam;
-                sm.coef[s][1][r] = sm.B[s][r] * gam;
-                sm.coef[s][2][r] = __expf(Gc - Gr);
-                sm.coef[s][3][r] = __expf(Gr - Gref);
-                sm.coef[s][4][r] = __expf(Gref - Gr);
-                mbar_arrive(&sm.coefb);
-            }
-            if (!ewait(cx, &sm.coefb, par)) { ok = false; break; }
-            const float *gam = sm.coef[s][0], *bg = sm.coef[s][1], *dec = sm.coef[s][2];
-            const float *ga = sm.coef[s][3], *gb = sm.coef[s][4];
-            const bool exact = (G[0] - G[63]) > 160.f;
-
-            // ---- T = Gamma ⊙ T' in place (rows 0-63 by quadrants 0 and 1)
-            if (e.q < 2) {
-                const int r = i;
+            // ---- T' D_c1 for the V term (exact form: T' <- Gamma ⊙ T' first, in place)
+            {
+                const int r = e.et >> 2, q4 = e.et & 3;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c16 = 4 * ch + cc;
-                    uint4 *ptr = reinterpret_cast<uint4 *>(tpt + sw128_offset(r, c16));
-                    uint4 v = *ptr;
-                    uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                for (int hc = 0; hc < 2; ++hc) {
+                    const int c16 = 2 * q4 + hc;
+                    uint4 *src = reinterpret_cast<uint4 *>(st + kOffTP + sw128_offset(r, c16));
+                    uint4 v = *src;
+                    uint32_t wv[4] = {v.x, v.y, v.z, v.w}, w1[4];
 #pragma unroll
                     for (int e2 = 0; e2 < 4; ++e2) {
                         const int m0 = 8 * c16 + 2 * e2;
                         float x0 = bf16_lo(wv[e2]), x1 = bf16_hi(wv[e2]);
-                        x0 = (r < len && m0 <= r) ? x0 * gamma_rm(G, ga, gb, exact, r, m0) : 0.f;
-                        x1 = (r < len && m0 + 1 <= r) ? x1 * gamma_rm(G, ga, gb, exact, r, m0 + 1) : 0.f;
-                        wv[e2] = pack_bf16x2(x0, x1);
+                        if (exact) {
+                            x0 = (r < len && m0 <= r) ? x0 * __expf(cf.G[r] - cf.G[m0]) : 0.f;
+                            x1 = (r < len && m0 + 1 <= r) ? x1 * __expf(cf.G[r] - cf.G[m0 + 1]) : 0.f;
+                            wv[e2] = pack_bf16x2(x0, x1);
+                            x0 = bf16_lo(wv[e2]);
+                            x1 = bf16_hi(wv[e2]);
+                        }
+                        w1[e2] = pack_bf16x2(x0 * cf.c1[m0], x1 * cf.c1[m0 + 1]);
                     }
-                    *ptr = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    if (exact) *src = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    *reinterpret_cast<uint4 *>(st + kOffT1 + sw128_offset(r, c16)) =
+                        make_uint4(w1[0], w1[1], w1[2], w1[3]);
                 }
                 fence_proxy_async_smem();
-            }
-            // ---- beta_r V[r][i] for this thread's 32 rows
-            float vb[32];
-            {
-                const int half = i >> 6, col = i & 63;
-#pragma unroll
-                for (int rr = 0; rr < 32; ++rr) {
-                    const int r = 32 * ch + rr;
-                    const uint16_t raw = *reinterpret_cast<const uint16_t *>(
-                        vt + half * 8192 + sw128_offset(r, col >> 3) + (col & 7) * 2);
-                    vb[rr] = ident ? 0.f : sm.B[s][r] * __uint_as_float(static_cast<uint32_t>(raw) << 16);
-                }
+                mbar_arrive(&sm.pre);
             }
 
-            // ---- E1: S16 = bf16(S), S32 = gamma_C S
+            // ---- E1: S16 = bf16(S), S32 = gamma_C S   (critical: after MMA3 of the last chunk)
+            const float gC = cf.gC;
             if (c == it.c_start) {
                 if (pending) {
                     if (!ewait(cx, &sm.m3, (n - 1) & 1)) { ok = false; break; }
@@ -432,7 +570,7 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
                 for (int hh = 0; hh < 2; ++hh) {
                     float sv[32];
                     load_start_state32(cx, e, it, 64 * ch + 32 * hh, sv);
-                    store_state32(cx, e, hh, sv, gam[63]);
+                    store_state32(cx, e, hh, sv, gC);
                 }
             } else {
                 if (!ewait(cx, &sm.m3, (n - 1) & 1)) { ok = false; break; }
@@ -441,131 +579,106 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
                 for (int hh = 0; hh < 2; ++hh) {
                     float sv[32];
                     load_tile32(cx, e, kColS32 + 64 * ch + 32 * hh, sv);
-                    store_state32(cx, e, hh, sv, gam[63]);
+                    store_state32(cx, e, hh, sv, gC);
                 }
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&sm.e1);
 
-            // ---- output of the previous chunk
+            // ---- output of the previous chunk (under MMA1); then its stage is free
             if (n > 0) {
                 if (!ewait(cx, &sm.m4, (n - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                if (pv_out) {
-                    float d4[32];
-                    load_tile32(cx, e, kColD0 + 32 * ch, d4);
-                    if (pv_len == 64) {
-                        if (e.et == 0) {
-                            bulk_wait_group_read_all();
-                            mbar_arrive(&sm.ofree);
-                        }
-                        if (!ewait(cx, &sm.ofree, ocount & 1)) { ok = false; break; }
-                        const int half = i >> 6, col = i & 63;
-#pragma unroll
-                        for (int rr = 0; rr < 32; ++rr) {
-                            const int r = 32 * ch + rr;
-                            const __nv_bfloat16 b = __float2bfloat16_rn(p.scale * (pq[rr] + d4[rr]));
-                            *reinterpret_cast<__nv_bfloat16 *>(o_tile + half * 8192 + sw128_offset(r, col >> 3) +
-                                                               (col & 7) * 2) = b;
-                        }
-                        fence_proxy_async_smem();
-                        mbar_arrive(&sm.otile);
-                        if (e.et == 0) {
-                            if (!wait_or_abort(cx, &sm.otile, ocount & 1)) { ok = false; break; }
-                            tma_store_3d(&cx.maps->o, o_tile, 0, pv_h, pv_t0);
-                            tma_store_3d(&cx.maps->o, o_tile + 8192, 64, pv_h, pv_t0);
-                            bulk_commit_group();
-                        }
-                        ++ocount;
-                    } else {
-                        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.o);
-                        for (int rr = 0; rr < 32; ++rr) {
-                            const int r = 32 * ch + rr;
-                            if (r < pv_len)
-                                o[((size_t)(pv_t0 + r) * p.H + pv_h) * kD + i] =
-                                    __float2bfloat16_rn(p.scale * (pq[rr] + d4[rr]));
-                        }
-                    }
+                if (pv_out && !output_chunk(cx, e, sm.coef[pv_s], pv_exact, pv_pcol + 64 + 32 * ch, pv_ocol + 32 * ch,
+                                            pv_t0, pv_len, pv_h, ocount)) {
+                    ok = false;
+                    break;
                 }
                 tc_fence_before();
                 mbar_arrive(&sm.oepi);
+                mbar_arrive(&sm.empty[pv_s]);
             }
 
-            // ---- E2: V'^T = beta (V^T - gamma P_K^T)
+            // ---- E2: W2 = -c2 P_K   (critical: after MMA1)
             if (!ewait(cx, &sm.m1, par)) { ok = false; break; }
             tc_fence_after();
             {
                 float pk[32];
-                load_tile32(cx, e, kColP + 32 * ch, pk);
-                uint32_t vp[16];
+                load_tile32(cx, e, pcol + 32 * ch, pk);
+                uint32_t w2[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int r0 = 32 * ch + 2 * j;
-                    vp[j] = pack_bf16x2(vb[2 * j] - bg[r0] * pk[2 * j], vb[2 * j + 1] - bg[r0 + 1] * pk[2 * j + 1]);
+                    w2[j] = pack_bf16x2(-cf.c2[r0] * pk[2 * j], -cf.c2[r0 + 1] * pk[2 * j + 1]);
                 }
-                tmem_st16(cx.tbase + e.lane_base + kColP + 16 + 16 * ch, vp);
+                tmem_st16(cx.tbase + e.lane_base + pcol + 16 + 16 * ch, w2);
                 tmem_wait_st();
             }
             tc_fence_before();
             mbar_arrive(&sm.e2);
 
-            // ---- P_Q and the masked Q K^T
+            // ---- masked Q K^T (under MMA2); the exact form also applies Gamma
             if (!ewait(cx, &sm.p0, par)) { ok = false; break; }
             tc_fence_after();
-            if (out) {
-                load_tile32(cx, e, kColP + 64 + 32 * ch, pq);
+            if (out && e.q >= 2) {
+                const int r = i - 64;
+                float qk[32];
+                load_tile32(cx, e, ocol + 32 * ch, qk);
 #pragma unroll
-                for (int rr = 0; rr < 32; ++rr) pq[rr] *= gam[32 * ch + rr];
-                if (e.q >= 2) {
-                    const int r = i - 64;
-                    float qk[32];
-                    load_tile32(cx, e, kColD0 + 32 * ch, qk);
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t wv[4];
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t wv[4];
-#pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            const int mm = 8 * cc + 2 * e2;
-                            const int m0 = 32 * ch + mm;
-                            const float x0 =
-                                (r < len && m0 <= r) ? qk[mm] * gamma_rm(G, ga, gb, exact, r, m0) : 0.f;
-                            const float x1 =
-                                (r < len && m0 + 1 <= r) ? qk[mm + 1] * gamma_rm(G, ga, gb, exact, r, m0 + 1) : 0.f;
-                            wv[e2] = pack_bf16x2(x0, x1);
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const int mm = 8 * cc + 2 * e2;
+                        const int m0 = 32 * ch + mm;
+                        float x0 = (r < len && m0 <= r) ? qk[mm] : 0.f;
+                        float x1 = (r < len && m0 + 1 <= r) ? qk[mm + 1] : 0.f;
+                        if (exact) {
+                            x0 *= (r < len && m0 <= r) ? __expf(cf.G[r] - cf.G[m0]) : 0.f;
+                            x1 *= (r < len && m0 + 1 <= r) ? __expf(cf.G[r] - cf.G[m0 + 1]) : 0.f;
                         }
-                        *reinterpret_cast<uint4 *>(qm_tile + sw128_offset(r, 4 * ch + cc)) =
-                            make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        wv[e2] = pack_bf16x2(x0, x1);
                     }
-                    fence_proxy_async_smem();
+                    *reinterpret_cast<uint4 *>(qm_tile + sw128_offset(r, 4 * ch + cc)) =
+                        make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
+                fence_proxy_async_smem();
             }
 
-            // ---- E3: Ut^T = U^T diag(gamma_C / gamma), U^T in bf16 for the output MMA
+            // ---- E3: Ut = e U' for the state, W4 = f U' for the output   (critical: after MMA2)
             if (!ewait(cx, &sm.m2, par)) { ok = false; break; }
             tc_fence_after();
             {
                 float u[32];
                 load_tile32(cx, e, kColU + 32 * ch, u);
-                uint32_t ut[16], ub[16];
+                if (len < 64) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (32 * ch + j >= len) u[j] = 0.f;
+                }
+                uint32_t ut[16], w4[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int r0 = 32 * ch + 2 * j;
-                    ut[j] = pack_bf16x2(u[2 * j] * dec[r0], u[2 * j + 1] * dec[r0 + 1]);
-                    ub[j] = pack_bf16x2(u[2 * j], u[2 * j + 1]);
+                    ut[j] = pack_bf16x2(u[2 * j] * cf.e[r0], u[2 * j + 1] * cf.e[r0 + 1]);
+                    w4[j] = pack_bf16x2(u[2 * j] * cf.f[r0], u[2 * j + 1] * cf.f[r0 + 1]);
                 }
                 tmem_st16(cx.tbase + e.lane_base + kColU + 16 + 16 * ch, ut);
-                tmem_st16(cx.tbase + e.lane_base + kColU16 + 16 * ch, ub);
+                tmem_st16(cx.tbase + e.lane_base + pcol + 16 + 16 * ch, w4);
                 tmem_wait_st();
             }
             tc_fence_before();
             mbar_arrive(&sm.e3);
-            mbar_arrive(&sm.empty[s]);
 
             pv_out = out;
             pv_t0 = t0;
             pv_len = len;
             pv_h = it.head;
+            pv_s = s;
+            pv_exact = exact;
+            pv_pcol = pcol;
+            pv_ocol = ocol;
         }
         if (!ok) break;
         prev_item = it;
@@ -575,16 +688,9 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
     if (ok && n > 0) {
         if (ewait(cx, &sm.m4, (n - 1) & 1)) {
             tc_fence_after();
-            if (pv_out) {
-                float d4[32];
-                load_tile32(cx, e, kColD0 + 32 * ch, d4);
-                __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.o);
-                for (int rr = 0; rr < 32; ++rr) {
-                    const int r = 32 * ch + rr;
-                    if (r < pv_len)
-                        o[((size_t)(pv_t0 + r) * p.H + pv_h) * kD + i] = __float2bfloat16_rn(p.scale * (pq[rr] + d4[rr]));
-                }
-            }
+            if (pv_out)
+                output_chunk(cx, e, sm.coef[pv_s], pv_exact, pv_pcol + 64 + 32 * ch, pv_ocol + 32 * ch, pv_t0, pv_len,
+                             pv_h, ocount);
         }
         if (pending && ewait(cx, &sm.m3, (n - 1) & 1)) {
             tc_fence_after();
@@ -604,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Small &sm = *reinterpret_cast<Small *>(smem + kOffSmall);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.full[s], 32);
             mbar_init(&sm.empty[s], 1 + kEpiThreads);
         }
@@ -612,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.e2, kEpiThreads);
         mbar_init(&sm.e3, kEpiThreads);
         mbar_init(&sm.oepi, kEpiThreads);
-        mbar_init(&sm.coefb, 64);
+        mbar_init(&sm.pre, kEpiThreads);
         mbar_init(&sm.ofree, 1);
         mbar_init(&sm.otile, kEpiThreads);
         mbar_init(&sm.m1, 1);

@@ -247,3 +247,15 @@ def test_tcgen05_kernel_matches_cuda_core_kernel():
     o_si, s_si = gpu_run(inp, opts_for("simt", cp_mode=gdn.CP_FORCE, chunks_per_segment=3))
     assert_close("o", oracle.to_f64(o_tc), oracle.to_f64(o_si), 4e-3, 2e-2)
     assert_close("final_state", oracle.to_f64(s_tc), oracle.to_f64(s_si), 4e-3, 2e-2)
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+def test_extreme_gates_take_the_exact_form(kernel):
+    """Heads whose gate cumsum falls far within a chunk (per-token |g| up to
+    ~4) exercise the element-wise Gamma path; other heads stay factored."""
+    cfg = CONFIGS[1].scaled(B=2, T=330, H=4, a_range=(-3.0, 1.5), s0_std=0.02)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    o_ref, sf_ref = full_reference(inp)
+    o, sf = gpu_run(inp, opts_for(kernel, cp_mode=gdn.CP_FORCE, chunks_per_segment=2))
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
