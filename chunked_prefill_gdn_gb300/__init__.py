@@ -27,6 +27,7 @@ __all__ = [
     "load_library", "library_path", "default_options",
     "gdn_default_options", "gdn_plan_query", "gdn_chunk_fwd_workspace_size", "gdn_workspace_query",
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
+    "gdn_chunk_fwd_static",
     "gdn_status_string", "gdn_version", "gdn_last_error_detail", "chunk_fwd", "chunk_fwd_host", "workspace_for", "GdnError",
     "CP_AUTO", "CP_OFF", "CP_FORCE", "KERNEL_AUTO", "KERNEL_TC", "KERNEL_SIMT", "BF16", "F32",
     "STAGE_PREP", "STAGE_INVERSE", "STAGE_CORRECTION", "STAGE_FUSED",
@@ -114,6 +115,8 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_chunk_fwd_host_buffer_size.restype = sz
     lib.gdn_chunk_fwd_host.argtypes = fwd_args
     lib.gdn_chunk_fwd_host.restype = i32
+    lib.gdn_chunk_fwd_static.argtypes = fwd_args[:17] + [vp, opt, vp]
+    lib.gdn_chunk_fwd_static.restype = i32
     lib.gdn_status_string.argtypes = [i32]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_version.argtypes = []
@@ -177,6 +180,12 @@ def gdn_chunk_fwd_host_buffer_size(B, T, H, dk, dv, n_seqs, varlen, has_initial_
 
 def gdn_chunk_fwd_host(*args) -> int:
     return int(load_library().gdn_chunk_fwd_host(*args))
+
+
+def gdn_chunk_fwd_static(*args) -> int:
+    """gdn_chunk_fwd without a workspace argument: the scratch is the library's
+    fixed 64 MiB device array (for callers that must not allocate)."""
+    return int(load_library().gdn_chunk_fwd_static(*args))
 
 
 def gdn_status_string(status: int) -> str:

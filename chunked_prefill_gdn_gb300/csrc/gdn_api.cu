@@ -203,6 +203,8 @@ void set_error_detail(const char *where, cudaError_t e, int driver_result) {
     else
         snprintf(g_error_detail, sizeof(g_error_detail), "%s: %s", where, cudaGetErrorName(e));
 }
+
+void set_error_text(const char *text) { snprintf(g_error_detail, sizeof(g_error_detail), "%s", text); }
 }  // namespace gdn
 
 extern "C" {

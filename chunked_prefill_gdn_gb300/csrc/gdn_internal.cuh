@@ -59,6 +59,8 @@ struct Layout {
 
 // Records the CUDA error behind a GDN_ERR_CUDA for gdn_last_error_detail().
 void set_error_detail(const char *where, cudaError_t e, int driver_result = 0);
+// Records a plain message for gdn_last_error_detail().
+void set_error_text(const char *text);
 
 // Launchers (each returns cudaGetLastError() of its launch).
 cudaError_t launch_seqprep(const Problem &p, const Workspace &w, cudaStream_t s);

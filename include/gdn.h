@@ -30,9 +30,10 @@
  *
  * Ownership: the caller allocates every buffer (inputs, outputs, workspace)
  * and keeps them alive until the work on `stream` completes.  The library
- * allocates no device or host memory, keeps no state between calls besides a
- * per-device cache of device attributes and driver entry points, and never
- * synchronises the stream inside gdn_chunk_fwd.
+ * allocates no device or host memory at run time, keeps no state between calls
+ * besides a per-device cache of device attributes and driver entry points (and
+ * the fixed scratch array of gdn_chunk_fwd_static), and never synchronises the
+ * stream inside gdn_chunk_fwd.
  *
  * Errors: every call returns a gdn_status and never aborts.  Argument errors
  * are found on the host before any launch.  Errors found on the device (a
@@ -219,9 +220,51 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v,
                               void *device_buffer, size_t device_buffer_bytes,
                               const gdn_options *opts, gdn_stream_t stream);
 
+/*
+ * The same forward pass for callers that cannot allocate device memory while
+ * they run: a server that hands all of HBM to its own pool at start-up and
+ * forbids allocation on the request path, or a plugin that receives tensors
+ * from a host framework and has no allocator.  The paper has no counterpart;
+ * this is an addition of this library.
+ *
+ * Arguments are those of gdn_chunk_fwd without the workspace: the scratch is a
+ * static device array of 64 MiB inside the library, which every GPU that loads
+ * the library holds until the process exits.  A problem whose
+ * gdn_chunk_fwd_workspace_size() exceeds 64 MiB is rejected with
+ * GDN_ERR_WORKSPACE before anything is enqueued (gdn_last_error_detail() then
+ * says how many bytes it needed).  opts->stages must be 0 (the whole pass).
+ *
+ * The first call on a device looks up the array's device address and caches
+ * it (cudaGetSymbolAddress, no allocation); make that first call before any
+ * stream capture.  The call allocates nothing, host or device.
+ *
+ * Every call on a device shares the one array, which keeps the previous call's
+ * contents; the call clears what must start at zero (the error word and the
+ * work counters) on `stream` itself.  Calls whose GPU work overlaps (other
+ * streams, other host threads) race on the array and give wrong results: order
+ * them, e.g. on one stream.
+ *
+ * device_status: NULL makes the call synchronise `stream` and return the
+ * device-side status as gdn_chunk_fwd_check() does.  Otherwise it is a 4-byte
+ * aligned device int32 into which the call enqueues a copy of the device
+ * status word (0, or a gdn_status) after the pass, and the call returns
+ * without synchronising.
+ */
+gdn_status gdn_chunk_fwd_static(const void *q, const void *k, const void *v,
+                                const float *g, const float *beta,
+                                const float *initial_state,
+                                const int32_t *cu_seqlens, int n_seqs,
+                                float scale,
+                                int B, int T, int H, int dk, int dv, gdn_dtype dtype,
+                                void *o, float *final_state,
+                                int32_t *device_status,
+                                const gdn_options *opts, gdn_stream_t stream);
+
 /* The CUDA error (and, for tensor-map encoding, the driver result) behind the
  * most recent GDN_ERR_CUDA returned on the calling host thread, as text such
- * as "launch fused_tc: cudaErrorInvalidValue"; "" when there was none. */
+ * as "launch fused_tc: cudaErrorInvalidValue"; after gdn_chunk_fwd_static
+ * returns GDN_ERR_WORKSPACE, the scratch it would have needed; "" when there
+ * was none. */
 const char *gdn_last_error_detail(void);
 
 /* Human-readable name of a status. */
