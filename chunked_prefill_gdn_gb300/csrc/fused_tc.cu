@@ -10,29 +10,35 @@
 //   Gamma_rm = exp(G_r - G_m) = a_r b_m,  a_r = exp(G_r - G*), b_m = exp(G* - G_m),
 //
 // the gated inverse T = Gamma ⊙ T' = D_a T' D_b (Gamma-extraction paragraph),
-// so the inverse kernel's T' feeds the MMAs without an element-wise pass:
+// so the MMAs take T1 = T' D_c1 with c1 = b beta, which the inverse kernel
+// writes directly (it scales each column of T' before storing it):
 //
-//   MMA1   P    = S [K;Q]^T                    A = bf16(S) (TMEM), N = 128
-//   MMA2a  U'   = V^T (T' D_c1)^T              A = the V tile (smem, MN-major)
-//   E2     W2   = -c2 P_K                       (forward merge: "V - S first")
-//   MMA2b  U'  += W2 T'^T                       and U = D_a U'
-//   E3     Ut   = e U',  W4 = f U'              e = exp(G_C - G*), f = exp(-G*)
+//   P0     Q K^T                                 into the U' columns, masked
+//                                                (times exp(-G*)) by the side warps
+//   MMA1   P    = S [K;Q]^T                      A = bf16(S) (TMEM), N = 128
+//   MMA2a  U'   = V^T T1^T                       A = the V tile (smem, MN-major)
+//   E2     W2   = -gamma P_K                     (forward merge: "V - S first";
+//   MMA2b  U'  += W2 T1^T                         c1 gamma = b beta gamma), U = D_a U'
+//   E3     Ut   = e U',  W4 = U'                 e = exp(G_C - G*)
 //   MMA3   S   += Ut K           (S pre-scaled by gamma_C in E1)
-//   P0     Q K^T                                (off the chain)
-//   MMA4   P_Q += W4 tril(Q K^T)^T              since a_r / gamma_r = exp(-G*)
+//   MMA4   P_Q += W4 (exp(-G*) tril(Q K^T))^T   since a_r / gamma_r = exp(-G*)
 //   O      o    = scale gamma_r P_Q
 //
-// with c1 = b beta and c2 = b beta gamma.  f U' = U_m / gamma_m, so a chunk
-// whose gate cumsum falls below -80 (where that could overflow) takes the exact
-// form instead: a = b = 1, T = Gamma ⊙ T' element by element, and the output
-// term goes to its own TMEM columns (o = scale (gamma P_Q + D4)).
+// exp(-G*) U'_m = U_m / gamma_m, so a chunk whose gate cumsum falls below -80
+// (where that could overflow) takes the exact form instead: a = b = 1,
+// T = Gamma ⊙ T' element by element, and the output term goes to its own TMEM
+// columns (o = scale (gamma P_Q + D4)).
 //
-// W, U and the per-chunk states never reach HBM.  Warp roles: warps 0-7 are
-// the epilogue (warps w and w+4 share TMEM lane quadrant w % 4 and split the
-// columns), warp 8 feeds q/k/v/T' tiles by TMA into a three-stage ring and
-// computes the per-row gate coefficients, warp 9 allocates TMEM and issues the
-// MMAs.  Every wait is bounded: on timeout the kernel records GDN_ERR_TIMEOUT,
-// waits for its own copies in flight, frees TMEM and returns.
+// W, U and the per-chunk states never reach HBM.  Warp roles: warps 0-7 run
+// only the epilogues on the state chain (E1, E2, E3; warps w and w+4 share TMEM
+// lane quadrant w % 4 and split the columns), warps 8-11 run everything off the
+// chain (the masked Q K^T and the output), warp 12 feeds q/k/v/T1 tiles by TMA
+// into a three-stage ring and computes the per-row gate coefficients, warp 13
+// allocates TMEM and issues the MMAs in an order that keeps the chain E1, MMA1,
+// E2, MMA2b, E3, MMA3 free of work off it.  Every wait is bounded: on timeout
+// the kernel records GDN_ERR_TIMEOUT, waits for its own copies in flight, frees
+// TMEM and returns.
+#include <stddef.h>
 #include <string.h>
 
 #include <mutex>
@@ -47,26 +53,26 @@ using namespace tc;
 namespace {
 
 constexpr int kD = 128;
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 448;
+constexpr int kChainThreads = 256;  // warps 0-7
+constexpr int kSideThreads = 128;   // warps 8-11
+constexpr int kEpiThreads = kChainThreads + kSideThreads;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr uint32_t kKQBytes = 32768;  // [dk half][K rows 0-63 | Q rows 64-127][128 B]
 constexpr uint32_t kVBytes = 16384;   // [dv half][64 rows][128 B]
-constexpr uint32_t kTPBytes = 8192;   // [64 rows][128 B]: T' (exact form: Gamma ⊙ T')
-constexpr uint32_t kT1Bytes = 8192;   // [64 rows][128 B]: T' D_c1
+constexpr uint32_t kTPBytes = 8192;   // [64 rows][128 B]: T1 = T' D_c1
 constexpr uint32_t kOffV = kKQBytes;
 constexpr uint32_t kOffTP = kKQBytes + kVBytes;
-constexpr uint32_t kOffT1 = kOffTP + kTPBytes;
-constexpr uint32_t kStageBytes = kOffT1 + kT1Bytes;
+constexpr uint32_t kOffT1 = kOffTP;
+constexpr uint32_t kStageBytes = kOffTP + kTPBytes;
 constexpr uint32_t kTxBytes = kKQBytes + kVBytes + kTPBytes;  // bytes TMA brings per stage
 constexpr int kStages = 3;
-constexpr uint32_t kOffQM = kStages * kStageBytes;  // tril(Q K^T), [64][128 B]
-constexpr uint32_t kOffO = kOffQM + 8192;           // output tile [dv half][64][128 B]
-constexpr uint32_t kOffSmall = kOffO + 16384;
+constexpr uint32_t kOffQM = kStages * kStageBytes;  // two tril(Q K^T) tiles (chunk parity), [64][128 B]
+constexpr uint32_t kOffSmall = kOffQM + 16384;
 
 // TMEM columns (512 allocated)
 constexpr uint32_t kColS32 = 0;    // fp32 state
@@ -81,10 +87,8 @@ struct Coef {
     float G[64];     // chunk-local cumsum (rows past the end repeat the last)
     float gam[64];   // gamma_r
     float so[64];    // scale * gamma_r (output)
-    float c1[64];    // b_r beta_r           (multiplies V)
-    float c2[64];    // b_r beta_r gamma_r   (multiplies P_K)
     float e[64];     // a_r gamma_C / gamma_r   (Ut = e U')
-    float f[64];     // exp(-G*) (1 in the exact form)   (W4 = f U')
+    float f[64];     // exp(-G*) (1 in the exact form), the same for every row
     float gC;        // gamma_C
     int exact;       // 1: Gamma is applied element by element
     int pad[2];
@@ -93,8 +97,11 @@ struct Coef {
 struct Small {
     Coef coef[kStages];
     uint64_t full[kStages], empty[kStages];
-    uint64_t e1, e2, e3, oepi, pre, ofree, otile;
-    uint64_t m1, m2, m3, m4, p0, fin;
+    uint64_t e1, e2, e3, e4, qm;
+    // by chunk parity (chunk n: [n & 1], phase n >> 1)
+    uint64_t oepi[2];  // output of chunk n done
+    uint64_t m4x[2];   // MMA4 of chunk n done
+    uint64_t m1, m2, m3, p0, fin;
     uint32_t tmem_base;
     int abort;
 };
@@ -102,12 +109,13 @@ struct Small {
 constexpr uint32_t kSmemBytes = kOffSmall + sizeof(Small) + 1024;
 
 struct TcMaps {
-    CUtensorMap q, k, v, o, tp;
+    CUtensorMap q, k, v, tp;
 };
 
 struct Ctx {
     const TcMaps *maps;
     uint8_t *smem;
+    uint32_t sbase;  // shared-space address of smem
     Small *sm;
     const Problem *p;
     const Workspace *w;
@@ -116,10 +124,16 @@ struct Ctx {
     uint32_t tbase;
 };
 
-__device__ __forceinline__ bool wait_or_abort(const Ctx &cx, uint64_t *bar, uint32_t parity) {
+// Slow path of a wait, out of line so the per-chunk code stays small enough
+// for the instruction cache: bounded spin, then GDN_ERR_TIMEOUT.
+__device__ __noinline__ bool wait_slow(const Ctx &cx, uint64_t *bar, uint32_t parity) {
     if (mbar_wait(bar, parity, &cx.sm->abort, kTimeoutNs)) return true;
     if (atomicExch(&cx.sm->abort, 1) == 0) report_error(cx.w->err, GDN_ERR_TIMEOUT);
     return false;
+}
+
+__device__ __forceinline__ bool wait_or_abort(const Ctx &cx, uint64_t *bar, uint32_t parity) {
+    return mbar_try_wait(bar, parity) || wait_slow(cx, bar, parity);
 }
 
 // Epilogue waits: every lane waits, and the warp gives up together, so the
@@ -128,6 +142,9 @@ __device__ __forceinline__ bool ewait(const Ctx &cx, uint64_t *bar, uint32_t par
     const bool r = wait_or_abort(cx, bar, parity);
     return __all_sync(0xffffffffu, r);
 }
+
+// Shared-space address of coefficient array `field` of stage s.
+#define COEF_ADDR(cx, s, field) ((cx).sbase + kOffSmall + (s) * sizeof(Coef) + offsetof(Coef, field))
 
 // Stage ring: chunk n uses stage n % kStages; its use index is n / kStages.
 __device__ __forceinline__ int stage_of(uint32_t n) { return static_cast<int>(n % kStages); }
@@ -162,7 +179,7 @@ __device__ void producer_role(const Ctx &cx, const TcMaps &maps, int lane) {
     };
     // the gate values of the next chunk are fetched one step ahead, so their
     // latency overlaps the wait for a free stage
-    float pg0 = 0.f, pg1 = 0.f, pb0 = 0.f, pb1 = 0.f;
+    float pg0 = 0.f, pg1 = 0.f;
     int ph = 0, pt0 = 0, plen = 1;
     auto fetch = [&]() {
         const int4 ci = w.chunks[chunk0 + c];
@@ -172,14 +189,12 @@ __device__ void producer_role(const Ctx &cx, const TcMaps &maps, int lane) {
         const size_t gb = (size_t)ph * p.total_T + pt0;
         pg0 = w.G[gb + min(lane, plen - 1)];
         pg1 = w.G[gb + min(lane + 32, plen - 1)];
-        pb0 = lane < plen ? p.beta[(size_t)(pt0 + lane) * p.H + ph] : 0.f;
-        pb1 = lane + 32 < plen ? p.beta[(size_t)(pt0 + lane + 32) * p.H + ph] : 0.f;
     };
     bool more = advance();
     if (more) fetch();
     uint32_t n = 0;
     while (more) {
-        const float g0 = pg0, g1 = pg1, b0 = pb0, b1 = pb1;
+        const float g0 = pg0, g1 = pg1;
         const int h = ph, t0 = pt0;
         more = advance();
         if (more) fetch();
@@ -188,24 +203,22 @@ __device__ void producer_role(const Ctx &cx, const TcMaps &maps, int lane) {
         {
             const float Gfirst = __shfl_sync(0xffffffffu, g0, 0);
             const float Glast = __shfl_sync(0xffffffffu, g1, 31);  // row 63 repeats row len-1
-            // W4 = f U' equals U_m / gamma_m, so the factored form needs gamma_m > e^-80
-            // everywhere in the chunk; past that the exact form is used
+            // exp(-G*) U'_m equals U_m / gamma_m, so the factored form needs
+            // gamma_m > e^-80 everywhere in the chunk; past that the exact form is
+            // used (the inverse kernel takes the same decision from the same G)
             const bool exact = Glast < -80.f;
             const float Gs = 0.5f * (Gfirst + Glast);
             Coef &cf = sm.coef[s];
-            const float gg[2] = {g0, g1}, bb[2] = {b0, b1};
+            const float gg[2] = {g0, g1};
             const float fN = __expf(-Gs), eN = __expf(Glast - Gs);
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
                 const int r = lane + 32 * q2;
                 const float G = gg[q2];
                 const float gam = __expf(G);
-                const float b = exact ? 1.f : __expf(Gs - G);
                 cf.G[r] = G;
                 cf.gam[r] = gam;
                 cf.so[r] = p.scale * gam;
-                cf.c1[r] = b * bb[q2];
-                cf.c2[r] = b * bb[q2] * gam;
                 cf.e[r] = exact ? __expf(Glast - G) : eN;
                 cf.f[r] = exact ? 1.f : fN;
             }
@@ -240,6 +253,52 @@ __device__ void producer_role(const Ctx &cx, const TcMaps &maps, int lane) {
 }
 
 // --------------------------------------------------------------------- MMA
+// This CTA's chunks in order (items blockIdx.x, blockIdx.x + gridDim.x, ...;
+// empty items skipped), for the MMA warp, which looks one chunk ahead.
+struct MmaCursor {
+    int k, c, cend, cbegin, flags;
+    bool valid;
+};
+
+__device__ __forceinline__ void cursor_start(const Ctx &cx, MmaCursor &cu) {
+    cu.valid = false;
+    for (cu.k = blockIdx.x; cu.k < cx.n_items; cu.k += gridDim.x) {
+        const gdn_work_item it = cx.items[cu.k];
+        if (it.c_start < it.c_end) {
+            cu.c = it.c_start;
+            cu.cend = it.c_end;
+            cu.cbegin = it.c_begin;
+            cu.flags = it.flags;
+            cu.valid = true;
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ void cursor_next(const Ctx &cx, MmaCursor &cu) {
+    if (++cu.c < cu.cend) return;
+    cu.valid = false;
+    for (cu.k += gridDim.x; cu.k < cx.n_items; cu.k += gridDim.x) {
+        const gdn_work_item it = cx.items[cu.k];
+        if (it.c_start < it.c_end) {
+            cu.c = it.c_start;
+            cu.cend = it.c_end;
+            cu.cbegin = it.c_begin;
+            cu.flags = it.flags;
+            cu.valid = true;
+            return;
+        }
+    }
+}
+
+// Issue order per chunk n (the tensor pipe runs one thread's MMAs in order, so
+// work off the chain is placed where the chain is in an epilogue):
+//   (P0_n was issued after MMA3_{n-1}, into the U' columns, during E1_n)
+//   E1_n -> MMA1_n -> m1 | MMA4_{n-1} (during E2_n) | V term (after the side warps
+//   masked Q K^T) | E2_n -> MMA2b_n -> m2 | E3_n -> MMA3_n -> m3,
+//   stage free | P0_{n+1}
+// A chunk in the exact form issues its MMA4 right after MMA3 instead (its D4
+// goes to the other P buffer, which MMA1_{n+1} then waits to see emptied).
 __device__ void mma_role(const Ctx &cx) {
     Small &sm = *cx.sm;
     const uint32_t t = cx.tbase;
@@ -247,104 +306,107 @@ __device__ void mma_role(const Ctx &cx) {
     constexpr uint32_t I1 = idesc_bf16_f32(128, 128, 0, 0);   // P = S16 [K;Q]^T
     constexpr uint32_t I0 = idesc_bf16_f32(128, 64, 0, 0);    // [K;Q] K^T
     constexpr uint32_t I2a = idesc_bf16_f32(128, 64, 1, 0);   // U' = V^T (T' D_c1)^T, V^T MN-major
-    constexpr uint32_t I2b = idesc_bf16_f32(128, 64, 0, 0);   // U' += W2 T'^T
+    constexpr uint32_t I2b = idesc_bf16_f32(128, 64, 0, 0);   // U' += W2 T1^T
     constexpr uint32_t I3 = idesc_bf16_f32(128, 128, 0, 1);   // S += Ut K   (K as MN-major B)
     constexpr uint32_t I4 = idesc_bf16_f32(128, 64, 0, 0);    // P_Q (or D4) += W4 Qm^T
-    uint32_t n = 0;
-    bool ok = true, prev_exact = false;
-    for (int k = blockIdx.x; k < cx.n_items && ok; k += gridDim.x) {
-        const gdn_work_item it = cx.items[k];
-        for (int c = it.c_start; c < it.c_end; ++c, ++n) {
-            const int s = stage_of(n);
-            const uint32_t par = n & 1;
-            const bool out = (it.flags & GDN_ITEM_OUTPUT) && c >= it.c_begin;
-            const uint32_t st = smem0 + s * kStageBytes;
-            const uint32_t pc = t + kColP + (n & 1) * 128;        // this chunk's P buffer
-            const uint32_t po = t + kColP + ((n + 1) & 1) * 128;  // the other one
-            if (!wait_or_abort(cx, &sm.full[s], use_parity(n)) || !wait_or_abort(cx, &sm.e1, par)) {
-                ok = false;
-                break;
-            }
-            // the exact form keeps the previous output in the buffer MMA1 is about to write
-            if (prev_exact && !wait_or_abort(cx, &sm.oepi, (n - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            const bool exact = cx.sm->coef[s].exact;
-            tc_fence_after();
+    bool ok = true;
+    // P0 of a chunk: [K;Q] K^T into the U' columns (Q K^T in lanes 64-127)
+    auto issue_p0 = [&](uint32_t n, bool out) -> bool {
+        const int s = stage_of(n);
+        if (!wait_or_abort(cx, &sm.full[s], use_parity(n))) return false;
+        tc_fence_after();
+        if (out) {
+            const uint64_t dKQ = smem_desc_sw128(smem0 + s * kStageBytes, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t b = smem_desc_sw128(st + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                mma_ts(pc, t + kColS16 + 8 * kk, b, I1, kk > 0);
+                const uint64_t a = dKQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                mma_ss(t + kColU, a, a, I0, kk > 0);
             }
-            tc_commit(&sm.m1);
-            // V term of U' as soon as T' D_c1 is ready (U' is free once MMA3 of the last chunk is done)
-            if (!wait_or_abort(cx, &sm.pre, par)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // (correction-matrix items run with zero values: no V term)
-            const bool zero_v = it.flags & GDN_ITEM_FROM_IDENTITY;
-            if (!zero_v) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = smem_desc_sw128(st + kOffV + kk * 2048, 8192, 1024);
-                    const uint64_t b = smem_desc_sw128(st + kOffT1 + kk * 32, 16, 1024);
-                    mma_ss(t + kColU, a, b, I2a, kk > 0);
-                }
-            }
-            // Q K^T into the other buffer's first half, once MMA4 of the last chunk stopped reading it
-            if (n > 0 && !wait_or_abort(cx, &sm.m4, (n - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            if (out) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t a = smem_desc_sw128(st + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                    mma_ss(po, a, a, I0, kk > 0);
-                }
-            }
-            tc_commit(&sm.p0);
-            if (!wait_or_abort(cx, &sm.e2, par)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t b = smem_desc_sw128(st + kOffTP + kk * 32, 16, 1024);
-                mma_ts(t + kColU, pc + 16 + 8 * kk, b, I2b, (kk > 0 || !zero_v) ? 1u : 0u);
-            }
-            tc_commit(&sm.m2);
-            if (!wait_or_abort(cx, &sm.e3, par)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t b = smem_desc_sw128(st + kk * 2048, 16384, 1024);
-                mma_ts(t + kColS32, t + kColU + 16 + 8 * kk, b, I3, 1);
-            }
-            tc_commit(&sm.m3);
-            if (out) {
-                const uint32_t qm = smem0 + kOffQM;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t b = smem_desc_sw128(qm + kk * 32, 16, 1024);
-                    if (exact)
-                        mma_ts(po, pc + 16 + 8 * kk, b, I4, kk > 0);
-                    else
-                        mma_ts(pc + 64, pc + 16 + 8 * kk, b, I4, 1);
-                }
-            }
-            tc_commit(&sm.m4);
-            tc_commit(&sm.empty[s]);
-            prev_exact = out && exact;
         }
+        tc_commit(&sm.p0);
+        return true;
+    };
+    // MMA4 of chunk m: P_Q += W4 Qm^T (exact form: D4 = W4 Qm^T into the other buffer)
+    auto issue_mma4 = [&](uint32_t m, bool out, bool exact) -> bool {
+        if (!wait_or_abort(cx, &sm.e4, m & 1)) return false;
+        tc_fence_after();
+        if (out) {
+            const uint32_t pc = t + kColP + (m & 1) * 128, po = t + kColP + ((m + 1) & 1) * 128;
+            const uint64_t dQM = smem_desc_sw128(smem0 + kOffQM + (m & 1) * 8192, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t b = dQM + ((kk * 32) >> 4);
+                if (exact)
+                    mma_ts(po, pc + 16 + 8 * kk, b, I4, kk > 0);
+                else
+                    mma_ts(pc + 64, pc + 16 + 8 * kk, b, I4, 1);
+            }
+        }
+        tc_commit(&sm.m4x[m & 1]);
+        return true;
+    };
+
+    MmaCursor cu;
+    cursor_start(cx, cu);
+    uint32_t n = 0;
+    bool prev_exact = false, pend4 = false, pend4_out = false;  // MMA4 of chunk n-1 still to issue
+    if (cu.valid) ok = issue_p0(0, (cu.flags & GDN_ITEM_OUTPUT) && cu.c >= cu.cbegin);
+    while (ok && cu.valid) {
+        const int s = stage_of(n);
+        const uint32_t par = n & 1;
+        const bool out = (cu.flags & GDN_ITEM_OUTPUT) && cu.c >= cu.cbegin;
+        const bool zero_v = cu.flags & GDN_ITEM_FROM_IDENTITY;  // correction items: no V term
+        const uint32_t st = smem0 + s * kStageBytes;
+        const uint32_t pc = t + kColP + (n & 1) * 128;        // this chunk's P buffer
+        const bool exact = cx.sm->coef[s].exact;
+        const uint64_t dKQ = smem_desc_sw128(st, 16, 1024);             // K|Q rows, K-major
+        const uint64_t dV = smem_desc_sw128(st + kOffV, 8192, 1024);    // V^T, MN-major
+        const uint64_t dT1 = smem_desc_sw128(st + kOffT1, 16, 1024);
+        const uint64_t dK3 = smem_desc_sw128(st, 16384, 1024);          // K as MN-major B
+        // this chunk's P buffer last held chunk n-2, whose output must be out;
+        // in the exact form chunk n-1 keeps its D4 here too
+        if (n >= 2 && !wait_or_abort(cx, &sm.oepi[n & 1], ((n - 2) >> 1) & 1)) break;
+        if (prev_exact && !wait_or_abort(cx, &sm.oepi[(n - 1) & 1], ((n - 1) >> 1) & 1)) break;
+        if (!wait_or_abort(cx, &sm.e1, par)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_ts(pc, t + kColS16 + 8 * kk, dKQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), I1, kk > 0);
+        tc_commit(&sm.m1);
+        if (pend4 && !issue_mma4(n - 1, pend4_out, false)) break;
+        pend4 = false;
+        // V term of U' once Q K^T has left the U' columns
+        if (!wait_or_abort(cx, &sm.qm, par)) break;
+        tc_fence_after();
+        if (!zero_v) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ss(t + kColU, dV + ((kk * 2048) >> 4), dT1 + ((kk * 32) >> 4), I2a, kk > 0);
+        }
+        if (!wait_or_abort(cx, &sm.e2, par)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ts(t + kColU, pc + 16 + 8 * kk, dT1 + ((kk * 32) >> 4), I2b, (kk > 0 || !zero_v) ? 1u : 0u);
+        tc_commit(&sm.m2);
+        if (!wait_or_abort(cx, &sm.e3, par)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ts(t + kColS32, t + kColU + 16 + 8 * kk, dK3 + ((kk * 2048) >> 4), I3, 1);
+        tc_commit(&sm.m3);
+        tc_commit(&sm.empty[s]);
+        if (out && exact) {
+            if (!issue_mma4(n, true, true)) break;
+        } else {
+            pend4 = true;
+            pend4_out = out;
+        }
+        prev_exact = out && exact;
+        cursor_next(cx, cu);
+        ++n;
+        if (cu.valid && !issue_p0(n, (cu.flags & GDN_ITEM_OUTPUT) && cu.c >= cu.cbegin)) break;
     }
+    if (pend4) issue_mma4(n - 1, pend4_out, false);
     // all issued MMAs must finish before TMEM is released
     tc_commit(&sm.fin);
     int dummy = 0;
@@ -353,8 +415,8 @@ __device__ void mma_role(const Ctx &cx) {
 
 // ---------------------------------------------------------------- epilogue
 struct EpiThread {
-    int q, ch, i, et, lane;
-    uint32_t lane_base;  // TMEM lane field of this warp's quadrant
+    int q, ch, i, et, lane;   // lane quadrant, column half, TMEM lane (= value row i), index in the role
+    uint32_t lane_base;   // TMEM lane field of this warp's quadrant
 };
 
 __device__ __forceinline__ void load_tile32(const Ctx &cx, const EpiThread &e, uint32_t col, float *x) {
@@ -366,7 +428,8 @@ __device__ __forceinline__ void load_tile32(const Ctx &cx, const EpiThread &e, u
 }
 
 // Stores 32 state columns j0 .. j0+31 (key index) of this thread's value row.
-__device__ void write_state32(const Ctx &cx, const EpiThread &e, const gdn_work_item &it, int j0, const float *sv) {
+__device__ __noinline__ void write_state32(const Ctx &cx, const EpiThread &e, const gdn_work_item &it, int j0,
+                                           const float *sv) {
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
     const int i = e.i;
@@ -381,7 +444,8 @@ __device__ void write_state32(const Ctx &cx, const EpiThread &e, const gdn_work_
 }
 
 // Loads 32 start-state columns j0 .. j0+31 of this thread's value row.
-__device__ void load_start_state32(const Ctx &cx, const EpiThread &e, const gdn_work_item &it, int j0, float *sv) {
+__device__ __noinline__ void load_start_state32(const Ctx &cx, const EpiThread &e, const gdn_work_item &it, int j0,
+                                                float *sv) {
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
     const int i = e.i;
@@ -401,7 +465,7 @@ __device__ void load_start_state32(const Ctx &cx, const EpiThread &e, const gdn_
 }
 
 // Writes the state held in TMEM (this thread's row, its 64 columns) for `it`.
-__device__ void flush_state(const Ctx &cx, const EpiThread &e, const gdn_work_item &it) {
+__device__ __noinline__ void flush_state(const Ctx &cx, const EpiThread &e, const gdn_work_item &it) {
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
         float sv[32];
@@ -422,58 +486,8 @@ __device__ __forceinline__ void store_state32(const Ctx &cx, const EpiThread &e,
     tmem_st32(cx.tbase + e.lane_base + kColS32 + 64 * e.ch + 32 * hh, sc);
 }
 
-// Output of one finished chunk.  Usual form: o = scale gamma_r P_Q (P_Q already
-// holds the intra-chunk term); exact form: o = scale (gamma_r P_Q + D4).  Full
-// chunks go through the swizzled smem tile and a TMA store; a ragged last
-// chunk is stored row by row.
-__device__ bool output_chunk(const Ctx &cx, const EpiThread &e, const Coef &cf, bool exact, uint32_t pq_col,
-                             uint32_t d4_col, int t0, int len, int h, uint32_t &ocount) {
-    const Problem &p = *cx.p;
-    Small &sm = *cx.sm;
-    uint8_t *o_tile = cx.smem + kOffO;
-    float x[32];
-    load_tile32(cx, e, pq_col, x);
-    const int r0 = 32 * e.ch;
-#pragma unroll
-    for (int rr = 0; rr < 32; ++rr) x[rr] *= cf.so[r0 + rr];
-    if (exact) {
-        float d4[32];
-        load_tile32(cx, e, d4_col, d4);
-#pragma unroll
-        for (int rr = 0; rr < 32; ++rr) x[rr] = fmaf(p.scale, d4[rr], x[rr]);
-    }
-    const int i = e.i;
-    if (len == 64) {
-        if (e.et == 0) {
-            bulk_wait_group_read_all();
-            mbar_arrive(&sm.ofree);
-        }
-        if (!ewait(cx, &sm.ofree, ocount & 1)) return false;
-        const int half = i >> 6, col = i & 63;
-        uint8_t *base = o_tile + half * 8192 + (col & 7) * 2;
-#pragma unroll
-        for (int rr = 0; rr < 32; ++rr)
-            *reinterpret_cast<__nv_bfloat16 *>(base + sw128_offset(r0 + rr, col >> 3)) = __float2bfloat16_rn(x[rr]);
-        fence_proxy_async_smem();
-        mbar_arrive(&sm.otile);
-        if (e.et == 0) {
-            if (!wait_or_abort(cx, &sm.otile, ocount & 1)) return false;
-            tma_store_3d(&cx.maps->o, o_tile, 0, h, t0);
-            tma_store_3d(&cx.maps->o, o_tile + 8192, 64, h, t0);
-            bulk_commit_group();
-        }
-        ++ocount;
-    } else {
-        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.o);
-        for (int rr = 0; rr < 32; ++rr) {
-            const int r = r0 + rr;
-            if (r < len) o[((size_t)(t0 + r) * p.H + h) * kD + i] = __float2bfloat16_rn(x[rr]);
-        }
-    }
-    return true;
-}
-
-__device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
+// ---- the state chain: warps 0-7; warps w and w+4 share lane quadrant w % 4
+__device__ void chain_role(const Ctx &cx, int warp, int lane) {
     const Workspace &w = *cx.w;
     Small &sm = *cx.sm;
     EpiThread e;
@@ -483,13 +497,8 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
     e.et = threadIdx.x;
     e.lane = lane;
     e.lane_base = static_cast<uint32_t>(32 * e.q) << 16;
-    const int ch = e.ch, i = e.i;
-    uint8_t *qm_tile = cx.smem + kOffQM;
-
-    uint32_t n = 0, ocount = 0;
-    // the previous chunk, whose output is written one step later
-    int pv_out = 0, pv_t0 = 0, pv_len = 0, pv_h = 0, pv_s = 0, pv_exact = 0;
-    uint32_t pv_pcol = 0, pv_ocol = 0;
+    const int ch = e.ch;
+    uint32_t n = 0;
     // the item whose end state sits in TMEM and has not been written yet
     bool pending = false;
     gdn_work_item prev_item;
@@ -518,46 +527,12 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
         for (int c = it.c_start; c < it.c_end; ++c, ++n) {
             const int s = stage_of(n);
             const uint32_t par = n & 1;
-            const int4 ci = w.chunks[si.z + c];
-            const int t0 = ci.y, len = ci.z;
-            const bool out = (it.flags & GDN_ITEM_OUTPUT) && c >= it.c_begin;
-            uint8_t *st = cx.smem + s * kStageBytes;
-            const uint32_t pcol = kColP + (n & 1) * 128, ocol = kColP + ((n + 1) & 1) * 128;
+            const int len = w.chunks[si.z + c].z;
+            const uint32_t pcol = kColP + (n & 1) * 128;
             const Coef &cf = sm.coef[s];
             if (!ewait(cx, &sm.full[s], use_parity(n))) { ok = false; break; }
-            const bool exact = cf.exact;
 
-            // ---- T' D_c1 for the V term (exact form: T' <- Gamma ⊙ T' first, in place)
-            {
-                const int r = e.et >> 2, q4 = e.et & 3;
-#pragma unroll
-                for (int hc = 0; hc < 2; ++hc) {
-                    const int c16 = 2 * q4 + hc;
-                    uint4 *src = reinterpret_cast<uint4 *>(st + kOffTP + sw128_offset(r, c16));
-                    uint4 v = *src;
-                    uint32_t wv[4] = {v.x, v.y, v.z, v.w}, w1[4];
-#pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2) {
-                        const int m0 = 8 * c16 + 2 * e2;
-                        float x0 = bf16_lo(wv[e2]), x1 = bf16_hi(wv[e2]);
-                        if (exact) {
-                            x0 = (r < len && m0 <= r) ? x0 * __expf(cf.G[r] - cf.G[m0]) : 0.f;
-                            x1 = (r < len && m0 + 1 <= r) ? x1 * __expf(cf.G[r] - cf.G[m0 + 1]) : 0.f;
-                            wv[e2] = pack_bf16x2(x0, x1);
-                            x0 = bf16_lo(wv[e2]);
-                            x1 = bf16_hi(wv[e2]);
-                        }
-                        w1[e2] = pack_bf16x2(x0 * cf.c1[m0], x1 * cf.c1[m0 + 1]);
-                    }
-                    if (exact) *src = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                    *reinterpret_cast<uint4 *>(st + kOffT1 + sw128_offset(r, c16)) =
-                        make_uint4(w1[0], w1[1], w1[2], w1[3]);
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&sm.pre);
-            }
-
-            // ---- E1: S16 = bf16(S), S32 = gamma_C S   (critical: after MMA3 of the last chunk)
+            // ---- E1: S16 = bf16(S), S32 = gamma_C S   (after MMA3 of the last chunk)
             const float gC = cf.gC;
             if (c == it.c_start) {
                 if (pending) {
@@ -586,31 +561,19 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
             tc_fence_before();
             mbar_arrive(&sm.e1);
 
-            // ---- output of the previous chunk (under MMA1); then its stage is free
-            if (n > 0) {
-                if (!ewait(cx, &sm.m4, (n - 1) & 1)) { ok = false; break; }
-                tc_fence_after();
-                if (pv_out && !output_chunk(cx, e, sm.coef[pv_s], pv_exact, pv_pcol + 64 + 32 * ch, pv_ocol + 32 * ch,
-                                            pv_t0, pv_len, pv_h, ocount)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_before();
-                mbar_arrive(&sm.oepi);
-                mbar_arrive(&sm.empty[pv_s]);
-            }
-
-            // ---- E2: W2 = -c2 P_K   (critical: after MMA1)
+            // ---- E2: W2 = -gamma P_K   (after MMA1; it multiplies T1 = T' D_c1, and c2 = c1 gamma)
             if (!ewait(cx, &sm.m1, par)) { ok = false; break; }
             tc_fence_after();
             {
                 float pk[32];
                 load_tile32(cx, e, pcol + 32 * ch, pk);
+                const uint32_t c2a = COEF_ADDR(cx, s, gam) + 128 * ch;
                 uint32_t w2[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int r0 = 32 * ch + 2 * j;
-                    w2[j] = pack_bf16x2(-cf.c2[r0] * pk[2 * j], -cf.c2[r0 + 1] * pk[2 * j + 1]);
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 c = lds_f4(c2a + 16 * q4);
+                    w2[2 * q4] = pack_bf16x2(-c.x * pk[4 * q4], -c.y * pk[4 * q4 + 1]);
+                    w2[2 * q4 + 1] = pack_bf16x2(-c.z * pk[4 * q4 + 2], -c.w * pk[4 * q4 + 3]);
                 }
                 tmem_st16(cx.tbase + e.lane_base + pcol + 16 + 16 * ch, w2);
                 tmem_wait_st();
@@ -618,35 +581,8 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
             tc_fence_before();
             mbar_arrive(&sm.e2);
 
-            // ---- masked Q K^T (under MMA2); the exact form also applies Gamma
-            if (!ewait(cx, &sm.p0, par)) { ok = false; break; }
-            tc_fence_after();
-            if (out && e.q >= 2) {
-                const int r = i - 64;
-                float qk[32];
-                load_tile32(cx, e, ocol + 32 * ch, qk);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t wv[4];
-#pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2) {
-                        const int mm = 8 * cc + 2 * e2;
-                        const int m0 = 32 * ch + mm;
-                        float x0 = (r < len && m0 <= r) ? qk[mm] : 0.f;
-                        float x1 = (r < len && m0 + 1 <= r) ? qk[mm + 1] : 0.f;
-                        if (exact) {
-                            x0 *= (r < len && m0 <= r) ? __expf(cf.G[r] - cf.G[m0]) : 0.f;
-                            x1 *= (r < len && m0 + 1 <= r) ? __expf(cf.G[r] - cf.G[m0 + 1]) : 0.f;
-                        }
-                        wv[e2] = pack_bf16x2(x0, x1);
-                    }
-                    *reinterpret_cast<uint4 *>(qm_tile + sw128_offset(r, 4 * ch + cc)) =
-                        make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                }
-                fence_proxy_async_smem();
-            }
-
-            // ---- E3: Ut = e U' for the state, W4 = f U' for the output   (critical: after MMA2)
+            // ---- E3: Ut = e U' for the state (after MMA2); then W4 = U' for the output
+            // (the uniform factor exp(-G*) of the factored form rides on the masked Q K^T)
             if (!ewait(cx, &sm.m2, par)) { ok = false; break; }
             tc_fence_after();
             {
@@ -657,19 +593,188 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
                     for (int j = 0; j < 32; ++j)
                         if (32 * ch + j >= len) u[j] = 0.f;
                 }
-                uint32_t ut[16], w4[16];
+                const uint32_t ea = COEF_ADDR(cx, s, e) + 128 * ch;
+                uint32_t ut[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int r0 = 32 * ch + 2 * j;
-                    ut[j] = pack_bf16x2(u[2 * j] * cf.e[r0], u[2 * j + 1] * cf.e[r0 + 1]);
-                    w4[j] = pack_bf16x2(u[2 * j] * cf.f[r0], u[2 * j + 1] * cf.f[r0 + 1]);
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 ce = lds_f4(ea + 16 * q4);
+                    ut[2 * q4] = pack_bf16x2(u[4 * q4] * ce.x, u[4 * q4 + 1] * ce.y);
+                    ut[2 * q4 + 1] = pack_bf16x2(u[4 * q4 + 2] * ce.z, u[4 * q4 + 3] * ce.w);
                 }
                 tmem_st16(cx.tbase + e.lane_base + kColU + 16 + 16 * ch, ut);
-                tmem_st16(cx.tbase + e.lane_base + pcol + 16 + 16 * ch, w4);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sm.e3);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) ut[j] = pack_bf16x2(u[2 * j], u[2 * j + 1]);
+                tmem_st16(cx.tbase + e.lane_base + pcol + 16 + 16 * ch, ut);
                 tmem_wait_st();
             }
             tc_fence_before();
-            mbar_arrive(&sm.e3);
+            mbar_arrive(&sm.e4);
+            mbar_arrive(&sm.empty[s]);
+        }
+        if (!ok) break;
+        prev_item = it;
+        pending = true;
+    }
+    // tail: the last item's state
+    if (ok && pending && n > 0 && ewait(cx, &sm.m3, (n - 1) & 1)) {
+        tc_fence_after();
+        flush_state(cx, e, prev_item);
+    }
+}
+
+// Masked Q K^T -> the qm tile (side warps of lane quadrants 2-3: query row r =
+// lane index - 64; key columns m <= r < len kept).
+__device__ __forceinline__ void side_qmask(const Ctx &cx, const EpiThread &e, int len, uint32_t qm_tile, float f) {
+    const int r = e.i - 64;
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        float qk[32];
+        load_tile32(cx, e, kColU + 32 * hh, qk);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const int mm = 8 * cc + 2 * e2;
+                const int m0 = 32 * hh + mm;
+                const float x0 = (r < len && m0 <= r) ? f * qk[mm] : 0.f;
+                const float x1 = (r < len && m0 + 1 <= r) ? f * qk[mm + 1] : 0.f;
+                wv[e2] = pack_bf16x2(x0, x1);
+            }
+            sts_u4(qm_tile + sw128_offset(r, 4 * hh + cc), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+        }
+    }
+}
+
+// The same with Gamma applied element by element (exact form).
+__device__ __noinline__ void side_qmask_exact(const Ctx &cx, const EpiThread &e, const Coef &cf, int len,
+                                              uint8_t *qm_tile) {
+    const int r = e.i - 64;
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        float qk[32];
+        load_tile32(cx, e, kColU + 32 * hh, qk);
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const int mm = 8 * cc + 2 * e2;
+                const int m0 = 32 * hh + mm;
+                const float x0 = (r < len && m0 <= r) ? qk[mm] * __expf(cf.G[r] - cf.G[m0]) : 0.f;
+                const float x1 = (r < len && m0 + 1 <= r) ? qk[mm + 1] * __expf(cf.G[r] - cf.G[m0 + 1]) : 0.f;
+                wv[e2] = pack_bf16x2(x0, x1);
+            }
+            *reinterpret_cast<uint4 *>(qm_tile + sw128_offset(r, 4 * hh + cc)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+    }
+}
+
+// Exact form: x += scale D4 (D4 read from TMEM).  Inline: an out-of-line call
+// taking x by pointer would put x in local memory on every path.
+__device__ __forceinline__ void add_d4(const Ctx &cx, const EpiThread &e, uint32_t col, float scale, float *x) {
+    float d4[32];
+    load_tile32(cx, e, col, d4);
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr) x[rr] = fmaf(scale, d4[rr], x[rr]);
+}
+
+// Output of one finished chunk: usual form o = scale gamma_r P_Q (P_Q already
+// holds the intra-chunk term); exact form o = scale (gamma_r P_Q + D4).  Side
+// warps, lane = value row i, all 64 tokens; each store of a warp covers 64
+// contiguous bytes of one token's row of o.
+__device__ void output_chunk(const Ctx &cx, const EpiThread &e, int s, bool exact, uint32_t pq_col,
+                             uint32_t d4_col, int t0, int len, int h) {
+    const Problem &p = *cx.p;
+    const size_t rs = (size_t)p.H * kD;
+    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.o) + ((size_t)t0 * p.H + h) * kD + e.i;
+    const uint32_t soa = COEF_ADDR(cx, s, so);
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        float x[32];
+        load_tile32(cx, e, pq_col + 32 * hh, x);
+        const int r0 = 32 * hh;
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 so = lds_f4(soa + 4 * r0 + 16 * q4);
+            x[4 * q4 + 0] *= so.x;
+            x[4 * q4 + 1] *= so.y;
+            x[4 * q4 + 2] *= so.z;
+            x[4 * q4 + 3] *= so.w;
+        }
+        if (exact) add_d4(cx, e, d4_col + 32 * hh, p.scale, x);
+        __nv_bfloat16 *oh = o + (size_t)r0 * rs;
+        if (len >= r0 + 32) {
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) oh[rr * rs] = __float2bfloat16_rn(x[rr]);
+        } else {
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr)
+                if (r0 + rr < len) oh[rr * rs] = __float2bfloat16_rn(x[rr]);
+        }
+    }
+}
+
+// ---- off the chain: warps 8-11 (lane quadrant w % 4)
+__device__ void side_role(const Ctx &cx, int warp, int lane) {
+    const Workspace &w = *cx.w;
+    Small &sm = *cx.sm;
+    EpiThread e;
+    e.q = warp & 3;
+    e.ch = 0;
+    e.i = 32 * e.q + lane;
+    e.et = threadIdx.x - kChainThreads;
+    e.lane = lane;
+    e.lane_base = static_cast<uint32_t>(32 * e.q) << 16;
+
+    uint32_t n = 0;
+    // the previous chunk, whose output is written one step later
+    int pv_out = 0, pv_t0 = 0, pv_len = 0, pv_h = 0, pv_s = 0, pv_exact = 0;
+    uint32_t pv_pcol = 0, pv_ocol = 0;
+    bool ok = true;
+
+    for (int k = blockIdx.x; k < cx.n_items && ok; k += gridDim.x) {
+        const gdn_work_item it = cx.items[k];
+        const int4 si = w.seqinfo[it.seq];
+        for (int c = it.c_start; c < it.c_end; ++c, ++n) {
+            const int s = stage_of(n);
+            const uint32_t par = n & 1;
+            const int4 ci = w.chunks[si.z + c];
+            const int t0 = ci.y, len = ci.z;
+            const bool out = (it.flags & GDN_ITEM_OUTPUT) && c >= it.c_begin;
+            const uint32_t pcol = kColP + (n & 1) * 128, ocol = kColP + ((n + 1) & 1) * 128;
+            const Coef &cf = sm.coef[s];
+            if (!ewait(cx, &sm.full[s], use_parity(n))) { ok = false; break; }
+            const bool exact = cf.exact;
+
+            // ---- masked Q K^T (P0 put it in the U' columns; the qm tile is free once
+            // MMA4 of the last chunk is done); the exact form also applies Gamma
+            if (!ewait(cx, &sm.p0, par)) { ok = false; break; }
+            // this parity's qm tile was last read by MMA4 of chunk n-2
+            if (n >= 2 && !ewait(cx, &sm.m4x[n & 1], ((n - 2) >> 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            if (out && e.q >= 2) {
+                if (exact)
+                    side_qmask_exact(cx, e, cf, len, cx.smem + kOffQM + (n & 1) * 8192);
+                else
+                    side_qmask(cx, e, len, cx.sbase + kOffQM + (n & 1) * 8192, cf.f[0]);
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.qm);
+
+            // ---- output of the previous chunk (after its MMA4); then its stage is free
+            if (n > 0) {
+                if (!ewait(cx, &sm.m4x[(n - 1) & 1], ((n - 1) >> 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                if (pv_out) output_chunk(cx, e, pv_s, pv_exact, pv_pcol + 64, pv_ocol, pv_t0, pv_len, pv_h);
+                tc_fence_before();
+                mbar_arrive(&sm.oepi[(n - 1) & 1]);
+                mbar_arrive(&sm.empty[pv_s]);
+            }
 
             pv_out = out;
             pv_t0 = t0;
@@ -680,29 +785,18 @@ __device__ void epilogue_role(const Ctx &cx, int warp, int lane) {
             pv_pcol = pcol;
             pv_ocol = ocol;
         }
-        if (!ok) break;
-        prev_item = it;
-        pending = true;
     }
-    // tail: output of the last chunk and the last item's state
-    if (ok && n > 0) {
-        if (ewait(cx, &sm.m4, (n - 1) & 1)) {
-            tc_fence_after();
-            if (pv_out)
-                output_chunk(cx, e, sm.coef[pv_s], pv_exact, pv_pcol + 64 + 32 * ch, pv_ocol + 32 * ch, pv_t0, pv_len,
-                             pv_h, ocount);
-        }
-        if (pending && ewait(cx, &sm.m3, (n - 1) & 1)) {
-            tc_fence_after();
-            flush_state(cx, e, prev_item);
-        }
+    // tail: output of the last chunk
+    if (ok && n > 0 && ewait(cx, &sm.m4x[(n - 1) & 1], ((n - 1) >> 1) & 1)) {
+        tc_fence_after();
+        if (pv_out)
+            output_chunk(cx, e, pv_s, pv_exact, pv_pcol + 64, pv_ocol, pv_t0, pv_len, pv_h);
     }
-    if (e.et == 0) bulk_wait_group_all();
 }
 
 // ---------------------------------------------------------------- kernel
-// 10 warps share the 4 SM sub-partitions 3/3/2/2, so a thread may hold at most
-// 16384 / (3 * 32) registers: 168 after rounding.
+// 14 warps share the 4 SM sub-partitions 4/4/3/3, so a thread may hold at most
+// 16384 / (4 * 32) = 128 registers.
 __global__ void __launch_bounds__(kThreads, 1)
     fused_tc_kernel(const __grid_constant__ TcMaps maps, const Problem p, const Workspace w, const int pass) {
     extern __shared__ uint8_t smem_raw[];
@@ -714,17 +808,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.full[s], 32);
             mbar_init(&sm.empty[s], 1 + kEpiThreads);
         }
-        mbar_init(&sm.e1, kEpiThreads);
-        mbar_init(&sm.e2, kEpiThreads);
-        mbar_init(&sm.e3, kEpiThreads);
-        mbar_init(&sm.oepi, kEpiThreads);
-        mbar_init(&sm.pre, kEpiThreads);
-        mbar_init(&sm.ofree, 1);
-        mbar_init(&sm.otile, kEpiThreads);
+        mbar_init(&sm.e1, kChainThreads);
+        mbar_init(&sm.e2, kChainThreads);
+        mbar_init(&sm.e3, kChainThreads);
+        mbar_init(&sm.e4, kChainThreads);
+        mbar_init(&sm.m4x[0], 1);
+        mbar_init(&sm.m4x[1], 1);
+        mbar_init(&sm.oepi[0], kSideThreads);
+        mbar_init(&sm.oepi[1], kSideThreads);
+        mbar_init(&sm.qm, kSideThreads);
         mbar_init(&sm.m1, 1);
         mbar_init(&sm.m2, 1);
         mbar_init(&sm.m3, 1);
-        mbar_init(&sm.m4, 1);
         mbar_init(&sm.p0, 1);
         mbar_init(&sm.fin, 1);
         sm.abort = 0;
@@ -738,7 +833,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&maps.q);
         tma_prefetch_map(&maps.k);
         tma_prefetch_map(&maps.v);
-        tma_prefetch_map(&maps.o);
         tma_prefetch_map(&maps.tp);
     }
     tc_fence_before();
@@ -748,6 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ctx cx;
     cx.maps = &maps;
     cx.smem = smem;
+    cx.sbase = smem_u32(smem);
     cx.sm = &sm;
     cx.p = &p;
     cx.w = &w;
@@ -760,8 +855,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         if (lane == 0) mma_role(cx);
         __syncwarp();
+    } else if (warp < 8) {
+        chain_role(cx, warp, lane);
     } else {
-        epilogue_role(cx, warp, lane);
+        side_role(cx, warp, lane);
     }
 
     tc_fence_before();
@@ -825,7 +922,7 @@ cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int 
     cuuint32_t es[2] = {1, 1};
     int r;
     if ((r = encode_rows(fn, &maps.q, p.q, p.H, p.total_T)) || (r = encode_rows(fn, &maps.k, p.k, p.H, p.total_T)) ||
-        (r = encode_rows(fn, &maps.v, p.v, p.H, p.total_T)) || (r = encode_rows(fn, &maps.o, p.o, p.H, p.total_T)) ||
+        (r = encode_rows(fn, &maps.v, p.v, p.H, p.total_T)) ||
         (r = fn(&maps.tp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.tprime, dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE))) {

@@ -327,7 +327,7 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
         if ((e = launch_plan(p, w, pp, stream)) != cudaSuccess) return cuda_fail("launch plan", e);
     }
     if ((stages & GDN_STAGE_INVERSE) && L.max_chunks > 0) {
-        cudaError_t e = launch_inverse(p, w, stream);
+        cudaError_t e = launch_inverse(p, w, hp.kernel == GDN_KERNEL_TC, stream);
         if (e != cudaSuccess) return cuda_fail("launch inverse", e);
     }
     const bool tc = hp.kernel == GDN_KERNEL_TC;

@@ -33,7 +33,8 @@ struct Workspace {
     int *flags;             // [N*H]
     float *G;               // [H, total_T]
     float *totals;          // [H, max_chunks]
-    void *tprime;           // [H, total_T, C] bf16 (bf16 inputs) or fp32 (fp32 inputs)
+    void *tprime;           // [H, total_T, C] bf16 (bf16 inputs) or fp32 (fp32 inputs): T', or
+                            // T' diag(c1) when the tcgen05 fused kernel runs
     gdn_work_item *items2;  // [max_items]
     gdn_work_item *items1;  // [max_items1]
     int4 *scan_units;       // [max_cp_slots]: (seq, head, segments, first slot)
@@ -66,7 +67,9 @@ void set_error_text(const char *text);
 cudaError_t launch_seqprep(const Problem &p, const Workspace &w, cudaStream_t s);
 cudaError_t launch_gate(const Problem &p, const Workspace &w, cudaStream_t s);
 cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &pp, cudaStream_t s);
-cudaError_t launch_inverse(const Problem &p, const Workspace &w, cudaStream_t s);
+// for_tc: the tcgen05 fused kernel consumes the result, which is then T' diag(c1)
+// (the gate-scaled form that kernel multiplies by) instead of T' itself
+cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s);
 cudaError_t launch_scan(const Problem &p, const Workspace &w, cudaStream_t s);
 // pass 1 (state-only correction items) or pass 2 (output items) on the CUDA-core kernel
 cudaError_t launch_fused_simt(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s);

@@ -83,9 +83,11 @@ __global__ void __launch_bounds__(128) inverse_simt_kernel(Problem p, Workspace 
 //   warps 4-14   solvers: one unit per warp; lane j forward-substitutes column
 //                j of (I + A') X = I over rows 0..63 and then column 32 + j over
 //                rows 32..63, 16 rows at a time (block rows of A' read as
-//                broadcasts, solved blocks kept in registers); the finished
-//                bf16 tile is written into the dead slot and leaves with one
-//                bulk copy (the rows of a chunk are contiguous in T').
+//                broadcasts, solved blocks kept in tensor memory); each column
+//                is scaled by the gate factor the fused kernel expects (T1 =
+//                T' diag(c1), see below), and the finished bf16 tile is written
+//                into the dead slot and leaves with one bulk copy (the rows of
+//                a chunk are contiguous in the workspace).
 // All waits are bounded; a timeout sets the error word and the CTA drains.
 // ---------------------------------------------------------------------------
 namespace {
@@ -96,7 +98,7 @@ constexpr int kInvThreads = 32 * (kInvConv + kInvSolvers + 1);
 constexpr int kInvKStages = 3;
 constexpr int kInvL2Ahead = 6;                    // pairs between an L2 prefetch and its use
 constexpr uint32_t kInvPairBytes = 32768;         // two 64 x 128 bf16 key tiles
-constexpr int kInvSlotFloats = 10 * 256;          // the 10 lower 16 x 16 blocks of A'
+constexpr int kInvSlotFloats = 10 * 256 + 64;     // the 10 lower 16 x 16 blocks of A', then c1[64]
 
 constexpr uint32_t kInvSlotBytes = kInvSlotFloats * 4;
 constexpr uint32_t kInvOffSlots = kInvKStages * kInvPairBytes;
@@ -114,7 +116,7 @@ struct InvBars {
     uint64_t kfull[kInvKStages], kempty[kInvKStages];
     uint64_t tfull[2], tempty[2];
     uint64_t afull[kInvSolvers], aempty[kInvSolvers];
-    int4 unit[kInvSolvers];     // per slot: first token, length, head, store flag
+    int4 unit[kInvSolvers];     // per slot: first token, length, head, flags (1 store, 2 exact)
     uint32_t tmem_base;
     int abort;
 };
@@ -205,6 +207,17 @@ __device__ __forceinline__ void solve_blocked(uint32_t slot, uint32_t xcol, int 
     }
 }
 
+// Exact form: rows r0 .. r0+31 of one T' column (value index of column m):
+// x_r *= exp(G_r - G_m) (rows past the chunk reuse its last cumsum; T' is zero
+// above the diagonal, so only r >= m matters).
+__device__ __forceinline__ void exact_gamma_rows(uint32_t *v, int r0, const float *Gh, float Gm, int len) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+        const float Gr = Gh[min(r0 + t, len - 1)];
+        v[t] = __float_as_uint(__uint_as_float(v[t]) * __expf(fminf(Gr - Gm, 0.f)));
+    }
+}
+
 __device__ __forceinline__ void sts_u16(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<unsigned short>(v & 0xFFFFu)) : "memory");
 }
@@ -233,7 +246,7 @@ __device__ __forceinline__ PairInfo pair_info(const Problem &p, const Workspace 
 }
 
 __global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid_constant__ InvMaps maps, Problem p,
-                                                                     Workspace w) {
+                                                                     Workspace w, int gate_scaled) {
     extern __shared__ uint8_t inv_smem_raw[];
     uint8_t *smem =
         reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(inv_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -331,14 +344,25 @@ __global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid
             const int hd = half ? q.h1 : q.h0;
             return r < q.len ? __ldg(&p.beta[(size_t)(q.t0 + r) * p.H + hd]) : 0.f;
         };
+        // gate cumsum of this row, and the chunk's first and last (for c1)
+        auto gate_of = [&](const PairInfo &q) {
+            const int hd = half ? q.h1 : q.h0;
+            const float *Gh = w.G + (size_t)hd * p.total_T + q.t0;
+            return make_float3(Gh[min(r, q.len - 1)], Gh[0], Gh[q.len - 1]);
+        };
         PairInfo pi_next = pair_info(p, w, blockIdx.x);
         float br_next = beta_of(pi_next);
+        float3 g_next = gate_of(pi_next);
         PairInfo pi_next2 = n_local > 1 ? pair_info(p, w, blockIdx.x + gridDim.x) : pi_next;
         for (int i = 0; i < n_local; ++i) {
             const PairInfo pi = pi_next;
             const float br = br_next;
+            const float3 gr = g_next;
             pi_next = pi_next2;
-            if (i + 1 < n_local) br_next = beta_of(pi_next);
+            if (i + 1 < n_local) {
+                br_next = beta_of(pi_next);
+                g_next = gate_of(pi_next);
+            }
             if (i + 2 < n_local) pi_next2 = pair_info(p, w, blockIdx.x + (i + 2) * gridDim.x);
             if (warp == 0 && lane == 0 && i + kInvL2Ahead < n_local) {
                 const PairInfo pf = pair_info(p, w, blockIdx.x + (i + kInvL2Ahead) * gridDim.x);
@@ -376,8 +400,12 @@ __global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid
                     }
                 }
             }
+            // c1_r of the gate-scaled T1 = T' diag(c1) (factored form; exact form: beta_r)
+            const bool exact = gate_scaled && gr.z < -80.f;
+            sl[kInvSlotFloats - 64 + r] =
+                !gate_scaled ? 1.f : exact ? br : __expf(0.5f * (gr.y + gr.z) - gr.x) * br;
             if ((warp & 1) == 0 && lane == 0)
-                b.unit[slot] = make_int4(pi.t0, pi.len, head, (half && pi.h1 == pi.h0) ? 0 : 1);
+                b.unit[slot] = make_int4(pi.t0, pi.len, head, ((half && pi.h1 == pi.h0) ? 0 : 1) | (exact ? 2 : 0));
             tc::mbar_arrive(&b.afull[slot]);
         }
     } else {
@@ -393,25 +421,42 @@ __global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid
             if (!__all_sync(0xffffffffu, ok)) break;
             const int4 un = b.unit[s];
             const int len = un.y;
-            const bool store = un.w != 0;
+            const bool store = un.w & 1;
             uint8_t *slot_ptr = smem + kInvOffSlots + s * kInvSlotBytes;
             const uint32_t A = tc::smem_u32(slot_ptr);
+            // The fused kernel consumes T1 = T' diag(c1) with the factored gate
+            // c1_m = exp(G* - G_m) beta_m, G* the middle of the chunk's gate
+            // range; a chunk whose last cumsum is below -80 takes the exact
+            // form T1 = (Gamma ⊙ T') diag(beta) instead.  (The same rule, on
+            // the same G values, picks the form in the fused kernel.)
+            const bool exact = un.w & 2;
+            const float *Gh = w.G + (size_t)un.z * p.total_T + un.x;
+            const float *c1s = reinterpret_cast<const float *>(smem + kInvOffSlots + s * kInvSlotBytes) +
+                               (kInvSlotFloats - 64);
+            const float c1[2] = {c1s[j], c1s[32 + j]};
+            float Gc[2] = {0.f, 0.f};
+            if (exact) {
+                Gc[0] = Gh[min(j, len - 1)];
+                Gc[1] = Gh[min(32 + j, len - 1)];
+            }
             // pass A: column j over rows 0..63 -> x in columns xcol .. xcol+63;
-            // then packed to bf16 pairs of rows in columns xcol .. xcol+31
+            // then scaled and packed to bf16 pairs of rows in columns xcol .. xcol+31
             solve_blocked(A, xcol, j, 0);
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t v[32], pk[16];
                 tc::tmem_ld32(xcol + 32 * hh, v);
                 tc::tmem_wait_ld();
+                if (exact) exact_gamma_rows(v, 32 * hh, Gh, Gc[0], len);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) pk[t] = tc::pack_bf16x2(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+                for (int t = 0; t < 16; ++t)
+                    pk[t] = tc::pack_bf16x2(c1[0] * __uint_as_float(v[2 * t]), c1[0] * __uint_as_float(v[2 * t + 1]));
                 tc::tmem_st16(xcol + 16 * hh, pk);
                 tc::tmem_wait_st();
             }
             // pass B: column 32 + j over rows 32..63 -> columns xcol+32 .. xcol+63
             solve_blocked(A, xcol, 32 + j, 2);
-            // A' is dead: the slot becomes the row-major bf16 T' tile [64][64]
+            // A' is dead: the slot becomes the row-major bf16 T1 tile [64][64]
             __syncwarp();
             {
                 uint32_t v[32];
@@ -431,11 +476,13 @@ __global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid
                 }
                 tc::tmem_ld32(xcol + 32, v);
                 tc::tmem_wait_ld();
+                if (exact) exact_gamma_rows(v, 32, Gh, Gc[1], len);
 #pragma unroll
                 for (int r = 0; r < 32; ++r) sts_u16(A + r * 128 + 64 + 2 * j, 0u);
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
-                    const uint32_t pv = tc::pack_bf16x2(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+                    const uint32_t pv =
+                        tc::pack_bf16x2(c1[1] * __uint_as_float(v[2 * t]), c1[1] * __uint_as_float(v[2 * t + 1]));
                     sts_u16(A + (32 + 2 * t) * 128 + 64 + 2 * j, pv);
                     sts_u16(A + (32 + 2 * t + 1) * 128 + 64 + 2 * j, pv >> 16);
                 }
@@ -479,7 +526,7 @@ EncodeTiledFnInv inv_encode_fn() {
     return fn;
 }
 
-cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, cudaStream_t s) {
+cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, int gate_scaled, cudaStream_t s) {
     EncodeTiledFnInv fn = inv_encode_fn();
     if (!fn) {
         set_error_detail("driver entry point cuTensorMapEncodeTiled", cudaErrorNotSupported);
@@ -505,14 +552,14 @@ cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, cudaStream_t
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const long long pairs = (long long)w.max_chunks * ((p.H + 1) / 2);
     const int grid = (int)std::max(1LL, std::min<long long>(sms, pairs));
-    inverse_tc_kernel<<<grid, kInvThreads, kInvSmem, s>>>(maps, p, w);
+    inverse_tc_kernel<<<grid, kInvThreads, kInvSmem, s>>>(maps, p, w, gate_scaled);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_inverse(const Problem &p, const Workspace &w, cudaStream_t s) {
-    if (p.dtype == GDN_BF16 && p.dk == 128 && p.total_T > 0) return launch_inverse_tc(p, w, s);
+cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s) {
+    if (p.dtype == GDN_BF16 && p.dk == 128 && p.total_T > 0) return launch_inverse_tc(p, w, for_tc ? 1 : 0, s);
     const int smem = (kChunk * (p.dk + 1) + 2 * kChunk * 65) * (int)sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(inverse_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

@@ -154,6 +154,28 @@ def _workspace_views(inp, ws, opts=None):
     )
 
 
+def gate_scaled_tprime(Tp, G, beta, cu, C):
+    """T1 = T' diag(c1) per chunk and head, from the oracle's T' and chunk-local
+    gate cumsum G: the factored gate Gamma_rm = a_r b_m around the midpoint G* of
+    the chunk's first and last cumsum gives c1_m = b_m beta_m, b_m = exp(G* - G_m);
+    a chunk whose last cumsum is below -80 keeps Gamma element-wise instead:
+    T1 = (Gamma ⊙ T') diag(beta)."""
+    out = np.zeros_like(Tp)
+    for n in range(len(cu) - 1):
+        for t0 in range(int(cu[n]), int(cu[n + 1]), C):
+            L = min(C, int(cu[n + 1]) - t0)
+            for h in range(Tp.shape[1]):
+                Gc, bc = G[t0:t0 + L, h], beta[t0:t0 + L, h]
+                blk = Tp[t0:t0 + L, h, :L]
+                if Gc[-1] < -80.0:
+                    gam = np.exp(np.minimum(Gc[:, None] - Gc[None, :], 0.0))
+                    out[t0:t0 + L, h, :L] = blk * gam * bc[None, :]
+                else:
+                    b = np.exp(0.5 * (Gc[0] + Gc[-1]) - Gc)
+                    out[t0:t0 + L, h, :L] = blk * (b * bc)[None, :]
+    return out
+
+
 def test_gate_and_inverse_intermediates():
     cfg = CONFIGS[3].scaled(T=3000, H=3, n_seqs=5, zero_gate_heads=(1,))
     inp = to_device(make_inputs(cfg, "cpu"))
@@ -171,11 +193,14 @@ def test_gate_and_inverse_intermediates():
     assert nck == len(gate.chunk_table(cu, 64))
     assert np.abs(oracle.to_f64(views["totals"][:, :nck]).T - tot_ref).max() < 1e-4
     assert views["flags"].cpu().numpy().tolist() == gate.head_flags(g, cu).tolist()
-    # T' rows against the fp64 inverse (bf16 storage)
-    Tp_ref = chunked.inverse_rows(oracle.to_f64(inp["k"]).reshape(-1, 3, 128), oracle.to_f64(inp["beta"]).reshape(-1, 3),
-                                  cu, 64)
+    # T' rows against the fp64 inverse (bf16 storage).  The tcgen05 path stores
+    # the gate-scaled T1 = T' diag(c1) that its fused kernel multiplies by.
+    beta = oracle.to_f64(inp["beta"]).reshape(-1, 3)
+    Tp_ref = chunked.inverse_rows(oracle.to_f64(inp["k"]).reshape(-1, 3, 128), beta, cu, 64)
+    Tp_ref = gate_scaled_tprime(Tp_ref, G_ref, beta, cu, 64)
     Tp = oracle.to_f64(views["tprime"]).transpose(1, 0, 2)
-    assert np.abs(Tp - Tp_ref).max() < 2e-2
+    # element-wise: bf16 storage of entries that the gate scaling can make large
+    assert (np.abs(Tp - Tp_ref) / (1.0 + np.abs(Tp_ref))).max() < 2e-2
     assert np.linalg.norm(Tp - Tp_ref) / np.linalg.norm(Tp_ref) < 4e-3
 
 
