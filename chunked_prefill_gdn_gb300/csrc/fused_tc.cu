@@ -126,14 +126,15 @@ struct Ctx {
 
 // Slow path of a wait, out of line so the per-chunk code stays small enough
 // for the instruction cache: bounded spin, then GDN_ERR_TIMEOUT.
-__device__ __noinline__ bool wait_slow(const Ctx &cx, uint64_t *bar, uint32_t parity) {
-    if (mbar_wait(bar, parity, &cx.sm->abort, kTimeoutNs)) return true;
-    if (atomicExch(&cx.sm->abort, 1) == 0) report_error(cx.w->err, GDN_ERR_TIMEOUT);
+// (Scalars only: a reference to the context would force it into local memory.)
+__device__ __noinline__ bool wait_slow(int *abort, int *err, uint64_t *bar, uint32_t parity) {
+    if (mbar_wait(bar, parity, abort, kTimeoutNs)) return true;
+    if (atomicExch(abort, 1) == 0) report_error(err, GDN_ERR_TIMEOUT);
     return false;
 }
 
 __device__ __forceinline__ bool wait_or_abort(const Ctx &cx, uint64_t *bar, uint32_t parity) {
-    return mbar_try_wait(bar, parity) || wait_slow(cx, bar, parity);
+    return mbar_try_wait(bar, parity) || wait_slow(&cx.sm->abort, cx.w->err, bar, parity);
 }
 
 // Epilogue waits: every lane waits, and the warp gives up together, so the
@@ -310,39 +311,48 @@ __device__ void mma_role(const Ctx &cx) {
     constexpr uint32_t I3 = idesc_bf16_f32(128, 128, 0, 1);   // S += Ut K   (K as MN-major B)
     constexpr uint32_t I4 = idesc_bf16_f32(128, 64, 0, 0);    // P_Q (or D4) += W4 Qm^T
     bool ok = true;
+    // The whole warp runs this loop (so the warp-uniform descriptors can live in
+    // uniform registers); one elected lane issues the MMAs and their commits.
+    const bool leader = elect_one();
     // P0 of a chunk: [K;Q] K^T into the U' columns (Q K^T in lanes 64-127)
     auto issue_p0 = [&](uint32_t n, bool out) -> bool {
         const int s = stage_of(n);
         if (!wait_or_abort(cx, &sm.full[s], use_parity(n))) return false;
         tc_fence_after();
-        if (out) {
-            const uint64_t dKQ = smem_desc_sw128(smem0 + s * kStageBytes, 16, 1024);
+        const uint64_t dKQ = smem_desc_sw128(smem0 + s * kStageBytes, 16, 1024);
+        if (leader) {
+            if (out) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t a = dKQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                mma_ss(t + kColU, a, a, I0, kk > 0);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t a = dKQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                    mma_ss(t + kColU, a, a, I0, kk > 0);
+                }
             }
+            tc_commit(&sm.p0);
         }
-        tc_commit(&sm.p0);
+        __syncwarp();
         return true;
     };
     // MMA4 of chunk m: P_Q += W4 Qm^T (exact form: D4 = W4 Qm^T into the other buffer)
     auto issue_mma4 = [&](uint32_t m, bool out, bool exact) -> bool {
         if (!wait_or_abort(cx, &sm.e4, m & 1)) return false;
         tc_fence_after();
-        if (out) {
-            const uint32_t pc = t + kColP + (m & 1) * 128, po = t + kColP + ((m + 1) & 1) * 128;
-            const uint64_t dQM = smem_desc_sw128(smem0 + kOffQM + (m & 1) * 8192, 16, 1024);
+        const uint32_t pc = t + kColP + (m & 1) * 128, po = t + kColP + ((m + 1) & 1) * 128;
+        const uint64_t dQM = smem_desc_sw128(smem0 + kOffQM + (m & 1) * 8192, 16, 1024);
+        if (leader) {
+            if (out) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t b = dQM + ((kk * 32) >> 4);
-                if (exact)
-                    mma_ts(po, pc + 16 + 8 * kk, b, I4, kk > 0);
-                else
-                    mma_ts(pc + 64, pc + 16 + 8 * kk, b, I4, 1);
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t b = dQM + ((kk * 32) >> 4);
+                    if (exact)
+                        mma_ts(po, pc + 16 + 8 * kk, b, I4, kk > 0);
+                    else
+                        mma_ts(pc + 64, pc + 16 + 8 * kk, b, I4, 1);
+                }
             }
+            tc_commit(&sm.m4x[m & 1]);
         }
-        tc_commit(&sm.m4x[m & 1]);
+        __syncwarp();
         return true;
     };
 
@@ -369,32 +379,43 @@ __device__ void mma_role(const Ctx &cx) {
         if (prev_exact && !wait_or_abort(cx, &sm.oepi[(n - 1) & 1], ((n - 1) >> 1) & 1)) break;
         if (!wait_or_abort(cx, &sm.e1, par)) break;
         tc_fence_after();
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_ts(pc, t + kColS16 + 8 * kk, dKQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), I1, kk > 0);
-        tc_commit(&sm.m1);
+            for (int kk = 0; kk < 8; ++kk)
+                mma_ts(pc, t + kColS16 + 8 * kk, dKQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), I1, kk > 0);
+            tc_commit(&sm.m1);
+        }
+        __syncwarp();
         if (pend4 && !issue_mma4(n - 1, pend4_out, false)) break;
         pend4 = false;
         // V term of U' once Q K^T has left the U' columns
         if (!wait_or_abort(cx, &sm.qm, par)) break;
         tc_fence_after();
-        if (!zero_v) {
+        if (leader && !zero_v) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_ss(t + kColU, dV + ((kk * 2048) >> 4), dT1 + ((kk * 32) >> 4), I2a, kk > 0);
         }
+        __syncwarp();
         if (!wait_or_abort(cx, &sm.e2, par)) break;
         tc_fence_after();
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_ts(t + kColU, pc + 16 + 8 * kk, dT1 + ((kk * 32) >> 4), I2b, (kk > 0 || !zero_v) ? 1u : 0u);
-        tc_commit(&sm.m2);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ts(t + kColU, pc + 16 + 8 * kk, dT1 + ((kk * 32) >> 4), I2b, (kk > 0 || !zero_v) ? 1u : 0u);
+            tc_commit(&sm.m2);
+        }
+        __syncwarp();
         if (!wait_or_abort(cx, &sm.e3, par)) break;
         tc_fence_after();
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ts(t + kColS32, t + kColU + 16 + 8 * kk, dK3 + ((kk * 2048) >> 4), I3, 1);
-        tc_commit(&sm.m3);
-        tc_commit(&sm.empty[s]);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ts(t + kColS32, t + kColU + 16 + 8 * kk, dK3 + ((kk * 2048) >> 4), I3, 1);
+            tc_commit(&sm.m3);
+            tc_commit(&sm.empty[s]);
+        }
+        __syncwarp();
         if (out && exact) {
             if (!issue_mma4(n, true, true)) break;
         } else {
@@ -408,7 +429,8 @@ __device__ void mma_role(const Ctx &cx) {
     }
     if (pend4) issue_mma4(n - 1, pend4_out, false);
     // all issued MMAs must finish before TMEM is released
-    tc_commit(&sm.fin);
+    if (leader) tc_commit(&sm.fin);
+    __syncwarp();
     int dummy = 0;
     mbar_wait(&sm.fin, 0, &dummy, kTimeoutNs);
 }
@@ -428,7 +450,7 @@ __device__ __forceinline__ void load_tile32(const Ctx &cx, const EpiThread &e, u
 }
 
 // Stores 32 state columns j0 .. j0+31 (key index) of this thread's value row.
-__device__ __noinline__ void write_state32(const Ctx &cx, const EpiThread &e, const gdn_work_item &it, int j0,
+__device__ __noinline__ void write_state32(const Ctx cx, const EpiThread e, const gdn_work_item it, int j0,
                                            const float *sv) {
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
@@ -444,7 +466,7 @@ __device__ __noinline__ void write_state32(const Ctx &cx, const EpiThread &e, co
 }
 
 // Loads 32 start-state columns j0 .. j0+31 of this thread's value row.
-__device__ __noinline__ void load_start_state32(const Ctx &cx, const EpiThread &e, const gdn_work_item &it, int j0,
+__device__ __noinline__ void load_start_state32(const Ctx cx, const EpiThread e, const gdn_work_item it, int j0,
                                                 float *sv) {
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
@@ -465,7 +487,7 @@ __device__ __noinline__ void load_start_state32(const Ctx &cx, const EpiThread &
 }
 
 // Writes the state held in TMEM (this thread's row, its 64 columns) for `it`.
-__device__ __noinline__ void flush_state(const Ctx &cx, const EpiThread &e, const gdn_work_item &it) {
+__device__ __noinline__ void flush_state(const Ctx cx, const EpiThread e, const gdn_work_item it) {
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
         float sv[32];
@@ -650,7 +672,7 @@ __device__ __forceinline__ void side_qmask(const Ctx &cx, const EpiThread &e, in
 }
 
 // The same with Gamma applied element by element (exact form).
-__device__ __noinline__ void side_qmask_exact(const Ctx &cx, const EpiThread &e, const Coef &cf, int len,
+__device__ __noinline__ void side_qmask_exact(const Ctx cx, const EpiThread e, const Coef &cf, int len,
                                               uint8_t *qm_tile) {
     const int r = e.i - 64;
 #pragma unroll 1
@@ -853,8 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         producer_role(cx, maps, lane);
     } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_role(cx);
-        __syncwarp();
+        mma_role(cx);
     } else if (warp < 8) {
         chain_role(cx, warp, lane);
     } else {
