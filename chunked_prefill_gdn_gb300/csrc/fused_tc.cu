@@ -569,19 +569,33 @@ __device__ void chain_role(const Ctx &cx, int warp, int lane) {
                     load_start_state32(cx, e, it, 64 * ch + 32 * hh, sv);
                     store_state32(cx, e, hh, sv, gC);
                 }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sm.e1);
             } else {
+                // MMA1 needs only bf16(S): arrive as soon as it is in TMEM, then
+                // scale the fp32 state by gamma_C under MMA1 (MMA3, its next
+                // writer, is issued only after this warp's e3 below)
                 if (!ewait(cx, &sm.m3, (n - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    float sv[32];
-                    load_tile32(cx, e, kColS32 + 64 * ch + 32 * hh, sv);
-                    store_state32(cx, e, hh, sv, gC);
+                {
+                    uint32_t sv[64], pk[32];
+                    tmem_ld32(cx.tbase + e.lane_base + kColS32 + 64 * ch, sv);
+                    tmem_ld32(cx.tbase + e.lane_base + kColS32 + 64 * ch + 32, sv + 32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        pk[j] = pack_bf16x2(__uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]));
+                    tmem_st32(cx.tbase + e.lane_base + kColS16 + 32 * ch, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&sm.e1);
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) sv[j] = __float_as_uint(gC * __uint_as_float(sv[j]));
+                    tmem_st32(cx.tbase + e.lane_base + kColS32 + 64 * ch, sv);
+                    tmem_st32(cx.tbase + e.lane_base + kColS32 + 64 * ch + 32, sv + 32);
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&sm.e1);
 
             // ---- E2: W2 = -gamma P_K   (after MMA1; it multiplies T1 = T' D_c1, and c2 = c1 gamma)
             if (!ewait(cx, &sm.m1, par)) { ok = false; break; }

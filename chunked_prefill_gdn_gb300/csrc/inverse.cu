@@ -280,59 +280,63 @@ __global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid
     const uint32_t tbase = b.tmem_base;
 
     if (warp == kInvConv + kInvSolvers) {
-        // ---------------- TMA producer + MMA issuer (one thread)
-        if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 128, 0, 0);
-            PairInfo pi_next = pair_info(p, w, blockIdx.x);   // info of the next pair to load
-            auto load = [&](int i) -> bool {
-                const int st = i % kInvKStages;
-                const uint32_t use = i / kInvKStages;
-                if (!inv_wait(b, &b.kempty[st], (use & 1) ^ 1, w.err)) return false;
-                const PairInfo pi = pi_next;
-                if (i + 1 < n_local) pi_next = pair_info(p, w, blockIdx.x + (i + 1) * gridDim.x);
-                uint8_t *kt = smem + st * kInvPairBytes;
+        // ---------------- TMA producer + MMA issuer: the whole warp runs the loop
+        // (warp-uniform descriptors), one elected lane issues copies and MMAs
+        const bool leader = tc::elect_one();
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 128, 0, 0);
+        PairInfo pi_next = pair_info(p, w, blockIdx.x);   // info of the next pair to load
+        auto load = [&](int i) -> bool {
+            const int st = i % kInvKStages;
+            const uint32_t use = i / kInvKStages;
+            if (!inv_wait(b, &b.kempty[st], (use & 1) ^ 1, w.err)) return false;
+            const PairInfo pi = pi_next;
+            if (i + 1 < n_local) pi_next = pair_info(p, w, blockIdx.x + (i + 1) * gridDim.x);
+            uint8_t *kt = smem + st * kInvPairBytes;
+            if (leader) {
                 tc::mbar_arrive_expect_tx(&b.kfull[st], kInvPairBytes);
                 tc::tma_load_3d(kt + 0, &maps.k, &b.kfull[st], 0, pi.h0, pi.t0);
                 tc::tma_load_3d(kt + 8192, &maps.k, &b.kfull[st], 0, pi.h1, pi.t0);
                 tc::tma_load_3d(kt + 16384, &maps.k, &b.kfull[st], 64, pi.h0, pi.t0);
                 tc::tma_load_3d(kt + 24576, &maps.k, &b.kfull[st], 64, pi.h1, pi.t0);
-                return true;
-            };
-            bool ok = true;
-            int issued = 0, consumed = 0, mmas = 0;
-            for (; issued < n_local && issued < kInvKStages - 1 && ok; ++issued) ok = load(issued);
-            if (!ok) --issued;
-            for (int i = 0; i < n_local && ok; ++i) {
-                if (issued < n_local) {
-                    if (!load(issued)) break;
-                    ++issued;
-                }
-                const int st = i % kInvKStages, tb = i & 1;
-                if (!inv_wait(b, &b.kfull[st], (i / kInvKStages) & 1, w.err)) break;
-                ++consumed;
-                if (!inv_wait(b, &b.tempty[tb], ((i >> 1) & 1) ^ 1, w.err)) break;
-                tc::tc_fence_after();
-                const uint32_t kb = tc::smem_u32(smem + st * kInvPairBytes);
+            }
+            __syncwarp();
+            return true;
+        };
+        bool ok = true;
+        int issued = 0, consumed = 0, mmas = 0;
+        for (; issued < n_local && issued < kInvKStages - 1 && ok; ++issued) ok = load(issued);
+        if (!ok) --issued;
+        for (int i = 0; i < n_local && ok; ++i) {
+            if (issued < n_local) {
+                if (!load(issued)) break;
+                ++issued;
+            }
+            const int st = i % kInvKStages, tb = i & 1;
+            if (!inv_wait(b, &b.kfull[st], (i / kInvKStages) & 1, w.err)) break;
+            ++consumed;
+            if (!inv_wait(b, &b.tempty[tb], ((i >> 1) & 1) ^ 1, w.err)) break;
+            tc::tc_fence_after();
+            const uint64_t d0 = tc::smem_desc_sw128(tc::smem_u32(smem + st * kInvPairBytes), 16, 1024);
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t d = tc::smem_desc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t d = d0 + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
                     tc::mma_ss(tbase + tb * 128, d, d, idesc, kk > 0);
                 }
                 tc::tc_commit(&b.tfull[tb]);
                 tc::tc_commit(&b.kempty[st]);
-                ++mmas;
             }
-            // After an abort: no copy may land and no MMA may run once the CTA
-            // is gone.  Loads [consumed, issued) are each the latest use of their
-            // stage and the last MMA the latest phase of its buffer, so their
-            // parities are current.  (Waits are bounded; the abort flag is not
-            // consulted here.)
-            int never = 0;
-            for (int i = consumed; i < issued; ++i)
-                tc::mbar_wait(&b.kfull[i % kInvKStages], (i / kInvKStages) & 1, &never, kInvTimeoutNs);
-            if (mmas > 0)
-                tc::mbar_wait(&b.tfull[(mmas - 1) & 1], ((mmas - 1) >> 1) & 1, &never, kInvTimeoutNs);
+            __syncwarp();
+            ++mmas;
         }
+        // After an abort: no copy may land and no MMA may run once the CTA is
+        // gone.  Loads [consumed, issued) are each the latest use of their stage
+        // and the last MMA the latest phase of its buffer, so their parities are
+        // current.  (Waits are bounded; the abort flag is not consulted here.)
+        int never = 0;
+        for (int i = consumed; i < issued; ++i)
+            tc::mbar_wait(&b.kfull[i % kInvKStages], (i / kInvKStages) & 1, &never, kInvTimeoutNs);
+        if (mmas > 0) tc::mbar_wait(&b.tfull[(mmas - 1) & 1], ((mmas - 1) >> 1) & 1, &never, kInvTimeoutNs);
     } else if (warp < kInvConv) {
         // ---------------- converters: TMEM Gram rows -> packed A' rows
         const int half = warp >> 1;                 // unit 0 or 1 of the pair
