@@ -115,6 +115,21 @@ def dist_env():
     return ws, rank, local
 
 
+def replica_throughput(total_ms, steps, tokens_per_rank, dist=None, device="cpu"):
+    """Whole-job throughput of N independent replicas: the job's time is the
+    slowest rank's (max over ranks), and every rank processed tokens_per_rank.
+    Returns (ms per step, tokens/s of the whole job)."""
+    import torch
+    ws = 1
+    if dist is not None:
+        ws = dist.get_world_size()
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / steps
+    return ms_per_step, tokens_per_rank * ws / (ms_per_step * 1e-3)
+
+
 def reference_arm(args, cfg):
     """The fp64 oracle on the host cores, on a bounded sample of the workload."""
     ws, rank, _ = dist_env()
@@ -283,14 +298,7 @@ def main():
         if dist is not None:
             dist.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    tokens = cfg.total_tokens
-    value = tokens * ws / (ms_per_step * 1e-3)
+    ms_per_step, value = replica_throughput(sum(step_ms), args.steps, cfg.total_tokens, dist, dev)
 
     peaks, peak_src = load_peaks()
     nbytes, flops, per_th = algorithmic_work(cfg)

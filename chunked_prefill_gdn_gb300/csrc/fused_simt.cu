@@ -23,6 +23,7 @@ int fused_simt_smem_bytes(int dk, int dv) {
 }
 
 __global__ void __launch_bounds__(256, 1) fused_simt_kernel(Problem p, Workspace w, int pass) {
+    grid_dependency_wait();
     extern __shared__ float smem[];
     __shared__ int s_item;
     const int tid = threadIdx.x, nthr = blockDim.x;
@@ -169,7 +170,8 @@ cudaError_t launch_fused_simt(const Problem &p, const Workspace &w, int pass, in
     const int smem = fused_simt_smem_bytes(p.dk, p.dv);
     cudaError_t e = cudaFuncSetAttribute(fused_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    fused_simt_kernel<<<grid, 256, smem, s>>>(p, w, pass);
+    e = launch_dependent(fused_simt_kernel, dim3(grid), dim3(256), (size_t)smem, s, p, w, pass);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

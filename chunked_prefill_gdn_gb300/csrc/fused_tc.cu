@@ -152,7 +152,7 @@ __device__ __forceinline__ int stage_of(uint32_t n) { return static_cast<int>(n 
 __device__ __forceinline__ uint32_t use_parity(uint32_t n) { return (n / kStages) & 1u; }
 
 // ---------------------------------------------------------------- producer
-__device__ void producer_role(const Ctx &cx, const TcMaps &maps, int lane) {
+__device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps, int lane) {
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
     Small &sm = *cx.sm;
@@ -300,7 +300,7 @@ __device__ __forceinline__ void cursor_next(const Ctx &cx, MmaCursor &cu) {
 //   stage free | P0_{n+1}
 // A chunk in the exact form issues its MMA4 right after MMA3 instead (its D4
 // goes to the other P buffer, which MMA1_{n+1} then waits to see emptied).
-__device__ void mma_role(const Ctx &cx) {
+__device__ __forceinline__ void mma_role(const Ctx &cx) {
     Small &sm = *cx.sm;
     const uint32_t t = cx.tbase;
     const uint32_t smem0 = smem_u32(cx.smem);
@@ -509,7 +509,7 @@ __device__ __forceinline__ void store_state32(const Ctx &cx, const EpiThread &e,
 }
 
 // ---- the state chain: warps 0-7; warps w and w+4 share lane quadrant w % 4
-__device__ void chain_role(const Ctx &cx, int warp, int lane) {
+__device__ __forceinline__ void chain_role(const Ctx &cx, int warp, int lane) {
     const Workspace &w = *cx.w;
     Small &sm = *cx.sm;
     EpiThread e;
@@ -722,7 +722,7 @@ __device__ __forceinline__ void add_d4(const Ctx &cx, const EpiThread &e, uint32
 // holds the intra-chunk term); exact form o = scale (gamma_r P_Q + D4).  Side
 // warps, lane = value row i, all 64 tokens; each store of a warp covers 64
 // contiguous bytes of one token's row of o.
-__device__ void output_chunk(const Ctx &cx, const EpiThread &e, int s, bool exact, uint32_t pq_col,
+__device__ __forceinline__ void output_chunk(const Ctx &cx, const EpiThread &e, int s, bool exact, uint32_t pq_col,
                              uint32_t d4_col, int t0, int len, int h) {
     const Problem &p = *cx.p;
     const size_t rs = (size_t)p.H * kD;
@@ -755,7 +755,7 @@ __device__ void output_chunk(const Ctx &cx, const EpiThread &e, int s, bool exac
 }
 
 // ---- off the chain: warps 8-11 (lane quadrant w % 4)
-__device__ void side_role(const Ctx &cx, int warp, int lane) {
+__device__ __forceinline__ void side_role(const Ctx &cx, int warp, int lane) {
     const Workspace &w = *cx.w;
     Small &sm = *cx.sm;
     EpiThread e;
@@ -835,6 +835,7 @@ __device__ void side_role(const Ctx &cx, int warp, int lane) {
 // 16384 / (4 * 32) = 128 registers.
 __global__ void __launch_bounds__(kThreads, 1)
     fused_tc_kernel(const __grid_constant__ TcMaps maps, const Problem p, const Workspace w, const int pass) {
+    grid_dependency_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Small &sm = *reinterpret_cast<Small *>(smem + kOffSmall);
@@ -966,7 +967,8 @@ cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int 
     }
     cudaError_t e = cudaFuncSetAttribute(fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    fused_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(maps, p, w, pass);
+    e = launch_dependent(fused_tc_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, p, w, pass);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

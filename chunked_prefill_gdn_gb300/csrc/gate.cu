@@ -22,6 +22,7 @@ namespace gdn {
 // the chunk table, zero the counters and head flags.  One CTA.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) seqprep_kernel(Problem p, Workspace w) {
+    grid_dependency_wait();
     __shared__ int s_bad;
     __shared__ int s_carry;
     __shared__ int s_warp[32];
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(1024) seqprep_kernel(Problem p, Workspace w) {
 constexpr int kGateHeads = 64;
 
 __global__ void __launch_bounds__(256) gate_kernel(Problem p, Workspace w) {
+    grid_dependency_wait();
     __shared__ float tile[kChunk][kGateHeads + 1];
     __shared__ int s_nz[kGateHeads];
     const int cid = blockIdx.x;
@@ -127,19 +129,24 @@ __global__ void __launch_bounds__(256) gate_kernel(Problem p, Workspace w) {
         tile[r][hh] = r < len ? p.g[(size_t)(t0 + r) * p.H + h0 + hh] : 0.f;
     }
     __syncthreads();
-    for (int hh = threadIdx.x; hh < nh; hh += blockDim.x) {
-        float acc = 0.f;
-        int nz = 0;
-        for (int r = 0; r < len; ++r) {
-            float x = tile[r][hh];
-            nz |= (x != 0.f);
-            acc += x;
-            tile[r][hh] = acc;
+    // one warp per head: lane l holds rows 2l and 2l+1; a shuffle scan of the
+    // pair sums gives the inclusive cumsum (rows past the end are zero in the
+    // tile, so they keep the last cumsum)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int hh = warp; hh < nh; hh += blockDim.x >> 5) {
+        const float x0 = tile[2 * lane][hh], x1 = tile[2 * lane + 1][hh];
+        float incl = x0 + x1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
         }
-        // rows past the end keep the last cumsum (they never contribute)
-        for (int r = len; r < kChunk; ++r) tile[r][hh] = acc;
-        w.totals[(size_t)(h0 + hh) * w.max_chunks + cid] = acc;
-        s_nz[hh] = nz;
+        const float excl = incl - (x0 + x1);
+        tile[2 * lane][hh] = excl + x0;
+        tile[2 * lane + 1][hh] = incl;
+        const bool nz = __any_sync(0xffffffffu, x0 != 0.f || x1 != 0.f);
+        if (lane == 31) w.totals[(size_t)(h0 + hh) * w.max_chunks + cid] = incl;
+        if (lane == 0) s_nz[hh] = nz;
     }
     __syncthreads();
     for (int hh = threadIdx.x; hh < nh; hh += blockDim.x)
@@ -198,6 +205,7 @@ __device__ int lookback_window(const Workspace &w, int h, int chunk0, int c_begi
 constexpr int kMaxLookbackChunks = 256;
 
 __global__ void __launch_bounds__(1024) plan_kernel(Problem p, Workspace w, PlanParams pp) {
+    grid_dependency_wait();
     __shared__ int s_warp[32];
     __shared__ int s_tot[4];
     __shared__ int s_base[4];
@@ -315,12 +323,14 @@ cudaError_t launch_seqprep(const Problem &p, const Workspace &w, cudaStream_t s)
 
 cudaError_t launch_gate(const Problem &p, const Workspace &w, cudaStream_t s) {
     dim3 grid(w.max_chunks, (p.H + kGateHeads - 1) / kGateHeads);
-    gate_kernel<<<grid, 256, 0, s>>>(p, w);
+    cudaError_t e = launch_dependent(gate_kernel, grid, dim3(256), 0, s, p, w);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &pp, cudaStream_t s) {
-    plan_kernel<<<1, 1024, 0, s>>>(p, w, pp);
+    cudaError_t e = launch_dependent(plan_kernel, dim3(1), dim3(1024), 0, s, p, w, pp);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -90,6 +90,29 @@ __device__ __forceinline__ void finish_queue(int *item_counter, int *exit_counte
     }
 }
 
+// Programmatic dependent launch: every kernel of the path after the first is
+// launched with programmatic stream serialisation, so its launch overlaps the
+// end of the previous kernel; each kernel starts with grid_dependency_wait(),
+// which returns once the previous grid has completed and its memory is
+// visible (and at once when there is no such dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Records `code` in the error word unless one is already recorded.
 __device__ __forceinline__ void report_error(int *err, int code) { atomicCAS(err, 0, code); }
 

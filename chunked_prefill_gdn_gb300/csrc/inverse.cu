@@ -23,6 +23,7 @@ namespace gdn {
 // solves one column of (I + A') X = I by forward substitution; the columns are
 // independent, so the substitution needs no barrier.
 __global__ void __launch_bounds__(128) inverse_simt_kernel(Problem p, Workspace w) {
+    grid_dependency_wait();
     extern __shared__ float smem[];
     __shared__ float sb[kChunk];
     const int cid = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -247,6 +248,7 @@ __device__ __forceinline__ PairInfo pair_info(const Problem &p, const Workspace 
 
 __global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid_constant__ InvMaps maps, Problem p,
                                                                      Workspace w, int gate_scaled) {
+    grid_dependency_wait();
     extern __shared__ uint8_t inv_smem_raw[];
     uint8_t *smem =
         reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(inv_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -556,7 +558,8 @@ cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, int gate_sca
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const long long pairs = (long long)w.max_chunks * ((p.H + 1) / 2);
     const int grid = (int)std::max(1LL, std::min<long long>(sms, pairs));
-    inverse_tc_kernel<<<grid, kInvThreads, kInvSmem, s>>>(maps, p, w, gate_scaled);
+    e = launch_dependent(inverse_tc_kernel, dim3(grid), dim3(kInvThreads), kInvSmem, s, maps, p, w, gate_scaled);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -568,7 +571,8 @@ cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cu
     cudaError_t e = cudaFuncSetAttribute(inverse_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(w.max_chunks, p.H);
-    inverse_simt_kernel<<<grid, 128, smem, s>>>(p, w);
+    e = launch_dependent(inverse_simt_kernel, grid, dim3(128), (size_t)smem, s, p, w);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

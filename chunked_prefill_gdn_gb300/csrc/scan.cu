@@ -20,6 +20,7 @@ namespace gdn {
 constexpr int kScanCols = 16;
 
 __global__ void __launch_bounds__(256) scan_kernel(Problem p, Workspace w) {
+    grid_dependency_wait();
     __shared__ float X[128][kScanCols + 1];
     const int u = blockIdx.x;
     if (u >= w.num_items[2]) return;
@@ -68,7 +69,8 @@ __global__ void __launch_bounds__(256) scan_kernel(Problem p, Workspace w) {
 cudaError_t launch_scan(const Problem &p, const Workspace &w, cudaStream_t s) {
     if (w.max_cp_slots <= 0) return cudaSuccess;
     dim3 grid(w.max_cp_slots, (p.dv + kScanCols - 1) / kScanCols);
-    scan_kernel<<<grid, 256, 0, s>>>(p, w);
+    cudaError_t e = launch_dependent(scan_kernel, grid, dim3(256), 0, s, p, w);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
