@@ -137,16 +137,8 @@ __device__ __forceinline__ uint64_t dup2(float x) {
 __device__ __forceinline__ void fma2(uint64_t &acc, uint64_t a, uint64_t b) {
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
-__device__ __forceinline__ float lo2(uint64_t v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return lo;
-}
-__device__ __forceinline__ float hi2(uint64_t v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return hi;
-}
+__device__ __forceinline__ float lo2(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi2(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
 
 // Column `col` of (I + A') X = I for rows 16*I0 .. 63 (I0 = 0 or 2), given
 // x_r = 0 for r < 16*I0.  A' is stored as column-major 16 x 16 blocks, so one
