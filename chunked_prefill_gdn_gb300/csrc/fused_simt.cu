@@ -22,7 +22,7 @@ int fused_simt_smem_bytes(int dk, int dv) {
     return floats * (int)sizeof(float);
 }
 
-__global__ void __launch_bounds__(256, 1) fused_simt_kernel(Problem p, Workspace w, int pass) {
+__global__ void __launch_bounds__(256, 1) fused_simt_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w, int pass) {
     grid_dependency_wait();
     extern __shared__ float smem[];
     __shared__ int s_item;

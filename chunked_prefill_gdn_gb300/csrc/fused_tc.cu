@@ -834,7 +834,8 @@ __device__ __forceinline__ void side_role(const Ctx &cx, int warp, int lane) {
 // 14 warps share the 4 SM sub-partitions 4/4/3/3, so a thread may hold at most
 // 16384 / (4 * 32) = 128 registers.
 __global__ void __launch_bounds__(kThreads, 1)
-    fused_tc_kernel(const __grid_constant__ TcMaps maps, const Problem p, const Workspace w, const int pass) {
+    fused_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Problem p,
+                    const __grid_constant__ Workspace w, const int pass) {
     grid_dependency_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

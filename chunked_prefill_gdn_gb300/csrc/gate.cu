@@ -21,7 +21,7 @@ namespace gdn {
 // Sequence preparation: validate cu_seqlens, build the per-sequence table and
 // the chunk table, zero the counters and head flags.  One CTA.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) seqprep_kernel(Problem p, Workspace w) {
+__global__ void __launch_bounds__(1024) seqprep_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w) {
     grid_dependency_wait();
     __shared__ int s_bad;
     __shared__ int s_carry;
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(1024) seqprep_kernel(Problem p, Workspace w) {
 // ---------------------------------------------------------------------------
 constexpr int kGateHeads = 64;
 
-__global__ void __launch_bounds__(256) gate_kernel(Problem p, Workspace w) {
+__global__ void __launch_bounds__(256) gate_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w) {
     grid_dependency_wait();
     __shared__ float tile[kChunk][kGateHeads + 1];
     __shared__ int s_nz[kGateHeads];
@@ -204,7 +204,7 @@ __device__ int lookback_window(const Workspace &w, int h, int chunk0, int c_begi
 
 constexpr int kMaxLookbackChunks = 256;
 
-__global__ void __launch_bounds__(1024) plan_kernel(Problem p, Workspace w, PlanParams pp) {
+__global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w, const __grid_constant__ PlanParams pp) {
     grid_dependency_wait();
     __shared__ int s_warp[32];
     __shared__ int s_tot[4];

@@ -22,7 +22,7 @@ namespace gdn {
 // One CTA per (chunk, head).  K K^T on CUDA cores, then each of 64 threads
 // solves one column of (I + A') X = I by forward substitution; the columns are
 // independent, so the substitution needs no barrier.
-__global__ void __launch_bounds__(128) inverse_simt_kernel(Problem p, Workspace w) {
+__global__ void __launch_bounds__(128) inverse_simt_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w) {
     grid_dependency_wait();
     extern __shared__ float smem[];
     __shared__ float sb[kChunk];
@@ -238,8 +238,8 @@ __device__ __forceinline__ PairInfo pair_info(const Problem &p, const Workspace 
     return pi;
 }
 
-__global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid_constant__ InvMaps maps, Problem p,
-                                                                     Workspace w, int gate_scaled) {
+__global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid_constant__ InvMaps maps, const __grid_constant__ Problem p,
+                                                                     const __grid_constant__ Workspace w, int gate_scaled) {
     grid_dependency_wait();
     extern __shared__ uint8_t inv_smem_raw[];
     uint8_t *smem =

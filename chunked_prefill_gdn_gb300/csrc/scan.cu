@@ -19,7 +19,7 @@ namespace gdn {
 
 constexpr int kScanCols = 16;
 
-__global__ void __launch_bounds__(256) scan_kernel(Problem p, Workspace w) {
+__global__ void __launch_bounds__(256) scan_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w) {
     grid_dependency_wait();
     __shared__ float X[128][kScanCols + 1];
     const int u = blockIdx.x;
