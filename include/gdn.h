@@ -126,7 +126,11 @@ typedef struct {
     size_t gate_cumsum;    /* fp32 [H, total_T]: chunk-local inclusive cumsum of g */
     size_t chunk_totals;   /* fp32 [H, max_chunks]: sum of g per chunk (chunks in sequence order) */
     size_t head_flags;     /* int32 [N, H]: 1 when some g != 0 (alpha not identically 1) */
-    size_t tprime;         /* [H, total_T, 64] T' rows by token; bf16 for bf16 inputs, fp32 for fp32 */
+    size_t tprime;         /* [H, total_T, 64] T' rows by token; bf16 for bf16 inputs, fp32 for fp32.
+                              When the tcgen05 fused kernel runs (bf16, dk = dv = 128) this holds
+                              T' diag(c1) instead, c1_m = exp(G* - G_m) beta_m with G* the middle of
+                              the chunk's gate cumsum range, or (Gamma ⊙ T') diag(beta) for a chunk
+                              whose last cumsum is below -80 */
     size_t chunk_table;    /* int32x4 [max_chunks]: (seq, first token, length, chunk index in seq) */
     size_t num_chunks;     /* int32: chunks actually present */
     size_t items;          /* int32x8 [max_items]: fused-kernel work items (see gdn_work_item) */
