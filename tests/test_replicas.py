@@ -19,24 +19,24 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _rank(rank, port, out):
+def _rank(rank, port, outdir):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=2)
     try:
         # rank 1 is the slow one: 30 ms over 3 steps
         ms, value = bench.replica_throughput(15.0 if rank == 0 else 30.0, 3, 1000, dist, "cpu")
-        out[rank] = (ms, value)
+        with open(os.path.join(outdir, "rank%d" % rank), "w") as f:
+            f.write("%r %r" % (ms, value))
     finally:
         dist.destroy_process_group()
 
 
-def test_replica_timing_is_max_over_ranks():
+def test_replica_timing_is_max_over_ranks(tmp_path):
     port = _free_port()
-    out = mp.Manager().dict()
-    mp.spawn(_rank, args=(port, out), nprocs=2, join=True)
+    mp.spawn(_rank, args=(port, str(tmp_path)), nprocs=2, join=True)
     for rank in (0, 1):
-        ms, value = out[rank]
+        ms, value = map(float, open(tmp_path / ("rank%d" % rank)).read().split())
         assert ms == pytest.approx(10.0)
         assert value == pytest.approx(2 * 1000 / 10e-3)
 
