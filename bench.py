@@ -208,6 +208,7 @@ def main():
     ap.add_argument("--cp", default="auto", choices=["auto", "off", "force"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-qk-l2norm", action="store_true", help="skip timing the optional q/k normalisation pass")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-heads", type=int, default=2, help="heads per reference-arm step")
     ap.add_argument("--override", action="append", default=[],
@@ -338,6 +339,8 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    if not args.no_qk_l2norm:
+        result["qk_l2norm"] = qk_l2norm_measure(gdn, torch, q, k, flush, stream, peaks, peak_src)
     if not args.no_e2e:
         result["e2e"] = e2e_measure(gdn, torch, inp, cfg, opts, dev, args)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -363,6 +366,30 @@ def kernel_source_sha(kname):
     path = os.path.join(ROOT, "chunked_prefill_gdn_gb300", "csrc", "fused_tc.cu" if kname == "tc" else "fused_simt.cu")
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def qk_l2norm_measure(gdn, torch, q, k, flush, stream, peaks, peak_src, iters=10):
+    """The optional q/k L2 normalisation pass (opts.qk_l2norm; not part of the
+    timed step, whose inputs arrive normalised) timed alone on this workload's
+    q and k: CUDA events around each launch, L2 flushed before each one.
+    Algorithmic bytes: q and k read once and written once."""
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    for _ in range(3):
+        gdn.qk_l2norm(q, k, qo, ko, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for i, (a, b) in enumerate(evs):
+        flush.fill_((i + 7) & 0xFF)
+        a.record(stream)
+        gdn.qk_l2norm(q, k, qo, ko, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(q.device)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    nbytes = 2 * (q.numel() + k.numel()) * q.element_size()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "qk_l2norm_kernel (gdn_qk_l2norm)", "bound": "hbm", "kernel_ms": ms,
+            "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "alg_bytes_per_launch": nbytes, "launches": iters, "peak_source": peak_src,
+            "note": "optional step in front of the path (opts.qk_l2norm = 1); not inside the timed step"}
 
 
 def e2e_measure(gdn, torch, inp, cfg, opts, dev, args):

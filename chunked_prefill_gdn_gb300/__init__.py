@@ -27,7 +27,7 @@ __all__ = [
     "load_library", "library_path", "default_options",
     "gdn_default_options", "gdn_plan_query", "gdn_chunk_fwd_workspace_size", "gdn_workspace_query",
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
-    "gdn_chunk_fwd_static",
+    "gdn_chunk_fwd_static", "gdn_qk_l2norm", "qk_l2norm",
     "gdn_status_string", "gdn_version", "gdn_last_error_detail", "chunk_fwd", "chunk_fwd_host", "workspace_for", "GdnError",
     "CP_AUTO", "CP_OFF", "CP_FORCE", "KERNEL_AUTO", "KERNEL_TC", "KERNEL_SIMT", "BF16", "F32",
     "STAGE_PREP", "STAGE_INVERSE", "STAGE_CORRECTION", "STAGE_FUSED",
@@ -57,7 +57,7 @@ class GdnOptions(ctypes.Structure):
                 ("sw_eps", ctypes.c_float), ("sm_count", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("debug_checks", ctypes.c_int32),
                 ("prof_begin", ctypes.c_void_p), ("prof_end", ctypes.c_void_p),
-                ("reserved", ctypes.c_int32 * 4)]
+                ("qk_l2norm", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 class GdnPlanInfo(ctypes.Structure):
@@ -117,6 +117,8 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_chunk_fwd_host.restype = i32
     lib.gdn_chunk_fwd_static.argtypes = fwd_args[:17] + [vp, opt, vp]
     lib.gdn_chunk_fwd_static.restype = i32
+    lib.gdn_qk_l2norm.argtypes = [vp, vp, vp, vp, ctypes.c_int64, i32, i32, ctypes.c_float, vp]
+    lib.gdn_qk_l2norm.restype = i32
     lib.gdn_status_string.argtypes = [i32]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_version.argtypes = []
@@ -186,6 +188,10 @@ def gdn_chunk_fwd_static(*args) -> int:
     """gdn_chunk_fwd without a workspace argument: the scratch is the library's
     fixed 64 MiB device array (for callers that must not allocate)."""
     return int(load_library().gdn_chunk_fwd_static(*args))
+
+
+def gdn_qk_l2norm(*args) -> int:
+    return int(load_library().gdn_qk_l2norm(*args))
 
 
 def gdn_status_string(status: int) -> str:
@@ -273,6 +279,32 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
         if st != 0:
             raise GdnError(st, "device check")
     return out, final_state
+
+
+def qk_l2norm(q=None, k=None, q_out=None, k_out=None, eps: float = 0.0,
+              stream: Optional[torch.cuda.Stream] = None):
+    """Unit-L2-norm rows of q and/or k ([..., dk], contiguous CUDA tensors of one
+    dtype) through gdn_qk_l2norm; returns (q_hat, k_hat) (None where not given).
+    Pass q_out=q / k_out=k to normalise in place."""
+    ref = q if q is not None else k
+    if ref is None:
+        return None, None
+    for t in (q, k):
+        if t is not None and (not t.is_cuda or not t.is_contiguous() or t.dtype != ref.dtype
+                              or t.shape != ref.shape):
+            raise ValueError("q and k must be contiguous CUDA tensors of one shape and dtype")
+    dk = ref.shape[-1]
+    rows = ref.numel() // dk
+    if q is not None and q_out is None:
+        q_out = torch.empty_like(q)
+    if k is not None and k_out is None:
+        k_out = torch.empty_like(k)
+    stream = stream if stream is not None else torch.cuda.current_stream(ref.device)
+    st = gdn_qk_l2norm(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), rows, dk, _dtype_code(ref), float(eps),
+                       ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise GdnError(st, "gdn_qk_l2norm")
+    return q_out, k_out
 
 
 def chunk_fwd_host(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,

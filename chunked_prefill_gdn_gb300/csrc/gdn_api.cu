@@ -108,6 +108,7 @@ gdn_status make_plan(int B, int T, int H, int dk, int dv, int n_seqs, int varlen
     if (varlen && (B != 1 || n_seqs < 1)) return GDN_ERR_INVALID_ARG;
     if (opts.cp_mode < GDN_CP_AUTO || opts.cp_mode > GDN_CP_FORCE) return GDN_ERR_INVALID_ARG;
     if (opts.kernel < GDN_KERNEL_AUTO || opts.kernel > GDN_KERNEL_SIMT) return GDN_ERR_INVALID_ARG;
+    if (opts.qk_l2norm != 0 && opts.qk_l2norm != 1) return GDN_ERR_INVALID_ARG;
     const int N = varlen ? n_seqs : B;
     const long long total_T = varlen ? (long long)T : (long long)B * T;
     const long long nc_seq = ((long long)T + kChunk - 1) / kChunk;
@@ -173,6 +174,10 @@ gdn_status make_plan(int B, int T, int H, int dk, int dv, int n_seqs, int varlen
     lay.seq_order = take((size_t)N * 4);
     lay.cp_s = take((size_t)lay.max_cp_slots * dk * dv * 4);
     lay.cp_m = take((size_t)lay.max_cp_slots * dk * dk * 4);
+    // normalised copies of q and k when the library normalises them
+    const size_t qk_bytes = opts.qk_l2norm ? (size_t)total_T * H * dk * (dtype == GDN_BF16 ? 2 : 4) : 0;
+    lay.qn = take(qk_bytes);
+    lay.kn = take(qk_bytes);
     lay.total = off;
     hp->kernel = kernel;
     hp->cp = cp;
@@ -320,6 +325,16 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
     const int stages = opts.stages ? opts.stages : (GDN_STAGE_PREP | GDN_STAGE_INVERSE | GDN_STAGE_CORRECTION |
                                                     GDN_STAGE_FUSED);
     cudaGetLastError();  // clear a stale error so it is not blamed on these launches
+    if (opts.qk_l2norm) {
+        // every later step reads the unit-norm copies in the workspace
+        void *qn = base + L.qn, *kn = base + L.kn;
+        if ((stages & GDN_STAGE_PREP) && hp.total_T > 0) {
+            cudaError_t e = launch_qk_l2norm(q, k, qn, kn, hp.total_T * H, dk, dtype, kQkNormEps, stream);
+            if (e != cudaSuccess) return cuda_fail("launch qk_l2norm", e);
+        }
+        p.q = qn;
+        p.k = kn;
+    }
     if (stages & GDN_STAGE_PREP) {
         cudaError_t e = launch_seqprep(p, w, stream);
         if (e != cudaSuccess) return cuda_fail("launch seqprep", e);

@@ -54,7 +54,7 @@ struct PlanParams {
 // Host-side layout of the workspace for one problem.
 struct Layout {
     size_t err, counters, num_chunks, num_items, seqinfo, chunks, flags, G, totals, tprime,
-        items2, items1, scan_units, seq_order, cp_s, cp_m, total;
+        items2, items1, scan_units, seq_order, cp_s, cp_m, qn, kn, total;
     int max_chunks, max_items, max_items1, max_cp_slots;
 };
 
@@ -71,6 +71,11 @@ cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &
 // (the gate-scaled form that kernel multiplies by) instead of T' itself
 cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s);
 cudaError_t launch_scan(const Problem &p, const Workspace &w, cudaStream_t s);
+// q and k rows ([rows][dk] each, either may be NULL) scaled to unit L2 norm
+// into qo / ko (which may alias q / k)
+constexpr float kQkNormEps = 1e-6f;
+cudaError_t launch_qk_l2norm(const void *q, const void *k, void *qo, void *ko, long long rows, int dk, int dtype,
+                             float eps, cudaStream_t s);
 // pass 1 (state-only correction items) or pass 2 (output items) on the CUDA-core kernel
 cudaError_t launch_fused_simt(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s);
 // the tcgen05 kernel; returns cudaErrorNotSupported when this build/device cannot run it

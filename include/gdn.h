@@ -96,7 +96,11 @@ typedef struct {
     void *prof_begin;           /* optional cudaEvent_t, recorded on `stream` right before
                                    the fused output pass is launched */
     void *prof_end;             /* optional cudaEvent_t, recorded right after it */
-    int32_t reserved[4];
+    int32_t qk_l2norm;          /* 1: the library scales every q and k row to unit L2 norm
+                                   (gdn_qk_l2norm with eps 1e-6) into workspace copies
+                                   before the pass; 0 (default): the caller's rows are
+                                   used as they are (they should be unit-norm already) */
+    int32_t reserved[3];
 } gdn_options;
 
 enum {
@@ -263,6 +267,28 @@ gdn_status gdn_chunk_fwd_static(const void *q, const void *k, const void *v,
                                 void *o, float *final_state,
                                 int32_t *device_status,
                                 const gdn_options *opts, gdn_stream_t stream);
+
+/*
+ * L2 normalisation of q and k rows over the head dimension, the step in front
+ * of the recurrence (the sliding-window paragraph of the FlashQLA talk
+ * "Qwen系列模型线性注意力高性能优化实践" takes every key to have unit L2 norm):
+ *
+ *     x_hat[d] = x[d] / sqrt(sum_d' x[d']^2 + eps)
+ *
+ * with the sum in fp32 and one rounding to the output type.  q, k: device
+ * pointers to `rows` rows of dk contiguous elements (dk in {32, 64, 128};
+ * rows = tokens x heads for a [.., H, dk] tensor); either may be NULL, and
+ * then its output pointer must be NULL too.  q_out / k_out receive the
+ * normalised rows in the same layout and dtype; they may equal q / k (in
+ * place).  All pointers 16-byte aligned.  eps <= 0 selects 1e-6.  Enqueued on
+ * `stream`; nothing syncs.  gdn_chunk_fwd runs this pass itself, into copies
+ * in its workspace, when opts->qk_l2norm is 1.
+ * Errors: GDN_ERR_INVALID_ARG (sizes, dtype, alignment, a NULL pairing),
+ * GDN_ERR_CUDA (launch failure; see gdn_last_error_detail()).
+ */
+gdn_status gdn_qk_l2norm(const void *q, const void *k, void *q_out, void *k_out,
+                         int64_t rows, int dk, gdn_dtype dtype, float eps,
+                         gdn_stream_t stream);
 
 /* The CUDA error (and, for tensor-map encoding, the driver result) behind the
  * most recent GDN_ERR_CUDA returned on the calling host thread, as text such

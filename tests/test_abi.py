@@ -116,3 +116,31 @@ def test_host_argument_errors_before_launch(lib):
     assert call(wsb=ws - 1) == 3
     assert gdn.gdn_chunk_fwd(fake, fake, fake, fake, fake, None, None, 1, 0.0, 1, 256, 2, 48, 32, gdn.F32,
                              fake, fake, fake, ws, None, None) == 2
+
+
+def test_qk_l2norm_option_and_workspace(lib):
+    o = gdn.default_options()
+    assert o.qk_l2norm == 0 and ctypes.sizeof(gdn.GdnOptions) == 64
+    T, H, dk = 1000, 4, 128
+    plain = gdn.gdn_chunk_fwd_workspace_size(1, T, H, dk, 128, 1, 0, gdn.BF16, gdn.default_options(sm_count=152))
+    normed = gdn.gdn_chunk_fwd_workspace_size(1, T, H, dk, 128, 1, 0, gdn.BF16,
+                                              gdn.default_options(sm_count=152, qk_l2norm=1))
+    copy = -(-T * H * dk * 2 // 256) * 256            # one bf16 copy of q (or k), 256-byte aligned
+    assert normed - plain == 2 * copy
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_plan_query(1, T, H, dk, 128, 1, 0, gdn.BF16, gdn.default_options(qk_l2norm=2))
+
+
+def test_qk_l2norm_argument_errors_before_launch(lib):
+    """gdn_qk_l2norm rejects bad sizes, dtypes, alignment and NULL pairings on
+    the host, and zero rows enqueue nothing; none of these reach the GPU."""
+    fake = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    f = gdn.gdn_qk_l2norm
+    assert f(fake, fake, fake, fake, 10, 48, gdn.BF16, 0.0, None) == 1      # dk
+    assert f(fake, fake, fake, fake, -1, 128, gdn.BF16, 0.0, None) == 1     # rows
+    assert f(fake, fake, fake, fake, 10, 128, 7, 0.0, None) == 1            # dtype
+    assert f(mis, fake, fake, fake, 10, 128, gdn.BF16, 0.0, None) == 1      # alignment
+    assert f(fake, None, fake, fake, 10, 128, gdn.BF16, 0.0, None) == 1     # k NULL, k_out not
+    assert f(fake, fake, None, fake, 10, 128, gdn.BF16, 0.0, None) == 1     # q_out NULL, q not
+    assert f(fake, fake, fake, fake, 0, 128, gdn.BF16, 0.0, None) == 0      # nothing to do

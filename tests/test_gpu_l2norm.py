@@ -1,0 +1,120 @@
+"""GPU parity of the q/k L2 normalisation: gdn_qk_l2norm element by element
+against the oracle's fp64 normalisation, and the forward pass with
+opts.qk_l2norm = 1 on un-normalised inputs against the oracle's recurrence on
+the oracle-normalised q and k.
+
+Element bar: the device sums squares in fp32 and rounds once to the output
+type, so a bf16 result is within 2^-8 of the exact value relative to it (one
+rounding) plus the fp32 error of the sum and the reciprocal square root; fp32
+results are within 1e-5 relative.  The forward pass keeps the parity bar of the
+other GPU tests (relative L2 <= 5e-3, max-abs <= 2e-2)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.norm import l2_normalize
+import chunked_prefill_gdn_gb300 as gdn
+from chunked_prefill_gdn_gb300 import build as gdn_build
+from chunked_prefill_gdn_gb300.inputs import CONFIGS, make_inputs
+
+from gpu_helpers import assert_close, full_reference, gpu_run, to_device
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2.0 ** -8 + 2e-6, "f32": 1e-5}
+TORCH = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    gdn_build.build()
+    return gdn.load_library()
+
+
+def raw_rows(shape, dtype, seed):
+    """Rows whose norms spread over about four decades, plus a zero row and a
+    row of tiny norm (where eps matters)."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(*shape, generator=g) * torch.exp(2.0 * torch.randn(*shape[:-1], 1, generator=g))
+    flat = x.view(-1, shape[-1])
+    flat[0] = 0.0
+    flat[1] = 1e-4
+    return x.to(TORCH[dtype])
+
+
+def check_rows(y, x, dtype):
+    ref = l2_normalize(oracle.to_f64(x))
+    got = oracle.to_f64(y)
+    err = np.abs(got - ref)
+    assert np.all(err <= TOL[dtype] * np.abs(ref) + 1e-30), "max rel %.3e" % float(
+        np.max(err / np.maximum(np.abs(ref), 1e-30)))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dk", [32, 64, 128])
+def test_qk_l2norm_matches_oracle(dtype, dk):
+    # 1237 tokens x 3 heads: rows not a multiple of the 32 a block takes per step
+    q = raw_rows((1237, 3, dk), dtype, seed=dk).cuda()
+    k = raw_rows((1237, 3, dk), dtype, seed=dk + 1).cuda()
+    qn, kn = gdn.qk_l2norm(q, k)
+    torch.cuda.synchronize()
+    check_rows(qn, q, dtype)
+    check_rows(kn, k, dtype)
+    assert torch.all(qn.view(-1, dk)[0] == 0)
+
+
+def test_qk_l2norm_in_place_and_one_sided():
+    q = raw_rows((777, 2, 128), "bf16", seed=5).cuda()
+    k = raw_rows((777, 2, 128), "bf16", seed=6).cuda()
+    qn, kn = gdn.qk_l2norm(q, k)
+    q2, k2 = q.clone(), k.clone()
+    gdn.qk_l2norm(q2, k2, q_out=q2, k_out=k2)           # in place
+    only_k = gdn.qk_l2norm(None, k)[1]                  # q absent
+    torch.cuda.synchronize()
+    assert torch.equal(q2, qn) and torch.equal(k2, kn) and torch.equal(only_k, kn)
+
+
+def unnormalise(inp, seed):
+    """Scale every q and k row by a positive factor in [0.25, 4]: the forward
+    pass with qk_l2norm = 1 must undo it."""
+    g = torch.Generator().manual_seed(seed)
+    out = dict(inp)
+    for name in ("q", "k"):
+        t = inp[name]
+        s = torch.exp(torch.empty(*t.shape[:-1], 1).uniform_(-1.386, 1.386, generator=g))
+        out[name] = (t.float() * s.to(t.device)).to(t.dtype).contiguous()
+    return out
+
+
+def oracle_normalised(inp):
+    ref_inp = dict(inp)
+    for name in ("q", "k"):
+        ref_inp[name] = l2_normalize(oracle.to_f64(inp[name]))
+    return full_reference(ref_inp)
+
+
+@pytest.mark.parametrize("name,cfg,kw", [
+    ("tiny_f32", CONFIGS[0], {}),
+    ("layer_ragged_tc", CONFIGS[1].scaled(B=2, T=1000, H=4), {}),
+    ("layer_ragged_cp", CONFIGS[1].scaled(B=2, T=1000, H=4), dict(cp_mode=gdn.CP_FORCE, chunks_per_segment=5)),
+    ("varlen", CONFIGS[3].scaled(T=3000, H=3, n_seqs=5), {}),
+])
+def test_forward_with_qk_l2norm(name, cfg, kw):
+    inp = unnormalise(to_device(make_inputs(cfg, "cpu")), seed=11)
+    q_before, k_before = inp["q"].clone(), inp["k"].clone()
+    o_ref, sf_ref = oracle_normalised(inp)
+    o, sf = gpu_run(inp, gdn.default_options(qk_l2norm=1, **kw))
+    assert torch.equal(inp["q"], q_before) and torch.equal(inp["k"], k_before)   # caller's tensors untouched
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
+def test_forward_qk_l2norm_is_a_no_op_on_unit_rows():
+    """Inputs that are already unit-norm give the same result with and without
+    the option, to within the bf16 rounding of the re-normalised copies."""
+    inp = to_device(make_inputs(CONFIGS[1].scaled(B=1, T=700, H=2), "cpu"))
+    o0, sf0 = gpu_run(inp, gdn.default_options())
+    o1, sf1 = gpu_run(inp, gdn.default_options(qk_l2norm=1))
+    assert_close("o", oracle.to_f64(o1), oracle.to_f64(o0))
+    assert_close("final_state", oracle.to_f64(sf1), oracle.to_f64(sf0))
