@@ -113,6 +113,16 @@ __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_
                  : "memory");
 }
 
+// Plain bulk copy global -> shared (both 16-byte aligned, bytes a multiple of
+// 16), completing `bytes` of transaction count on the mbarrier.
+__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(sdst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void bulk_wait_group_read_all() {
