@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <new>
 
 #include "gdn_internal.cuh"
 
@@ -377,8 +378,14 @@ gdn_status gdn_chunk_fwd_check(const void *workspace, gdn_stream_t stream) {
 }
 
 namespace {
+// The host-buffer entry point streams a large problem through in parts
+// (groups of whole sequences): the copies of part p+1 in, the pass on part p
+// and the copies of part p-1 out overlap on three streams.
+constexpr int kMaxHostParts = 4;
+constexpr size_t kHostSplitBytes = size_t(64) << 20;   // below this, one part
+
 struct HostLayout {
-    size_t q, k, v, g, beta, s0, cu, o, sf, ws, total;
+    size_t q, k, v, g, beta, s0, cu, o, sf, status, ws, total;
 };
 
 bool host_layout(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, int has_s0, int dtype,
@@ -400,9 +407,10 @@ bool host_layout(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, in
     hl->g = take(ntok * H * 4);
     hl->beta = take(ntok * H * 4);
     hl->s0 = take(has_s0 ? N * H * dk * dv * 4 : 0);
-    hl->cu = take(varlen ? (N + 1) * 4 : 0);
+    hl->cu = take(varlen ? (N + 1 + kMaxHostParts) * 4 : 0);   // each part's rebased cu_seqlens
     hl->o = take(ntok * H * dv * e);
     hl->sf = take(N * H * dk * dv * 4);
+    hl->status = take(kMaxHostParts * 4);                       // each part's device status word
     hl->ws = take(info.workspace_bytes);
     hl->total = off;
     *ws_bytes = info.workspace_bytes;
@@ -417,6 +425,35 @@ size_t gdn_chunk_fwd_host_buffer_size(int B, int T, int H, int dk, int dv, int n
     if (!host_layout(B, T, H, dk, dv, n_seqs, varlen, has_initial_state, dtype, opts, &hl, &ws)) return 0;
     return hl.total;
 }
+
+namespace {
+// Copy streams of the host-buffer entry point, created once per device.
+struct HostStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+};
+std::mutex g_host_streams_mu;
+HostStreams g_host_streams[64];
+
+gdn_status host_streams(HostStreams *hs) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("host entry: cudaGetDevice", e);
+    if (dev < 0 || dev >= 64) return GDN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_host_streams_mu);
+    HostStreams &h = g_host_streams[dev];
+    if (!h.in && (e = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail("host entry: create copy-in stream", e);
+    if (!h.out && (e = cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail("host entry: create copy-out stream", e);
+    *hs = h;
+    return GDN_OK;
+}
+
+struct HostPart {
+    int s0, s1;           // sequences [s0, s1)
+    size_t t0, ntok;      // tokens [t0, t0 + ntok)
+};
+}  // namespace
 
 gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const float *g, const float *beta,
                               const float *initial_state, const int32_t *cu_seqlens, int n_seqs, float scale,
@@ -433,32 +470,165 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
     if (device_buffer_bytes < hl.total) return GDN_ERR_WORKSPACE;
     const size_t e = dtype == GDN_BF16 ? 2 : 4;
     const size_t ntok = varlen ? (size_t)T : (size_t)B * T;
-    const size_t N = varlen ? (size_t)n_seqs : (size_t)B;
+    const int N = varlen ? n_seqs : B;
     if (ntok > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
-    char *d = static_cast<char *>(device_buffer);
-    struct Copy { void *dst; const void *src; size_t n; };
-    const Copy in[] = {
-        {d + hl.q, q, ntok * H * dk * e}, {d + hl.k, k, ntok * H * dk * e}, {d + hl.v, v, ntok * H * dv * e},
-        {d + hl.g, g, ntok * H * 4}, {d + hl.beta, beta, ntok * H * 4},
-        {d + hl.s0, initial_state, initial_state ? N * H * dk * dv * 4 : 0},
-        {d + hl.cu, cu_seqlens, varlen ? (N + 1) * 4 : 0},
-    };
-    cudaGetLastError();
-    for (const Copy &c : in)
-        if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-            return GDN_ERR_CUDA;
-    gdn_status st = gdn_chunk_fwd(d + hl.q, d + hl.k, d + hl.v, reinterpret_cast<float *>(d + hl.g),
-                                  reinterpret_cast<float *>(d + hl.beta),
-                                  initial_state ? reinterpret_cast<float *>(d + hl.s0) : nullptr,
-                                  varlen ? reinterpret_cast<int32_t *>(d + hl.cu) : nullptr, n_seqs, scale, B, T, H,
-                                  dk, dv, dtype, d + hl.o, reinterpret_cast<float *>(d + hl.sf), d + hl.ws, ws_bytes,
-                                  opts, stream_in);
+    const size_t tok_in = (size_t)H * ((2 * dk + dv) * e + 8);   // input bytes per token
+    const size_t state = (size_t)H * dk * dv * 4;                // bytes per sequence state
+
+    // Parts: groups of whole sequences with about equal token counts.
+    HostPart parts[kMaxHostParts];
+    int P = 0;
+    int want = (ntok * tok_in >= kHostSplitBytes) ? std::min(N, kMaxHostParts) : 1;
+    if (varlen && want > 1) {
+        // splitting needs well-formed offsets; otherwise one part, and the
+        // device check reports the bad cu_seqlens as it does for gdn_chunk_fwd
+        for (int i = 0; i <= N && want > 1; ++i)
+            if ((i == 0 && cu_seqlens[0] != 0) || (i > 0 && cu_seqlens[i] < cu_seqlens[i - 1]) ||
+                (i == N && (size_t)cu_seqlens[N] != ntok))
+                want = 1;
+    }
+    if (varlen && want == 1) {
+        parts[P++] = {0, N, 0, ntok};
+    } else if (varlen) {
+        int s = 0;
+        for (int p = 0; p < want && s < N; ++p) {
+            int s1 = N;
+            if (p + 1 < want) {
+                const size_t target = ntok * (size_t)(p + 1) / want;
+                s1 = s + 1;
+                while (s1 < N && (size_t)cu_seqlens[s1] < target) ++s1;
+            }
+            parts[P++] = {s, s1, (size_t)cu_seqlens[s], (size_t)(cu_seqlens[s1] - cu_seqlens[s])};
+            s = s1;
+        }
+    } else {
+        for (int p = 0; p < want; ++p) {
+            const int s0 = (int)((long long)N * p / want), s1 = (int)((long long)N * (p + 1) / want);
+            if (s1 > s0) parts[P++] = {s0, s1, (size_t)s0 * T, (size_t)(s1 - s0) * T};
+        }
+    }
+
+    // Every part runs with the whole problem's plan decisions (CP on or off, the
+    // same segment length), so each fits the workspace sized for the whole.
+    gdn_options po;
+    if (opts) po = *opts; else default_options(&po);
+    if (P > 1) {
+        gdn_plan_info full;
+        if (gdn_plan_query(B, T, H, dk, dv, n_seqs, varlen, dtype, opts, &full) != GDN_OK) return GDN_ERR_INVALID_ARG;
+        po.cp_mode = full.cp_enabled ? GDN_CP_FORCE : GDN_CP_OFF;
+        po.chunks_per_segment = full.cp_enabled ? full.chunks_per_segment : 0;
+        po.sm_count = full.sm_count;
+    }
+
+    HostStreams hs;
+    gdn_status st = host_streams(&hs);
     if (st != GDN_OK) return st;
-    if (ntok && cudaMemcpyAsync(o, d + hl.o, ntok * H * dv * e, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    if (cudaMemcpyAsync(final_state, d + hl.sf, N * H * dk * dv * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    return gdn_chunk_fwd_check(d + hl.ws, stream_in);
+    cudaGetLastError();
+    char *d = static_cast<char *>(device_buffer);
+    cudaEvent_t ev_start = nullptr, ev_in[kMaxHostParts] = {}, ev_done[kMaxHostParts] = {};
+    auto make_event = [](cudaEvent_t *ev) { return cudaEventCreateWithFlags(ev, cudaEventDisableTiming); };
+    cudaError_t ce = make_event(&ev_start);
+    for (int p = 0; p < P && ce == cudaSuccess; ++p) {
+        ce = make_event(&ev_in[p]);
+        if (ce == cudaSuccess) ce = make_event(&ev_done[p]);
+    }
+    // rebased cu_seqlens of every part, in one host array (copied before the call returns)
+    int32_t cu_parts[kMaxHostParts * 2 + 2];
+    int32_t *cu_heap = nullptr;
+    int32_t *cu_host = cu_parts;
+    if (varlen && N + 1 + kMaxHostParts > (int)(sizeof(cu_parts) / sizeof(int32_t))) {
+        cu_heap = new (std::nothrow) int32_t[N + 1 + kMaxHostParts];
+        if (!cu_heap) ce = cudaErrorMemoryAllocation;
+        cu_host = cu_heap;
+    }
+    size_t cu_off[kMaxHostParts] = {};
+    if (varlen && ce == cudaSuccess) {
+        size_t at = 0;
+        for (int p = 0; p < P; ++p) {
+            cu_off[p] = at;
+            for (int i = parts[p].s0; i <= parts[p].s1; ++i) cu_host[at++] = cu_seqlens[i] - cu_seqlens[parts[p].s0];
+        }
+    }
+
+    // the device buffer may still be in use by work enqueued on `stream` before this call
+    if (ce == cudaSuccess) ce = cudaEventRecord(ev_start, stream);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(hs.in, ev_start, 0);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(hs.out, ev_start, 0);
+    // copies in, part by part
+    for (int p = 0; p < P && ce == cudaSuccess; ++p) {
+        const HostPart &pt = parts[p];
+        const size_t ns = pt.s1 - pt.s0;
+        struct Copy { size_t dst; const void *src; size_t off, n; };
+        const Copy in[] = {
+            {hl.q, q, pt.t0 * H * dk * e, pt.ntok * H * dk * e},
+            {hl.k, k, pt.t0 * H * dk * e, pt.ntok * H * dk * e},
+            {hl.v, v, pt.t0 * H * dv * e, pt.ntok * H * dv * e},
+            {hl.g, g, pt.t0 * H * 4, pt.ntok * H * 4},
+            {hl.beta, beta, pt.t0 * H * 4, pt.ntok * H * 4},
+            {hl.s0, initial_state, (size_t)pt.s0 * state, initial_state ? ns * state : 0},
+        };
+        for (const Copy &c : in)
+            if (ce == cudaSuccess && c.n)
+                ce = cudaMemcpyAsync(d + c.dst + c.off, static_cast<const char *>(c.src) + c.off, c.n,
+                                     cudaMemcpyHostToDevice, hs.in);
+        if (ce == cudaSuccess && varlen)
+            ce = cudaMemcpyAsync(d + hl.cu + cu_off[p] * 4, cu_host + cu_off[p], (ns + 1) * 4, cudaMemcpyHostToDevice,
+                                 hs.in);
+        if (ce == cudaSuccess) ce = cudaEventRecord(ev_in[p], hs.in);
+    }
+    // the pass on each part as soon as its inputs are in; its results out on the third stream
+    for (int p = 0; p < P && ce == cudaSuccess && st == GDN_OK; ++p) {
+        const HostPart &pt = parts[p];
+        const int ns = pt.s1 - pt.s0;
+        ce = cudaStreamWaitEvent(stream, ev_in[p], 0);
+        if (ce != cudaSuccess) break;
+        const int Bp = varlen ? 1 : ns, Tp = varlen ? (int)pt.ntok : T;
+        st = gdn_chunk_fwd(d + hl.q + pt.t0 * H * dk * e, d + hl.k + pt.t0 * H * dk * e,
+                           d + hl.v + pt.t0 * H * dv * e, reinterpret_cast<float *>(d + hl.g) + pt.t0 * H,
+                           reinterpret_cast<float *>(d + hl.beta) + pt.t0 * H,
+                           initial_state ? reinterpret_cast<float *>(d + hl.s0 + (size_t)pt.s0 * state) : nullptr,
+                           varlen ? reinterpret_cast<int32_t *>(d + hl.cu) + cu_off[p] : nullptr, ns, scale, Bp, Tp,
+                           H, dk, dv, dtype, d + hl.o + pt.t0 * H * dv * e,
+                           reinterpret_cast<float *>(d + hl.sf + (size_t)pt.s0 * state), d + hl.ws, ws_bytes, &po,
+                           stream_in);
+        if (st != GDN_OK) break;
+        // keep this part's device status: the next part's pass starts by clearing the word
+        ce = cudaMemcpyAsync(d + hl.status + 4 * p, d + hl.ws, 4, cudaMemcpyDeviceToDevice, stream);
+        if (ce == cudaSuccess) ce = cudaEventRecord(ev_done[p], stream);
+        if (ce == cudaSuccess) ce = cudaStreamWaitEvent(hs.out, ev_done[p], 0);
+        if (ce == cudaSuccess && pt.ntok)
+            ce = cudaMemcpyAsync(static_cast<char *>(o) + pt.t0 * H * dv * e, d + hl.o + pt.t0 * H * dv * e,
+                                 pt.ntok * H * dv * e, cudaMemcpyDeviceToHost, hs.out);
+        if (ce == cudaSuccess)
+            ce = cudaMemcpyAsync(reinterpret_cast<char *>(final_state) + (size_t)pt.s0 * state,
+                                 d + hl.sf + (size_t)pt.s0 * state, (size_t)ns * state, cudaMemcpyDeviceToHost,
+                                 hs.out);
+    }
+    // everything this call enqueued has finished before it returns
+    const cudaError_t e_in = cudaStreamSynchronize(hs.in);
+    const cudaError_t e_run = cudaStreamSynchronize(stream);
+    const cudaError_t e_out = cudaStreamSynchronize(hs.out);
+    int status[kMaxHostParts] = {0, 0, 0, 0};
+    cudaError_t e_st = cudaSuccess;
+    if (ce == cudaSuccess && st == GDN_OK && e_in == cudaSuccess && e_run == cudaSuccess && e_out == cudaSuccess)
+        e_st = cudaMemcpy(status, d + hl.status, 4 * P, cudaMemcpyDeviceToHost);
+    if (ev_start) cudaEventDestroy(ev_start);
+    for (int p = 0; p < P; ++p) {
+        if (ev_in[p]) cudaEventDestroy(ev_in[p]);
+        if (ev_done[p]) cudaEventDestroy(ev_done[p]);
+    }
+    delete[] cu_heap;
+    if (st != GDN_OK) return st;
+    if (ce != cudaSuccess) return cuda_fail("host entry: copy or event", ce);
+    if (e_in != cudaSuccess) return cuda_fail("host entry: synchronize copy-in stream", e_in);
+    if (e_run != cudaSuccess) return cuda_fail("host entry: synchronize stream", e_run);
+    if (e_out != cudaSuccess) return cuda_fail("host entry: synchronize copy-out stream", e_out);
+    if (e_st != cudaSuccess) return cuda_fail("host entry: read status", e_st);
+    for (int p = 0; p < P; ++p) {
+        if (status[p] == GDN_ERR_TIMEOUT) return GDN_ERR_TIMEOUT;
+        if (status[p] != 0) return GDN_ERR_DEVICE_CHECK;
+    }
+    return GDN_OK;
 }
 
 const char *gdn_status_string(gdn_status s) {

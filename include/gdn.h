@@ -214,9 +214,17 @@ size_t gdn_chunk_fwd_host_buffer_size(int B, int T, int H, int dk, int dv, int n
  * The same forward pass for inputs and outputs in HOST memory (pinned memory
  * makes the copies asynchronous).  The call copies the inputs into
  * `device_buffer` (gdn_chunk_fwd_host_buffer_size() bytes, caller-owned), runs
- * gdn_chunk_fwd on `stream`, copies o and final_state back, synchronises the
- * stream and returns the device error status as gdn_chunk_fwd_check does.
+ * gdn_chunk_fwd on `stream`, copies o and final_state back, waits for all of
+ * it and returns the device error status as gdn_chunk_fwd_check does.
  * cu_seqlens is a host array here.
+ *
+ * Above 64 MB of input the problem goes through in up to four parts of whole
+ * sequences (about equal token counts): part p+1 is copied in on a library
+ * copy stream while the pass runs part p on `stream` and part p-1 is copied out
+ * on a second library copy stream (both created once per device, non-blocking;
+ * they first wait for the work already on `stream`).  Every part keeps the
+ * whole problem's plan (CP on or off, the segment length), so the result is the
+ * one gdn_chunk_fwd gives on the whole problem, bit for bit.
  */
 gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v,
                               const float *g, const float *beta,

@@ -232,6 +232,32 @@ def test_host_buffer_entry_point():
     assert_close("final_state", oracle.to_f64(sf), sf_ref)
 
 
+@pytest.mark.parametrize("case", ["batched", "varlen"])
+def test_host_entry_streams_large_problems_in_parts(case):
+    """Above 64 MB of input the host-buffer entry point copies, runs and copies
+    back in parts of whole sequences on three streams; every part keeps the
+    whole problem's plan, so the result equals the device entry point's bit
+    for bit."""
+    if case == "batched":
+        cfg = CONFIGS[1].scaled(B=4, T=2048, H=32, s0_std=0.02)     # 203 MB of input, four parts
+    else:
+        cfg = CONFIGS[3].scaled(T=65536, H=16, n_seqs=13, s0_std=0.02)
+    inp = make_inputs(cfg, "cpu")
+    pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    o, sf = gdn.chunk_fwd_host(pinned["q"], pinned["k"], pinned["v"], pinned["g"], pinned["beta"],
+                               pinned["initial_state"], pinned["cu_seqlens"], inp["scale"])
+    dev = to_device(inp)
+    o_d, sf_d = gpu_run(dev)
+    assert torch.equal(o, o_d.cpu()) and torch.equal(sf, sf_d.cpu())
+    # and a sampled check against the oracle
+    cu = seq_bounds(inp)
+    seqs, heads, rows = [0, len(cu) - 2], [0, cfg.H - 1], [0, 77]
+    o_ref, sf_ref, idx = sampled_reference(inp, seqs, heads, rows)
+    o_s, sf_s = gpu_sampled(o, sf, inp, seqs, heads, rows, idx)
+    assert_close("o", o_s, o_ref)
+    assert_close("final_state", sf_s, sf_ref)
+
+
 # ---------------------------------------------- full sizes, sampled outputs
 
 FULL_SAMPLES = {
