@@ -217,6 +217,40 @@ __device__ int lookback_window(const Workspace &w, int h, int chunk0, int c_begi
 
 constexpr int kMaxLookbackChunks = 256;
 
+// Segments per unit for the units that need correction matrices, when every
+// unit has nc chunks and the planner's segment length gives NS0 segments.
+// Per-pass cost model in chunk steps of the persistent passes on `grid` CTAs
+// (the talk's auto-CP paragraph: one-wave model T = lambda1 L + lambda2 N / L,
+// refined per pass): pass 1 runs 2 NS - 3 items per such unit (S* and M of
+// every segment but the last, S* of the first), pass 2 one item per segment of
+// every unit (n_s units keep NS0 segments and re-run a look-back of about four
+// chunks), the scan about half a chunk step per segment; a pass takes as many
+// waves as its items need, each as long as its longest item.  Fewer, longer
+// segments can save a whole wave of pass 1.  Returns 0 to keep NS0 (unless
+// another count is at least 5% cheaper).
+__device__ int correction_segments(int nc, int NS0, int n_m, int n_s, int grid) {
+    if (n_m <= 0 || NS0 <= 2 || grid <= 0) return 0;
+    const int Ls = (nc + NS0 - 1) / NS0 + (n_s > 0 ? 4 : 0);
+    auto cost = [&](int ns) {
+        const int Lm = (nc + ns - 1) / ns;
+        const long long it1 = (long long)n_m * (2 * ns - 3);
+        const long long it2 = (long long)n_m * ns + (long long)n_s * NS0;
+        return (double)((it1 + grid - 1) / grid) * Lm + (double)((it2 + grid - 1) / grid) * max(Lm, n_s > 0 ? Ls : 0) +
+               0.5 * ns;
+    };
+    const double c0 = cost(NS0);
+    int best = NS0;
+    double cb = c0;
+    for (int ns = NS0 - 1; ns >= 2; --ns) {
+        const double c = cost(ns);
+        if (c < cb) {
+            cb = c;
+            best = ns;
+        }
+    }
+    return (best != NS0 && cb < 0.95 * c0) ? best : 0;
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w, const __grid_constant__ PlanParams pp) {
     grid_dependency_wait();
     __shared__ int s_warp[32];
@@ -240,8 +274,31 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Prob
         for (int n = tid; n < N; n += blockDim.x) w.seq_order[n] = n;
     }
     if (tid < 4) s_base[tid] = 0;
-    __syncthreads();
     const int units = N * H;
+    // 2. segment count of the units that need correction matrices (heads with
+    //    alpha identically 1, or every split head without sliding); batched
+    //    inputs only, where every sequence has the same chunk count
+    __shared__ int s_nm, s_ns_m;
+    if (tid == 0) {
+        s_nm = 0;
+        s_ns_m = 0;
+    }
+    __syncthreads();
+    if (pp.cp_enabled && !p.varlen && units > 0) {
+        const int nc = w.seqinfo[0].w;
+        int NS0 = nc > pp.L ? (nc + pp.L - 1) / pp.L : 1;
+        NS0 = nc > 0 ? (nc + max(1, (nc + NS0 - 1) / NS0) - 1) / max(1, (nc + NS0 - 1) / NS0) : 1;
+        if (NS0 > 2) {
+            int mine = 0;
+            for (int u = tid; u < units; u += blockDim.x)
+                if (!(w.flags[u] != 0 && pp.sliding)) ++mine;      // flags are [N, H]: unit u = (u / H, u % H)
+            if (mine) atomicAdd(&s_nm, mine);
+            __syncthreads();
+            if (tid == 0) s_ns_m = correction_segments(nc, NS0, s_nm, units - s_nm, pp.grid);
+            __syncthreads();
+        }
+    }
+    const int ns_m = s_ns_m;
     const int max_walk = min(pp.L, kMaxLookbackChunks);
     for (int ubase = 0; ubase < units; ubase += blockDim.x) {
         const int u = ubase + tid;
@@ -257,6 +314,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Prob
             Lu = max(1, (nc + NS - 1) / NS);
             NS = nc > 0 ? (nc + Lu - 1) / Lu : 1;
             const bool flagged = w.flags[seq * H + h] != 0;
+            if (ns_m > 0 && NS > ns_m && !(flagged && pp.sliding)) {
+                Lu = (nc + ns_m - 1) / ns_m;
+                NS = (nc + Lu - 1) / Lu;
+            }
             if (NS > 1) {
                 mpath = !(flagged && pp.sliding);
                 for (int j = 1; j < NS && !mpath; ++j)

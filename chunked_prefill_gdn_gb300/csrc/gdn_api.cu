@@ -9,7 +9,6 @@
 
 #include <algorithm>
 #include <mutex>
-#include <new>
 
 #include "gdn_internal.cuh"
 
@@ -322,6 +321,7 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
     pp.cp_enabled = hp.cp;
     pp.sliding = opts.sliding ? 1 : 0;
     pp.ln_eps = logf(opts.sw_eps);
+    pp.grid = hp.grid;
 
     const int stages = opts.stages ? opts.stages : (GDN_STAGE_PREP | GDN_STAGE_INVERSE | GDN_STAGE_CORRECTION |
                                                     GDN_STAGE_FUSED);
@@ -532,28 +532,30 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
         ce = make_event(&ev_in[p]);
         if (ce == cudaSuccess) ce = make_event(&ev_done[p]);
     }
-    // rebased cu_seqlens of every part, in one host array (copied before the call returns)
-    int32_t cu_parts[kMaxHostParts * 2 + 2];
-    int32_t *cu_heap = nullptr;
-    int32_t *cu_host = cu_parts;
-    if (varlen && N + 1 + kMaxHostParts > (int)(sizeof(cu_parts) / sizeof(int32_t))) {
-        cu_heap = new (std::nothrow) int32_t[N + 1 + kMaxHostParts];
-        if (!cu_heap) ce = cudaErrorMemoryAllocation;
-        cu_host = cu_heap;
-    }
+    // each part's cu_seqlens, rebased to start at 0, one after another in the
+    // device buffer (offsets in int32 elements)
     size_t cu_off[kMaxHostParts] = {};
-    if (varlen && ce == cudaSuccess) {
-        size_t at = 0;
-        for (int p = 0; p < P; ++p) {
-            cu_off[p] = at;
-            for (int i = parts[p].s0; i <= parts[p].s1; ++i) cu_host[at++] = cu_seqlens[i] - cu_seqlens[parts[p].s0];
-        }
-    }
+    for (int p = 1; p < P; ++p) cu_off[p] = cu_off[p - 1] + (parts[p - 1].s1 - parts[p - 1].s0) + 1;
 
     // the device buffer may still be in use by work enqueued on `stream` before this call
     if (ce == cudaSuccess) ce = cudaEventRecord(ev_start, stream);
     if (ce == cudaSuccess) ce = cudaStreamWaitEvent(hs.in, ev_start, 0);
     if (ce == cudaSuccess) ce = cudaStreamWaitEvent(hs.out, ev_start, 0);
+    // the parts' offsets first, through a small stack array (a copy from pageable
+    // memory has read its source when cudaMemcpyAsync returns, and waits for the
+    // stream, which is still empty of this call's large copies here)
+    for (int p = 0; p < P && varlen && ce == cudaSuccess; ++p) {
+        const size_t ns = parts[p].s1 - parts[p].s0;
+        int32_t stage[256];
+        for (size_t i = 0; i <= ns && ce == cudaSuccess; i += 256) {
+            const size_t n = std::min<size_t>(256, ns + 1 - i);
+            // (one part: the caller's values as they are, so that the device
+            // check still sees a malformed array)
+            const int32_t base = P > 1 ? cu_seqlens[parts[p].s0] : 0;
+            for (size_t t = 0; t < n; ++t) stage[t] = cu_seqlens[parts[p].s0 + i + t] - base;
+            ce = cudaMemcpyAsync(d + hl.cu + (cu_off[p] + i) * 4, stage, n * 4, cudaMemcpyHostToDevice, hs.in);
+        }
+    }
     // copies in, part by part
     for (int p = 0; p < P && ce == cudaSuccess; ++p) {
         const HostPart &pt = parts[p];
@@ -571,9 +573,6 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
             if (ce == cudaSuccess && c.n)
                 ce = cudaMemcpyAsync(d + c.dst + c.off, static_cast<const char *>(c.src) + c.off, c.n,
                                      cudaMemcpyHostToDevice, hs.in);
-        if (ce == cudaSuccess && varlen)
-            ce = cudaMemcpyAsync(d + hl.cu + cu_off[p] * 4, cu_host + cu_off[p], (ns + 1) * 4, cudaMemcpyHostToDevice,
-                                 hs.in);
         if (ce == cudaSuccess) ce = cudaEventRecord(ev_in[p], hs.in);
     }
     // the pass on each part as soon as its inputs are in; its results out on the third stream
@@ -617,7 +616,6 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
         if (ev_in[p]) cudaEventDestroy(ev_in[p]);
         if (ev_done[p]) cudaEventDestroy(ev_done[p]);
     }
-    delete[] cu_heap;
     if (st != GDN_OK) return st;
     if (ce != cudaSuccess) return cuda_fail("host entry: copy or event", ce);
     if (e_in != cudaSuccess) return cuda_fail("host entry: synchronize copy-in stream", e_in);

@@ -49,6 +49,7 @@ struct PlanParams {
     int cp_enabled;
     int sliding;
     float ln_eps;
+    int grid;         // CTAs of the persistent fused passes
 };
 
 // Host-side layout of the workspace for one problem.

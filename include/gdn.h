@@ -31,9 +31,10 @@
  * Ownership: the caller allocates every buffer (inputs, outputs, workspace)
  * and keeps them alive until the work on `stream` completes.  The library
  * allocates no device or host memory at run time, keeps no state between calls
- * besides a per-device cache of device attributes and driver entry points (and
- * the fixed scratch array of gdn_chunk_fwd_static), and never synchronises the
- * stream inside gdn_chunk_fwd.
+ * besides per-device caches of device attributes, driver entry points and the
+ * two copy streams of gdn_chunk_fwd_host (and the fixed scratch array of
+ * gdn_chunk_fwd_static), and never synchronises the stream inside
+ * gdn_chunk_fwd.
  *
  * Errors: every call returns a gdn_status and never aborts.  Argument errors
  * are found on the host before any launch.  Errors found on the device (a

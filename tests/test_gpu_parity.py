@@ -176,6 +176,26 @@ def gate_scaled_tprime(Tp, G, beta, cu, C):
     return out
 
 
+def test_planner_gives_correction_heads_fewer_segments_when_a_wave_is_saved():
+    """With 16 CTAs, 3 heads with alpha == 1 and 5 decaying heads split into 16
+    segments, pass 1 would need six waves of 4-chunk items; the device planner's
+    per-pass model gives the alpha == 1 heads fewer, longer segments (the
+    decaying heads keep 16), and the result still matches the oracle."""
+    cfg = CONFIGS[2].scaled(T=4096, H=8, zero_gate_heads=(0, 1, 2))
+    inp = to_device(make_inputs(cfg, "cpu"))
+    opts = gdn.default_options(cp_mode=gdn.CP_FORCE, chunks_per_segment=4, sm_count=16)
+    ws = gdn.workspace_for(inp["q"], inp["v"], None, opts)
+    o, sf = gpu_run(inp, opts, workspace=ws)
+    views = _workspace_views(inp, ws, opts)
+    items = views["items"][:views["num_items"][0]].cpu().numpy()
+    per_head = {h: int((items[:, 1] == h).sum()) for h in range(8)}
+    assert all(per_head[h] == 16 for h in range(3, 8)), per_head
+    assert all(2 <= per_head[h] < 16 for h in range(3)), per_head
+    o_ref, sf_ref = full_reference(inp)
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
 def test_gate_and_inverse_intermediates():
     cfg = CONFIGS[3].scaled(T=3000, H=3, n_seqs=5, zero_gate_heads=(1,))
     inp = to_device(make_inputs(cfg, "cpu"))
