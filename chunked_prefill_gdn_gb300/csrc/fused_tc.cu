@@ -147,6 +147,16 @@ __device__ __forceinline__ bool ewait(const Ctx &cx, uint64_t *bar, uint32_t par
 // Shared-space address of coefficient array `field` of stage s.
 #define COEF_ADDR(cx, s, field) ((cx).sbase + kOffSmall + (s) * sizeof(Coef) + offsetof(Coef, field))
 
+// Items of this CTA: round r takes item r G + c in even rounds and
+// r G + G - 1 - c in odd ones (c = blockIdx.x, G = gridDim.x).  The planner
+// lists items longest first, so the rounds snake the long ones over the CTAs
+// instead of stacking them on the first ones.  Every role of the CTA walks the
+// same sequence; it ends at the first index past the list.
+__device__ __forceinline__ int cta_item(int r) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return r * G + ((r & 1) ? G - 1 - c : c);
+}
+
 // Stage ring: chunk n uses stage n % kStages; its use index is n / kStages.
 __device__ __forceinline__ int stage_of(uint32_t n) { return static_cast<int>(n % kStages); }
 __device__ __forceinline__ uint32_t use_parity(uint32_t n) { return (n / kStages) & 1u; }
@@ -157,17 +167,17 @@ __device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps,
     const Workspace &w = *cx.w;
     Small &sm = *cx.sm;
     // cursor over this CTA's chunks, items in order, empty items skipped
-    int k = blockIdx.x, c = 0, cend = 0, chunk0 = 0, head = 0;
+    int r = 0, c = 0, cend = 0, chunk0 = 0, head = 0;
     bool started = false;
     auto advance = [&]() -> bool {
         if (started && c + 1 < cend) {
             ++c;
             return true;
         }
-        if (started) k += gridDim.x;
+        if (started) ++r;
         started = true;
-        for (; k < cx.n_items; k += gridDim.x) {
-            const gdn_work_item it = cx.items[k];
+        for (; cta_item(r) < cx.n_items; ++r) {
+            const gdn_work_item it = cx.items[cta_item(r)];
             if (it.c_start < it.c_end) {
                 c = it.c_start;
                 cend = it.c_end;
@@ -254,17 +264,17 @@ __device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps,
 }
 
 // --------------------------------------------------------------------- MMA
-// This CTA's chunks in order (items blockIdx.x, blockIdx.x + gridDim.x, ...;
-// empty items skipped), for the MMA warp, which looks one chunk ahead.
+// This CTA's chunks in order (its items cta_item(0), cta_item(1), ...; empty
+// items skipped), for the MMA warp, which looks one chunk ahead.
 struct MmaCursor {
-    int k, c, cend, cbegin, flags;
+    int r, c, cend, cbegin, flags;
     bool valid;
 };
 
 __device__ __forceinline__ void cursor_start(const Ctx &cx, MmaCursor &cu) {
     cu.valid = false;
-    for (cu.k = blockIdx.x; cu.k < cx.n_items; cu.k += gridDim.x) {
-        const gdn_work_item it = cx.items[cu.k];
+    for (cu.r = 0; cta_item(cu.r) < cx.n_items; ++cu.r) {
+        const gdn_work_item it = cx.items[cta_item(cu.r)];
         if (it.c_start < it.c_end) {
             cu.c = it.c_start;
             cu.cend = it.c_end;
@@ -279,8 +289,8 @@ __device__ __forceinline__ void cursor_start(const Ctx &cx, MmaCursor &cu) {
 __device__ __forceinline__ void cursor_next(const Ctx &cx, MmaCursor &cu) {
     if (++cu.c < cu.cend) return;
     cu.valid = false;
-    for (cu.k += gridDim.x; cu.k < cx.n_items; cu.k += gridDim.x) {
-        const gdn_work_item it = cx.items[cu.k];
+    for (++cu.r; cta_item(cu.r) < cx.n_items; ++cu.r) {
+        const gdn_work_item it = cx.items[cta_item(cu.r)];
         if (it.c_start < it.c_end) {
             cu.c = it.c_start;
             cu.cend = it.c_end;
@@ -527,8 +537,8 @@ __device__ __forceinline__ void chain_role(const Ctx &cx, int warp, int lane) {
     prev_item.flags = 0;
     bool ok = true;
 
-    for (int k = blockIdx.x; k < cx.n_items && ok; k += gridDim.x) {
-        const gdn_work_item it = cx.items[k];
+    for (int r = 0; cta_item(r) < cx.n_items && ok; ++r) {
+        const gdn_work_item it = cx.items[cta_item(r)];
         const int4 si = w.seqinfo[it.seq];
         if (it.c_start >= it.c_end) {
             // an empty sequence: its end state is its start state
@@ -772,8 +782,8 @@ __device__ __forceinline__ void side_role(const Ctx &cx, int warp, int lane) {
     uint32_t pv_pcol = 0, pv_ocol = 0;
     bool ok = true;
 
-    for (int k = blockIdx.x; k < cx.n_items && ok; k += gridDim.x) {
-        const gdn_work_item it = cx.items[k];
+    for (int r = 0; cta_item(r) < cx.n_items && ok; ++r) {
+        const gdn_work_item it = cx.items[cta_item(r)];
         const int4 si = w.seqinfo[it.seq];
         for (int c = it.c_start; c < it.c_end; ++c, ++n) {
             const int s = stage_of(n);

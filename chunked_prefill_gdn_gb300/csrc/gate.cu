@@ -191,26 +191,13 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *s_warp, int *s_t
 // then takes the exact correction-matrix path instead).
 __device__ int lookback_window(const Workspace &w, int h, int chunk0, int c_begin, float ln_eps,
                                int max_walk) {
-    const float *tot = w.totals + (size_t)h * w.max_chunks + chunk0;
     float acc = 0.f;
     int wnd = 0;
     while (wnd < c_begin) {
-        // eight totals per round as independent loads, then the same running
-        // sum chunk by chunk (one load latency per round instead of per chunk)
-        float t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int c = c_begin - 1 - wnd - i;
-            t[i] = c >= 0 ? tot[c] : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (wnd >= c_begin) return wnd;
-            if (wnd >= max_walk) return -1;
-            acc += t[i];
-            ++wnd;
-            if (acc <= ln_eps) return wnd;
-        }
+        if (wnd >= max_walk) return -1;
+        acc += w.totals[(size_t)h * w.max_chunks + chunk0 + c_begin - 1 - wnd];
+        ++wnd;
+        if (acc <= ln_eps) break;
     }
     return wnd;
 }
