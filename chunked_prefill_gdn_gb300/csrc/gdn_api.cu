@@ -378,14 +378,17 @@ gdn_status gdn_chunk_fwd_check(const void *workspace, gdn_stream_t stream) {
 }
 
 namespace {
-// The host-buffer entry point streams a large problem through in parts
-// (groups of whole sequences): the copies of part p+1 in, the pass on part p
-// and the copies of part p-1 out overlap on three streams.
-constexpr int kMaxHostParts = 4;
+// The host-buffer entry point streams a large problem through in parts: the
+// copies of part p+1 in, the pass on part p and the copies of part p-1 out
+// overlap on three streams.  A part is a group of whole sequences, or, when
+// there are fewer sequences than parts and the plan runs every (sequence,
+// head) as one unit, a piece of one sequence (64-token aligned) that carries
+// the state of the previous piece through a device buffer.
+constexpr int kMaxHostParts = 8;
 constexpr size_t kHostSplitBytes = size_t(64) << 20;   // below this, one part
 
 struct HostLayout {
-    size_t q, k, v, g, beta, s0, cu, o, sf, status, ws, total;
+    size_t q, k, v, g, beta, s0, cu, o, sf, mid, status, ws, total;
 };
 
 bool host_layout(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, int has_s0, int dtype,
@@ -410,6 +413,7 @@ bool host_layout(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, in
     hl->cu = take(varlen ? (N + 1 + kMaxHostParts) * 4 : 0);   // each part's rebased cu_seqlens
     hl->o = take(ntok * H * dv * e);
     hl->sf = take(N * H * dk * dv * 4);
+    hl->mid = take(varlen ? 0 : 2 * N * H * dk * dv * 4);       // states between pieces of a sequence
     hl->status = take(kMaxHostParts * 4);                       // each part's device status word
     hl->ws = take(info.workspace_bytes);
     hl->total = off;
@@ -451,7 +455,10 @@ gdn_status host_streams(HostStreams *hs) {
 
 struct HostPart {
     int s0, s1;           // sequences [s0, s1)
-    size_t t0, ntok;      // tokens [t0, t0 + ntok)
+    size_t t0, ntok;      // tokens [t0, t0 + ntok) of the token axis
+    int Tp;               // tokens per sequence (batched) or packed tokens (varlen)
+    int src, dst;         // state in: -1 the caller's initial state, 0/1 a middle buffer;
+                          // state out: -1 final_state, 0/1 a middle buffer
 };
 }  // namespace
 
@@ -475,10 +482,22 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
     const size_t tok_in = (size_t)H * ((2 * dk + dv) * e + 8);   // input bytes per token
     const size_t state = (size_t)H * dk * dv * 4;                // bytes per sequence state
 
-    // Parts: groups of whole sequences with about equal token counts.
+    // Every part runs with the whole problem's plan decisions (CP on or off, the
+    // same segment length), so each fits the workspace sized for the whole and
+    // gives the whole problem's result.
+    gdn_plan_info full;
+    if (gdn_plan_query(B, T, H, dk, dv, n_seqs, varlen, dtype, opts, &full) != GDN_OK) return GDN_ERR_INVALID_ARG;
+    gdn_options po;
+    if (opts) po = *opts; else default_options(&po);
+    po.cp_mode = full.cp_enabled ? GDN_CP_FORCE : GDN_CP_OFF;
+    po.chunks_per_segment = full.cp_enabled ? full.chunks_per_segment : 0;
+    po.sm_count = full.sm_count;
+
+    // Parts.
     HostPart parts[kMaxHostParts];
     int P = 0;
-    int want = (ntok * tok_in >= kHostSplitBytes) ? std::min(N, kMaxHostParts) : 1;
+    const bool big = ntok * tok_in >= kHostSplitBytes;
+    int want = big ? std::min(N, kMaxHostParts) : 1;
     if (varlen && want > 1) {
         // splitting needs well-formed offsets; otherwise one part, and the
         // device check reports the bad cu_seqlens as it does for gdn_chunk_fwd
@@ -487,8 +506,11 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
                 (i == N && (size_t)cu_seqlens[N] != ntok))
                 want = 1;
     }
+    const int pieces = (!varlen && big && !full.cp_enabled && N < kMaxHostParts)
+                           ? std::max(1, std::min(kMaxHostParts / N, T / 64))
+                           : 1;
     if (varlen && want == 1) {
-        parts[P++] = {0, N, 0, ntok};
+        parts[P++] = {0, N, 0, ntok, T, -1, -1};
     } else if (varlen) {
         int s = 0;
         for (int p = 0; p < want && s < N; ++p) {
@@ -498,26 +520,29 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
                 s1 = s + 1;
                 while (s1 < N && (size_t)cu_seqlens[s1] < target) ++s1;
             }
-            parts[P++] = {s, s1, (size_t)cu_seqlens[s], (size_t)(cu_seqlens[s1] - cu_seqlens[s])};
+            const size_t t0 = cu_seqlens[s], n = cu_seqlens[s1] - cu_seqlens[s];
+            parts[P++] = {s, s1, t0, n, (int)n, -1, -1};
             s = s1;
+        }
+    } else if (pieces > 1) {
+        // each sequence in `pieces` pieces of whole chunks, in order
+        for (int b = 0; b < N; ++b) {
+            int u0 = 0, j = 0;
+            for (int q = 1; q <= pieces; ++q) {
+                const int u1 = q == pieces ? T : (int)(((long long)T * q / pieces) / 64 * 64);
+                if (u1 <= u0) continue;
+                const bool last = u1 == T;
+                parts[P++] = {b, b + 1, (size_t)b * T + u0, (size_t)(u1 - u0), u1 - u0, j == 0 ? -1 : (j - 1) & 1,
+                              last ? -1 : j & 1};
+                u0 = u1;
+                ++j;
+            }
         }
     } else {
         for (int p = 0; p < want; ++p) {
             const int s0 = (int)((long long)N * p / want), s1 = (int)((long long)N * (p + 1) / want);
-            if (s1 > s0) parts[P++] = {s0, s1, (size_t)s0 * T, (size_t)(s1 - s0) * T};
+            if (s1 > s0) parts[P++] = {s0, s1, (size_t)s0 * T, (size_t)(s1 - s0) * T, T, -1, -1};
         }
-    }
-
-    // Every part runs with the whole problem's plan decisions (CP on or off, the
-    // same segment length), so each fits the workspace sized for the whole.
-    gdn_options po;
-    if (opts) po = *opts; else default_options(&po);
-    if (P > 1) {
-        gdn_plan_info full;
-        if (gdn_plan_query(B, T, H, dk, dv, n_seqs, varlen, dtype, opts, &full) != GDN_OK) return GDN_ERR_INVALID_ARG;
-        po.cp_mode = full.cp_enabled ? GDN_CP_FORCE : GDN_CP_OFF;
-        po.chunks_per_segment = full.cp_enabled ? full.chunks_per_segment : 0;
-        po.sm_count = full.sm_count;
     }
 
     HostStreams hs;
@@ -567,7 +592,7 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
             {hl.v, v, pt.t0 * H * dv * e, pt.ntok * H * dv * e},
             {hl.g, g, pt.t0 * H * 4, pt.ntok * H * 4},
             {hl.beta, beta, pt.t0 * H * 4, pt.ntok * H * 4},
-            {hl.s0, initial_state, (size_t)pt.s0 * state, initial_state ? ns * state : 0},
+            {hl.s0, initial_state, (size_t)pt.s0 * state, (initial_state && pt.src < 0) ? ns * state : 0},
         };
         for (const Copy &c : in)
             if (ce == cudaSuccess && c.n)
@@ -581,14 +606,17 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
         const int ns = pt.s1 - pt.s0;
         ce = cudaStreamWaitEvent(stream, ev_in[p], 0);
         if (ce != cudaSuccess) break;
-        const int Bp = varlen ? 1 : ns, Tp = varlen ? (int)pt.ntok : T;
+        const int Bp = varlen ? 1 : ns;
+        const float *s_in = pt.src >= 0 ? reinterpret_cast<float *>(d + hl.mid + ((size_t)pt.src * N + pt.s0) * state)
+                            : initial_state ? reinterpret_cast<float *>(d + hl.s0 + (size_t)pt.s0 * state)
+                                            : nullptr;
+        float *s_out = pt.dst >= 0 ? reinterpret_cast<float *>(d + hl.mid + ((size_t)pt.dst * N + pt.s0) * state)
+                                   : reinterpret_cast<float *>(d + hl.sf + (size_t)pt.s0 * state);
         st = gdn_chunk_fwd(d + hl.q + pt.t0 * H * dk * e, d + hl.k + pt.t0 * H * dk * e,
                            d + hl.v + pt.t0 * H * dv * e, reinterpret_cast<float *>(d + hl.g) + pt.t0 * H,
-                           reinterpret_cast<float *>(d + hl.beta) + pt.t0 * H,
-                           initial_state ? reinterpret_cast<float *>(d + hl.s0 + (size_t)pt.s0 * state) : nullptr,
-                           varlen ? reinterpret_cast<int32_t *>(d + hl.cu) + cu_off[p] : nullptr, ns, scale, Bp, Tp,
-                           H, dk, dv, dtype, d + hl.o + pt.t0 * H * dv * e,
-                           reinterpret_cast<float *>(d + hl.sf + (size_t)pt.s0 * state), d + hl.ws, ws_bytes, &po,
+                           reinterpret_cast<float *>(d + hl.beta) + pt.t0 * H, s_in,
+                           varlen ? reinterpret_cast<int32_t *>(d + hl.cu) + cu_off[p] : nullptr, ns, scale, Bp,
+                           pt.Tp, H, dk, dv, dtype, d + hl.o + pt.t0 * H * dv * e, s_out, d + hl.ws, ws_bytes, &po,
                            stream_in);
         if (st != GDN_OK) break;
         // keep this part's device status: the next part's pass starts by clearing the word
@@ -598,7 +626,7 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
         if (ce == cudaSuccess && pt.ntok)
             ce = cudaMemcpyAsync(static_cast<char *>(o) + pt.t0 * H * dv * e, d + hl.o + pt.t0 * H * dv * e,
                                  pt.ntok * H * dv * e, cudaMemcpyDeviceToHost, hs.out);
-        if (ce == cudaSuccess)
+        if (ce == cudaSuccess && pt.dst < 0)
             ce = cudaMemcpyAsync(reinterpret_cast<char *>(final_state) + (size_t)pt.s0 * state,
                                  d + hl.sf + (size_t)pt.s0 * state, (size_t)ns * state, cudaMemcpyDeviceToHost,
                                  hs.out);
@@ -607,7 +635,7 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v, const
     const cudaError_t e_in = cudaStreamSynchronize(hs.in);
     const cudaError_t e_run = cudaStreamSynchronize(stream);
     const cudaError_t e_out = cudaStreamSynchronize(hs.out);
-    int status[kMaxHostParts] = {0, 0, 0, 0};
+    int status[kMaxHostParts] = {};
     cudaError_t e_st = cudaSuccess;
     if (ce == cudaSuccess && st == GDN_OK && e_in == cudaSuccess && e_run == cudaSuccess && e_out == cudaSuccess)
         e_st = cudaMemcpy(status, d + hl.status, 4 * P, cudaMemcpyDeviceToHost);

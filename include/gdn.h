@@ -219,13 +219,16 @@ size_t gdn_chunk_fwd_host_buffer_size(int B, int T, int H, int dk, int dv, int n
  * it and returns the device error status as gdn_chunk_fwd_check does.
  * cu_seqlens is a host array here.
  *
- * Above 64 MB of input the problem goes through in up to four parts of whole
- * sequences (about equal token counts): part p+1 is copied in on a library
- * copy stream while the pass runs part p on `stream` and part p-1 is copied out
- * on a second library copy stream (both created once per device, non-blocking;
- * they first wait for the work already on `stream`).  Every part keeps the
- * whole problem's plan (CP on or off, the segment length), so the result is the
- * one gdn_chunk_fwd gives on the whole problem, bit for bit.
+ * Above 64 MB of input the problem goes through in up to eight parts: groups
+ * of whole sequences with about equal token counts or, when there are fewer
+ * sequences than parts and the plan runs every (sequence, head) as one unit,
+ * 64-token-aligned pieces of each sequence, each starting from the state the
+ * previous piece left in the device buffer.  Part p+1 is copied in on a
+ * library copy stream while the pass runs part p on `stream` and part p-1 is
+ * copied out on a second library copy stream (both created once per device,
+ * non-blocking; they first wait for the work already on `stream`).  Every part
+ * keeps the whole problem's plan (CP on or off, the segment length), so the
+ * result is the one gdn_chunk_fwd gives on the whole problem, bit for bit.
  */
 gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v,
                               const float *g, const float *beta,

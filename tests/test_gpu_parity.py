@@ -255,11 +255,12 @@ def test_host_buffer_entry_point():
 @pytest.mark.parametrize("case", ["batched", "varlen"])
 def test_host_entry_streams_large_problems_in_parts(case):
     """Above 64 MB of input the host-buffer entry point copies, runs and copies
-    back in parts of whole sequences on three streams; every part keeps the
-    whole problem's plan, so the result equals the device entry point's bit
-    for bit."""
+    back in parts on three streams (batched: two 1024-token pieces of each of
+    the four sequences, the state handed on through the device buffer; varlen:
+    eight groups of whole sequences); every part keeps the whole problem's
+    plan, so the result equals the device entry point's bit for bit."""
     if case == "batched":
-        cfg = CONFIGS[1].scaled(B=4, T=2048, H=32, s0_std=0.02)     # 203 MB of input, four parts
+        cfg = CONFIGS[1].scaled(B=4, T=2048, H=32, s0_std=0.02)     # 203 MB of input, eight parts
     else:
         cfg = CONFIGS[3].scaled(T=65536, H=16, n_seqs=13, s0_std=0.02)
     inp = make_inputs(cfg, "cpu")
