@@ -115,7 +115,7 @@ __device__ __forceinline__ void store_e(float *dst, const float *x) {
 // Rows [0, rows) are q, rows [rows, 2 rows) are k (a NULL tensor contributes
 // no rows: its half of the index range is skipped).
 template <typename T, int DK>
-__global__ void __launch_bounds__(32 * kNormWarps) qk_l2norm_kernel(const T *q, const T *k, T *qo, T *ko,
+__global__ void __launch_bounds__(32 * kNormWarps, 8) qk_l2norm_kernel(const T *q, const T *k, T *qo, T *ko,
                                                                     long long rows, float eps) {
     constexpr int E = DK / 32;
     const int lane = threadIdx.x & 31;
