@@ -166,6 +166,9 @@ __device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps,
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
     Small &sm = *cx.sm;
+    // the timeout probe: no tile ever arrives, so every consumer's bounded wait
+    // runs out and the CTA leaves through its error path (no copy was issued)
+    if (p.timeout_probe) return;
     // cursor over this CTA's chunks, items in order, empty items skipped
     int r = 0, c = 0, cend = 0, chunk0 = 0, head = 0;
     bool started = false;

@@ -291,6 +291,7 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
     p.B = B; p.T = T; p.H = H; p.dk = dk; p.dv = dv; p.N = hp.N; p.total_T = (int)hp.total_T;
     p.varlen = varlen; p.dtype = dtype;
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)dk);
+    p.timeout_probe = (opts.debug_checks & GDN_DEBUG_TIMEOUT_PROBE) ? 1 : 0;
 
     char *base = static_cast<char *>(workspace);
     const Layout &L = hp.lay;

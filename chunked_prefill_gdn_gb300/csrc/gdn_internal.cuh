@@ -20,6 +20,8 @@ struct Problem {
     float *sf;
     int B, T, H, dk, dv, N, total_T, varlen, dtype;
     float scale;
+    int timeout_probe;      // GDN_DEBUG_TIMEOUT_PROBE: the fused tcgen05 pass's producer
+                            // withholds every arrival (its consumers' bounded waits run out)
 };
 
 // Device pointers into the caller's workspace.

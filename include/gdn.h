@@ -93,7 +93,7 @@ typedef struct {
                                    selected are skipped and their workspace outputs must
                                    already be there from an earlier call on the same
                                    problem and workspace) */
-    int32_t debug_checks;       /* reserved, 0 */
+    int32_t debug_checks;       /* 0, or GDN_DEBUG_* bits (tests of the error paths) */
     void *prof_begin;           /* optional cudaEvent_t, recorded on `stream` right before
                                    the fused output pass is launched */
     void *prof_end;             /* optional cudaEvent_t, recorded right after it */
@@ -103,6 +103,13 @@ typedef struct {
                                    used as they are (they should be unit-norm already) */
     int32_t reserved[3];
 } gdn_options;
+
+/* GDN_DEBUG_TIMEOUT_PROBE: the tile producer of the tcgen05 fused pass signals
+ * nothing, so every bounded wait of that pass runs out (about 2 s): the pass
+ * records GDN_ERR_TIMEOUT, frees what it holds and returns, and the next call
+ * on the same workspace runs normally.  It exists to test the timeout path
+ * without faulting or hanging the GPU; the CUDA-core pass ignores it. */
+enum { GDN_DEBUG_TIMEOUT_PROBE = 1 };
 
 enum {
     GDN_STAGE_PREP = 1,         /* sequence tables, gate kernel, device planner */

@@ -242,6 +242,23 @@ def test_bad_cu_seqlens_is_reported_not_faulted():
     assert torch.isfinite(o.float()).all()
 
 
+def test_bounded_wait_runs_out_and_reports_timeout():
+    """GDN_DEBUG_TIMEOUT_PROBE: the tcgen05 fused pass's tile producer signals
+    nothing, so every bounded wait of that pass runs out (about 2 s) without a
+    fault or a hang; the call reports GDN_ERR_TIMEOUT through the device check,
+    and the next call on the same workspace is unaffected."""
+    cfg = CONFIGS[1].scaled(B=1, T=300, H=2)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    ws = gdn.workspace_for(inp["q"], inp["v"])
+    with pytest.raises(gdn.GdnError) as e:
+        gpu_run(inp, gdn.default_options(cp_mode=gdn.CP_OFF, kernel=gdn.KERNEL_TC, debug_checks=1), workspace=ws)
+    assert e.value.status == 6
+    o, sf = gpu_run(inp, gdn.default_options(cp_mode=gdn.CP_OFF, kernel=gdn.KERNEL_TC), workspace=ws)
+    o_ref, sf_ref = full_reference(inp)
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
 def test_host_buffer_entry_point():
     inp = make_inputs(CONFIGS[3].scaled(T=2500, H=2, n_seqs=3, s0_std=0.02), "cpu")
     pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
