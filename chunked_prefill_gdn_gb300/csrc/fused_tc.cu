@@ -78,9 +78,9 @@ constexpr uint32_t kOffSmall = kOffQM + 16384;
 constexpr uint32_t kColS32 = 0;    // fp32 state
 constexpr uint32_t kColS16 = 128;  // bf16 state (MMA1 A operand)
 constexpr uint32_t kColP = 192;    // two P buffers of 128 columns (chunk parity):
-                                   //   +0..63 P_K (W2, then W4, bf16 at +16..+47), +64..127 P_Q (+ output)
-                                   //   the other buffer's +0..63 takes Q K^T (and the exact-form D4)
-constexpr uint32_t kColU = 448;    // U' fp32 (Ut bf16 at +16..+47)
+                                   //   +0..63 P_K (W2, then W4, bf16 at +16..+47), +64..127 P_Q (+ output);
+                                   //   in the exact form the other buffer's +0..63 takes D4
+constexpr uint32_t kColU = 448;    // Q K^T (P0, lanes 64-127) until masked, then U' fp32 (Ut bf16 at +16..+47)
 
 // Per-chunk gate coefficients (written by the producer warp with the tiles).
 struct Coef {
