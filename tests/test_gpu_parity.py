@@ -242,6 +242,49 @@ def test_bad_cu_seqlens_is_reported_not_faulted():
     assert torch.isfinite(o.float()).all()
 
 
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+@pytest.mark.parametrize("cp", ["off", "force"])
+def test_zero_beta_only_decays_the_initial_state(kernel, cp):
+    """beta = 0 everywhere: no token writes the state, so S_t = (prod alpha) S_0
+    and o_t = scale gamma_t S_0 q_t, on every path (both fused kernels, with and
+    without the segment split)."""
+    cfg = CONFIGS[1].scaled(B=2, T=700, H=3, s0_std=0.5)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    inp["beta"] = torch.zeros_like(inp["beta"])
+    kw = dict(cp_mode=gdn.CP_OFF) if cp == "off" else dict(cp_mode=gdn.CP_FORCE, chunks_per_segment=3)
+    o, sf = gpu_run(inp, opts_for(kernel, **kw))
+    g = oracle.to_f64(inp["g"])                                   # [B, T, H]
+    G = np.cumsum(g, axis=1)
+    s0 = oracle.to_f64(inp["initial_state"])                      # [B, H, dk, dv], [j][i] = S[i][j]
+    q = oracle.to_f64(inp["q"])                                   # [B, T, H, dk]
+    o_ref = inp["scale"] * np.exp(G)[..., None] * np.einsum("bthj,bhji->bthi", q, s0)
+    sf_ref = np.exp(G[:, -1])[..., None, None] * s0
+    assert_close("o", oracle.to_f64(o), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
+def test_orthonormal_keys_with_full_writes_store_the_values_exactly():
+    """alpha = 1, beta = 1 and orthonormal keys (T <= dk): each token overwrites
+    the state along its key, so the final state maps every key to its value,
+    S_T k_t = v_t (fp32, CUDA-core kernel), whatever the initial state."""
+    T, dk = 32, 32
+    cfg = CONFIGS[0].scaled(T=T, H=2, s0_std=0.3)
+    inp = make_inputs(cfg, "cpu")
+    g = torch.Generator().manual_seed(7)
+    for h in range(2):
+        qmat, _ = torch.linalg.qr(torch.randn(dk, dk, generator=g, dtype=torch.float64))
+        inp["k"][0, :, h, :] = qmat[:, :T].T.to(torch.float32)      # rows: orthonormal keys
+    inp["g"] = torch.zeros_like(inp["g"])
+    inp["beta"] = torch.ones_like(inp["beta"])
+    inp = to_device(inp)
+    _, sf = gpu_run(inp, opts_for("simt", cp_mode=gdn.CP_OFF))
+    S = oracle.to_f64(sf)[0]                                      # [H, dk, dv], [j][i] = S[i][j]
+    k = oracle.to_f64(inp["k"])[0]                                # [T, H, dk]
+    v = oracle.to_f64(inp["v"])[0]                                # [T, H, dv]
+    recalled = np.einsum("hji,thj->thi", S, k)                    # S_T k_t
+    assert np.abs(recalled - v).max() < 2e-4
+
+
 def test_bounded_wait_runs_out_and_reports_timeout():
     """GDN_DEBUG_TIMEOUT_PROBE: the tcgen05 fused pass's tile producer signals
     nothing, so every bounded wait of that pass runs out (about 2 s) without a
