@@ -1,0 +1,124 @@
+"""Pins for the oracle's backward pass (oracle/backward.py).
+
+The gradients are pinned to central finite differences of the forward oracle
+(the token-by-token recurrence of the talk "Qwen系列模型线性注意力高性能优化实践",
+itself pinned in test_oracle_pins.py) on tiny problems: a code path that shares
+nothing with the backward's derivation.  A dropped or mis-signed term moves some
+gradient far outside the finite-difference error, which the last test checks
+for the terms that are easiest to get wrong."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle.backward import _unit_backward, gdn_backward_reference
+
+EPS = 1e-6
+
+
+def tiny(seed=0, lens=(6,), H=2, dk=3, dv=4):
+    rng = np.random.default_rng(seed)
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    N = len(lens)
+    return dict(
+        q=rng.standard_normal((T, H, dk)), k=rng.standard_normal((T, H, dk)) * 0.6,
+        v=rng.standard_normal((T, H, dv)), g=-rng.uniform(0.01, 0.7, (T, H)), beta=rng.uniform(0.1, 0.9, (T, H)),
+        s0=rng.standard_normal((N, H, dk, dv)) * 0.5, cu=cu,
+        do=rng.standard_normal((T, H, dv)), dsT=rng.standard_normal((N, H, dk, dv)), scale=0.7)
+
+
+def loss(p):
+    o, sf = oracle.gdn_reference(p["q"], p["k"], p["v"], p["g"], p["beta"], p["s0"], p["cu"], scale=p["scale"])
+    return float(np.sum(o * p["do"]) + np.sum(sf * p["dsT"]))
+
+
+def numeric_grad(p, name):
+    x = p[name]
+    grad = np.zeros_like(x)
+    for idx in np.ndindex(*x.shape):
+        orig = x[idx]
+        x[idx] = orig + EPS
+        lp = loss(p)
+        x[idx] = orig - EPS
+        lm = loss(p)
+        x[idx] = orig
+        grad[idx] = (lp - lm) / (2 * EPS)
+    return grad
+
+
+def analytic(p):
+    return gdn_backward_reference(p["q"], p["k"], p["v"], p["g"], p["beta"], p["s0"], p["cu"], scale=p["scale"],
+                                  do=p["do"], d_final_state=p["dsT"])
+
+
+@pytest.mark.parametrize("lens", [(6,), (4, 1, 5)])
+def test_gradients_match_finite_differences(lens):
+    p = tiny(seed=len(lens), lens=lens)
+    got = dict(zip(["q", "k", "v", "g", "beta", "s0"], analytic(p)))
+    for name in ["q", "k", "v", "g", "beta", "s0"]:
+        num = numeric_grad(p, name)
+        scale = max(1.0, float(np.abs(num).max()))
+        assert np.abs(got[name] - num).max() <= 1e-6 * scale, name
+
+
+def test_no_upstream_gradient_gives_zero():
+    p = tiny(seed=3)
+    p["do"] = np.zeros_like(p["do"])
+    p["dsT"] = np.zeros_like(p["dsT"])
+    for x in analytic(p):
+        assert np.all(x == 0.0)
+
+
+def test_linear_in_the_upstream_gradients():
+    p = tiny(seed=4)
+    a = analytic(p)
+    p2 = dict(p, do=np.random.default_rng(9).standard_normal(p["do"].shape), dsT=np.zeros_like(p["dsT"]))
+    b = analytic(p2)
+    p3 = dict(p, do=2.0 * p["do"] - 3.0 * p2["do"], dsT=2.0 * p["dsT"])
+    c = analytic(p3)
+    for x, y, z in zip(a, b, c):
+        np.testing.assert_allclose(z, 2.0 * x - 3.0 * y, rtol=1e-10, atol=1e-12)
+
+
+def test_zero_beta_closed_forms():
+    """beta = 0: S_t = gamma_t S_0, so dv = dk = 0, dq_t = scale gamma_t S_0^T do_t
+    and dS_0 = sum_t scale gamma_t do_t q_t^T + gamma_T dS_T."""
+    p = tiny(seed=5, lens=(7,), H=1)
+    p["beta"] = np.zeros_like(p["beta"])
+    dq, dk, dv, dg, db, ds0 = analytic(p)
+    assert np.all(dk == 0.0) and np.all(dv == 0.0)
+    gam = np.exp(np.cumsum(p["g"][:, 0]))
+    S0 = p["s0"][0, 0].T                                     # dv x dk
+    dq_ref = p["scale"] * gam[:, None] * (p["do"][:, 0] @ S0)
+    np.testing.assert_allclose(dq[:, 0], dq_ref, rtol=1e-12, atol=1e-12)
+    dS0 = p["scale"] * np.einsum("t,ti,tj->ij", gam, p["do"][:, 0], p["q"][:, 0]) + gam[-1] * p["dsT"][0, 0].T
+    np.testing.assert_allclose(ds0[0, 0], dS0.T, rtol=1e-12, atol=1e-12)
+
+
+def test_finite_differences_catch_a_dropped_term():
+    """The check above is sharp: dk without the dA^T half of the symmetric term,
+    or dbeta without its decay term, misses the finite differences by far more
+    than their error."""
+    p = tiny(seed=6, lens=(5,), H=1)
+    num_k = numeric_grad(p, "k")[:, 0]
+    num_b = numeric_grad(p, "beta")[:, 0]
+    q, k, v, g, b = (p[n][:, 0] for n in ("q", "k", "v", "g", "beta"))
+    dq, dk, dv, dg, db, _ = _unit_backward(q, k, v, g, b, p["s0"][0, 0].T, p["do"][:, 0], p["dsT"][0, 0].T,
+                                           p["scale"])
+    assert np.abs(dk - num_k).max() < 1e-6 and np.abs(db - num_b).max() < 1e-6
+    # rebuild the two terms and drop them
+    alpha = np.exp(g)
+    S = [p["s0"][0, 0].T]
+    for t in range(len(g)):
+        A = alpha[t] * (np.eye(3) - b[t] * np.outer(k[t], k[t]))
+        S.append(S[-1] @ A + b[t] * np.outer(v[t], k[t]))
+    G = p["dsT"][0, 0].T.copy()
+    wrong_k, wrong_b = dk.copy(), db.copy()
+    for t in range(len(g) - 1, -1, -1):
+        G = G + p["scale"] * np.outer(p["do"][t, 0], q[t])
+        dA = S[t].T @ G
+        wrong_k[t] += alpha[t] * b[t] * (dA.T @ k[t])          # removes the dA^T k half
+        wrong_b[t] += alpha[t] * (k[t] @ dA @ k[t])            # removes the decay term
+        G = G @ (alpha[t] * (np.eye(3) - b[t] * np.outer(k[t], k[t]))).T
+    assert np.abs(wrong_k - num_k).max() > 1e-3
+    assert np.abs(wrong_b - num_b).max() > 1e-3
