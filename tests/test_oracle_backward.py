@@ -122,3 +122,19 @@ def test_finite_differences_catch_a_dropped_term():
         G = G @ (alpha[t] * (np.eye(3) - b[t] * np.outer(k[t], k[t]))).T
     assert np.abs(wrong_k - num_k).max() > 1e-3
     assert np.abs(wrong_b - num_b).max() > 1e-3
+
+
+@pytest.mark.parametrize("lens,C", [((6,), 64), ((13,), 4), ((9, 1, 7), 3), ((70,), 16)])
+def test_chunked_form_matches_the_token_backward(lens, C):
+    """The chunked (WY) backward — the algebra a chunked kernel runs, one chunk
+    at a time with the start states of a forward sweep and dS0 handed to the
+    chunk before — gives the token recurrence's gradients to rounding, with
+    ragged last chunks and packed sequences."""
+    from oracle.backward import gdn_backward_chunked
+    p = tiny(seed=len(lens) + C, lens=lens, dk=5, dv=4)
+    args = (p["q"], p["k"], p["v"], p["g"], p["beta"], p["s0"], p["cu"])
+    kw = dict(scale=p["scale"], do=p["do"], d_final_state=p["dsT"])
+    a = gdn_backward_reference(*args, **kw)
+    b = gdn_backward_chunked(*args, C=C, **kw)
+    for x, y in zip(a, b):
+        assert np.abs(x - y).max() <= 1e-11 * max(1.0, float(np.abs(x).max()))
