@@ -81,7 +81,7 @@ cudaError_t launch_qk_l2norm(const void *q, const void *k, void *qo, void *ko, l
                              float eps, cudaStream_t s);
 // pass 1 (state-only correction items) or pass 2 (output items) on the CUDA-core kernel
 cudaError_t launch_fused_simt(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s);
-// the tcgen05 kernel; returns cudaErrorNotSupported when this build/device cannot run it
+// the tcgen05 kernel; returns cudaErrorNotSupported when the compiled library or the device cannot run it
 cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s);
 bool fused_tc_supported(int dtype, int dk, int dv);
 int fused_simt_smem_bytes(int dk, int dv);

@@ -61,7 +61,7 @@ typedef struct CUstream_st *gdn_stream_t;
 typedef enum {
     GDN_OK = 0,
     GDN_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer */
-    GDN_ERR_UNSUPPORTED = 2,   /* shape/dtype/device this build does not handle */
+    GDN_ERR_UNSUPPORTED = 2,   /* shape/dtype/device the library does not handle */
     GDN_ERR_WORKSPACE = 3,     /* workspace smaller than gdn_chunk_fwd_workspace_size() */
     GDN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
     GDN_ERR_DEVICE_CHECK = 5,  /* the device found bad input (e.g. cu_seqlens) */
