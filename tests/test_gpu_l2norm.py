@@ -118,3 +118,17 @@ def test_forward_qk_l2norm_is_a_no_op_on_unit_rows():
     o1, sf1 = gpu_run(inp, gdn.default_options(qk_l2norm=1))
     assert_close("o", oracle.to_f64(o1), oracle.to_f64(o0))
     assert_close("final_state", oracle.to_f64(sf1), oracle.to_f64(sf0))
+
+
+def test_host_entry_streams_with_normalisation():
+    """The host-buffer entry point with opts.qk_l2norm = 1 on a problem large
+    enough to go through in parts (each part normalises its own slice into its
+    workspace copies) gives the device entry point's result bit for bit."""
+    cfg = CONFIGS[1].scaled(B=4, T=2048, H=32)
+    inp = unnormalise(make_inputs(cfg, "cpu"), seed=5)
+    opts = gdn.default_options(qk_l2norm=1)
+    pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    o_h, sf_h = gdn.chunk_fwd_host(pinned["q"], pinned["k"], pinned["v"], pinned["g"], pinned["beta"],
+                                   pinned["initial_state"], pinned["cu_seqlens"], inp["scale"], opts=opts)
+    o_d, sf_d = gpu_run(to_device(inp), opts)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(sf_h, sf_d.cpu())
