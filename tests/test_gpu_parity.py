@@ -285,6 +285,23 @@ def test_orthonormal_keys_with_full_writes_store_the_values_exactly():
     assert np.abs(recalled - v).max() < 2e-4
 
 
+@pytest.mark.parametrize("cp", ["off", "force"])
+def test_stages_run_separately_equal_one_call(cp):
+    """opts.stages: the prep and inverse stages in one call and the correction
+    and fused stages in a second call on the same workspace give the one-call
+    result bit for bit (each stage reads only what earlier stages left in the
+    workspace)."""
+    cfg = CONFIGS[3].scaled(T=3000, H=3, n_seqs=5, s0_std=0.02)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    kw = dict(cp_mode=gdn.CP_OFF) if cp == "off" else dict(cp_mode=gdn.CP_FORCE, chunks_per_segment=4)
+    ws = gdn.workspace_for(inp["q"], inp["v"], inp["cu_seqlens"], gdn.default_options(**kw))
+    o1, sf1 = gpu_run(inp, gdn.default_options(**kw), workspace=ws)
+    o1, sf1 = o1.clone(), sf1.clone()
+    gpu_run(inp, gdn.default_options(stages=gdn.STAGE_PREP | gdn.STAGE_INVERSE, **kw), workspace=ws)
+    o2, sf2 = gpu_run(inp, gdn.default_options(stages=gdn.STAGE_CORRECTION | gdn.STAGE_FUSED, **kw), workspace=ws)
+    assert torch.equal(o1, o2) and torch.equal(sf1, sf2)
+
+
 def test_bounded_wait_runs_out_and_reports_timeout():
     """GDN_DEBUG_TIMEOUT_PROBE: the tcgen05 fused pass's tile producer signals
     nothing, so every bounded wait of that pass runs out (about 2 s) without a
