@@ -285,6 +285,17 @@ def test_orthonormal_keys_with_full_writes_store_the_values_exactly():
     assert np.abs(recalled - v).max() < 2e-4
 
 
+def test_many_heads_span_several_gate_groups():
+    """H = 70: the gate kernel takes heads in groups of 64, so a second, partial
+    group; 3 x 70 units fill more than one wave of the persistent passes."""
+    cfg = CONFIGS[1].scaled(B=3, T=200, H=70, s0_std=0.02)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    o_ref, sf_ref = full_reference(inp)
+    o, sf = gpu_run(inp, opts_for(cp_mode=gdn.CP_OFF))
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
 @pytest.mark.parametrize("cp", ["off", "force"])
 def test_stages_run_separately_equal_one_call(cp):
     """opts.stages: the prep and inverse stages in one call and the correction
