@@ -209,6 +209,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-qk-l2norm", action="store_true", help="skip timing the optional q/k normalisation pass")
+    ap.add_argument("--no-backward", action="store_true", help="skip timing the backward pass")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-heads", type=int, default=2, help="heads per reference-arm step")
     ap.add_argument("--override", action="append", default=[],
@@ -341,6 +342,8 @@ def main():
     }
     if not args.no_qk_l2norm:
         result["qk_l2norm"] = qk_l2norm_measure(gdn, torch, q, k, flush, stream, peaks, peak_src)
+    if not args.no_backward:
+        result["backward"] = backward_measure(gdn, torch, inp, cfg, flush, stream)
     if not args.no_e2e:
         result["e2e"] = e2e_measure(gdn, torch, inp, cfg, opts, dev, args)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -390,6 +393,70 @@ def qk_l2norm_measure(gdn, torch, q, k, flush, stream, peaks, peak_src, iters=10
             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
             "alg_bytes_per_launch": nbytes, "launches": iters, "peak_source": peak_src,
             "note": "optional step in front of the path (opts.qk_l2norm = 1); not inside the timed step"}
+
+
+# FP32 CUDA-core peak of a GB300 at its maximum SM clock: 152 SMs x 128 FP32
+# lanes x 2 flops (FMA) x 2.07 GHz.
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def backward_flops(dk, dv, chunks, H):
+    """Algorithmic flops of the chunked backward (2 per multiply-add), per
+    (chunk, head) with C = 64: the forward pieces it needs once (K K^T, the
+    triangular inverse, X = K S0, U = T B, the state update) and the backward
+    products (Q K^T, Q S0, K dS, dU, dB, dM, dA, the five dK terms, the two dQ
+    terms, the two dS0 terms); a short last chunk counts as a whole one."""
+    C = 64
+    fwd = C * C * dk + C ** 3 / 3 + C * dk * dv + C * C * dv + C * dk * dv
+    bwd = (C * C * dk + 2 * C * dk * dv + 4 * C * C * dv + 3 * C * C * dk + 2 * C * dk * dv
+           + C * C * dk + C * dk * dv + 2 * C * dk * dv)
+    return 2.0 * (fwd + bwd) * chunks * H
+
+
+def backward_measure(gdn, torch, inp, cfg, flush, stream, iters=3):
+    """The backward pass (gdn_chunk_bwd) on this workload with seeded upstream
+    gradients: CUDA events around each launch sequence (the main kernel and the
+    slice reduction), L2 flushed before each.  Reported against the FP32
+    CUDA-core peak (the kernel runs on CUDA cores)."""
+    from chunked_prefill_gdn_gb300.inputs import make_grad_inputs
+    grads = make_grad_inputs(cfg, inp["q"].device)
+    do, dsf = grads["do"], grads["d_final_state"]
+    q = inp["q"]
+    B, T, H, dk = q.shape
+    dv = inp["v"].shape[-1]
+    dt = gdn.BF16 if q.dtype == torch.bfloat16 else gdn.F32
+    ws = torch.empty(gdn.gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, cfg.num_seqs, inp["cu_seqlens"] is not None,
+                                                      dt), dtype=torch.uint8, device=q.device)
+
+    def run():
+        return gdn.chunk_bwd(q, inp["k"], inp["v"], inp["g"], inp["beta"], do, inp["initial_state"],
+                             inp["cu_seqlens"], inp["scale"], dsf, workspace=ws, stream=stream)
+    run()
+    st = gdn.gdn_chunk_bwd_check(ctypes_ptr(ws), ctypes_ptr_stream(stream))
+    if st != 0:
+        raise SystemExit("backward device check failed: %s" % gdn.gdn_status_string(st))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for i, (a, b) in enumerate(evs):
+        flush.fill_((i + 11) & 0xFF)
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize(q.device)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if inp["cu_seqlens"] is not None:
+        lens = inp["cu_seqlens"].cpu().diff().tolist()
+        chunks = sum(-(-n // 64) for n in lens)
+    else:
+        chunks = B * -(-T // 64)
+    flops = backward_flops(dk, dv, chunks, H)
+    achieved = flops / (ms * 1e-3) / 1e12
+    slices = dv // 32
+    return {"kernel": "bwd_kernel + bwd_reduce_kernel (gdn_chunk_bwd)", "ms": ms,
+            "tokens_per_s": cfg.total_tokens / (ms * 1e-3), "bound": "alu", "achieved": achieved,
+            "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": achieved / FP32_ALU_TFLOPS,
+            "alg_flops": flops, "launches": iters * (1 + (4 if slices > 1 else 0)),
+            "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
+            "note": "fp32 CUDA-core kernel, one CTA per (32 value columns, head, sequence); not inside the timed step"}
 
 
 def e2e_measure(gdn, torch, inp, cfg, opts, dev, args):

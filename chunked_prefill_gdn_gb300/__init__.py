@@ -7,6 +7,7 @@ call raises.
 
     o, final_state = chunk_fwd(q, k, v, g, beta, initial_state=None,
                                cu_seqlens=None, scale=None)
+    dq, dk, dv, dg, dbeta, d_initial_state = chunk_bwd(q, k, v, g, beta, do, ...)
 
 q, k [B,T,H,dk] and v [B,T,H,dv] in bf16 or fp32, g and beta [B,T,H] fp32,
 initial_state [N,H,dk,dv] fp32, cu_seqlens int32 [N+1] (then B = 1), all on
@@ -28,6 +29,7 @@ __all__ = [
     "gdn_default_options", "gdn_plan_query", "gdn_chunk_fwd_workspace_size", "gdn_workspace_query",
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
     "gdn_chunk_fwd_static", "gdn_qk_l2norm", "qk_l2norm",
+    "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd", "gdn_chunk_bwd_check", "chunk_bwd",
     "gdn_status_string", "gdn_version", "gdn_last_error_detail", "chunk_fwd", "chunk_fwd_host", "workspace_for", "GdnError",
     "CP_AUTO", "CP_OFF", "CP_FORCE", "KERNEL_AUTO", "KERNEL_TC", "KERNEL_SIMT", "BF16", "F32",
     "STAGE_PREP", "STAGE_INVERSE", "STAGE_CORRECTION", "STAGE_FUSED",
@@ -119,6 +121,12 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_chunk_fwd_static.restype = i32
     lib.gdn_qk_l2norm.argtypes = [vp, vp, vp, vp, ctypes.c_int64, i32, i32, ctypes.c_float, vp]
     lib.gdn_qk_l2norm.restype = i32
+    lib.gdn_chunk_bwd_workspace_size.argtypes = [i32] * 8
+    lib.gdn_chunk_bwd_workspace_size.restype = sz
+    lib.gdn_chunk_bwd.argtypes = [vp] * 7 + [i32, f32] + [i32] * 6 + [vp] * 8 + [vp, sz, vp]
+    lib.gdn_chunk_bwd.restype = i32
+    lib.gdn_chunk_bwd_check.argtypes = [vp, vp]
+    lib.gdn_chunk_bwd_check.restype = i32
     lib.gdn_status_string.argtypes = [i32]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_version.argtypes = []
@@ -192,6 +200,18 @@ def gdn_chunk_fwd_static(*args) -> int:
 
 def gdn_qk_l2norm(*args) -> int:
     return int(load_library().gdn_qk_l2norm(*args))
+
+
+def gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, n_seqs, varlen, dtype) -> int:
+    return int(load_library().gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, n_seqs, int(varlen), dtype))
+
+
+def gdn_chunk_bwd(*args) -> int:
+    return int(load_library().gdn_chunk_bwd(*args))
+
+
+def gdn_chunk_bwd_check(workspace_ptr, stream_ptr) -> int:
+    return int(load_library().gdn_chunk_bwd_check(workspace_ptr, stream_ptr))
 
 
 def gdn_status_string(status: int) -> str:
@@ -334,3 +354,48 @@ def chunk_fwd_host(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=
     if st != 0:
         raise GdnError(st, "gdn_chunk_fwd_host")
     return out, final_state
+
+
+def chunk_bwd(q, k, v, g, beta, do, initial_state=None, cu_seqlens=None, scale=None, d_final_state=None,
+              workspace=None, stream: Optional[torch.cuda.Stream] = None, check: bool = False):
+    """Gradients of sum <o, do> + <final_state, d_final_state> through
+    gdn_chunk_bwd; returns fp32 (dq, dk, dv, dg, dbeta, d_initial_state)."""
+    B, T, H, dk, dv, N = _shape(q, v, cu_seqlens)
+    dt = _dtype_code(q)
+    for name, t in dict(k=k, v=v, do=do).items():
+        if t.dtype != q.dtype:
+            raise TypeError("%s must have q's dtype" % name)
+    for name, t in dict(q=q, k=k, v=v, g=g, beta=beta, do=do).items():
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    for name, t in dict(initial_state=initial_state, d_final_state=d_final_state).items():
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise TypeError("%s must be contiguous float32" % name)
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    f32, dev = torch.float32, q.device
+    dq = torch.empty(B, T, H, dk, dtype=f32, device=dev)
+    dk_ = torch.empty(B, T, H, dk, dtype=f32, device=dev)
+    dv_ = torch.empty(B, T, H, dv, dtype=f32, device=dev)
+    dg = torch.empty(B, T, H, dtype=f32, device=dev)
+    db = torch.empty(B, T, H, dtype=f32, device=dev)
+    ds0 = torch.empty(N, H, dk, dv, dtype=f32, device=dev)
+    if workspace is None:
+        n = gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, N, cu_seqlens is not None, dt)
+        if n == 0:
+            raise GdnError(1, "gdn_chunk_bwd_workspace_size")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    stream = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
+                       N, float(scale) if scale is not None else 0.0, B, T, H, dk, dv, dt,
+                       _ptr(do), _ptr(d_final_state), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(db), _ptr(ds0),
+                       _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise GdnError(st, "gdn_chunk_bwd")
+    if check:
+        st = gdn_chunk_bwd_check(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise GdnError(st, "device check")
+    return dq, dk_, dv_, dg, db, ds0

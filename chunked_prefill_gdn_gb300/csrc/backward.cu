@@ -1,0 +1,689 @@
+// Backward pass of the chunked GDN forward: gradients of q, k, v, g, beta and
+// the initial state from the gradients of o and of the final state.
+//
+// The talk "Qwen系列模型线性注意力高性能优化实践" (backward paragraph) runs the
+// backward chunk by chunk in the WY form with the dA and dA^T terms merged; it
+// prints no formulas.  The algebra here is the chain rule through one chunk of
+// the forward (math orientation, S dv x dk, C = 64 tokens, start state S0,
+// chunk-local G = cumsum g, gamma = exp(G), Gamma_ri = exp(G_r - G_i),
+// e_i = exp(G_C - G_i)):
+//
+//   forward   A = strictlower(diag(beta)(Gamma . K K^T)),  T = (I + A)^-1
+//             X = D_gamma K S0^T,  B = diag(beta)(V - X),  U = T B
+//             M = Gamma . tril(Q K^T),  O = scale (D_gamma Q S0^T + M U)
+//             S_C = gamma_C S0 + U^T D_e K
+//   backward  dU = scale M^T dO + D_e K dS_C^T,   dB = T^T dU
+//             dM = scale dO U^T (lower),  dA = -dB U^T (strictly lower)
+//             dV = diag(beta) dB,   dX = -diag(beta) dB
+//             P = dA . Gamma . beta_r,  R = dM . Gamma
+//             dK = (P + P^T) K + R^T Q + D_gamma dX S0 + D_e U dS_C
+//             dQ = R K + scale D_gamma dO S0
+//             dS0 = scale dO^T D_gamma Q + dX^T D_gamma K + gamma_C dS_C
+//             dbeta, dg from every place beta, G enter (then dg is the reverse
+//             cumsum of dG inside the chunk)
+//
+// Design: one CTA per (value-column slice of 32, head, sequence).  The state's
+// rows along dv evolve independently, so a slice runs the whole recurrence on
+// its own columns: a forward sweep stores every chunk's start state (slice)
+// in the workspace, then a reverse sweep carries dS from the last chunk to the
+// first.  dv, dS0 come out complete per slice; dq, dk, dg, dbeta are sums over
+// the dv columns, so each slice writes its partial and a second kernel adds the
+// slices in a fixed order (deterministic, no atomics).  Everything is fp32 on
+// CUDA cores with operands in shared memory (padded strides, conflict-free).
+#include <math.h>
+
+#include <algorithm>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kBwdCols = 32;      // value columns per CTA
+constexpr int kBwdThreads = 256;  // 8 warps
+constexpr int kBwdWarps = kBwdThreads / 32;
+constexpr int C = kChunk;
+constexpr int CP = C + 1;         // padded row stride of C x C tiles
+constexpr int WP = kBwdCols + 1;  // padded row stride of C x 32 and dk x 32 tiles
+
+// Shared-memory layout (in floats) for head dimension DK.
+template <int DK>
+struct BwdSmem {
+    static constexpr int KP = DK + 1;
+    static constexpr int kK = 0;                 // K      [C][KP]
+    static constexpr int kQ = kK + C * KP;       // Q      [C][KP]
+    static constexpr int kS0 = kQ + C * KP;      // S0     [DK][WP]  chunk start state (slice)
+    static constexpr int kdS = kS0 + DK * WP;    // dS     [DK][WP]  gradient of the chunk's end state
+    static constexpr int kV = kdS + DK * WP;     // V      [C][WP]
+    static constexpr int kdO = kV + C * WP;      // dO     [C][WP]
+    static constexpr int kY = kdO + C * WP;      // K S0   [C][WP]
+    static constexpr int kKdS = kY + C * WP;     // K dS   [C][WP]
+    static constexpr int kU = kKdS + C * WP;     // U      [C][WP]
+    static constexpr int kTmp = kU + C * WP;     // B, then dU
+    static constexpr int kdB = kTmp + C * WP;    // dB     [C][WP]
+    static constexpr int kKK = kdB + C * WP;     // K K^T (strictly lower), then E
+    static constexpr int kGam = kKK + C * CP;    // Gamma (lower), then R
+    static constexpr int kA = kGam + C * CP;     // A, then Q K^T (lower)
+    static constexpr int kT = kA + C * CP;       // T, then P' = dA . Gamma
+    static constexpr int kG = kT + C * CP;       // vectors of C
+    static constexpr int kGamma = kG + C;
+    static constexpr int kE = kGamma + C;
+    static constexpr int kBeta = kE + C;
+    static constexpr int kDgam = kBeta + C;      // scale dO . (Q S0) per row
+    static constexpr int kDe = kDgam + C;
+    static constexpr int kDb = kDe + C;
+    static constexpr int kDG = kDb + C;
+    static constexpr int kRed = kDG + C;         // [kBwdWarps]
+    static constexpr int kFloats = kRed + kBwdWarps;
+    static constexpr size_t kBytes = (size_t)kFloats * sizeof(float);
+};
+static_assert(BwdSmem<128>::kBytes <= 232448, "backward tile set exceeds the shared memory of a CTA");
+
+struct BwdArgs {
+    const void *q, *k, *v, *dout;
+    const float *g, *beta, *s0, *dsf;
+    const int32_t *cu;
+    float *gq, *gk, *gv, *gg, *gbeta, *gs0;   // gradients; gq, gk, gg, gbeta: per-slice partials
+                                              // when slices > 1
+    float *states;                            // [slots][H][DK][dv] chunk start states
+    int *err;
+    long long part_stride_k;                  // total_T * H * DK: slice stride of the dq / dk partials
+    long long part_stride_t;                  // total_T * H: slice stride of the dg / dbeta partials
+    int T, H, dv, N, total_T, varlen;
+    float scale;
+};
+
+template <typename TI>
+__device__ __forceinline__ float ld_in(const void *base, size_t i) {
+    return static_cast<float>(reinterpret_cast<const TI *>(base)[i]);
+}
+template <>
+__device__ __forceinline__ float ld_in<__nv_bfloat16>(const void *base, size_t i) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// Loads one chunk (rows >= len zero, g = 0 and beta = 0 there, which leaves the
+// algebra of a short chunk unchanged) and forms G, gamma, e in warp 0.
+template <int DK, typename TI>
+__device__ void load_chunk(const BwdArgs &a, float *sm, int t0, int len, int h, int col0, bool with_q) {
+    using L = BwdSmem<DK>;
+    constexpr int KP = L::KP;
+    const int tid = threadIdx.x;
+    const int H = a.H;
+    for (int idx = tid; idx < C * DK; idx += kBwdThreads) {
+        const int r = idx / DK, d = idx % DK;
+        float kv = 0.f, qv = 0.f;
+        if (r < len) {
+            const size_t off = ((size_t)(t0 + r) * H + h) * DK + d;
+            kv = ld_in<TI>(a.k, off);
+            if (with_q) qv = ld_in<TI>(a.q, off);
+        }
+        sm[L::kK + r * KP + d] = kv;
+        if (with_q) sm[L::kQ + r * KP + d] = qv;
+    }
+    for (int idx = tid; idx < C * kBwdCols; idx += kBwdThreads) {
+        const int r = idx / kBwdCols, w = idx % kBwdCols;
+        float vv = 0.f, ov = 0.f;
+        if (r < len) {
+            const size_t off = ((size_t)(t0 + r) * H + h) * a.dv + col0 + w;
+            vv = ld_in<TI>(a.v, off);
+            if (with_q) ov = ld_in<TI>(a.dout, off);
+        }
+        sm[L::kV + r * WP + w] = vv;
+        if (with_q) sm[L::kdO + r * WP + w] = ov;
+    }
+    if (tid < 32) {
+        const int lane = tid;
+        float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+        if (lane < len) {
+            g0 = a.g[(size_t)(t0 + lane) * H + h];
+            b0 = a.beta[(size_t)(t0 + lane) * H + h];
+        }
+        if (32 + lane < len) {
+            g1 = a.g[(size_t)(t0 + 32 + lane) * H + h];
+            b1 = a.beta[(size_t)(t0 + 32 + lane) * H + h];
+        }
+        for (int off = 1; off < 32; off <<= 1) {      // inclusive scans of both halves
+            const float y0 = __shfl_up_sync(0xffffffffu, g0, off);
+            const float y1 = __shfl_up_sync(0xffffffffu, g1, off);
+            if (lane >= off) { g0 += y0; g1 += y1; }
+        }
+        g1 += __shfl_sync(0xffffffffu, g0, 31);
+        const float glast = __shfl_sync(0xffffffffu, g1, 31);   // = G at row len-1 (zero-padded g)
+        sm[L::kG + lane] = g0;
+        sm[L::kG + 32 + lane] = g1;
+        sm[L::kGamma + lane] = expf(g0);
+        sm[L::kGamma + 32 + lane] = expf(g1);
+        sm[L::kE + lane] = expf(glast - g0);
+        sm[L::kE + 32 + lane] = expf(glast - g1);
+        sm[L::kBeta + lane] = b0;
+        sm[L::kBeta + 32 + lane] = b1;
+    }
+}
+
+// K K^T (strictly lower), Gamma (lower), A; then T = (I + A)^-1 by forward
+// substitution, one column per thread of warps 0-1.  Ends synchronised.
+template <int DK>
+__device__ void chunk_inverse(float *sm) {
+    using L = BwdSmem<DK>;
+    constexpr int KP = L::KP;
+    const int tid = threadIdx.x;
+    const float *sK = sm + L::kK;
+    for (int idx = tid; idx < C * C; idx += kBwdThreads) {
+        const int r = idx / C, i = idx % C;            // a warp holds one r and 32 consecutive i
+        float kk = 0.f, gm = 0.f;
+        if (i <= r) {
+            gm = expf(sm[L::kG + r] - sm[L::kG + i]);
+            if (i < r) {
+#pragma unroll 8
+                for (int d = 0; d < DK; ++d) kk += sK[r * KP + d] * sK[i * KP + d];
+            }
+        }
+        sm[L::kKK + r * CP + i] = kk;
+        sm[L::kGam + r * CP + i] = gm;
+        sm[L::kA + r * CP + i] = (i < r) ? sm[L::kBeta + r] * gm * kk : 0.f;
+    }
+    __syncthreads();
+    if (tid < C) {
+        const int j = tid;
+        const float *sA = sm + L::kA;
+        float *sT = sm + L::kT;
+        for (int r = 0; r < C; ++r) {
+            float a0 = (r == j) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            int i = 0;
+            for (; i + 4 <= r; i += 4) {
+                a0 -= sA[r * CP + i] * sT[i * CP + j];
+                a1 -= sA[r * CP + i + 1] * sT[(i + 1) * CP + j];
+                a2 -= sA[r * CP + i + 2] * sT[(i + 2) * CP + j];
+                a3 -= sA[r * CP + i + 3] * sT[(i + 3) * CP + j];
+            }
+            for (; i < r; ++i) a0 -= sA[r * CP + i] * sT[i * CP + j];
+            sT[r * CP + j] = (a0 + a1) + (a2 + a3);
+        }
+    }
+    __syncthreads();
+}
+
+// B = diag(beta)(V - gamma Y) into the scratch tile, then U = T B.  Expects Y
+// in place and ends synchronised.
+template <int DK>
+__device__ void chunk_u(float *sm) {
+    using L = BwdSmem<DK>;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int idx = tid; idx < C * kBwdCols; idx += kBwdThreads) {
+        const int r = idx / kBwdCols, w = idx % kBwdCols;
+        sm[L::kTmp + r * WP + w] =
+            sm[L::kBeta + r] * (sm[L::kV + r * WP + w] - sm[L::kGamma + r] * sm[L::kY + r * WP + w]);
+    }
+    __syncthreads();
+    for (int r = warp; r < C; r += kBwdWarps) {
+        float u = 0.f;
+        for (int i = 0; i <= r; ++i) u += sm[L::kT + r * CP + i] * sm[L::kTmp + i * WP + lane];
+        sm[L::kU + r * WP + lane] = u;
+    }
+    __syncthreads();
+}
+
+template <int DK, typename TI>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
+    using L = BwdSmem<DK>;
+    constexpr int KP = L::KP;
+    constexpr int DPL = DK / 32;    // head-dimension elements per lane
+    extern __shared__ float sm[];
+    const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = a.H, dv = a.dv, col0 = slice * kBwdCols;
+    const float scale = a.scale;
+
+    int t_begin, len_seq;
+    if (a.varlen) {
+        const int c0 = a.cu[n], c1 = a.cu[n + 1];
+        const bool bad = c0 < 0 || c1 < c0 || c1 > a.total_T || (n == 0 && c0 != 0) ||
+                         (n == a.N - 1 && c1 != a.total_T);
+        if (bad) {                                   // uniform over the CTA
+            if (tid == 0) report_error(a.err, GDN_ERR_DEVICE_CHECK);
+            return;
+        }
+        t_begin = c0;
+        len_seq = c1 - c0;
+    } else {
+        t_begin = n * a.T;
+        len_seq = a.T;
+    }
+    const int nc = (len_seq + C - 1) / C;
+    // chunk c of this sequence stores its start state in slot (first token)/C + n:
+    // distinct for distinct chunks and below total_T/C + N
+    auto state_ptr = [&](int t0) {
+        return a.states + ((size_t)(t0 / C + n) * H + h) * DK * dv + col0;
+    };
+
+    float *sS0 = sm + L::kS0;
+    float *sdS = sm + L::kdS;
+    const float *sK = sm + L::kK;
+    const float *sQ = sm + L::kQ;
+
+    // ---------------- forward sweep: the start state of every chunk ----------------
+    for (int idx = tid; idx < DK * kBwdCols; idx += kBwdThreads) {
+        const int d = idx / kBwdCols, w = idx % kBwdCols;
+        sS0[d * WP + w] = a.s0 ? a.s0[(((size_t)n * H + h) * DK + d) * dv + col0 + w] : 0.f;
+    }
+    for (int c = 0; c < nc; ++c) {
+        const int t0 = t_begin + c * C;
+        const int len = min(C, t_begin + len_seq - t0);
+        __syncthreads();
+        load_chunk<DK, TI>(a, sm, t0, len, h, col0, false);
+        float *st = state_ptr(t0);
+        for (int idx = tid; idx < DK * kBwdCols; idx += kBwdThreads) {
+            const int d = idx / kBwdCols, w = idx % kBwdCols;
+            st[(size_t)d * dv + w] = sS0[d * WP + w];
+        }
+        __syncthreads();
+        chunk_inverse<DK>(sm);
+        for (int r = warp; r < C; r += kBwdWarps) {     // Y = K S0
+            float y = 0.f;
+#pragma unroll 8
+            for (int d = 0; d < DK; ++d) y += sK[r * KP + d] * sS0[d * WP + lane];
+            sm[L::kY + r * WP + lane] = y;
+        }
+        __syncthreads();
+        chunk_u<DK>(sm);
+        const float gC = sm[L::kGamma + C - 1];
+        for (int d = warp; d < DK; d += kBwdWarps) {    // S_C = gamma_C S0 + K^T D_e U
+            float acc = 0.f;
+            for (int r = 0; r < C; ++r) acc += sK[r * KP + d] * sm[L::kE + r] * sm[L::kU + r * WP + lane];
+            sS0[d * WP + lane] = gC * sS0[d * WP + lane] + acc;
+        }
+    }
+
+    // ---------------- reverse sweep ----------------
+    __syncthreads();
+    for (int idx = tid; idx < DK * kBwdCols; idx += kBwdThreads) {
+        const int d = idx / kBwdCols, w = idx % kBwdCols;
+        sdS[d * WP + w] = a.dsf ? a.dsf[(((size_t)n * H + h) * DK + d) * dv + col0 + w] : 0.f;
+    }
+    float *pdq = a.gq + (size_t)slice * a.part_stride_k;
+    float *pdk = a.gk + (size_t)slice * a.part_stride_k;
+    float *pdg = a.gg + (size_t)slice * a.part_stride_t;
+    float *pdb = a.gbeta + (size_t)slice * a.part_stride_t;
+    for (int c = nc - 1; c >= 0; --c) {
+        const int t0 = t_begin + c * C;
+        const int len = min(C, t_begin + len_seq - t0);
+        __syncthreads();
+        load_chunk<DK, TI>(a, sm, t0, len, h, col0, true);
+        const float *st = state_ptr(t0);
+        for (int idx = tid; idx < DK * kBwdCols; idx += kBwdThreads) {
+            const int d = idx / kBwdCols, w = idx % kBwdCols;
+            sS0[d * WP + w] = st[(size_t)d * dv + w];
+        }
+        __syncthreads();
+        chunk_inverse<DK>(sm);
+
+        // Q K^T (lower) over A; Y = K S0; K dS; scale dO . (Q S0) per row
+        for (int idx = tid; idx < C * C; idx += kBwdThreads) {
+            const int r = idx / C, i = idx % C;
+            float qk = 0.f;
+            if (i <= r) {
+#pragma unroll 8
+                for (int d = 0; d < DK; ++d) qk += sQ[r * KP + d] * sK[i * KP + d];
+            }
+            sm[L::kA + r * CP + i] = qk;
+        }
+        for (int r = warp; r < C; r += kBwdWarps) {
+            float y = 0.f, qs = 0.f, kd = 0.f;
+#pragma unroll 4
+            for (int d = 0; d < DK; ++d) {
+                const float s0 = sS0[d * WP + lane];
+                const float kr = sK[r * KP + d];
+                y += kr * s0;
+                qs += sQ[r * KP + d] * s0;
+                kd += kr * sdS[d * WP + lane];
+            }
+            sm[L::kY + r * WP + lane] = y;
+            sm[L::kKdS + r * WP + lane] = kd;
+            const float t = warp_sum(sm[L::kdO + r * WP + lane] * qs);
+            if (lane == 0) sm[L::kDgam + r] = scale * t;
+        }
+        __syncthreads();
+        chunk_u<DK>(sm);
+
+        // dU = scale M^T dO + D_e K dS  (into the scratch tile; B is dead)
+        for (int i = warp; i < C; i += kBwdWarps) {
+            float acc = 0.f;
+            for (int r = i; r < C; ++r)
+                acc += sm[L::kGam + r * CP + i] * sm[L::kA + r * CP + i] * sm[L::kdO + r * WP + lane];
+            sm[L::kTmp + i * WP + lane] = scale * acc + sm[L::kE + i] * sm[L::kKdS + i * WP + lane];
+        }
+        __syncthreads();
+        // dB = T^T dU; dv = beta dB (complete for this slice's columns)
+        for (int r = warp; r < C; r += kBwdWarps) {
+            float acc = 0.f;
+            for (int i = r; i < C; ++i) acc += sm[L::kT + i * CP + r] * sm[L::kTmp + i * WP + lane];
+            sm[L::kdB + r * WP + lane] = acc;
+            if (r < len) a.gv[((size_t)(t0 + r) * H + h) * dv + col0 + lane] = sm[L::kBeta + r] * acc;
+        }
+        __syncthreads();
+        // P' = dA . Gamma over T (dead), R = dM . Gamma over Gamma (same element, same thread)
+        for (int idx = tid; idx < C * C; idx += kBwdThreads) {
+            const int r = idx / C, i = idx % C;
+            float pa = 0.f, rm = 0.f;
+            if (i <= r) {
+                float dbu = 0.f, dou = 0.f;
+#pragma unroll 8
+                for (int w = 0; w < kBwdCols; ++w) {
+                    const float u = sm[L::kU + i * WP + w];
+                    dbu += sm[L::kdB + r * WP + w] * u;
+                    dou += sm[L::kdO + r * WP + w] * u;
+                }
+                const float gm = sm[L::kGam + r * CP + i];
+                if (i < r) pa = -gm * dbu;
+                rm = gm * scale * dou;
+            }
+            sm[L::kT + r * CP + i] = pa;
+            sm[L::kGam + r * CP + i] = rm;
+        }
+        __syncthreads();
+        // per-row sums: dbeta, dG's gamma and e terms; and <dS, S0> for gamma_C
+        for (int r = warp; r < C; r += kBwdWarps) {
+            const float db = sm[L::kdB + r * WP + lane], y = sm[L::kY + r * WP + lane];
+            const float a1 = warp_sum((sm[L::kV + r * WP + lane] - sm[L::kGamma + r] * y) * db);
+            const float a2 = warp_sum(db * y);
+            const float a3 = warp_sum(sm[L::kU + r * WP + lane] * sm[L::kKdS + r * WP + lane]);
+            const float a4 = warp_sum(sm[L::kT + r * CP + lane] * sm[L::kKK + r * CP + lane] +
+                                      sm[L::kT + r * CP + 32 + lane] * sm[L::kKK + r * CP + 32 + lane]);
+            if (lane == 0) {
+                sm[L::kDb + r] = a1 + a4;
+                const float dgam = sm[L::kDgam + r] - sm[L::kBeta + r] * a2;
+                sm[L::kDG + r] = dgam * sm[L::kGamma + r] - a3 * sm[L::kE + r];
+                sm[L::kDe + r] = a3;
+            }
+        }
+        {
+            float part = 0.f;
+            for (int idx = tid; idx < DK * kBwdCols; idx += kBwdThreads) {
+                const int d = idx / kBwdCols, w = idx % kBwdCols;
+                part += sdS[d * WP + w] * sS0[d * WP + w];
+            }
+            part = warp_sum(part);
+            if (lane == 0) sm[L::kRed + warp] = part;
+        }
+        __syncthreads();
+        // E = beta_r P' . KK + R . QK (where Gamma enters A and M), over K K^T
+        for (int idx = tid; idx < C * C; idx += kBwdThreads) {
+            const int r = idx / C, i = idx % C;
+            sm[L::kKK + r * CP + i] = sm[L::kBeta + r] * sm[L::kT + r * CP + i] * sm[L::kKK + r * CP + i] +
+                                      sm[L::kGam + r * CP + i] * sm[L::kA + r * CP + i];
+        }
+        __syncthreads();
+        if (tid < C) {
+            const int r = tid;
+            float rs = 0.f, cs = 0.f;
+            for (int i = 0; i < C; ++i) {
+                rs += sm[L::kKK + r * CP + i];
+                cs += sm[L::kKK + i * CP + r];
+            }
+            sm[L::kDG + r] += rs - cs;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // gamma_C = exp(G_{len-1}) and the numerators of e enter at row len-1
+            float t = sm[L::kDe + lane] * sm[L::kE + lane] + sm[L::kDe + 32 + lane] * sm[L::kE + 32 + lane];
+            t = warp_sum(t);
+            float ss = 0.f;
+            for (int w = 0; w < kBwdWarps; ++w) ss += sm[L::kRed + w];
+            const float extra = t + sm[L::kGamma + C - 1] * ss;
+            float x0 = sm[L::kDG + lane], x1 = sm[L::kDG + 32 + lane];
+            if (lane == len - 1) x0 += extra;
+            if (32 + lane == len - 1) x1 += extra;
+            for (int off = 1; off < 32; off <<= 1) {    // suffix sums (reverse cumsum)
+                const float y0 = __shfl_down_sync(0xffffffffu, x0, off);
+                const float y1 = __shfl_down_sync(0xffffffffu, x1, off);
+                if (lane + off < 32) { x0 += y0; x1 += y1; }
+            }
+            x0 += __shfl_sync(0xffffffffu, x1, 0);
+            if (lane < len) {
+                pdg[(size_t)(t0 + lane) * H + h] = x0;
+                pdb[(size_t)(t0 + lane) * H + h] = sm[L::kDb + lane];
+            }
+            if (32 + lane < len) {
+                pdg[(size_t)(t0 + 32 + lane) * H + h] = x1;
+                pdb[(size_t)(t0 + 32 + lane) * H + h] = sm[L::kDb + 32 + lane];
+            }
+        }
+        // dK = (P + P^T) K + R^T Q + D_gamma dX S0 + D_e U dS;  dQ = R K + scale D_gamma dO S0
+        for (int r = warp; r < len; r += kBwdWarps) {
+            float ak[DPL], aq[DPL];
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) ak[j] = aq[j] = 0.f;
+            const float br = sm[L::kBeta + r];
+            for (int i = 0; i < C; ++i) {
+                const float c1 = br * sm[L::kT + r * CP + i] + sm[L::kBeta + i] * sm[L::kT + i * CP + r];
+                const float rir = sm[L::kGam + i * CP + r];
+                const float rri = sm[L::kGam + r * CP + i];
+#pragma unroll
+                for (int j = 0; j < DPL; ++j) {
+                    const float kv = sK[i * KP + lane + 32 * j];
+                    ak[j] += c1 * kv + rir * sQ[i * KP + lane + 32 * j];
+                    aq[j] += rri * kv;
+                }
+            }
+            const float gr = sm[L::kGamma + r], er = sm[L::kE + r];
+            for (int w = 0; w < kBwdCols; ++w) {
+                const float dx = -br * sm[L::kdB + r * WP + w];
+                const float u = sm[L::kU + r * WP + w];
+                const float dov = sm[L::kdO + r * WP + w];
+#pragma unroll
+                for (int j = 0; j < DPL; ++j) {
+                    const int d = lane + 32 * j;
+                    const float s0 = sS0[d * WP + w];
+                    ak[j] += gr * dx * s0 + er * u * sdS[d * WP + w];
+                    aq[j] += scale * gr * dov * s0;
+                }
+            }
+            const size_t base = ((size_t)(t0 + r) * H + h) * DK;
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) {
+                pdk[base + lane + 32 * j] = ak[j];
+                pdq[base + lane + 32 * j] = aq[j];
+            }
+        }
+        __syncthreads();
+        // dS for the chunk before: scale Q^T D_gamma dO + K^T D_gamma dX + gamma_C dS
+        {
+            const float gC = sm[L::kGamma + C - 1];
+            for (int d = warp; d < DK; d += kBwdWarps) {
+                float acc = 0.f;
+                for (int r = 0; r < C; ++r)
+                    acc += sm[L::kGamma + r] * (scale * sQ[r * KP + d] * sm[L::kdO + r * WP + lane] -
+                                                sK[r * KP + d] * sm[L::kBeta + r] * sm[L::kdB + r * WP + lane]);
+                sdS[d * WP + lane] = gC * sdS[d * WP + lane] + acc;
+            }
+        }
+    }
+    __syncthreads();
+    if (a.gs0) {
+        for (int idx = tid; idx < DK * kBwdCols; idx += kBwdThreads) {
+            const int d = idx / kBwdCols, w = idx % kBwdCols;
+            a.gs0[(((size_t)n * H + h) * DK + d) * dv + col0 + w] = sdS[d * WP + w];
+        }
+    }
+}
+
+// out[i] = sum over slices s of part[s * stride + i], the slices added in order
+// (V = float4 for the dq / dk partials, float for dg / dbeta).
+template <typename V>
+__device__ __forceinline__ V add_v(V a, V b);
+template <>
+__device__ __forceinline__ float add_v<float>(float a, float b) { return a + b; }
+template <>
+__device__ __forceinline__ float4 add_v<float4>(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+template <typename V>
+__global__ void __launch_bounds__(256) bwd_reduce_kernel(const V *part, V *out, long long n, long long stride,
+                                                         int slices) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        V s = part[i];
+        for (int sl = 1; sl < slices; ++sl) s = add_v(s, part[(size_t)sl * stride + i]);
+        out[i] = s;
+    }
+}
+
+template <int DK, typename TI>
+cudaError_t launch_bwd_t(const BwdArgs &a, int slices, cudaStream_t s) {
+    const size_t smem = BwdSmem<DK>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<DK, TI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    bwd_kernel<DK, TI><<<dim3(slices, a.H, a.N), kBwdThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+// n elements per slice, slices `stride` elements apart
+cudaError_t launch_reduce(const float *part, float *out, long long n, long long stride, int slices, int sms,
+                          cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    const bool vec = (n % 4 == 0) && (stride % 4 == 0);
+    const long long m = vec ? n / 4 : n;
+    const long long blocks = std::min<long long>((m + 255) / 256, (long long)sms * 8);
+    if (vec)
+        bwd_reduce_kernel<float4><<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4 *>(part),
+                                                                   reinterpret_cast<float4 *>(out), m, stride / 4,
+                                                                   slices);
+    else
+        bwd_reduce_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(part, out, m, stride, slices);
+    return cudaGetLastError();
+}
+
+bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+size_t round_up(size_t x) { return (x + 255) / 256 * 256; }
+
+struct BwdLayout {
+    size_t err, states, pdq, pdk, pdg, pdb, total;
+    int slices;
+    long long total_T;
+    int N;
+};
+
+bool bwd_layout(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, int dtype, BwdLayout *L) {
+    if (B < 1 || T < 0 || H < 1 || H > 4096) return false;
+    if (dtype != GDN_BF16 && dtype != GDN_F32) return false;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return false;
+    if (varlen && (B != 1 || n_seqs < 1)) return false;
+    const int N = varlen ? n_seqs : B;
+    if (N > 65535) return false;
+    const long long total_T = varlen ? (long long)T : (long long)B * T;
+    if (total_T * H * 128 >= (1LL << 40) || total_T >= (1LL << 31)) return false;
+    const long long slots = total_T / C + N;
+    L->slices = dv / kBwdCols;
+    L->total_T = total_T;
+    L->N = N;
+    size_t off = 0;
+    L->err = off;
+    off = round_up(off + sizeof(int));
+    L->states = off;
+    off = round_up(off + (size_t)slots * H * dk * dv * sizeof(float));
+    L->pdq = L->pdk = L->pdg = L->pdb = 0;
+    if (L->slices > 1) {
+        const size_t nk = (size_t)L->slices * total_T * H * dk * sizeof(float);
+        const size_t nt = (size_t)L->slices * total_T * H * sizeof(float);
+        L->pdq = off; off = round_up(off + nk);
+        L->pdk = off; off = round_up(off + nk);
+        L->pdg = off; off = round_up(off + nt);
+        L->pdb = off; off = round_up(off + nt);
+    }
+    L->total = off;
+    return true;
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, gdn_dtype dtype) {
+    BwdLayout L;
+    if (!bwd_layout(B, T, H, dk, dv, n_seqs, varlen, dtype, &L)) return 0;
+    return L.total;
+}
+
+gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                         const float *initial_state, const int32_t *cu_seqlens, int n_seqs, float scale,
+                         int B, int T, int H, int dk, int dv, gdn_dtype dtype,
+                         const void *d_o, const float *d_final_state,
+                         float *dq, float *dk_out, float *dv_out, float *dg, float *dbeta,
+                         float *d_initial_state, void *workspace, size_t workspace_bytes, gdn_stream_t stream_in) {
+    const int varlen = cu_seqlens != nullptr;
+    if (dtype != GDN_BF16 && dtype != GDN_F32) return GDN_ERR_INVALID_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
+    BwdLayout L;
+    if (!bwd_layout(B, T, H, dk, dv, n_seqs, varlen, dtype, &L)) return GDN_ERR_INVALID_ARG;
+    if (!workspace) return GDN_ERR_INVALID_ARG;
+    if (L.total_T > 0 && (!q || !k || !v || !g || !beta || !d_o || !dq || !dk_out || !dv_out || !dg || !dbeta))
+        return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, beta, initial_state, d_o, d_final_state, dq, dk_out, dv_out, dg, dbeta,
+                          d_initial_state, workspace};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    if (workspace_bytes < L.total) return GDN_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_in);
+
+    char *base = static_cast<char *>(workspace);
+    BwdArgs a;
+    a.q = q; a.k = k; a.v = v; a.dout = d_o;
+    a.g = g; a.beta = beta; a.s0 = initial_state; a.dsf = d_final_state; a.cu = cu_seqlens;
+    a.gv = dv_out; a.gs0 = d_initial_state;
+    a.states = reinterpret_cast<float *>(base + L.states);
+    a.err = reinterpret_cast<int *>(base + L.err);
+    if (L.slices > 1) {
+        a.gq = reinterpret_cast<float *>(base + L.pdq);
+        a.gk = reinterpret_cast<float *>(base + L.pdk);
+        a.gg = reinterpret_cast<float *>(base + L.pdg);
+        a.gbeta = reinterpret_cast<float *>(base + L.pdb);
+    } else {
+        a.gq = dq; a.gk = dk_out; a.gg = dg; a.gbeta = dbeta;
+    }
+    a.part_stride_k = L.total_T * H * dk;
+    a.part_stride_t = L.total_T * H;
+    a.T = T; a.H = H; a.N = L.N; a.total_T = (int)L.total_T; a.varlen = varlen;
+    a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)dk);
+
+    cudaError_t e = cudaMemsetAsync(a.err, 0, sizeof(int), s);
+    if (e != cudaSuccess) { set_error_detail("clear error word", e); return GDN_ERR_CUDA; }
+    const bool bf = dtype == GDN_BF16;
+    if (dk == 32) e = bf ? launch_bwd_t<32, __nv_bfloat16>(a, L.slices, s) : launch_bwd_t<32, float>(a, L.slices, s);
+    else if (dk == 64) e = bf ? launch_bwd_t<64, __nv_bfloat16>(a, L.slices, s) : launch_bwd_t<64, float>(a, L.slices, s);
+    else e = bf ? launch_bwd_t<128, __nv_bfloat16>(a, L.slices, s) : launch_bwd_t<128, float>(a, L.slices, s);
+    if (e != cudaSuccess) { set_error_detail("launch backward", e); return GDN_ERR_CUDA; }
+    if (L.slices > 1) {
+        int dev = 0, sms = 152;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            sms = 152;
+        }
+        const long long nk = L.total_T * H * dk, nt = L.total_T * H;
+        if ((e = launch_reduce(a.gq, dq, nk, nk, L.slices, sms, s)) != cudaSuccess ||
+            (e = launch_reduce(a.gk, dk_out, nk, nk, L.slices, sms, s)) != cudaSuccess ||
+            (e = launch_reduce(a.gg, dg, nt, nt, L.slices, sms, s)) != cudaSuccess ||
+            (e = launch_reduce(a.gbeta, dbeta, nt, nt, L.slices, sms, s)) != cudaSuccess) {
+            set_error_detail("launch backward reduce", e);
+            return GDN_ERR_CUDA;
+        }
+    }
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_bwd_check(const void *workspace, gdn_stream_t stream) {
+    return gdn_chunk_fwd_check(workspace, stream);
+}
+
+}  // extern "C"

@@ -29,7 +29,7 @@ from typing import Optional, Sequence
 
 import torch
 
-__all__ = ["WorkloadConfig", "CONFIGS", "config", "make_inputs", "varlen_lengths"]
+__all__ = ["WorkloadConfig", "CONFIGS", "config", "make_inputs", "make_grad_inputs", "varlen_lengths"]
 
 
 @dataclass(frozen=True)
@@ -190,3 +190,15 @@ def make_inputs(cfg: WorkloadConfig, device="cpu", chunk_tokens: int = 1 << 18) 
     return dict(q=q, k=k, v=v, g=g, beta=beta, initial_state=s0,
                 cu_seqlens=None if cu is None else cu.to(device),
                 scale=dk ** -0.5, config=cfg)
+
+
+def make_grad_inputs(cfg: WorkloadConfig, device="cpu", seed_offset: int = 1000, ds_std: float = 0.1) -> dict:
+    """Upstream gradients for the backward pass of workload `cfg`: do like o
+    ([B,T,H,dv], cfg.dtype, standard normal) and d_final_state like the final
+    state ([N,H,dk,dv] fp32, normal with std ds_std), from their own seed."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device).manual_seed(cfg.seed + seed_offset)
+    B, T, H, dk, dv = cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv
+    do = _normal((B, T, H, dv), gen, device).to(_torch_dtype(cfg.dtype))
+    dsf = ds_std * _normal((cfg.num_seqs, H, dk, dv), gen, device)
+    return dict(do=do, d_final_state=dsf)

@@ -1,6 +1,6 @@
 /*
  * gdn.h — C ABI of the GB300 (sm_103a) Gated Delta Network chunked-prefill
- * forward pass.
+ * forward pass (and its backward, gdn_chunk_bwd).
  *
  * The operation (FlashQLA talk "Qwen系列模型线性注意力高性能优化实践", the
  * recurrent-form and GDN paragraphs): for every sequence n and head h, with the
@@ -308,6 +308,51 @@ gdn_status gdn_chunk_fwd_static(const void *q, const void *k, const void *v,
 gdn_status gdn_qk_l2norm(const void *q, const void *k, void *q_out, void *k_out,
                          int64_t rows, int dk, gdn_dtype dtype, float eps,
                          gdn_stream_t stream);
+
+/*
+ * The backward pass: gradients of L = sum <o, d_o> + <final_state,
+ * d_final_state> with respect to q, k, v, g, beta and initial_state, for the
+ * forward pass gdn_chunk_fwd computes (the backward paragraph of the FlashQLA
+ * talk "Qwen系列模型线性注意力高性能优化实践": chunk by chunk in the WY form,
+ * the dA and dA^T terms merged).  The library recomputes the chunk start
+ * states itself (a forward sweep), so the forward's outputs are not inputs.
+ *
+ * Inputs as gdn_chunk_fwd (q, k, v in `dtype`; g, beta, initial_state fp32;
+ * initial_state and cu_seqlens may be NULL), plus
+ *   d_o             [B, T, H, dv]   dtype, the gradient of o
+ *   d_final_state   [N, H, dk, dv]  fp32 or NULL (zero)
+ * Outputs, all fp32 and written in full (no accumulation into them):
+ *   dq, dk          [B, T, H, dk]
+ *   dv              [B, T, H, dv]
+ *   dg, dbeta       [B, T, H]
+ *   d_initial_state [N, H, dk, dv]  (may be NULL: not written)
+ * All pointers are device pointers, 16-byte aligned.  The workspace must hold
+ * gdn_chunk_bwd_workspace_size() bytes (no initialisation needed; it keeps the
+ * chunk start states and, for dv > 32, the per-slice partial sums).  Enqueued
+ * on `stream`; nothing syncs.  The result does not depend on the launch order
+ * of CTAs (partial sums are added in a fixed order).
+ * Errors: GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED / GDN_ERR_WORKSPACE before
+ * any launch; GDN_ERR_CUDA on a launch failure; a malformed cu_seqlens is
+ * written to the workspace's error word, which gdn_chunk_bwd_check() reads.
+ * Preconditions as gdn_chunk_fwd's; n_seqs (or B) at most 65535.
+ */
+size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int n_seqs, int varlen,
+                                    gdn_dtype dtype);
+
+gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v,
+                         const float *g, const float *beta,
+                         const float *initial_state,
+                         const int32_t *cu_seqlens, int n_seqs,
+                         float scale,
+                         int B, int T, int H, int dk, int dv, gdn_dtype dtype,
+                         const void *d_o, const float *d_final_state,
+                         float *dq, float *dk_out, float *dv_out, float *dg, float *dbeta,
+                         float *d_initial_state,
+                         void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/* Synchronises `stream` and reads the error word of a gdn_chunk_bwd
+ * workspace: GDN_OK or GDN_ERR_DEVICE_CHECK (bad cu_seqlens). */
+gdn_status gdn_chunk_bwd_check(const void *workspace, gdn_stream_t stream);
 
 /* The CUDA error (and, for tensor-map encoding, the driver result) behind the
  * most recent GDN_ERR_CUDA returned on the calling host thread, as text such

@@ -144,3 +144,39 @@ def test_qk_l2norm_argument_errors_before_launch(lib):
     assert f(fake, None, fake, fake, 10, 128, gdn.BF16, 0.0, None) == 1     # k NULL, k_out not
     assert f(fake, fake, None, fake, 10, 128, gdn.BF16, 0.0, None) == 1     # q_out NULL, q not
     assert f(fake, fake, fake, fake, 0, 128, gdn.BF16, 0.0, None) == 0      # nothing to do
+
+
+def test_backward_workspace_size(lib):
+    """The backward's workspace holds the chunk start states and, above 32 value
+    columns, the per-slice partial sums; bad shapes give 0."""
+    a = gdn.gdn_chunk_bwd_workspace_size(1, 1000, 4, 128, 32, 1, 0, gdn.BF16)
+    b = gdn.gdn_chunk_bwd_workspace_size(1, 2000, 4, 128, 32, 1, 0, gdn.BF16)
+    c = gdn.gdn_chunk_bwd_workspace_size(1, 2000, 4, 128, 128, 1, 0, gdn.BF16)
+    assert 0 < a < b < c
+    # states: (T/64 + N) slots of H x dk x dv fp32 at least
+    assert b >= (2000 // 64 + 1) * 4 * 128 * 32 * 4
+    # partials of dq, dk (4 slices each) on top of the states for dv = 128
+    assert c >= (2000 // 64 + 1) * 4 * 128 * 128 * 4 + 2 * 4 * 2000 * 4 * 128 * 4
+    assert gdn.gdn_chunk_bwd_workspace_size(1, 10, 4, 48, 128, 1, 0, gdn.BF16) == 0
+    assert gdn.gdn_chunk_bwd_workspace_size(2, 10, 4, 64, 64, 2, 1, gdn.BF16) == 0    # varlen needs B == 1
+    assert gdn.gdn_chunk_bwd_workspace_size(1, 10, 4, 64, 64, 70000, 1, gdn.BF16) == 0
+
+
+def test_backward_argument_errors_before_launch(lib):
+    """Null or misaligned pointers, unsupported head sizes and a short workspace
+    are rejected on the host; these calls never reach the GPU."""
+    fake = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    ws = gdn.gdn_chunk_bwd_workspace_size(1, 256, 2, 32, 64, 1, 0, gdn.F32)
+
+    def call(q=fake, do=fake, dq=fake, wsp=fake, wsb=ws, dk=32, dv=64):
+        return gdn.gdn_chunk_bwd(q, fake, fake, fake, fake, None, None, 1, 0.0, 1, 256, 2, dk, dv, gdn.F32,
+                                 do, None, dq, fake, fake, fake, fake, None, wsp, wsb, None)
+    assert call(q=None) == 1
+    assert call(do=None) == 1
+    assert call(dq=None) == 1
+    assert call(dq=mis) == 1
+    assert call(wsp=None) == 1
+    assert call(wsb=ws - 1) == 3
+    assert call(dk=48) == 2
+    assert call(dv=16) == 2
