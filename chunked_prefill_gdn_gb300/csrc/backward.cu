@@ -637,7 +637,7 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_in);
 
     char *base = static_cast<char *>(workspace);
-    BwdArgs a;
+    BwdArgs a = {};
     a.q = q; a.k = k; a.v = v; a.dout = d_o;
     a.g = g; a.beta = beta; a.s0 = initial_state; a.dsf = d_final_state; a.cu = cu_seqlens;
     a.gv = dv_out; a.gs0 = d_initial_state;
@@ -653,7 +653,7 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
     }
     a.part_stride_k = L.total_T * H * dk;
     a.part_stride_t = L.total_T * H;
-    a.T = T; a.H = H; a.N = L.N; a.total_T = (int)L.total_T; a.varlen = varlen;
+    a.T = T; a.H = H; a.dv = dv; a.N = L.N; a.total_T = (int)L.total_T; a.varlen = varlen;
     a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)dk);
 
     cudaError_t e = cudaMemsetAsync(a.err, 0, sizeof(int), s);
