@@ -40,7 +40,7 @@ namespace gdn {
 namespace {
 
 constexpr int kBwdCols = 32;      // value columns per CTA
-constexpr int kBwdThreads = 256;  // 8 warps
+constexpr int kBwdThreads = 512;  // 16 warps
 constexpr int kBwdWarps = kBwdThreads / 32;
 constexpr int C = kChunk;
 constexpr int CP = C + 1;         // padded row stride of C x C tiles
@@ -78,6 +78,7 @@ struct BwdSmem {
     static constexpr size_t kBytes = (size_t)kFloats * sizeof(float);
 };
 static_assert(BwdSmem<128>::kBytes <= 232448, "backward tile set exceeds the shared memory of a CTA");
+static_assert(kChunk % kBwdWarps == 0 && 32 % kBwdWarps == 0, "rows per warp must divide evenly");
 
 struct BwdArgs {
     const void *q, *k, *v, *dout;
@@ -166,10 +167,9 @@ __device__ void load_chunk(const BwdArgs &a, float *sm, int t0, int len, int h, 
     }
 }
 
-// K K^T (strictly lower), Gamma (lower), A; then T = (I + A)^-1 by forward
-// substitution, one column per thread of warps 0-1.  Ends synchronised.
+// K K^T (strictly lower), Gamma (lower) and A.  Ends synchronised.
 template <int DK>
-__device__ void chunk_inverse(float *sm) {
+__device__ void chunk_gram(float *sm) {
     using L = BwdSmem<DK>;
     constexpr int KP = L::KP;
     const int tid = threadIdx.x;
@@ -189,8 +189,15 @@ __device__ void chunk_inverse(float *sm) {
         sm[L::kA + r * CP + i] = (i < r) ? sm[L::kBeta + r] * gm * kk : 0.f;
     }
     __syncthreads();
-    if (tid < C) {
-        const int j = tid;
+}
+
+// T = (I + A)^-1 by forward substitution, one column per thread; called by
+// warps 0-1 only (the other warps work on tiles it does not touch meanwhile).
+template <int DK>
+__device__ void chunk_solve(float *sm) {
+    using L = BwdSmem<DK>;
+    {
+        const int j = threadIdx.x;
         const float *sA = sm + L::kA;
         float *sT = sm + L::kT;
         for (int r = 0; r < C; ++r) {
@@ -206,7 +213,6 @@ __device__ void chunk_inverse(float *sm) {
             sT[r * CP + j] = (a0 + a1) + (a2 + a3);
         }
     }
-    __syncthreads();
 }
 
 // B = diag(beta)(V - gamma Y) into the scratch tile, then U = T B.  Expects Y
@@ -233,7 +239,9 @@ template <int DK, typename TI>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
     using L = BwdSmem<DK>;
     constexpr int KP = L::KP;
-    constexpr int DPL = DK / 32;    // head-dimension elements per lane
+    constexpr int DPL = DK / 32;          // head-dimension elements per lane
+    constexpr int DPW = DK / kBwdWarps;   // state rows per warp
+    constexpr int RPW = C / kBwdWarps;    // chunk rows per warp
     extern __shared__ float sm[];
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -283,20 +291,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
             st[(size_t)d * dv + w] = sS0[d * WP + w];
         }
         __syncthreads();
-        chunk_inverse<DK>(sm);
-        for (int r = warp; r < C; r += kBwdWarps) {     // Y = K S0
-            float y = 0.f;
+        chunk_gram<DK>(sm);
+        if (warp < 2) {
+            chunk_solve<DK>(sm);
+        } else {
+            for (int r = warp - 2; r < C; r += kBwdWarps - 2) {     // Y = K S0
+                float y = 0.f;
 #pragma unroll 8
-            for (int d = 0; d < DK; ++d) y += sK[r * KP + d] * sS0[d * WP + lane];
-            sm[L::kY + r * WP + lane] = y;
+                for (int d = 0; d < DK; ++d) y += sK[r * KP + d] * sS0[d * WP + lane];
+                sm[L::kY + r * WP + lane] = y;
+            }
         }
         __syncthreads();
         chunk_u<DK>(sm);
-        const float gC = sm[L::kGamma + C - 1];
-        for (int d = warp; d < DK; d += kBwdWarps) {    // S_C = gamma_C S0 + K^T D_e U
-            float acc = 0.f;
-            for (int r = 0; r < C; ++r) acc += sK[r * KP + d] * sm[L::kE + r] * sm[L::kU + r * WP + lane];
-            sS0[d * WP + lane] = gC * sS0[d * WP + lane] + acc;
+        {                                               // S_C = gamma_C S0 + K^T D_e U
+            const float gC = sm[L::kGamma + C - 1];
+            float acc[DPW];
+#pragma unroll
+            for (int m = 0; m < DPW; ++m) acc[m] = 0.f;
+            for (int r = 0; r < C; ++r) {
+                const float eu = sm[L::kE + r] * sm[L::kU + r * WP + lane];
+#pragma unroll
+                for (int m = 0; m < DPW; ++m) acc[m] += sK[r * KP + warp + kBwdWarps * m] * eu;
+            }
+#pragma unroll
+            for (int m = 0; m < DPW; ++m) {
+                const int d = warp + kBwdWarps * m;
+                sS0[d * WP + lane] = gC * sS0[d * WP + lane] + acc[m];
+            }
         }
     }
 
@@ -321,9 +343,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
             sS0[d * WP + w] = st[(size_t)d * dv + w];
         }
         __syncthreads();
-        chunk_inverse<DK>(sm);
-
-        // Q K^T (lower) over A; Y = K S0; K dS; scale dO . (Q S0) per row
+        chunk_gram<DK>(sm);
+        if (warp < 2) {
+            chunk_solve<DK>(sm);
+        } else {
+            // while T is solved: Y = K S0; K dS; scale dO . (Q S0) per row
+            for (int r = warp - 2; r < C; r += kBwdWarps - 2) {
+                float y = 0.f, qs = 0.f, kd = 0.f;
+#pragma unroll 4
+            for (int d = 0; d < DK; ++d) {
+                const float s0 = sS0[d * WP + lane];
+                const float kr = sK[r * KP + d];
+                y += kr * s0;
+                qs += sQ[r * KP + d] * s0;
+                kd += kr * sdS[d * WP + lane];
+            }
+                sm[L::kY + r * WP + lane] = y;
+                sm[L::kKdS + r * WP + lane] = kd;
+                const float t = warp_sum(sm[L::kdO + r * WP + lane] * qs);
+                if (lane == 0) sm[L::kDgam + r] = scale * t;
+            }
+        }
+        __syncthreads();
+        // Q K^T (lower) over A (the solve is done with it)
         for (int idx = tid; idx < C * C; idx += kBwdThreads) {
             const int r = idx / C, i = idx % C;
             float qk = 0.f;
@@ -333,22 +375,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
             }
             sm[L::kA + r * CP + i] = qk;
         }
-        for (int r = warp; r < C; r += kBwdWarps) {
-            float y = 0.f, qs = 0.f, kd = 0.f;
-#pragma unroll 4
-            for (int d = 0; d < DK; ++d) {
-                const float s0 = sS0[d * WP + lane];
-                const float kr = sK[r * KP + d];
-                y += kr * s0;
-                qs += sQ[r * KP + d] * s0;
-                kd += kr * sdS[d * WP + lane];
-            }
-            sm[L::kY + r * WP + lane] = y;
-            sm[L::kKdS + r * WP + lane] = kd;
-            const float t = warp_sum(sm[L::kdO + r * WP + lane] * qs);
-            if (lane == 0) sm[L::kDgam + r] = scale * t;
-        }
-        __syncthreads();
         chunk_u<DK>(sm);
 
         // dU = scale M^T dO + D_e K dS  (into the scratch tile; B is dead)
@@ -412,11 +438,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
             if (lane == 0) sm[L::kRed + warp] = part;
         }
         __syncthreads();
-        // E = beta_r P' . KK + R . QK (where Gamma enters A and M), over K K^T
+        // E = beta_r P' . KK + R . QK (where Gamma enters A and M), over K K^T;
+        // the scaled tiles of the products below over tiles that are dead now:
+        // GX = gamma dX = -gamma beta dB (over dU), GO = scale gamma dO (over Y),
+        // EU = e U (over K dS)
         for (int idx = tid; idx < C * C; idx += kBwdThreads) {
             const int r = idx / C, i = idx % C;
             sm[L::kKK + r * CP + i] = sm[L::kBeta + r] * sm[L::kT + r * CP + i] * sm[L::kKK + r * CP + i] +
                                       sm[L::kGam + r * CP + i] * sm[L::kA + r * CP + i];
+        }
+        for (int idx = tid; idx < C * kBwdCols; idx += kBwdThreads) {
+            const int r = idx / kBwdCols, w = idx % kBwdCols;
+            const float gr = sm[L::kGamma + r];
+            sm[L::kTmp + r * WP + w] = -gr * sm[L::kBeta + r] * sm[L::kdB + r * WP + w];
+            sm[L::kY + r * WP + w] = scale * gr * sm[L::kdO + r * WP + w];
+            sm[L::kKdS + r * WP + w] = sm[L::kE + r] * sm[L::kU + r * WP + w];
         }
         __syncthreads();
         if (tid < C) {
@@ -454,53 +490,92 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
                 pdb[(size_t)(t0 + 32 + lane) * H + h] = sm[L::kDb + 32 + lane];
             }
         }
-        // dK = (P + P^T) K + R^T Q + D_gamma dX S0 + D_e U dS;  dQ = R K + scale D_gamma dO S0
-        for (int r = warp; r < len; r += kBwdWarps) {
-            float ak[DPL], aq[DPL];
+        // dK = (P + P^T) K + R^T Q + D_gamma dX S0 + D_e U dS;  dQ = R K + scale D_gamma dO S0.
+        // Each warp takes rows warp + 16 m (m < RPW) together, so every K, Q and
+        // S0 / dS element it loads serves RPW rows.
+        {
+            float ak[RPW][DPL], aq[RPW][DPL];
 #pragma unroll
-            for (int j = 0; j < DPL; ++j) ak[j] = aq[j] = 0.f;
-            const float br = sm[L::kBeta + r];
+            for (int m = 0; m < RPW; ++m)
+#pragma unroll
+                for (int j = 0; j < DPL; ++j) ak[m][j] = aq[m][j] = 0.f;
             for (int i = 0; i < C; ++i) {
-                const float c1 = br * sm[L::kT + r * CP + i] + sm[L::kBeta + i] * sm[L::kT + i * CP + r];
-                const float rir = sm[L::kGam + i * CP + r];
-                const float rri = sm[L::kGam + r * CP + i];
+                const float bi = sm[L::kBeta + i];
+                float c1[RPW], rir[RPW], rri[RPW];
+#pragma unroll
+                for (int m = 0; m < RPW; ++m) {
+                    const int r = warp + kBwdWarps * m;
+                    c1[m] = sm[L::kBeta + r] * sm[L::kT + r * CP + i] + bi * sm[L::kT + i * CP + r];
+                    rir[m] = sm[L::kGam + i * CP + r];
+                    rri[m] = sm[L::kGam + r * CP + i];
+                }
 #pragma unroll
                 for (int j = 0; j < DPL; ++j) {
                     const float kv = sK[i * KP + lane + 32 * j];
-                    ak[j] += c1 * kv + rir * sQ[i * KP + lane + 32 * j];
-                    aq[j] += rri * kv;
+                    const float qv = sQ[i * KP + lane + 32 * j];
+#pragma unroll
+                    for (int m = 0; m < RPW; ++m) {
+                        ak[m][j] += c1[m] * kv + rir[m] * qv;
+                        aq[m][j] += rri[m] * kv;
+                    }
                 }
             }
-            const float gr = sm[L::kGamma + r], er = sm[L::kE + r];
             for (int w = 0; w < kBwdCols; ++w) {
-                const float dx = -br * sm[L::kdB + r * WP + w];
-                const float u = sm[L::kU + r * WP + w];
-                const float dov = sm[L::kdO + r * WP + w];
+                float gx[RPW], eu[RPW], go[RPW];
+#pragma unroll
+                for (int m = 0; m < RPW; ++m) {
+                    const int r = warp + kBwdWarps * m;
+                    gx[m] = sm[L::kTmp + r * WP + w];
+                    go[m] = sm[L::kY + r * WP + w];
+                    eu[m] = sm[L::kKdS + r * WP + w];
+                }
 #pragma unroll
                 for (int j = 0; j < DPL; ++j) {
                     const int d = lane + 32 * j;
                     const float s0 = sS0[d * WP + w];
-                    ak[j] += gr * dx * s0 + er * u * sdS[d * WP + w];
-                    aq[j] += scale * gr * dov * s0;
+                    const float ds = sdS[d * WP + w];
+#pragma unroll
+                    for (int m = 0; m < RPW; ++m) {
+                        ak[m][j] += gx[m] * s0 + eu[m] * ds;
+                        aq[m][j] += go[m] * s0;
+                    }
                 }
             }
-            const size_t base = ((size_t)(t0 + r) * H + h) * DK;
 #pragma unroll
-            for (int j = 0; j < DPL; ++j) {
-                pdk[base + lane + 32 * j] = ak[j];
-                pdq[base + lane + 32 * j] = aq[j];
+            for (int m = 0; m < RPW; ++m) {
+                const int r = warp + kBwdWarps * m;
+                if (r < len) {
+                    const size_t base = ((size_t)(t0 + r) * H + h) * DK;
+#pragma unroll
+                    for (int j = 0; j < DPL; ++j) {
+                        pdk[base + lane + 32 * j] = ak[m][j];
+                        pdq[base + lane + 32 * j] = aq[m][j];
+                    }
+                }
             }
         }
         __syncthreads();
         // dS for the chunk before: scale Q^T D_gamma dO + K^T D_gamma dX + gamma_C dS
+        // (GO and GX hold scale gamma dO and gamma dX); each warp takes state rows
+        // warp + 16 m (m < DPW) together
         {
             const float gC = sm[L::kGamma + C - 1];
-            for (int d = warp; d < DK; d += kBwdWarps) {
-                float acc = 0.f;
-                for (int r = 0; r < C; ++r)
-                    acc += sm[L::kGamma + r] * (scale * sQ[r * KP + d] * sm[L::kdO + r * WP + lane] -
-                                                sK[r * KP + d] * sm[L::kBeta + r] * sm[L::kdB + r * WP + lane]);
-                sdS[d * WP + lane] = gC * sdS[d * WP + lane] + acc;
+            float acc[DPW];
+#pragma unroll
+            for (int m = 0; m < DPW; ++m) acc[m] = 0.f;
+            for (int r = 0; r < C; ++r) {
+                const float go = sm[L::kY + r * WP + lane];
+                const float gx = sm[L::kTmp + r * WP + lane];
+#pragma unroll
+                for (int m = 0; m < DPW; ++m) {
+                    const int d = warp + kBwdWarps * m;
+                    acc[m] += sQ[r * KP + d] * go + sK[r * KP + d] * gx;
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < DPW; ++m) {
+                const int d = warp + kBwdWarps * m;
+                sdS[d * WP + lane] = gC * sdS[d * WP + lane] + acc[m];
             }
         }
     }
