@@ -8,6 +8,12 @@
 // chunk-local G = cumsum g, gamma = exp(G), Gamma_ri = exp(G_r - G_i),
 // e_i = exp(G_C - G_i)):
 //
+// With bf16 inputs and dk = 128 the two Gram products K K^T and Q K^T (exact
+// bf16 operands, fp32 accumulation) run on the tensor cores: one tcgen05 MMA
+// chain per chunk, [K;Q] (128 x 128, bf16, 128-byte swizzle, written by the
+// chunk loader into shared memory that is dead at that point) times K^T into 64
+// tensor-memory columns, read back by the lane-quadrant warps.
+//
 //   forward   A = strictlower(diag(beta)(Gamma . K K^T)),  T = (I + A)^-1
 //             X = D_gamma K S0^T,  B = diag(beta)(V - X),  U = T B
 //             M = Gamma . tril(Q K^T),  O = scale (D_gamma Q S0^T + M U)
@@ -33,11 +39,15 @@
 #include <math.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "gdn_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace gdn {
 namespace {
+
+using namespace tc;
 
 constexpr int kBwdCols = 32;      // value columns per CTA
 constexpr int kBwdThreads = 512;  // 16 warps
@@ -74,10 +84,16 @@ struct BwdSmem {
     static constexpr int kDb = kDe + C;
     static constexpr int kDG = kDb + C;
     static constexpr int kRed = kDG + C;         // [kBwdWarps]
-    static constexpr int kFloats = kRed + kBwdWarps;
+    static constexpr int kBar = (kRed + kBwdWarps + 1) & ~1;   // mbarrier (8-byte aligned)
+    static constexpr int kTslot = kBar + 2;      // tensor-memory base address, then a zero word
+                                                 // (the bounded wait's abort flag: never set)
+    static constexpr int kFloats = kTslot + 2;
     static constexpr size_t kBytes = (size_t)kFloats * sizeof(float);
 };
 static_assert(BwdSmem<128>::kBytes <= 232448, "backward tile set exceeds the shared memory of a CTA");
+// the [K;Q] operand tile of the tensor-core Gram (32 KB, 1024-byte aligned)
+// lives in the Y .. dB tiles, dead while the Gram runs
+static_assert((BwdSmem<128>::kdB + C * WP - BwdSmem<128>::kY) * 4 >= 32768 + 1008, "operand tile does not fit");
 static_assert(kChunk % kBwdWarps == 0 && 32 % kBwdWarps == 0, "rows per warp must divide evenly");
 
 struct BwdArgs {
@@ -108,6 +124,15 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+// The tensor-core Gram runs for bf16 inputs with dk = 128.
+template <int DK, typename TI>
+constexpr bool kTcGram = DK == 128 && std::is_same<TI, __nv_bfloat16>::value;
+
+template <int DK>
+__device__ __forceinline__ uint32_t operand_tile(float *sm) {
+    return (smem_u32(sm + BwdSmem<DK>::kY) + 1023u) & ~1023u;
+}
+
 // Loads one chunk (rows >= len zero, g = 0 and beta = 0 there, which leaves the
 // algebra of a short chunk unchanged) and forms G, gamma, e in warp 0.
 template <int DK, typename TI>
@@ -116,16 +141,48 @@ __device__ void load_chunk(const BwdArgs &a, float *sm, int t0, int len, int h, 
     constexpr int KP = L::KP;
     const int tid = threadIdx.x;
     const int H = a.H;
-    for (int idx = tid; idx < C * DK; idx += kBwdThreads) {
-        const int r = idx / DK, d = idx % DK;
-        float kv = 0.f, qv = 0.f;
-        if (r < len) {
-            const size_t off = ((size_t)(t0 + r) * H + h) * DK + d;
-            kv = ld_in<TI>(a.k, off);
-            if (with_q) qv = ld_in<TI>(a.q, off);
+    if constexpr (kTcGram<DK, TI>) {
+        // 16-byte loads; fp32 copies plus the bf16 [K;Q] operand tile (two
+        // 16 KB halves of 64 features; row r at r * 128 B, 16-byte chunk c
+        // at (c ^ (r & 7)) * 16), then the proxy fence for the MMA's reads
+        const uint32_t opnd = operand_tile<DK>(sm);
+        for (int idx = tid; idx < C * 16; idx += kBwdThreads) {
+            const int r = idx >> 4, c16 = idx & 15;
+            uint4 kv = make_uint4(0u, 0u, 0u, 0u), qv = kv;
+            if (r < len) {
+                const size_t off = ((size_t)(t0 + r) * H + h) * DK + c16 * 8;
+                kv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.k) + off);
+                if (with_q) qv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.q) + off);
+            }
+            const uint32_t hoff = (uint32_t)(c16 >> 3) * 16384u;
+            sts_u4(opnd + hoff + sw128_offset((uint32_t)r, (uint32_t)(c16 & 7)), kv);
+            if (with_q) sts_u4(opnd + hoff + sw128_offset((uint32_t)(64 + r), (uint32_t)(c16 & 7)), qv);
+            const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w}, qw[4] = {qv.x, qv.y, qv.z, qv.w};
+            float *dk_ = sm + L::kK + r * KP + c16 * 8;
+            float *dq_ = sm + L::kQ + r * KP + c16 * 8;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                dk_[2 * e] = bf16_lo(kw[e]);
+                dk_[2 * e + 1] = bf16_hi(kw[e]);
+                if (with_q) {
+                    dq_[2 * e] = bf16_lo(qw[e]);
+                    dq_[2 * e + 1] = bf16_hi(qw[e]);
+                }
+            }
         }
-        sm[L::kK + r * KP + d] = kv;
-        if (with_q) sm[L::kQ + r * KP + d] = qv;
+        fence_proxy_async_smem();
+    } else {
+        for (int idx = tid; idx < C * DK; idx += kBwdThreads) {
+            const int r = idx / DK, d = idx % DK;
+            float kv = 0.f, qv = 0.f;
+            if (r < len) {
+                const size_t off = ((size_t)(t0 + r) * H + h) * DK + d;
+                kv = ld_in<TI>(a.k, off);
+                if (with_q) qv = ld_in<TI>(a.q, off);
+            }
+            sm[L::kK + r * KP + d] = kv;
+            if (with_q) sm[L::kQ + r * KP + d] = qv;
+        }
     }
     for (int idx = tid; idx < C * kBwdCols; idx += kBwdThreads) {
         const int r = idx / kBwdCols, w = idx % kBwdCols;
@@ -189,6 +246,80 @@ __device__ void chunk_gram(float *sm) {
         sm[L::kA + r * CP + i] = (i < r) ? sm[L::kBeta + r] * gm * kk : 0.f;
     }
     __syncthreads();
+}
+
+// The Gram on the tensor cores: [K;Q] K^T into tensor memory (lanes 0-63
+// K K^T, lanes 64-127 Q K^T; column i), then K K^T, Gamma and A as
+// chunk_gram writes them, from the quadrant-0/1 warps.  Q K^T stays in tensor
+// memory until tc_read_qk.  Ends synchronised.
+template <int DK>
+__device__ void tc_gram(float *sm, uint32_t tbase, uint32_t &phase, int *err) {
+    using L = BwdSmem<DK>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
+    if (warp == 0) {
+        tc_fence_after();
+        if (elect_one()) {
+            constexpr uint32_t I0 = idesc_bf16_f32(128, 64, 0, 0);
+            const uint64_t d = smem_desc_sw128(operand_tile<DK>(sm), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t o = d + ((uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                mma_ss(tbase, o, o, I0, kk > 0);
+            }
+            tc_commit(bar);
+        }
+        __syncwarp();
+    }
+    // bounded (2 s): a wait that runs out records GDN_ERR_TIMEOUT
+    if (!mbar_wait(bar, phase & 1u, reinterpret_cast<volatile int *>(sm + L::kTslot + 1), 2000000000ull) &&
+        threadIdx.x == 0)
+        report_error(err, GDN_ERR_TIMEOUT);
+    ++phase;
+    tc_fence_after();
+    const int q = warp & 3, cb = warp >> 2;
+    if (q < 2) {
+        uint32_t v[16];
+        tmem_ld16(tbase + ((uint32_t)(32 * q) << 16) + 16 * cb, v);
+        tmem_wait_ld();
+        const int r = 32 * q + lane;
+        const float gr = sm[L::kG + r], br = sm[L::kBeta + r];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int i = 16 * cb + u;
+            float kk = 0.f, gm = 0.f;
+            if (i <= r) {
+                gm = expf(gr - sm[L::kG + i]);
+                if (i < r) kk = __uint_as_float(v[u]);
+            }
+            sm[L::kKK + r * CP + i] = kk;
+            sm[L::kGam + r * CP + i] = gm;
+            sm[L::kA + r * CP + i] = (i < r) ? br * gm * kk : 0.f;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+}
+
+// Q K^T (lower) from tensor memory into the A tile (quadrant-2/3 warps).
+template <int DK>
+__device__ void tc_read_qk(float *sm, uint32_t tbase) {
+    using L = BwdSmem<DK>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3, cb = warp >> 2;
+    if (q >= 2) {
+        tc_fence_after();
+        uint32_t v[16];
+        tmem_ld16(tbase + ((uint32_t)(32 * q) << 16) + 16 * cb, v);
+        tmem_wait_ld();
+        const int r = 32 * (q - 2) + lane;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int i = 16 * cb + u;
+            sm[L::kA + r * CP + i] = (i <= r) ? __uint_as_float(v[u]) : 0.f;
+        }
+        tc_fence_before();
+    }
 }
 
 // T = (I + A)^-1 by forward substitution, one column per thread; called by
@@ -264,6 +395,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         len_seq = a.T;
     }
     const int nc = (len_seq + C - 1) / C;
+    constexpr bool TC = kTcGram<DK, TI>;
+    uint32_t tbase = 0, phase = 0;
+    if constexpr (TC) {
+        if (tid == 0) {
+            mbar_init(reinterpret_cast<uint64_t *>(sm + L::kBar), 1);
+            reinterpret_cast<int *>(sm + L::kTslot)[1] = 0;
+            fence_barrier_init();
+        }
+        if (warp == 0) {
+            tmem_alloc(reinterpret_cast<uint32_t *>(sm + L::kTslot), 64);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        tbase = *reinterpret_cast<volatile uint32_t *>(sm + L::kTslot);
+    }
     // chunk c of this sequence stores its start state in slot (first token)/C + n:
     // distinct for distinct chunks and below total_T/C + N
     auto state_ptr = [&](int t0) {
@@ -291,7 +439,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
             st[(size_t)d * dv + w] = sS0[d * WP + w];
         }
         __syncthreads();
-        chunk_gram<DK>(sm);
+        if constexpr (TC) tc_gram<DK>(sm, tbase, phase, a.err); else chunk_gram<DK>(sm);
         if (warp < 2) {
             chunk_solve<DK>(sm);
         } else {
@@ -343,7 +491,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
             sS0[d * WP + w] = st[(size_t)d * dv + w];
         }
         __syncthreads();
-        chunk_gram<DK>(sm);
+        if constexpr (TC) tc_gram<DK>(sm, tbase, phase, a.err); else chunk_gram<DK>(sm);
         if (warp < 2) {
             chunk_solve<DK>(sm);
         } else {
@@ -366,14 +514,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         }
         __syncthreads();
         // Q K^T (lower) over A (the solve is done with it)
-        for (int idx = tid; idx < C * C; idx += kBwdThreads) {
-            const int r = idx / C, i = idx % C;
-            float qk = 0.f;
-            if (i <= r) {
+        if constexpr (TC) {
+            tc_read_qk<DK>(sm, tbase);
+        } else {
+            for (int idx = tid; idx < C * C; idx += kBwdThreads) {
+                const int r = idx / C, i = idx % C;
+                float qk = 0.f;
+                if (i <= r) {
 #pragma unroll 8
-                for (int d = 0; d < DK; ++d) qk += sQ[r * KP + d] * sK[i * KP + d];
+                    for (int d = 0; d < DK; ++d) qk += sQ[r * KP + d] * sK[i * KP + d];
+                }
+                sm[L::kA + r * CP + i] = qk;
             }
-            sm[L::kA + r * CP + i] = qk;
         }
         chunk_u<DK>(sm);
 
@@ -579,11 +731,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
             }
         }
     }
+    if constexpr (TC) tc_fence_before();
     __syncthreads();
     if (a.gs0) {
         for (int idx = tid; idx < DK * kBwdCols; idx += kBwdThreads) {
             const int d = idx / kBwdCols, w = idx % kBwdCols;
             a.gs0[(((size_t)n * H + h) * DK + d) * dv + col0 + w] = sdS[d * WP + w];
+        }
+    }
+    if constexpr (TC) {
+        if (warp == 0) {
+            tc_fence_after();
+            tmem_dealloc(tbase, 64);
         }
     }
 }
