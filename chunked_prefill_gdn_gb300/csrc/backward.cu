@@ -56,10 +56,13 @@ constexpr int C = kChunk;
 constexpr int CP = C + 1;         // padded row stride of C x C tiles
 constexpr int WP = kBwdCols + 1;  // padded row stride of C x 32 and dk x 32 tiles
 
-// Shared-memory layout (in floats) for head dimension DK.
-template <int DK>
+// Shared-memory layout (in floats) for head dimension DK.  K and Q rows are
+// padded to an odd length (conflict-free column walks of the CUDA-core Gram),
+// or with W (the tensor-core Gram, no column walks) to a multiple of four
+// floats, so that a row's elements load four at a time.
+template <int DK, bool W = false>
 struct BwdSmem {
-    static constexpr int KP = DK + 1;
+    static constexpr int KP = W ? DK + 4 : DK + 1;
     static constexpr int kK = 0;                 // K      [C][KP]
     static constexpr int kQ = kK + C * KP;       // Q      [C][KP]
     static constexpr int kS0 = kQ + C * KP;      // S0     [DK][WP]  chunk start state (slice)
@@ -90,10 +93,12 @@ struct BwdSmem {
     static constexpr int kFloats = kTslot + 2;
     static constexpr size_t kBytes = (size_t)kFloats * sizeof(float);
 };
-static_assert(BwdSmem<128>::kBytes <= 232448, "backward tile set exceeds the shared memory of a CTA");
+static_assert(BwdSmem<128>::kBytes <= 232448 && BwdSmem<128, true>::kBytes <= 232448,
+              "backward tile set exceeds the shared memory of a CTA");
 // the [K;Q] operand tile of the tensor-core Gram (32 KB, 1024-byte aligned)
 // lives in the Y .. dB tiles, dead while the Gram runs
-static_assert((BwdSmem<128>::kdB + C * WP - BwdSmem<128>::kY) * 4 >= 32768 + 1008, "operand tile does not fit");
+static_assert((BwdSmem<128, true>::kdB + C * WP - BwdSmem<128, true>::kY) * 4 >= 32768 + 1008,
+              "operand tile does not fit");
 static_assert(kChunk % kBwdWarps == 0 && 32 % kBwdWarps == 0, "rows per warp must divide evenly");
 
 struct BwdArgs {
@@ -119,6 +124,14 @@ __device__ __forceinline__ float ld_in<__nv_bfloat16>(const void *base, size_t i
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
 }
 
+// Four consecutive floats: one 16-byte load when the row layout keeps them
+// 16-byte aligned (V), else four loads.
+template <bool V>
+__device__ __forceinline__ float4 ld4f(const float *p) {
+    if constexpr (V) return *reinterpret_cast<const float4 *>(p);
+    else return make_float4(p[0], p[1], p[2], p[3]);
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
     for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
     return x;
@@ -128,16 +141,16 @@ __device__ __forceinline__ float warp_sum(float x) {
 template <int DK, typename TI>
 constexpr bool kTcGram = DK == 128 && std::is_same<TI, __nv_bfloat16>::value;
 
-template <int DK>
+template <int DK, bool W>
 __device__ __forceinline__ uint32_t operand_tile(float *sm) {
-    return (smem_u32(sm + BwdSmem<DK>::kY) + 1023u) & ~1023u;
+    return (smem_u32(sm + BwdSmem<DK, W>::kY) + 1023u) & ~1023u;
 }
 
 // Loads one chunk (rows >= len zero, g = 0 and beta = 0 there, which leaves the
 // algebra of a short chunk unchanged) and forms G, gamma, e in warp 0.
 template <int DK, typename TI>
 __device__ void load_chunk(const BwdArgs &a, float *sm, int t0, int len, int h, int col0, bool with_q) {
-    using L = BwdSmem<DK>;
+    using L = BwdSmem<DK, kTcGram<DK, TI>>;
     constexpr int KP = L::KP;
     const int tid = threadIdx.x;
     const int H = a.H;
@@ -145,7 +158,7 @@ __device__ void load_chunk(const BwdArgs &a, float *sm, int t0, int len, int h, 
         // 16-byte loads; fp32 copies plus the bf16 [K;Q] operand tile (two
         // 16 KB halves of 64 features; row r at r * 128 B, 16-byte chunk c
         // at (c ^ (r & 7)) * 16), then the proxy fence for the MMA's reads
-        const uint32_t opnd = operand_tile<DK>(sm);
+        const uint32_t opnd = operand_tile<DK, true>(sm);
         for (int idx = tid; idx < C * 16; idx += kBwdThreads) {
             const int r = idx >> 4, c16 = idx & 15;
             uint4 kv = make_uint4(0u, 0u, 0u, 0u), qv = kv;
@@ -157,17 +170,13 @@ __device__ void load_chunk(const BwdArgs &a, float *sm, int t0, int len, int h, 
             const uint32_t hoff = (uint32_t)(c16 >> 3) * 16384u;
             sts_u4(opnd + hoff + sw128_offset((uint32_t)r, (uint32_t)(c16 & 7)), kv);
             if (with_q) sts_u4(opnd + hoff + sw128_offset((uint32_t)(64 + r), (uint32_t)(c16 & 7)), qv);
-            const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w}, qw[4] = {qv.x, qv.y, qv.z, qv.w};
-            float *dk_ = sm + L::kK + r * KP + c16 * 8;
-            float *dq_ = sm + L::kQ + r * KP + c16 * 8;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                dk_[2 * e] = bf16_lo(kw[e]);
-                dk_[2 * e + 1] = bf16_hi(kw[e]);
-                if (with_q) {
-                    dq_[2 * e] = bf16_lo(qw[e]);
-                    dq_[2 * e + 1] = bf16_hi(qw[e]);
-                }
+            float4 *dk4 = reinterpret_cast<float4 *>(sm + L::kK + r * KP + c16 * 8);   // KP % 4 == 0
+            dk4[0] = make_float4(bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y));
+            dk4[1] = make_float4(bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w));
+            if (with_q) {
+                float4 *dq4 = reinterpret_cast<float4 *>(sm + L::kQ + r * KP + c16 * 8);
+                dq4[0] = make_float4(bf16_lo(qv.x), bf16_hi(qv.x), bf16_lo(qv.y), bf16_hi(qv.y));
+                dq4[1] = make_float4(bf16_lo(qv.z), bf16_hi(qv.z), bf16_lo(qv.w), bf16_hi(qv.w));
             }
         }
         fence_proxy_async_smem();
@@ -225,9 +234,9 @@ __device__ void load_chunk(const BwdArgs &a, float *sm, int t0, int len, int h, 
 }
 
 // K K^T (strictly lower), Gamma (lower) and A.  Ends synchronised.
-template <int DK>
+template <int DK, bool W>
 __device__ void chunk_gram(float *sm) {
-    using L = BwdSmem<DK>;
+    using L = BwdSmem<DK, W>;
     constexpr int KP = L::KP;
     const int tid = threadIdx.x;
     const float *sK = sm + L::kK;
@@ -252,16 +261,16 @@ __device__ void chunk_gram(float *sm) {
 // K K^T, lanes 64-127 Q K^T; column i), then K K^T, Gamma and A as
 // chunk_gram writes them, from the quadrant-0/1 warps.  Q K^T stays in tensor
 // memory until tc_read_qk.  Ends synchronised.
-template <int DK>
+template <int DK, bool W>
 __device__ void tc_gram(float *sm, uint32_t tbase, uint32_t &phase, int *err) {
-    using L = BwdSmem<DK>;
+    using L = BwdSmem<DK, W>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
     if (warp == 0) {
         tc_fence_after();
         if (elect_one()) {
             constexpr uint32_t I0 = idesc_bf16_f32(128, 64, 0, 0);
-            const uint64_t d = smem_desc_sw128(operand_tile<DK>(sm), 16, 1024);
+            const uint64_t d = smem_desc_sw128(operand_tile<DK, W>(sm), 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t o = d + ((uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
@@ -302,9 +311,9 @@ __device__ void tc_gram(float *sm, uint32_t tbase, uint32_t &phase, int *err) {
 }
 
 // Q K^T (lower) from tensor memory into the A tile (quadrant-2/3 warps).
-template <int DK>
+template <int DK, bool W>
 __device__ void tc_read_qk(float *sm, uint32_t tbase) {
-    using L = BwdSmem<DK>;
+    using L = BwdSmem<DK, W>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, cb = warp >> 2;
     if (q >= 2) {
@@ -324,9 +333,9 @@ __device__ void tc_read_qk(float *sm, uint32_t tbase) {
 
 // T = (I + A)^-1 by forward substitution, one column per thread; called by
 // warps 0-1 only (the other warps work on tiles it does not touch meanwhile).
-template <int DK>
+template <int DK, bool W>
 __device__ void chunk_solve(float *sm) {
-    using L = BwdSmem<DK>;
+    using L = BwdSmem<DK, W>;
     {
         const int j = threadIdx.x;
         const float *sA = sm + L::kA;
@@ -348,9 +357,9 @@ __device__ void chunk_solve(float *sm) {
 
 // B = diag(beta)(V - gamma Y) into the scratch tile, then U = T B.  Expects Y
 // in place and ends synchronised.
-template <int DK>
+template <int DK, bool W>
 __device__ void chunk_u(float *sm) {
-    using L = BwdSmem<DK>;
+    using L = BwdSmem<DK, W>;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int idx = tid; idx < C * kBwdCols; idx += kBwdThreads) {
         const int r = idx / kBwdCols, w = idx % kBwdCols;
@@ -368,12 +377,13 @@ __device__ void chunk_u(float *sm) {
 
 template <int DK, typename TI>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
-    using L = BwdSmem<DK>;
+    constexpr bool TC = kTcGram<DK, TI>;
+    using L = BwdSmem<DK, TC>;
     constexpr int KP = L::KP;
     constexpr int DPL = DK / 32;          // head-dimension elements per lane
-    constexpr int DPW = DK / kBwdWarps;   // state rows per warp
+    constexpr int DPW = DK / kBwdWarps;   // state rows per warp (a contiguous block)
     constexpr int RPW = C / kBwdWarps;    // chunk rows per warp
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = a.H, dv = a.dv, col0 = slice * kBwdCols;
@@ -395,7 +405,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         len_seq = a.T;
     }
     const int nc = (len_seq + C - 1) / C;
-    constexpr bool TC = kTcGram<DK, TI>;
     uint32_t tbase = 0, phase = 0;
     if constexpr (TC) {
         if (tid == 0) {
@@ -439,32 +448,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
             st[(size_t)d * dv + w] = sS0[d * WP + w];
         }
         __syncthreads();
-        if constexpr (TC) tc_gram<DK>(sm, tbase, phase, a.err); else chunk_gram<DK>(sm);
+        if constexpr (TC) tc_gram<DK, TC>(sm, tbase, phase, a.err); else chunk_gram<DK, TC>(sm);
         if (warp < 2) {
-            chunk_solve<DK>(sm);
+            chunk_solve<DK, TC>(sm);
         } else {
             for (int r = warp - 2; r < C; r += kBwdWarps - 2) {     // Y = K S0
                 float y = 0.f;
-#pragma unroll 8
-                for (int d = 0; d < DK; ++d) y += sK[r * KP + d] * sS0[d * WP + lane];
+#pragma unroll 2
+                for (int d = 0; d < DK; d += 4) {
+                    const float4 k4 = ld4f<TC>(sK + r * KP + d);
+                    y += k4.x * sS0[d * WP + lane] + k4.y * sS0[(d + 1) * WP + lane] +
+                         k4.z * sS0[(d + 2) * WP + lane] + k4.w * sS0[(d + 3) * WP + lane];
+                }
                 sm[L::kY + r * WP + lane] = y;
             }
         }
         __syncthreads();
-        chunk_u<DK>(sm);
+        chunk_u<DK, TC>(sm);
         {                                               // S_C = gamma_C S0 + K^T D_e U
             const float gC = sm[L::kGamma + C - 1];
             float acc[DPW];
 #pragma unroll
             for (int m = 0; m < DPW; ++m) acc[m] = 0.f;
+            const int d0 = warp * DPW;                  // this warp's state rows d0 .. d0 + DPW - 1
             for (int r = 0; r < C; ++r) {
                 const float eu = sm[L::kE + r] * sm[L::kU + r * WP + lane];
+                if constexpr (DPW % 4 == 0) {
 #pragma unroll
-                for (int m = 0; m < DPW; ++m) acc[m] += sK[r * KP + warp + kBwdWarps * m] * eu;
+                    for (int m = 0; m < DPW; m += 4) {
+                        const float4 k4 = ld4f<TC>(sK + r * KP + d0 + m);
+                        acc[m] += k4.x * eu; acc[m + 1] += k4.y * eu; acc[m + 2] += k4.z * eu; acc[m + 3] += k4.w * eu;
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < DPW; ++m) acc[m] += sK[r * KP + d0 + m] * eu;
+                }
             }
 #pragma unroll
             for (int m = 0; m < DPW; ++m) {
-                const int d = warp + kBwdWarps * m;
+                const int d = d0 + m;
                 sS0[d * WP + lane] = gC * sS0[d * WP + lane] + acc[m];
             }
         }
@@ -491,21 +513,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
             sS0[d * WP + w] = st[(size_t)d * dv + w];
         }
         __syncthreads();
-        if constexpr (TC) tc_gram<DK>(sm, tbase, phase, a.err); else chunk_gram<DK>(sm);
+        if constexpr (TC) tc_gram<DK, TC>(sm, tbase, phase, a.err); else chunk_gram<DK, TC>(sm);
         if (warp < 2) {
-            chunk_solve<DK>(sm);
+            chunk_solve<DK, TC>(sm);
         } else {
             // while T is solved: Y = K S0; K dS; scale dO . (Q S0) per row
             for (int r = warp - 2; r < C; r += kBwdWarps - 2) {
                 float y = 0.f, qs = 0.f, kd = 0.f;
-#pragma unroll 4
-            for (int d = 0; d < DK; ++d) {
-                const float s0 = sS0[d * WP + lane];
-                const float kr = sK[r * KP + d];
-                y += kr * s0;
-                qs += sQ[r * KP + d] * s0;
-                kd += kr * sdS[d * WP + lane];
-            }
+#pragma unroll 2
+                for (int d = 0; d < DK; d += 4) {
+                    const float4 k4 = ld4f<TC>(sK + r * KP + d);
+                    const float4 q4 = ld4f<TC>(sQ + r * KP + d);
+                    const float s0a = sS0[d * WP + lane], s0b = sS0[(d + 1) * WP + lane];
+                    const float s0c = sS0[(d + 2) * WP + lane], s0d = sS0[(d + 3) * WP + lane];
+                    y += k4.x * s0a + k4.y * s0b + k4.z * s0c + k4.w * s0d;
+                    qs += q4.x * s0a + q4.y * s0b + q4.z * s0c + q4.w * s0d;
+                    kd += k4.x * sdS[d * WP + lane] + k4.y * sdS[(d + 1) * WP + lane] +
+                          k4.z * sdS[(d + 2) * WP + lane] + k4.w * sdS[(d + 3) * WP + lane];
+                }
                 sm[L::kY + r * WP + lane] = y;
                 sm[L::kKdS + r * WP + lane] = kd;
                 const float t = warp_sum(sm[L::kdO + r * WP + lane] * qs);
@@ -515,7 +540,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         __syncthreads();
         // Q K^T (lower) over A (the solve is done with it)
         if constexpr (TC) {
-            tc_read_qk<DK>(sm, tbase);
+            tc_read_qk<DK, TC>(sm, tbase);
         } else {
             for (int idx = tid; idx < C * C; idx += kBwdThreads) {
                 const int r = idx / C, i = idx % C;
@@ -527,7 +552,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
                 sm[L::kA + r * CP + i] = qk;
             }
         }
-        chunk_u<DK>(sm);
+        chunk_u<DK, TC>(sm);
 
         // dU = scale M^T dO + D_e K dS  (into the scratch tile; B is dead)
         for (int i = warp; i < C; i += kBwdWarps) {
@@ -708,25 +733,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         }
         __syncthreads();
         // dS for the chunk before: scale Q^T D_gamma dO + K^T D_gamma dX + gamma_C dS
-        // (GO and GX hold scale gamma dO and gamma dX); each warp takes state rows
-        // warp + 16 m (m < DPW) together
+        // (GO and GX hold scale gamma dO and gamma dX); each warp takes DPW
+        // consecutive state rows together
         {
             const float gC = sm[L::kGamma + C - 1];
             float acc[DPW];
 #pragma unroll
             for (int m = 0; m < DPW; ++m) acc[m] = 0.f;
+            const int d0 = warp * DPW;                  // this warp's state rows d0 .. d0 + DPW - 1
             for (int r = 0; r < C; ++r) {
                 const float go = sm[L::kY + r * WP + lane];
                 const float gx = sm[L::kTmp + r * WP + lane];
+                if constexpr (DPW % 4 == 0) {
 #pragma unroll
-                for (int m = 0; m < DPW; ++m) {
-                    const int d = warp + kBwdWarps * m;
-                    acc[m] += sQ[r * KP + d] * go + sK[r * KP + d] * gx;
+                    for (int m = 0; m < DPW; m += 4) {
+                        const float4 q4 = ld4f<TC>(sQ + r * KP + d0 + m);
+                        const float4 k4 = ld4f<TC>(sK + r * KP + d0 + m);
+                        acc[m] += q4.x * go + k4.x * gx;
+                        acc[m + 1] += q4.y * go + k4.y * gx;
+                        acc[m + 2] += q4.z * go + k4.z * gx;
+                        acc[m + 3] += q4.w * go + k4.w * gx;
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < DPW; ++m) acc[m] += sQ[r * KP + d0 + m] * go + sK[r * KP + d0 + m] * gx;
                 }
             }
 #pragma unroll
             for (int m = 0; m < DPW; ++m) {
-                const int d = warp + kBwdWarps * m;
+                const int d = d0 + m;
                 sdS[d * WP + lane] = gC * sdS[d * WP + lane] + acc[m];
             }
         }
@@ -771,7 +806,7 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(const V *part, V *out, 
 
 template <int DK, typename TI>
 cudaError_t launch_bwd_t(const BwdArgs &a, int slices, cudaStream_t s) {
-    const size_t smem = BwdSmem<DK>::kBytes;
+    const size_t smem = BwdSmem<DK, kTcGram<DK, TI>>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(bwd_kernel<DK, TI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     bwd_kernel<DK, TI><<<dim3(slices, a.H, a.N), kBwdThreads, smem, s>>>(a);
