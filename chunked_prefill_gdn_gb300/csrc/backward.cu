@@ -8,12 +8,6 @@
 // chunk-local G = cumsum g, gamma = exp(G), Gamma_ri = exp(G_r - G_i),
 // e_i = exp(G_C - G_i)):
 //
-// With bf16 inputs and dk = 128 the two Gram products K K^T and Q K^T (exact
-// bf16 operands, fp32 accumulation) run on the tensor cores: one tcgen05 MMA
-// chain per chunk, [K;Q] (128 x 128, bf16, 128-byte swizzle, written by the
-// chunk loader into shared memory that is dead at that point) times K^T into 64
-// tensor-memory columns, read back by the lane-quadrant warps.
-//
 //   forward   A = strictlower(diag(beta)(Gamma . K K^T)),  T = (I + A)^-1
 //             X = D_gamma K S0^T,  B = diag(beta)(V - X),  U = T B
 //             M = Gamma . tril(Q K^T),  O = scale (D_gamma Q S0^T + M U)
@@ -34,8 +28,15 @@
 // in the workspace, then a reverse sweep carries dS from the last chunk to the
 // first.  dv, dS0 come out complete per slice; dq, dk, dg, dbeta are sums over
 // the dv columns, so each slice writes its partial and a second kernel adds the
-// slices in a fixed order (deterministic, no atomics).  Everything is fp32 on
-// CUDA cores with operands in shared memory (padded strides, conflict-free).
+// slices in a fixed order (deterministic, no atomics).
+//
+// With bf16 inputs and dk = 128 the two Gram products K K^T and Q K^T (exact
+// bf16 operands, fp32 accumulation) run on the tensor cores: one tcgen05 MMA
+// chain per chunk, [K;Q] (128 x 128, bf16, 128-byte swizzle, written by the
+// chunk loader into shared memory that is dead at that point) times K^T into 64
+// tensor-memory columns, read back by the lane-quadrant warps.  All other
+// products are fp32 on CUDA cores with operands in shared memory (padded
+// strides, conflict-free), the work of each phase spread over the 16 warps.
 #include <math.h>
 
 #include <algorithm>

@@ -1,4 +1,4 @@
-// Inline-PTX wrappers for the sm_103a fused kernel: mbarriers with bounded
+// Inline-PTX wrappers for the sm_103a kernels: mbarriers with bounded
 // waits, TMA tensor copies, and the tcgen05 tensor-memory / MMA instructions.
 #pragma once
 

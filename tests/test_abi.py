@@ -180,3 +180,4 @@ def test_backward_argument_errors_before_launch(lib):
     assert call(wsb=ws - 1) == 3
     assert call(dk=48) == 2
     assert call(dv=16) == 2
+    assert gdn.gdn_chunk_bwd_check(None, None) == 1
