@@ -8,6 +8,7 @@ call raises.
     o, final_state = chunk_fwd(q, k, v, g, beta, initial_state=None,
                                cu_seqlens=None, scale=None)
     dq, dk, dv, dg, dbeta, d_initial_state = chunk_bwd(q, k, v, g, beta, do, ...)
+    o, final_state = chunk_gated_delta_rule(q, k, v, g, beta, ...)   # autograd
 
 q, k [B,T,H,dk] and v [B,T,H,dv] in bf16 or fp32, g and beta [B,T,H] fp32,
 initial_state [N,H,dk,dv] fp32, cu_seqlens int32 [N+1] (then B = 1), all on
@@ -30,6 +31,7 @@ __all__ = [
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
     "gdn_chunk_fwd_static", "gdn_qk_l2norm", "qk_l2norm",
     "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd", "gdn_chunk_bwd_check", "chunk_bwd",
+    "chunk_gated_delta_rule",
     "gdn_status_string", "gdn_version", "gdn_last_error_detail", "chunk_fwd", "chunk_fwd_host", "workspace_for", "GdnError",
     "CP_AUTO", "CP_OFF", "CP_FORCE", "KERNEL_AUTO", "KERNEL_TC", "KERNEL_SIMT", "BF16", "F32",
     "STAGE_PREP", "STAGE_INVERSE", "STAGE_CORRECTION", "STAGE_FUSED",
@@ -399,3 +401,49 @@ def chunk_bwd(q, k, v, g, beta, do, initial_state=None, cu_seqlens=None, scale=N
         if st != 0:
             raise GdnError(st, "device check")
     return dq, dk_, dv_, dg, db, ds0
+
+
+class _ChunkGDN(torch.autograd.Function):
+    """gdn_chunk_fwd forward, gdn_chunk_bwd backward (the fp32 gradients of q,
+    k, v are handed back in the inputs' dtype)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, scale, opts):
+        o, final_state = chunk_fwd(q, k, v, g, beta, initial_state, cu_seqlens, scale, opts=opts)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
+        ctx.scale = scale
+        return o, final_state
+
+    @staticmethod
+    def backward(ctx, do, d_final_state):
+        q, k, v, g, beta, initial_state, cu_seqlens = ctx.saved_tensors
+        if do is None:
+            do = torch.zeros(*q.shape[:-1], v.shape[-1], dtype=q.dtype, device=q.device)
+        dq, dk, dv, dg, dbeta, ds0 = chunk_bwd(
+            q, k, v, g, beta, do.contiguous(), initial_state, cu_seqlens, ctx.scale,
+            d_final_state.contiguous() if d_final_state is not None else None)
+        dt = q.dtype
+        return (dq.to(dt), dk.to(dt), dv.to(dt), dg, dbeta, (ds0 if initial_state is not None else None),
+                None, None, None)
+
+
+def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
+                           cu_seqlens=None, use_qk_l2norm_in_kernel=False, cp_mode=CP_AUTO):
+    """The high-level entry point with autograd: o (and the final state when
+    output_final_state) from q, k [B,T,H,dk], v [B,T,H,dv] (bf16 or fp32), the
+    log-decay gate g and beta [B,T,H] (fp32), an optional initial state
+    [N,H,dk,dv] (fp32) and cu_seqlens (int32, packed batch with B = 1).
+    Gradients flow to q, k, v, g, beta and the initial state through
+    gdn_chunk_bwd.  use_qk_l2norm_in_kernel normalises q and k inside the
+    forward (opts.qk_l2norm); it has no backward here, so it is refused when a
+    gradient is needed."""
+    needs_grad = torch.is_grad_enabled() and any(
+        t is not None and t.requires_grad for t in (q, k, v, g, beta, initial_state))
+    if use_qk_l2norm_in_kernel and needs_grad:
+        raise NotImplementedError("use_qk_l2norm_in_kernel has no backward; normalise q and k before the call")
+    q, k, v, g, beta = (t.contiguous() for t in (q, k, v, g, beta))
+    if initial_state is not None:
+        initial_state = initial_state.contiguous()
+    opts = default_options(qk_l2norm=1 if use_qk_l2norm_in_kernel else 0, cp_mode=cp_mode)
+    o, final_state = _ChunkGDN.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, opts)
+    return o, (final_state if output_final_state else None)

@@ -181,3 +181,13 @@ def test_backward_argument_errors_before_launch(lib):
     assert call(dk=48) == 2
     assert call(dv=16) == 2
     assert gdn.gdn_chunk_bwd_check(None, None) == 1
+
+
+def test_autograd_entry_refuses_in_kernel_normalisation_with_gradients():
+    """The in-kernel q/k normalisation has no backward: asking for gradients
+    with it is refused on the host, before any device call."""
+    import torch
+    q = torch.zeros(1, 4, 1, 32, requires_grad=True)
+    with pytest.raises(NotImplementedError):
+        gdn.chunk_gated_delta_rule(q, q, q, torch.zeros(1, 4, 1), torch.zeros(1, 4, 1),
+                                   use_qk_l2norm_in_kernel=True)

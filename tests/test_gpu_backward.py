@@ -150,3 +150,28 @@ def test_backward_full_layer_sampled():
         for name, x, r in zip(NAMES, got, ref):
             x = x[n:n + 1, h:h + 1] if name == "d_initial_state" else x[n:n + 1, :, h:h + 1]
             check("layer n=%d h=%d %s" % (n, h, name), x.cpu(), r)
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "layer_bf16"])
+def test_autograd_entry_matches_oracle(name):
+    """chunk_gated_delta_rule under autograd: loss.backward() through the
+    forward and backward kernels gives the oracle's gradients for q, k, v, g,
+    beta and the initial state (bf16 gradients carry one more rounding)."""
+    cfg = CONFIGS[0] if name == "tiny_f32" else CONFIGS[1].scaled(B=1, T=150, H=2)
+    inp = with_initial_state(make_inputs(cfg, "cpu"), seed=9)
+    names = ("q", "k", "v", "g", "beta", "initial_state")
+    leaves = {n: inp[n].cuda().clone().requires_grad_() for n in names}
+    o, sf = gdn.chunk_gated_delta_rule(leaves["q"], leaves["k"], leaves["v"], leaves["g"], leaves["beta"],
+                                       scale=inp["scale"], initial_state=leaves["initial_state"],
+                                       output_final_state=True)
+    gen = torch.Generator().manual_seed(4)
+    w_o = torch.randn(o.shape, generator=gen).to(o.dtype)
+    w_s = 0.1 * torch.randn(sf.shape, generator=gen)
+    loss = (o.float() * w_o.cuda().float()).sum() + (sf * w_s.cuda()).sum()
+    loss.backward()
+    torch.cuda.synchronize()
+    ref = gdn_backward_reference(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["initial_state"], None,
+                                 scale=inp["scale"], do=w_o, d_final_state=w_s)
+    for n, r in zip(names, ref):
+        assert leaves[n].grad is not None and leaves[n].grad.dtype == leaves[n].dtype, n
+        check("%s/%s" % (name, n), leaves[n].grad.float().cpu(), r)
