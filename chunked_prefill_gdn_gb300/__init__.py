@@ -29,7 +29,7 @@ __all__ = [
     "load_library", "library_path", "default_options",
     "gdn_default_options", "gdn_plan_query", "gdn_chunk_fwd_workspace_size", "gdn_workspace_query",
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
-    "gdn_chunk_fwd_static", "gdn_qk_l2norm", "qk_l2norm",
+    "gdn_chunk_fwd_static", "gdn_qk_l2norm", "qk_l2norm", "gdn_qk_l2norm_bwd", "qk_l2norm_backward",
     "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd", "gdn_chunk_bwd_check", "chunk_bwd",
     "chunk_gated_delta_rule",
     "gdn_status_string", "gdn_version", "gdn_last_error_detail", "chunk_fwd", "chunk_fwd_host", "workspace_for", "GdnError",
@@ -123,6 +123,8 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_chunk_fwd_static.restype = i32
     lib.gdn_qk_l2norm.argtypes = [vp, vp, vp, vp, ctypes.c_int64, i32, i32, ctypes.c_float, vp]
     lib.gdn_qk_l2norm.restype = i32
+    lib.gdn_qk_l2norm_bwd.argtypes = [vp, vp, vp, ctypes.c_int64, i32, i32, ctypes.c_float, vp]
+    lib.gdn_qk_l2norm_bwd.restype = i32
     lib.gdn_chunk_bwd_workspace_size.argtypes = [i32] * 8
     lib.gdn_chunk_bwd_workspace_size.restype = sz
     lib.gdn_chunk_bwd.argtypes = [vp] * 7 + [i32, f32] + [i32] * 6 + [vp] * 8 + [vp, sz, vp]
@@ -202,6 +204,10 @@ def gdn_chunk_fwd_static(*args) -> int:
 
 def gdn_qk_l2norm(*args) -> int:
     return int(load_library().gdn_qk_l2norm(*args))
+
+
+def gdn_qk_l2norm_bwd(*args) -> int:
+    return int(load_library().gdn_qk_l2norm_bwd(*args))
 
 
 def gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, n_seqs, varlen, dtype) -> int:
@@ -329,6 +335,26 @@ def qk_l2norm(q=None, k=None, q_out=None, k_out=None, eps: float = 0.0,
     return q_out, k_out
 
 
+def qk_l2norm_backward(x, dy, dx=None, eps: float = 0.0, stream: Optional[torch.cuda.Stream] = None):
+    """fp32 gradient of the rows x (the tensor qk_l2norm normalised) from the
+    fp32 gradient dy of their normalised copies, through gdn_qk_l2norm_bwd.
+    Pass dx=dy to overwrite dy."""
+    for name, t in (("x", x), ("dy", dy)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if dy.dtype != torch.float32 or dy.shape != x.shape:
+        raise ValueError("dy must be float32 with x's shape")
+    if dx is None:
+        dx = torch.empty_like(dy)
+    dk = x.shape[-1]
+    stream = stream if stream is not None else torch.cuda.current_stream(x.device)
+    st = gdn_qk_l2norm_bwd(_ptr(x), _ptr(dy), _ptr(dx), x.numel() // dk, dk, _dtype_code(x), float(eps),
+                           ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise GdnError(st, "gdn_qk_l2norm_bwd")
+    return dx
+
+
 def chunk_fwd_host(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
                    opts: Optional[GdnOptions] = None, out=None, final_state=None, device_buffer=None,
                    stream: Optional[torch.cuda.Stream] = None, device=None):
@@ -405,26 +431,33 @@ def chunk_bwd(q, k, v, g, beta, do, initial_state=None, cu_seqlens=None, scale=N
 
 class _ChunkGDN(torch.autograd.Function):
     """gdn_chunk_fwd forward, gdn_chunk_bwd backward (the fp32 gradients of q,
-    k, v are handed back in the inputs' dtype)."""
+    k, v are handed back in the inputs' dtype).  With norm_qk, q and k are first
+    normalised by gdn_qk_l2norm, and their gradients go back through
+    gdn_qk_l2norm_bwd in fp32."""
 
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, scale, opts):
-        o, final_state = chunk_fwd(q, k, v, g, beta, initial_state, cu_seqlens, scale, opts=opts)
-        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
+    def forward(ctx, q, k, v, g, beta, initial_state, cu_seqlens, scale, opts, norm_qk):
+        qn, kn = qk_l2norm(q, k) if norm_qk else (q, k)
+        o, final_state = chunk_fwd(qn, kn, v, g, beta, initial_state, cu_seqlens, scale, opts=opts)
+        ctx.save_for_backward(q, k, qn, kn, v, g, beta, initial_state, cu_seqlens)
         ctx.scale = scale
+        ctx.norm_qk = norm_qk
         return o, final_state
 
     @staticmethod
     def backward(ctx, do, d_final_state):
-        q, k, v, g, beta, initial_state, cu_seqlens = ctx.saved_tensors
+        q, k, qn, kn, v, g, beta, initial_state, cu_seqlens = ctx.saved_tensors
         if do is None:
             do = torch.zeros(*q.shape[:-1], v.shape[-1], dtype=q.dtype, device=q.device)
         dq, dk, dv, dg, dbeta, ds0 = chunk_bwd(
-            q, k, v, g, beta, do.contiguous(), initial_state, cu_seqlens, ctx.scale,
+            qn, kn, v, g, beta, do.contiguous(), initial_state, cu_seqlens, ctx.scale,
             d_final_state.contiguous() if d_final_state is not None else None)
+        if ctx.norm_qk:
+            qk_l2norm_backward(q, dq, dx=dq)
+            qk_l2norm_backward(k, dk, dx=dk)
         dt = q.dtype
         return (dq.to(dt), dk.to(dt), dv.to(dt), dg, dbeta, (ds0 if initial_state is not None else None),
-                None, None, None)
+                None, None, None, None)
 
 
 def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
@@ -434,16 +467,16 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, out
     log-decay gate g and beta [B,T,H] (fp32), an optional initial state
     [N,H,dk,dv] (fp32) and cu_seqlens (int32, packed batch with B = 1).
     Gradients flow to q, k, v, g, beta and the initial state through
-    gdn_chunk_bwd.  use_qk_l2norm_in_kernel normalises q and k inside the
-    forward (opts.qk_l2norm); it has no backward here, so it is refused when a
-    gradient is needed."""
+    gdn_chunk_bwd.  use_qk_l2norm_in_kernel normalises q and k first: inside
+    the forward pass (opts.qk_l2norm) when no gradient is needed, else by
+    gdn_qk_l2norm in front of it, with gdn_qk_l2norm_bwd on the way back."""
     needs_grad = torch.is_grad_enabled() and any(
         t is not None and t.requires_grad for t in (q, k, v, g, beta, initial_state))
-    if use_qk_l2norm_in_kernel and needs_grad:
-        raise NotImplementedError("use_qk_l2norm_in_kernel has no backward; normalise q and k before the call")
     q, k, v, g, beta = (t.contiguous() for t in (q, k, v, g, beta))
     if initial_state is not None:
         initial_state = initial_state.contiguous()
-    opts = default_options(qk_l2norm=1 if use_qk_l2norm_in_kernel else 0, cp_mode=cp_mode)
-    o, final_state = _ChunkGDN.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, opts)
+    in_pass = bool(use_qk_l2norm_in_kernel) and not needs_grad
+    opts = default_options(qk_l2norm=1 if in_pass else 0, cp_mode=cp_mode)
+    o, final_state = _ChunkGDN.apply(q, k, v, g, beta, initial_state, cu_seqlens, scale, opts,
+                                     bool(use_qk_l2norm_in_kernel) and needs_grad)
     return o, (final_state if output_final_state else None)

@@ -7,8 +7,14 @@
 //     x_hat = x * rsqrt(sum_d x_d^2 + eps)          (fp32 sum, one rounding to the
 //                                                     output type)
 //
-// The pass is a pure stream over q and k (one read, one write of each), so it
-// is written for HBM: one warp per row, four rows in flight per warp, vector
+// and its backward, for an upstream gradient dy of x_hat,
+//
+//     dx = dy * inv - x * (x . dy) * inv^3,      inv = rsqrt(sum_d x_d^2 + eps)
+//
+// (the Jacobian of x / n is I / n - x x^T / n^3), in fp32 with dy and dx fp32.
+//
+// Both passes are pure streams (one read, one write of each row), so they are
+// written for HBM: one warp per row, four rows in flight per warp, vector
 // loads of the lane's dk / 32 consecutive elements, the sum by shuffles, and a
 // grid of eight 256-thread blocks per SM striding over the rows.
 #include <cuda_bf16.h>
@@ -159,6 +165,54 @@ __global__ void __launch_bounds__(32 * kNormWarps, 8) qk_l2norm_kernel(const T *
     }
 }
 
+// dx rows from x (T) and dy (fp32); dx may alias dy.  Two rows of inputs per
+// row in flight, so four blocks per SM (64 registers) instead of eight.
+template <typename T, int DK>
+__global__ void __launch_bounds__(32 * kNormWarps, 4) qk_l2norm_bwd_kernel(const T *x, const float *dy, float *dx,
+                                                                        long long rows, float eps) {
+    constexpr int E = DK / 32;
+    const int lane = threadIdx.x & 31;
+    const long long warp0 = (long long)blockIdx.x * kNormWarps + (threadIdx.x >> 5);
+    const long long stride = (long long)gridDim.x * kNormWarps * kNormRows;
+    for (long long base = warp0 * kNormRows; base < rows; base += stride) {
+        float xv[kNormRows][E], gv[kNormRows][E];
+#pragma unroll
+        for (int u = 0; u < kNormRows; ++u) {
+            const long long r = base + u;
+            if (r < rows) {
+                load_e<E>(x + r * DK + lane * E, xv[u]);
+                load_e<E>(dy + r * DK + lane * E, gv[u]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) xv[u][e] = gv[u][e] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kNormRows; ++u) {
+            float ss = 0.f, xd = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                ss = fmaf(xv[u][e], xv[u][e], ss);
+                xd = fmaf(xv[u][e], gv[u][e], xd);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                xd += __shfl_xor_sync(0xffffffffu, xd, off);
+            }
+            const float inv = rsqrtf(ss + eps);
+            const float c = xd * inv * inv * inv;
+#pragma unroll
+            for (int e = 0; e < E; ++e) gv[u][e] = gv[u][e] * inv - xv[u][e] * c;
+        }
+#pragma unroll
+        for (int u = 0; u < kNormRows; ++u) {
+            const long long r = base + u;
+            if (r < rows) store_e<E>(dx + r * DK + lane * E, gv[u]);
+        }
+    }
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -186,6 +240,20 @@ cudaError_t launch_typed(const void *q, const void *k, void *qo, void *ko, long 
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_bwd_typed(const void *x, const float *dy, float *dx, long long rows, int dk, float eps,
+                             cudaStream_t s) {
+    const int sms = sm_count();
+    const long long warps_needed = (rows + kNormRows - 1) / kNormRows;
+    const long long blocks_needed = (warps_needed + kNormWarps - 1) / kNormWarps;
+    const int grid = (int)std::min<long long>(blocks_needed, (long long)sms * 4);
+    const T *xt = static_cast<const T *>(x);
+    if (dk == 32) qk_l2norm_bwd_kernel<T, 32><<<grid, 32 * kNormWarps, 0, s>>>(xt, dy, dx, rows, eps);
+    else if (dk == 64) qk_l2norm_bwd_kernel<T, 64><<<grid, 32 * kNormWarps, 0, s>>>(xt, dy, dx, rows, eps);
+    else qk_l2norm_bwd_kernel<T, 128><<<grid, 32 * kNormWarps, 0, s>>>(xt, dy, dx, rows, eps);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_qk_l2norm(const void *q, const void *k, void *qo, void *ko, long long rows, int dk, int dtype,
@@ -210,6 +278,26 @@ extern "C" gdn_status gdn_qk_l2norm(const void *q, const void *k, void *q_out, v
                                                 reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         gdn::set_error_detail("launch qk_l2norm", e);
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
+extern "C" gdn_status gdn_qk_l2norm_bwd(const void *x, const float *dy, float *dx, int64_t rows, int dk,
+                                        gdn_dtype dtype, float eps, gdn_stream_t stream) {
+    if (rows < 0 || (dk != 32 && dk != 64 && dk != 128)) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 && dtype != GDN_F32) return GDN_ERR_INVALID_ARG;
+    if (rows > 0 && (!x || !dy || !dx)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, dy, dx};
+    for (const void *ptr : ptrs)
+        if (ptr && (reinterpret_cast<uintptr_t>(ptr) & 15u)) return GDN_ERR_INVALID_ARG;
+    if (rows == 0) return GDN_OK;
+    if (!(eps > 0.f)) eps = gdn::kQkNormEps;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = dtype == GDN_BF16 ? gdn::launch_bwd_typed<__nv_bfloat16>(x, dy, dx, rows, dk, eps, s)
+                                            : gdn::launch_bwd_typed<float>(x, dy, dx, rows, dk, eps, s);
+    if (e != cudaSuccess) {
+        gdn::set_error_detail("launch qk_l2norm_bwd", e);
         return GDN_ERR_CUDA;
     }
     return GDN_OK;

@@ -310,6 +310,21 @@ gdn_status gdn_qk_l2norm(const void *q, const void *k, void *q_out, void *k_out,
                          gdn_stream_t stream);
 
 /*
+ * Backward of gdn_qk_l2norm for one tensor: with n = sqrt(sum_d x_d^2 + eps)
+ * and dy the gradient of x_hat = x / n,
+ *
+ *     dx = dy / n - x (x . dy) / n^3        (the Jacobian of x / n)
+ *
+ * in fp32.  x: `rows` rows of dk elements in `dtype` (the tensor that was
+ * normalised); dy, dx: fp32 rows in the same layout (dx may equal dy).  All
+ * pointers 16-byte aligned, non-NULL when rows > 0; dk in {32, 64, 128};
+ * eps <= 0 selects 1e-6 (the forward's default).  Enqueued on `stream`.
+ * Errors: GDN_ERR_INVALID_ARG (sizes, dtype, alignment, NULL), GDN_ERR_CUDA.
+ */
+gdn_status gdn_qk_l2norm_bwd(const void *x, const float *dy, float *dx, int64_t rows, int dk,
+                             gdn_dtype dtype, float eps, gdn_stream_t stream);
+
+/*
  * The backward pass: gradients of L = sum <o, d_o> + <final_state,
  * d_final_state> with respect to q, k, v, g, beta and initial_state, for the
  * forward pass gdn_chunk_fwd computes (the backward paragraph of the FlashQLA

@@ -12,12 +12,17 @@ the queries the same way.  The pages give no epsilon; the reading taken here is
 which is the exact unit vector for any row whose squared norm is far above
 eps and maps a zero row to zero.  Computed row by row in fp64 from the values
 the device sees.
+
+Its backward (the chain rule through x_hat = x / n, n = sqrt(|x|^2 + eps)):
+the Jacobian is I / n - x x^T / n^3, so for an upstream gradient dy
+
+    dx = dy / n - x (x . dy) / n^3.
 """
 from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["L2NORM_EPS", "l2_normalize"]
+__all__ = ["L2NORM_EPS", "l2_normalize", "l2_normalize_backward"]
 
 L2NORM_EPS = 1e-6
 
@@ -27,3 +32,12 @@ def l2_normalize(x, eps: float = L2NORM_EPS) -> np.ndarray:
     a = np.asarray(x, dtype=np.float64)
     ss = np.sum(a * a, axis=-1, keepdims=True)   # squared norm of each row
     return a / np.sqrt(ss + eps)
+
+
+def l2_normalize_backward(x, dy, eps: float = L2NORM_EPS) -> np.ndarray:
+    """Gradient with respect to the rows x of <l2_normalize(x), dy> (fp64)."""
+    a = np.asarray(x, dtype=np.float64)
+    g = np.asarray(dy, dtype=np.float64)
+    n = np.sqrt(np.sum(a * a, axis=-1, keepdims=True) + eps)
+    xdy = np.sum(a * g, axis=-1, keepdims=True)
+    return g / n - a * xdy / n ** 3

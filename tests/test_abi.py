@@ -183,11 +183,14 @@ def test_backward_argument_errors_before_launch(lib):
     assert gdn.gdn_chunk_bwd_check(None, None) == 1
 
 
-def test_autograd_entry_refuses_in_kernel_normalisation_with_gradients():
-    """The in-kernel q/k normalisation has no backward: asking for gradients
-    with it is refused on the host, before any device call."""
-    import torch
-    q = torch.zeros(1, 4, 1, 32, requires_grad=True)
-    with pytest.raises(NotImplementedError):
-        gdn.chunk_gated_delta_rule(q, q, q, torch.zeros(1, 4, 1), torch.zeros(1, 4, 1),
-                                   use_qk_l2norm_in_kernel=True)
+def test_qk_l2norm_backward_argument_errors_before_launch(lib):
+    """Sizes, dtype, NULL and misaligned pointers are rejected on the host (no
+    GPU is touched); zero rows is a no-op."""
+    fake = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    assert gdn.gdn_qk_l2norm_bwd(fake, fake, fake, 10, 48, gdn.BF16, 0.0, None) == 1
+    assert gdn.gdn_qk_l2norm_bwd(fake, fake, fake, 10, 64, 7, 0.0, None) == 1
+    assert gdn.gdn_qk_l2norm_bwd(fake, None, fake, 10, 64, gdn.BF16, 0.0, None) == 1
+    assert gdn.gdn_qk_l2norm_bwd(fake, fake, mis, 10, 64, gdn.BF16, 0.0, None) == 1
+    assert gdn.gdn_qk_l2norm_bwd(fake, fake, fake, -1, 64, gdn.BF16, 0.0, None) == 1
+    assert gdn.gdn_qk_l2norm_bwd(None, None, None, 0, 64, gdn.BF16, 0.0, None) == 0

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from oracle.norm import l2_normalize
+from oracle.norm import l2_normalize, l2_normalize_backward
 import chunked_prefill_gdn_gb300 as gdn
 from chunked_prefill_gdn_gb300 import build as gdn_build
 from chunked_prefill_gdn_gb300.inputs import CONFIGS, make_inputs
@@ -132,3 +132,63 @@ def test_host_entry_streams_with_normalisation():
                                    pinned["initial_state"], pinned["cu_seqlens"], inp["scale"], opts=opts)
     o_d, sf_d = gpu_run(to_device(inp), opts)
     assert torch.equal(o_h, o_d.cpu()) and torch.equal(sf_h, sf_d.cpu())
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dk", [32, 64, 128])
+def test_qk_l2norm_backward_matches_oracle(dtype, dk):
+    """gdn_qk_l2norm_bwd element by element against the oracle's closed form,
+    on rows whose norms spread over decades, a zero row and a tiny-norm row.
+    fp32 arithmetic: each element within 1e-5 of its row's scale
+    max|dy| / n + max|x| |x . dy| / n^3."""
+    x = raw_rows((1237, 3, dk), dtype, seed=dk + 10).cuda()
+    g = torch.Generator().manual_seed(dk)
+    dy = torch.randn(1237, 3, dk, generator=g).cuda()
+    dx = gdn.qk_l2norm_backward(x, dy)
+    dy2 = dy.clone()
+    gdn.qk_l2norm_backward(x, dy2, dx=dy2)                     # in place
+    torch.cuda.synchronize()
+    assert torch.equal(dx, dy2)
+    x64, dy64 = oracle.to_f64(x), oracle.to_f64(dy)
+    ref = l2_normalize_backward(x64, dy64)
+    n = np.sqrt(np.sum(x64 * x64, axis=-1, keepdims=True) + 1e-6)
+    row_scale = (np.abs(dy64).max(axis=-1, keepdims=True) / n +
+                 np.abs(x64).max(axis=-1, keepdims=True) * np.abs(np.sum(x64 * dy64, axis=-1, keepdims=True)) / n ** 3)
+    err = np.abs(oracle.to_f64(dx) - ref)
+    assert np.all(err <= 1e-5 * row_scale), "max %.3e of row scale" % float(np.max(err / row_scale))
+
+
+@pytest.mark.parametrize("name,cfg", [
+    ("tiny_f32", CONFIGS[0]),
+    ("layer_bf16", CONFIGS[1].scaled(B=1, T=150, H=2)),
+])
+def test_autograd_with_in_kernel_normalisation(name, cfg):
+    """chunk_gated_delta_rule(use_qk_l2norm_in_kernel=True) under autograd on
+    un-normalised q and k: the gradients equal the oracle's chain — exact
+    normalisation, the recurrence's gradients on the normalised rows, then the
+    normalisation's backward — within the parity bar (the device's normalised
+    copies are rounded to the input dtype, as in the forward test above)."""
+    from oracle.backward import gdn_backward_reference
+    inp = unnormalise(make_inputs(cfg, "cpu"), seed=13)
+    names = ("q", "k", "v", "g", "beta")
+    leaves = {n: inp[n].cuda().clone().requires_grad_() for n in names}
+    o, sf = gdn.chunk_gated_delta_rule(leaves["q"], leaves["k"], leaves["v"], leaves["g"], leaves["beta"],
+                                       scale=inp["scale"], output_final_state=True, use_qk_l2norm_in_kernel=True)
+    gen = torch.Generator().manual_seed(6)
+    w_o = torch.randn(o.shape, generator=gen).to(o.dtype)
+    w_s = 0.1 * torch.randn(sf.shape, generator=gen)
+    ((o.float() * w_o.cuda().float()).sum() + (sf * w_s.cuda()).sum()).backward()
+    torch.cuda.synchronize()
+    q64, k64 = oracle.to_f64(inp["q"]), oracle.to_f64(inp["k"])
+    qn, kn = l2_normalize(q64), l2_normalize(k64)
+    dqn, dkn, dv, dg, db, _ = gdn_backward_reference(qn, kn, inp["v"], inp["g"], inp["beta"], None, None,
+                                                     scale=inp["scale"], do=w_o, d_final_state=w_s)
+    ref = dict(q=l2_normalize_backward(q64.reshape(dqn.shape), dqn), k=l2_normalize_backward(k64.reshape(dkn.shape), dkn),
+               v=dv, g=dg, beta=db)
+    for n in names:
+        got = oracle.to_f64(leaves[n].grad).reshape(ref[n].shape)
+        assert np.isfinite(got).all(), n
+        rel = np.linalg.norm(got - ref[n]) / np.linalg.norm(ref[n])
+        mab = np.abs(got - ref[n]).max()
+        assert rel <= 5e-3 and mab <= 2e-2 * max(1.0, np.abs(ref[n]).max()), "%s %s: rel %.3e max-abs %.3e" % (
+            name, n, rel, mab)

@@ -7,7 +7,7 @@ I - beta k k^T; the epsilon 1e-6 under the square root is this library's
 reading (the pages give none)."""
 import numpy as np
 
-from oracle.norm import L2NORM_EPS, l2_normalize
+from oracle.norm import L2NORM_EPS, l2_normalize, l2_normalize_backward
 
 
 def rows(n=200, d=64, seed=0):
@@ -85,3 +85,43 @@ def test_batched_shapes_normalise_the_last_axis():
     assert y.shape == x.shape
     for idx in np.ndindex(*x.shape[:-1]):
         np.testing.assert_allclose(y[idx], l2_normalize(x[idx][None])[0], rtol=0, atol=1e-15)
+
+
+def test_backward_matches_finite_differences():
+    """The backward against central differences of the forward: a code path
+    that shares nothing with the Jacobian's closed form (a dropped x x^T term
+    or a wrong power of n misses by far more than the differencing error)."""
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((5, 6)) * np.array([[1e-2], [0.3], [1.0], [7.0], [40.0]])
+    dy = rng.standard_normal((5, 6))
+    got = l2_normalize_backward(x, dy)
+    num = np.zeros_like(x)
+    for i in range(x.shape[0]):
+        h = 1e-6 * max(1.0, np.abs(x[i]).max())
+        for j in range(x.shape[1]):
+            xp, xm = x.copy(), x.copy()
+            xp[i, j] += h
+            xm[i, j] -= h
+            num[i, j] = (np.sum(l2_normalize(xp[i]) * dy[i]) - np.sum(l2_normalize(xm[i]) * dy[i])) / (2 * h)
+    for i in range(x.shape[0]):
+        scale = max(1.0, np.abs(num[i]).max())
+        assert np.abs(got[i] - num[i]).max() <= 1e-6 * scale, i
+
+
+def test_backward_is_orthogonal_to_the_row_and_scales_inversely():
+    """x . dx = (x . dy) eps / n^3 (zero as eps -> 0: the output cannot grow
+    along x); and dx at c x is dx at x divided by c (the map is scale-free)."""
+    x = rows(n=50, d=32, seed=3)
+    dy = np.random.default_rng(4).standard_normal(x.shape)
+    dx = l2_normalize_backward(x, dy)
+    n = np.sqrt(np.sum(x * x, axis=1) + L2NORM_EPS)
+    np.testing.assert_allclose(np.sum(x * dx, axis=1), np.sum(x * dy, axis=1) * L2NORM_EPS / n ** 3,
+                               rtol=1e-6, atol=1e-12)
+    sel = n > 1.0                                    # rows where eps is negligible
+    big, dyb = x[sel], dy[sel]
+    assert len(big) > 10
+    ref = l2_normalize_backward(big, dyb) / 3.0
+    # eps shifts both sides by about eps / n^2 relative to the size of the terms
+    # that cancel inside dx, hence an absolute floor at that scale
+    np.testing.assert_allclose(l2_normalize_backward(3.0 * big, dyb), ref, rtol=1e-5,
+                               atol=1e-5 * np.abs(ref).max())
