@@ -138,3 +138,45 @@ def test_chunked_form_matches_the_token_backward(lens, C):
     b = gdn_backward_chunked(*args, C=C, **kw)
     for x, y in zip(a, b):
         assert np.abs(x - y).max() <= 1e-11 * max(1.0, float(np.abs(x).max()))
+
+
+def test_value_column_slices_sum_to_the_gradients():
+    """The state's value rows evolve independently (S_t's row i sees only
+    v_t[i] and its own past), so the problem restricted to a set of value
+    columns (v, S0, dO, dS_T cut to those columns) is a GDN problem of its own:
+    its dv and dS0 are the full problem's columns, and the full dq, dk, dg and
+    dbeta are the sums of the slices' — the decomposition a backward that
+    splits the value dimension across workers relies on."""
+    p = tiny(seed=11, lens=(9, 4), H=2, dk=3, dv=6)
+    args = (p["q"], p["k"], p["v"], p["g"], p["beta"], p["s0"], p["cu"])
+    full = gdn_backward_reference(*args, scale=p["scale"], do=p["do"], d_final_state=p["dsT"])
+    sums = [np.zeros_like(full[i]) for i in (0, 1, 3, 4)]
+    for cols in (slice(0, 2), slice(2, 5), slice(5, 6)):
+        part = gdn_backward_reference(p["q"], p["k"], p["v"][..., cols], p["g"], p["beta"], p["s0"][..., cols],
+                                      p["cu"], scale=p["scale"], do=p["do"][..., cols],
+                                      d_final_state=p["dsT"][..., cols])
+        np.testing.assert_allclose(part[2], full[2][..., cols], rtol=1e-12, atol=1e-12)   # dv
+        np.testing.assert_allclose(part[5], full[5][..., cols], rtol=1e-12, atol=1e-12)   # dS0
+        for acc, i in zip(sums, (0, 1, 3, 4)):
+            acc += part[i]
+    for acc, i in zip(sums, (0, 1, 3, 4)):
+        np.testing.assert_allclose(acc, full[i], rtol=1e-10, atol=1e-12)
+
+
+def test_zero_padding_leaves_the_real_gradients_unchanged():
+    """Tokens with q = k = v = 0, beta = 0, g = 0 and dO = 0 appended to a
+    sequence are identity steps (A_t = I, no write, no output), so the real
+    tokens' gradients and dS0 do not change — the padding a chunked kernel
+    applies to a short last chunk.  (The padded tokens' own dg need not be zero:
+    their gate still scales the state; a kernel never writes those rows.)"""
+    p = tiny(seed=12, lens=(7,), H=2, dk=3, dv=4)
+    base = gdn_backward_reference(p["q"], p["k"], p["v"], p["g"], p["beta"], p["s0"], p["cu"], scale=p["scale"],
+                                  do=p["do"], d_final_state=p["dsT"])
+    pad = 5
+    z = lambda a: np.concatenate([a, np.zeros((pad,) + a.shape[1:])])
+    cu = np.array([0, 7 + pad], dtype=np.int64)
+    padded = gdn_backward_reference(z(p["q"]), z(p["k"]), z(p["v"]), z(p["g"]), z(p["beta"]), p["s0"], cu,
+                                    scale=p["scale"], do=z(p["do"]), d_final_state=p["dsT"])
+    for i in range(5):
+        np.testing.assert_allclose(padded[i][:7], base[i], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(padded[5], base[5], rtol=1e-12, atol=1e-12)
