@@ -262,6 +262,28 @@ def _shape(q, v, cu_seqlens):
     return B, T, H, dk, dv, N
 
 
+def _expect(name, t, shape):
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+def _check_shapes(q, k, v, g, beta, initial_state=None, cu_seqlens=None):
+    """Every input's shape against q's and v's, before any pointer reaches the
+    library (which sees plain pointers and cannot check them); returns
+    (B, T, H, dk, dv, N)."""
+    if v.dim() != 4:
+        raise ValueError("v must be [B, T, H, dv]")
+    if cu_seqlens is not None and (cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2):
+        raise ValueError("cu_seqlens must be 1-D with at least two entries")
+    B, T, H, dk, dv, N = _shape(q, v, cu_seqlens)
+    _expect("k", k, (B, T, H, dk))
+    _expect("v", v, (B, T, H, dv))
+    _expect("g", g, (B, T, H))
+    _expect("beta", beta, (B, T, H))
+    _expect("initial_state", initial_state, (N, H, dk, dv))
+    return B, T, H, dk, dv, N
+
+
 def workspace_for(q, v, cu_seqlens=None, opts: Optional[GdnOptions] = None) -> torch.Tensor:
     B, T, H, dk, dv, N = _shape(q, v, cu_seqlens)
     n = gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, N, cu_seqlens is not None, _dtype_code(q), opts)
@@ -274,7 +296,9 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
               opts: Optional[GdnOptions] = None, out=None, final_state=None, workspace=None,
               stream: Optional[torch.cuda.Stream] = None, check: bool = False):
     """GDN chunked-prefill forward on the GPU; returns (o, final_state)."""
-    B, T, H, dk, dv, N = _shape(q, v, cu_seqlens)
+    B, T, H, dk, dv, N = _check_shapes(q, k, v, g, beta, initial_state, cu_seqlens)
+    _expect("out", out, (B, T, H, dv))
+    _expect("final_state", final_state, (N, H, dk, dv))
     dt = _dtype_code(q)
     for name, t in (("k", k), ("v", v)):
         if t.dtype != q.dtype:
@@ -360,7 +384,9 @@ def chunk_fwd_host(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=
                    stream: Optional[torch.cuda.Stream] = None, device=None):
     """The same pass for CPU (ideally pinned) tensors through gdn_chunk_fwd_host:
     the library copies inputs in, runs, copies results out and syncs."""
-    B, T, H, dk, dv, N = _shape(q, v, cu_seqlens)
+    B, T, H, dk, dv, N = _check_shapes(q, k, v, g, beta, initial_state, cu_seqlens)
+    _expect("out", out, (B, T, H, dv))
+    _expect("final_state", final_state, (N, H, dk, dv))
     dt = _dtype_code(q)
     for name, t in dict(q=q, k=k, v=v, g=g, beta=beta).items():
         if t.is_cuda or not t.is_contiguous():
@@ -388,7 +414,9 @@ def chunk_bwd(q, k, v, g, beta, do, initial_state=None, cu_seqlens=None, scale=N
               workspace=None, stream: Optional[torch.cuda.Stream] = None, check: bool = False):
     """Gradients of sum <o, do> + <final_state, d_final_state> through
     gdn_chunk_bwd; returns fp32 (dq, dk, dv, dg, dbeta, d_initial_state)."""
-    B, T, H, dk, dv, N = _shape(q, v, cu_seqlens)
+    B, T, H, dk, dv, N = _check_shapes(q, k, v, g, beta, initial_state, cu_seqlens)
+    _expect("do", do, (B, T, H, dv))
+    _expect("d_final_state", d_final_state, (N, H, dk, dv))
     dt = _dtype_code(q)
     for name, t in dict(k=k, v=v, do=do).items():
         if t.dtype != q.dtype:

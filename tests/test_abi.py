@@ -194,3 +194,42 @@ def test_qk_l2norm_backward_argument_errors_before_launch(lib):
     assert gdn.gdn_qk_l2norm_bwd(fake, fake, mis, 10, 64, gdn.BF16, 0.0, None) == 1
     assert gdn.gdn_qk_l2norm_bwd(fake, fake, fake, -1, 64, gdn.BF16, 0.0, None) == 1
     assert gdn.gdn_qk_l2norm_bwd(None, None, None, 0, 64, gdn.BF16, 0.0, None) == 0
+
+
+def test_binding_rejects_mismatched_shapes_before_the_library():
+    """The C ABI sees plain pointers, so the binding checks every tensor's shape
+    against q's and v's first (a short k or state would otherwise be read out
+    of bounds on the device); these raise on the host, before any CUDA call.
+    The tensors here live on the CPU, so a call that passes the shape checks
+    stops at the device check instead (the control below)."""
+    import torch
+    q = torch.zeros(1, 8, 2, 32)
+    v = torch.zeros(1, 8, 2, 64)
+    g = torch.zeros(1, 8, 2)
+    good = dict(q=q, k=q, v=v, g=g, beta=g)
+    with pytest.raises(ValueError, match="CUDA"):                                   # control
+        gdn.chunk_fwd(q, q, v, g, g)
+    with pytest.raises(ValueError, match="CUDA"):
+        gdn.chunk_bwd(q, q, v, g, g, torch.zeros(1, 8, 2, 64))
+    cases = [
+        dict(k=torch.zeros(1, 8, 2, 16)),
+        dict(v=torch.zeros(1, 7, 2, 64)),
+        dict(g=torch.zeros(1, 8, 3)),
+        dict(beta=torch.zeros(8, 2)),
+    ]
+    for bad in cases:
+        a = dict(good, **bad)
+        with pytest.raises(ValueError, match="shape"):
+            gdn.chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"])
+    with pytest.raises(ValueError, match="initial_state has shape"):
+        gdn.chunk_fwd(q, q, v, g, g, initial_state=torch.zeros(1, 2, 32, 32))
+    with pytest.raises(ValueError, match="out has shape"):
+        gdn.chunk_fwd(q, q, v, g, g, out=torch.zeros(1, 8, 2, 32))
+    with pytest.raises(ValueError, match="cu_seqlens"):
+        gdn.chunk_fwd(q, q, v, g, g, cu_seqlens=torch.zeros(1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="do has shape"):
+        gdn.chunk_bwd(q, q, v, g, g, torch.zeros(1, 8, 2, 32))                       # do like o
+    with pytest.raises(ValueError, match="d_final_state has shape"):
+        gdn.chunk_bwd(q, q, v, g, g, torch.zeros(1, 8, 2, 64), d_final_state=torch.zeros(2, 2, 32, 64))
+    with pytest.raises(ValueError, match="beta has shape"):
+        gdn.chunk_fwd_host(q, q, v, g, torch.zeros(1, 8, 1))
