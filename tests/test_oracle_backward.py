@@ -180,3 +180,18 @@ def test_zero_padding_leaves_the_real_gradients_unchanged():
     for i in range(5):
         np.testing.assert_allclose(padded[i][:7], base[i], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(padded[5], base[5], rtol=1e-12, atol=1e-12)
+
+
+def test_chunked_form_without_initial_state_or_final_gradient():
+    """initial_state = None (zero) and d_final_state = None (zero) take the
+    same paths in both forms, as the full-size GPU check uses them."""
+    from oracle.backward import gdn_backward_chunked
+    p = tiny(seed=13, lens=(21, 2), dk=4, dv=3)
+    args = (p["q"], p["k"], p["v"], p["g"], p["beta"], None, p["cu"])
+    a = gdn_backward_reference(*args, scale=p["scale"], do=p["do"], d_final_state=None)
+    b = gdn_backward_chunked(*args, scale=p["scale"], do=p["do"], d_final_state=None, C=8)
+    z = gdn_backward_reference(p["q"], p["k"], p["v"], p["g"], p["beta"], np.zeros_like(p["s0"]), p["cu"],
+                               scale=p["scale"], do=p["do"], d_final_state=np.zeros_like(p["dsT"]))
+    for x, y, w in zip(a, b, z):
+        assert np.abs(x - y).max() <= 1e-11 * max(1.0, float(np.abs(x).max()))
+        np.testing.assert_array_equal(x, w)
