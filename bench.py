@@ -417,7 +417,7 @@ def backward_measure(gdn, torch, inp, cfg, flush, stream, iters=3):
     """The backward pass (gdn_chunk_bwd) on this workload with seeded upstream
     gradients: CUDA events around each launch sequence (the main kernel and the
     slice reduction), L2 flushed before each.  Reported against the FP32
-    CUDA-core peak (the kernel runs on CUDA cores)."""
+    CUDA-core peak (all but its two Gram products run on CUDA cores)."""
     from chunked_prefill_gdn_gb300.inputs import make_grad_inputs
     grads = make_grad_inputs(cfg, inp["q"].device)
     do, dsf = grads["do"], grads["d_final_state"]
@@ -456,7 +456,8 @@ def backward_measure(gdn, torch, inp, cfg, flush, stream, iters=3):
             "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": achieved / FP32_ALU_TFLOPS,
             "alg_flops": flops, "launches": iters * (1 + (4 if slices > 1 else 0)),
             "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
-            "note": "fp32 CUDA-core kernel, one CTA per (32 value columns, head, sequence); not inside the timed step"}
+            "note": "Gram products on tcgen05 (bf16, d=128), the other products fp32 on CUDA cores; one CTA per "
+                    "(32 value columns, head, sequence); not inside the timed step"}
 
 
 def e2e_measure(gdn, torch, inp, cfg, opts, dev, args):
