@@ -284,6 +284,32 @@ def _check_shapes(q, k, v, g, beta, initial_state=None, cu_seqlens=None):
     return B, T, H, dk, dv, N
 
 
+def _check_dtypes(named, dtypes):
+    """Each given tensor's dtype against the one the C ABI expects for it (a
+    wrong element size would make the kernels read or write past its end)."""
+    for name, t in named.items():
+        if t is not None and t.dtype != dtypes[name]:
+            raise TypeError("%s must be %s, got %s" % (name, dtypes[name], t.dtype))
+
+
+def _check_placement(kind, device, named):
+    """Every given tensor contiguous, of device type `kind` ("cuda" for the
+    device entry points, "cpu" for the host-buffer one) and, when `device` is
+    given, on that device: the library receives bare pointers and would
+    dereference a host pointer on the GPU (or a pointer into another GPU's
+    memory) without any way to tell."""
+    for name, t in named.items():
+        if t is None:
+            continue
+        if t.device.type != kind:
+            raise ValueError("%s must be a contiguous %s tensor, got one on %s" % (
+                name, "CUDA" if kind == "cuda" else kind.upper(), t.device))
+        if device is not None and t.device != device:
+            raise ValueError("%s is on %s but q is on %s" % (name, t.device, device))
+        if not t.is_contiguous():
+            raise ValueError("%s must be a contiguous %s tensor" % (name, "CUDA" if kind == "cuda" else kind.upper()))
+
+
 def workspace_for(q, v, cu_seqlens=None, opts: Optional[GdnOptions] = None) -> torch.Tensor:
     B, T, H, dk, dv, N = _shape(q, v, cu_seqlens)
     n = gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, N, cu_seqlens is not None, _dtype_code(q), opts)
@@ -300,36 +326,33 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
     _expect("out", out, (B, T, H, dv))
     _expect("final_state", final_state, (N, H, dk, dv))
     dt = _dtype_code(q)
-    for name, t in (("k", k), ("v", v)):
-        if t.dtype != q.dtype:
-            raise TypeError("%s must have q's dtype" % name)
-    tensors = dict(q=q, k=k, v=v, g=g, beta=beta)
-    for name, t in tensors.items():
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("%s must be a contiguous CUDA tensor" % name)
-    if g.dtype != torch.float32 or beta.dtype != torch.float32:
-        raise TypeError("g and beta must be float32")
-    if initial_state is not None and (initial_state.dtype != torch.float32 or not initial_state.is_contiguous()):
-        raise TypeError("initial_state must be contiguous float32")
-    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
-        raise TypeError("cu_seqlens must be int32")
-    if out is None:
-        out = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
-    if final_state is None:
-        final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
-    if workspace is None:
-        workspace = workspace_for(q, v, cu_seqlens, opts)
-    stream = stream if stream is not None else torch.cuda.current_stream(q.device)
-    st = gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
-                       N, float(scale) if scale is not None else 0.0, B, T, H, dk, dv, dt,
-                       _ptr(out), _ptr(final_state), _ptr(workspace), workspace.numel(),
-                       ctypes.byref(opts) if opts is not None else None, ctypes.c_void_p(stream.cuda_stream))
-    if st != 0:
-        raise GdnError(st, "gdn_chunk_fwd")
-    if check:
-        st = gdn_chunk_fwd_check(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream))
+    f32 = torch.float32
+    _check_dtypes(dict(k=k, v=v, g=g, beta=beta, initial_state=initial_state, cu_seqlens=cu_seqlens, out=out,
+                       final_state=final_state, workspace=workspace),
+                  dict(k=q.dtype, v=q.dtype, g=f32, beta=f32, initial_state=f32, cu_seqlens=torch.int32,
+                       out=q.dtype, final_state=f32, workspace=torch.uint8))
+    _check_placement("cuda", None, dict(q=q))
+    _check_placement("cuda", q.device, dict(k=k, v=v, g=g, beta=beta, initial_state=initial_state,
+                                            cu_seqlens=cu_seqlens, out=out, final_state=final_state,
+                                            workspace=workspace))
+    with torch.cuda.device(q.device):
+        if out is None:
+            out = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+        if final_state is None:
+            final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
+        if workspace is None:
+            workspace = workspace_for(q, v, cu_seqlens, opts)
+        stream = stream if stream is not None else torch.cuda.current_stream(q.device)
+        st = gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
+                           N, float(scale) if scale is not None else 0.0, B, T, H, dk, dv, dt,
+                           _ptr(out), _ptr(final_state), _ptr(workspace), workspace.numel(),
+                           ctypes.byref(opts) if opts is not None else None, ctypes.c_void_p(stream.cuda_stream))
         if st != 0:
-            raise GdnError(st, "device check")
+            raise GdnError(st, "gdn_chunk_fwd")
+        if check:
+            st = gdn_chunk_fwd_check(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream))
+            if st != 0:
+                raise GdnError(st, "device check")
     return out, final_state
 
 
@@ -345,17 +368,22 @@ def qk_l2norm(q=None, k=None, q_out=None, k_out=None, eps: float = 0.0,
         if t is not None and (not t.is_cuda or not t.is_contiguous() or t.dtype != ref.dtype
                               or t.shape != ref.shape):
             raise ValueError("q and k must be contiguous CUDA tensors of one shape and dtype")
+    for name, t in (("q_out", q_out), ("k_out", k_out)):
+        if t is not None and (t.dtype != ref.dtype or t.shape != ref.shape):
+            raise ValueError("%s must have the inputs' shape and dtype" % name)
+    _check_placement("cuda", ref.device, dict(q=q, k=k, q_out=q_out, k_out=k_out))
     dk = ref.shape[-1]
     rows = ref.numel() // dk
-    if q is not None and q_out is None:
-        q_out = torch.empty_like(q)
-    if k is not None and k_out is None:
-        k_out = torch.empty_like(k)
-    stream = stream if stream is not None else torch.cuda.current_stream(ref.device)
-    st = gdn_qk_l2norm(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), rows, dk, _dtype_code(ref), float(eps),
-                       ctypes.c_void_p(stream.cuda_stream))
-    if st != 0:
-        raise GdnError(st, "gdn_qk_l2norm")
+    with torch.cuda.device(ref.device):
+        if q is not None and q_out is None:
+            q_out = torch.empty_like(q)
+        if k is not None and k_out is None:
+            k_out = torch.empty_like(k)
+        stream = stream if stream is not None else torch.cuda.current_stream(ref.device)
+        st = gdn_qk_l2norm(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), rows, dk, _dtype_code(ref), float(eps),
+                           ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise GdnError(st, "gdn_qk_l2norm")
     return q_out, k_out
 
 
@@ -368,14 +396,18 @@ def qk_l2norm_backward(x, dy, dx=None, eps: float = 0.0, stream: Optional[torch.
             raise ValueError("%s must be a contiguous CUDA tensor" % name)
     if dy.dtype != torch.float32 or dy.shape != x.shape:
         raise ValueError("dy must be float32 with x's shape")
-    if dx is None:
-        dx = torch.empty_like(dy)
+    if dx is not None and (dx.dtype != torch.float32 or dx.shape != x.shape):
+        raise ValueError("dx must be float32 with x's shape")
+    _check_placement("cuda", x.device, dict(dy=dy, dx=dx))
     dk = x.shape[-1]
-    stream = stream if stream is not None else torch.cuda.current_stream(x.device)
-    st = gdn_qk_l2norm_bwd(_ptr(x), _ptr(dy), _ptr(dx), x.numel() // dk, dk, _dtype_code(x), float(eps),
-                           ctypes.c_void_p(stream.cuda_stream))
-    if st != 0:
-        raise GdnError(st, "gdn_qk_l2norm_bwd")
+    with torch.cuda.device(x.device):
+        if dx is None:
+            dx = torch.empty_like(dy)
+        stream = stream if stream is not None else torch.cuda.current_stream(x.device)
+        st = gdn_qk_l2norm_bwd(_ptr(x), _ptr(dy), _ptr(dx), x.numel() // dk, dk, _dtype_code(x), float(eps),
+                               ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise GdnError(st, "gdn_qk_l2norm_bwd")
     return dx
 
 
@@ -388,25 +420,36 @@ def chunk_fwd_host(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=
     _expect("out", out, (B, T, H, dv))
     _expect("final_state", final_state, (N, H, dk, dv))
     dt = _dtype_code(q)
-    for name, t in dict(q=q, k=k, v=v, g=g, beta=beta).items():
-        if t.is_cuda or not t.is_contiguous():
-            raise ValueError("%s must be a contiguous host tensor" % name)
+    f32 = torch.float32
+    _check_dtypes(dict(k=k, v=v, g=g, beta=beta, initial_state=initial_state, cu_seqlens=cu_seqlens, out=out,
+                       final_state=final_state, device_buffer=device_buffer),
+                  dict(k=q.dtype, v=q.dtype, g=f32, beta=f32, initial_state=f32, cu_seqlens=torch.int32,
+                       out=q.dtype, final_state=f32, device_buffer=torch.uint8))
+    _check_placement("cpu", None, dict(q=q, k=k, v=v, g=g, beta=beta, initial_state=initial_state,
+                                       cu_seqlens=cu_seqlens, out=out, final_state=final_state))
+    if device_buffer is not None:
+        device = device_buffer.device if device is None else torch.device(device)
+        _check_placement("cuda", device, dict(device_buffer=device_buffer))
     device = torch.device(device or "cuda")
-    if out is None:
-        out = torch.empty(B, T, H, dv, dtype=q.dtype, pin_memory=True)
-    if final_state is None:
-        final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, pin_memory=True)
-    if device_buffer is None:
-        n = gdn_chunk_fwd_host_buffer_size(B, T, H, dk, dv, N, cu_seqlens is not None,
-                                           initial_state is not None, dt, opts)
-        device_buffer = torch.empty(n, dtype=torch.uint8, device=device)
-    stream = stream if stream is not None else torch.cuda.current_stream(device)
-    st = gdn_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
-                            N, float(scale) if scale is not None else 0.0, B, T, H, dk, dv, dt,
-                            _ptr(out), _ptr(final_state), _ptr(device_buffer), device_buffer.numel(),
-                            ctypes.byref(opts) if opts is not None else None, ctypes.c_void_p(stream.cuda_stream))
-    if st != 0:
-        raise GdnError(st, "gdn_chunk_fwd_host")
+    if device.type != "cuda":
+        raise ValueError("device must be a CUDA device, got %s" % device)
+    with torch.cuda.device(device):
+        if out is None:
+            out = torch.empty(B, T, H, dv, dtype=q.dtype, pin_memory=True)
+        if final_state is None:
+            final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, pin_memory=True)
+        if device_buffer is None:
+            n = gdn_chunk_fwd_host_buffer_size(B, T, H, dk, dv, N, cu_seqlens is not None,
+                                               initial_state is not None, dt, opts)
+            device_buffer = torch.empty(n, dtype=torch.uint8, device=device)
+        stream = stream if stream is not None else torch.cuda.current_stream(device)
+        st = gdn_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                _ptr(cu_seqlens), N, float(scale) if scale is not None else 0.0, B, T, H, dk, dv, dt,
+                                _ptr(out), _ptr(final_state), _ptr(device_buffer), device_buffer.numel(),
+                                ctypes.byref(opts) if opts is not None else None,
+                                ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise GdnError(st, "gdn_chunk_fwd_host")
     return out, final_state
 
 
@@ -418,42 +461,37 @@ def chunk_bwd(q, k, v, g, beta, do, initial_state=None, cu_seqlens=None, scale=N
     _expect("do", do, (B, T, H, dv))
     _expect("d_final_state", d_final_state, (N, H, dk, dv))
     dt = _dtype_code(q)
-    for name, t in dict(k=k, v=v, do=do).items():
-        if t.dtype != q.dtype:
-            raise TypeError("%s must have q's dtype" % name)
-    for name, t in dict(q=q, k=k, v=v, g=g, beta=beta, do=do).items():
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("%s must be a contiguous CUDA tensor" % name)
-    if g.dtype != torch.float32 or beta.dtype != torch.float32:
-        raise TypeError("g and beta must be float32")
-    for name, t in dict(initial_state=initial_state, d_final_state=d_final_state).items():
-        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
-            raise TypeError("%s must be contiguous float32" % name)
-    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
-        raise TypeError("cu_seqlens must be int32")
     f32, dev = torch.float32, q.device
-    dq = torch.empty(B, T, H, dk, dtype=f32, device=dev)
-    dk_ = torch.empty(B, T, H, dk, dtype=f32, device=dev)
-    dv_ = torch.empty(B, T, H, dv, dtype=f32, device=dev)
-    dg = torch.empty(B, T, H, dtype=f32, device=dev)
-    db = torch.empty(B, T, H, dtype=f32, device=dev)
-    ds0 = torch.empty(N, H, dk, dv, dtype=f32, device=dev)
-    if workspace is None:
-        n = gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, N, cu_seqlens is not None, dt)
-        if n == 0:
-            raise GdnError(1, "gdn_chunk_bwd_workspace_size")
-        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
-    stream = stream if stream is not None else torch.cuda.current_stream(dev)
-    st = gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
-                       N, float(scale) if scale is not None else 0.0, B, T, H, dk, dv, dt,
-                       _ptr(do), _ptr(d_final_state), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(db), _ptr(ds0),
-                       _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
-    if st != 0:
-        raise GdnError(st, "gdn_chunk_bwd")
-    if check:
-        st = gdn_chunk_bwd_check(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream))
+    _check_dtypes(dict(k=k, v=v, do=do, g=g, beta=beta, initial_state=initial_state, cu_seqlens=cu_seqlens,
+                       d_final_state=d_final_state, workspace=workspace),
+                  dict(k=q.dtype, v=q.dtype, do=q.dtype, g=f32, beta=f32, initial_state=f32,
+                       cu_seqlens=torch.int32, d_final_state=f32, workspace=torch.uint8))
+    _check_placement("cuda", None, dict(q=q))
+    _check_placement("cuda", dev, dict(k=k, v=v, g=g, beta=beta, do=do, initial_state=initial_state,
+                                       cu_seqlens=cu_seqlens, d_final_state=d_final_state, workspace=workspace))
+    with torch.cuda.device(dev):
+        dq = torch.empty(B, T, H, dk, dtype=f32, device=dev)
+        dk_ = torch.empty(B, T, H, dk, dtype=f32, device=dev)
+        dv_ = torch.empty(B, T, H, dv, dtype=f32, device=dev)
+        dg = torch.empty(B, T, H, dtype=f32, device=dev)
+        db = torch.empty(B, T, H, dtype=f32, device=dev)
+        ds0 = torch.empty(N, H, dk, dv, dtype=f32, device=dev)
+        if workspace is None:
+            n = gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, N, cu_seqlens is not None, dt)
+            if n == 0:
+                raise GdnError(1, "gdn_chunk_bwd_workspace_size")
+            workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+        stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        st = gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
+                           N, float(scale) if scale is not None else 0.0, B, T, H, dk, dv, dt,
+                           _ptr(do), _ptr(d_final_state), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(db),
+                           _ptr(ds0), _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
         if st != 0:
-            raise GdnError(st, "device check")
+            raise GdnError(st, "gdn_chunk_bwd")
+        if check:
+            st = gdn_chunk_bwd_check(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream))
+            if st != 0:
+                raise GdnError(st, "device check")
     return dq, dk_, dv_, dg, db, ds0
 
 

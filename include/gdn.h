@@ -263,7 +263,14 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v,
  *
  * The first call on a device looks up the array's device address and caches
  * it (cudaGetSymbolAddress, no allocation); make that first call before any
- * stream capture.  The call allocates nothing, host or device.
+ * stream capture.  With lazy module loading (the CUDA default) that first
+ * call is also when the runtime loads the library's device code and reserves
+ * the 64 MiB array on the device, so a caller whose pool takes the rest of
+ * HBM at start-up must make one call (any size, e.g. an empty batch) before
+ * the pool reserves its memory.  The cached address belongs to the device's
+ * current primary context: after cudaDeviceReset() in the same process this
+ * entry point must not be called again.  Apart from that first load the call
+ * allocates nothing, host or device.
  *
  * Every call on a device shares the one array, which keeps the previous call's
  * contents; the call clears what must start at zero (the error word and the

@@ -233,3 +233,64 @@ def test_binding_rejects_mismatched_shapes_before_the_library():
         gdn.chunk_bwd(q, q, v, g, g, torch.zeros(1, 8, 2, 64), d_final_state=torch.zeros(2, 2, 32, 64))
     with pytest.raises(ValueError, match="beta has shape"):
         gdn.chunk_fwd_host(q, q, v, g, torch.zeros(1, 8, 1))
+
+
+def test_binding_rejects_wrong_dtypes_before_the_library():
+    """A tensor of the wrong element type would be read or written past its end
+    by the kernels (an fp32 state written into a bf16 buffer, an int64
+    cu_seqlens read as int32 pairs), so the binding checks every dtype first.
+    These tensors are on the CPU, so passing the dtype checks would stop at the
+    placement check instead (the control)."""
+    import torch
+    q = torch.zeros(1, 8, 2, 32, dtype=torch.bfloat16)
+    v = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    g = torch.zeros(1, 8, 2)
+    with pytest.raises(ValueError, match="CUDA"):                                   # control
+        gdn.chunk_fwd(q, q, v, g, g)
+    cases = [
+        dict(final_state=torch.zeros(1, 2, 32, 64, dtype=torch.bfloat16)),
+        dict(out=torch.zeros(1, 8, 2, 64, dtype=torch.float32)),
+        dict(initial_state=torch.zeros(1, 2, 32, 64, dtype=torch.float64)),
+        dict(cu_seqlens=torch.tensor([0, 8], dtype=torch.int64)),
+        dict(workspace=torch.zeros(16, dtype=torch.int32)),
+    ]
+    for kw in cases:
+        with pytest.raises(TypeError, match=next(iter(kw))):
+            gdn.chunk_fwd(q, q, v, g, g, **kw)
+    with pytest.raises(TypeError, match="g must be"):
+        gdn.chunk_fwd(q, q, v, g.double(), g)
+    with pytest.raises(TypeError, match="v must be"):
+        gdn.chunk_fwd(q, q, v.float(), g, g)
+    with pytest.raises(TypeError, match="do must be"):
+        gdn.chunk_bwd(q, q, v, g, g, torch.zeros(1, 8, 2, 64))
+    with pytest.raises(TypeError, match="d_final_state must be"):
+        gdn.chunk_bwd(q, q, v, g, g, torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16),
+                      d_final_state=torch.zeros(1, 2, 32, 64, dtype=torch.bfloat16))
+    with pytest.raises(TypeError, match="final_state must be"):
+        gdn.chunk_fwd_host(q, q, v, g, g, final_state=torch.zeros(1, 2, 32, 64, dtype=torch.bfloat16))
+
+
+def test_binding_placement_check():
+    """Every tensor handed to a device entry point must live on q's device, and
+    every tensor of the host-buffer entry point in host memory: the library
+    receives bare pointers.  Without a GPU here the device rule is exercised on
+    the 'meta' device type (same code path: type first, then the device, then
+    contiguity)."""
+    import torch
+    meta = torch.empty(4, 4, device="meta")
+    cpu = torch.zeros(4, 4)
+    gdn._check_placement("meta", meta.device, dict(a=meta, b=None))
+    with pytest.raises(ValueError, match="initial_state must be a contiguous META tensor"):
+        gdn._check_placement("meta", meta.device, dict(q=meta, initial_state=cpu))
+    with pytest.raises(ValueError, match="cu_seqlens must be a contiguous CUDA tensor"):
+        gdn._check_placement("cuda", None, dict(cu_seqlens=cpu))
+    with pytest.raises(ValueError, match="contiguous"):
+        gdn._check_placement("cpu", cpu.device, dict(x=cpu.t()))
+    # the host-buffer entry point: a device-side (here: meta) input is refused
+    q = torch.zeros(1, 8, 2, 32)
+    v = torch.zeros(1, 8, 2, 64)
+    g = torch.zeros(1, 8, 2)
+    with pytest.raises(ValueError, match="initial_state must be a contiguous CPU tensor"):
+        gdn.chunk_fwd_host(q, q, v, g, g, initial_state=torch.empty(1, 2, 32, 64, device="meta"))
+    with pytest.raises(ValueError, match="device_buffer must be a contiguous CUDA tensor"):
+        gdn.chunk_fwd_host(q, q, v, g, g, device_buffer=torch.zeros(16, dtype=torch.uint8))

@@ -9,8 +9,10 @@ forward pass with it in place of a caller workspace.
 The test calls that entry point through the C ABI twice in a row, on two
 different problems (so the second call finds the first call's leftovers in the
 shared array), and checks both results against gdn_chunk_fwd with a workspace
-of its own, within the parity tolerance of the other GPU tests.  The file name
-makes pytest collect it last.
+of its own: the two entry points run the same kernels with the same plan, so
+the results must agree bit for bit (and within the parity tolerance of the
+other GPU tests, which that implies).  The file name makes pytest collect it
+last.
 """
 import ctypes
 
@@ -83,6 +85,7 @@ def test_static_scratch_matches_workspace_entry_point_twice(lib):
         o_ref, sf_ref = run_workspace(inp)
         assert_close("o", oracle.to_f64(o), oracle.to_f64(o_ref), REL_L2, MAX_ABS)
         assert_close("final_state", oracle.to_f64(sf), oracle.to_f64(sf_ref), REL_L2, MAX_ABS)
+        assert torch.equal(o, o_ref) and torch.equal(sf, sf_ref)
 
 
 def test_static_scratch_rejects_oversized_problem(lib):
