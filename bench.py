@@ -27,7 +27,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "GDN chunked-prefill fwd tokens/s & % roofline (B=4,T=8192,H=32,d=128)"
+METRIC_PREFIX = "GDN chunked-prefill fwd tokens/s & % roofline"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
@@ -43,6 +43,33 @@ def load_peaks():
         return p, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def shape_label(cfg):
+    """The workload's shape as the metric names it, e.g. B=4,T=8192,H=32,d=128
+    (packed batches: N sequences, T total tokens)."""
+    d = "d=%d" % cfg.dk if cfg.dk == cfg.dv else "dk=%d,dv=%d" % (cfg.dk, cfg.dv)
+    if cfg.varlen:
+        return "N=%d varlen,T=%d,H=%d,%s" % (cfg.n_seqs, cfg.T, cfg.H, d)
+    return "B=%d,T=%d,H=%d,%s" % (cfg.B, cfg.T, cfg.H, d)
+
+
+def metric_for(cfg):
+    return "%s (%s)" % (METRIC_PREFIX, shape_label(cfg))
+
+
+def workload_label(cfg):
+    return "GDN fwd %s %s %s" % (cfg.name, shape_label(cfg).replace(",", " "), cfg.dtype)
+
+
+def input_bytes(cfg):
+    """Bytes of the step's inputs resident in HBM (q, k, v, g, beta, initial state)."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    th = cfg.total_tokens * cfg.H
+    n = th * ((2 * cfg.dk + cfg.dv) * e + 8)
+    if cfg.s0_std is not None:
+        n += cfg.num_seqs * cfg.H * cfg.dk * cfg.dv * 4
+    return n
 
 
 def algorithmic_work(cfg):
@@ -142,21 +169,22 @@ def reference_arm(args, cfg):
     step_times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.gdn_reference(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, None,
-                             scale=inp["scale"], heads=heads)
+        oracle.gdn_reference(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["initial_state"],
+                             inp["cu_seqlens"], scale=inp["scale"], heads=heads)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             step_times.append(dt)
     per = statistics.mean(step_times)
     token_heads = cfg.T * len(heads)
     value = token_heads / per / cfg.H                  # tokens/s of the full-width layer
-    sample = "1 of %d sequences x %d of %d heads (all %d tokens, all %d value rows) per step" % (
-        cfg.B, len(heads), cfg.H, cfg.T, cfg.dv)
+    sample = "%s x %d of %d heads (all %d tokens, all %d value rows) per step" % (
+        "all %d packed sequences" % cfg.n_seqs if cfg.varlen else "1 of %d sequences" % cfg.B,
+        len(heads), cfg.H, cfg.T, cfg.dv)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "impl": "reference", "metric": metric_for(cfg), "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "GDN fwd layer B=4 T=8192 H=32 dk=dv=128 (%s)" % cfg.name,
+        "config": {"workload": workload_label(cfg),
                    "global_batch": cfg.B, "seq_len": cfg.T, "heads": cfg.H, "head_dim": cfg.dk,
                    "parallelism": "host cores (OpenMP)", "sample": sample},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.oracle_threads(), "kind": "oracle",
@@ -174,8 +202,8 @@ def cpu_baseline(cfg, budget_s):
     from chunked_prefill_gdn_gb300.inputs import make_inputs
     inp = make_inputs(cfg.scaled(B=1), "cpu")
     t0 = time.perf_counter()
-    oracle.gdn_reference(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, None, scale=inp["scale"],
-                         heads=[0])
+    oracle.gdn_reference(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["initial_state"],
+                         inp["cu_seqlens"], scale=inp["scale"], heads=[0])
     per_unit = max(time.perf_counter() - t0, 1e-4)       # one head of one sequence
     units = int(min(cfg.B * cfg.H, max(1, budget_s / per_unit)))
     nseq = min(cfg.B, -(-units // cfg.H))
@@ -187,14 +215,15 @@ def cpu_baseline(cfg, budget_s):
             break
         seq_inp = inp if b == 0 else make_inputs(cfg.scaled(B=1, seed=cfg.seed + 1000 + b), "cpu")
         t0 = time.perf_counter()
-        oracle.gdn_reference(seq_inp["q"], seq_inp["k"], seq_inp["v"], seq_inp["g"], seq_inp["beta"], None, None,
-                             scale=seq_inp["scale"], heads=heads)
+        oracle.gdn_reference(seq_inp["q"], seq_inp["k"], seq_inp["v"], seq_inp["g"], seq_inp["beta"],
+                             seq_inp["initial_state"], seq_inp["cu_seqlens"], scale=seq_inp["scale"], heads=heads)
         elapsed += time.perf_counter() - t0
         done += len(heads)
     value = cfg.T * done / elapsed / cfg.H
     return {"value": value, "unit": "tokens/s", "cores": oracle.oracle_threads(), "kind": "oracle",
-            "sample": "%d (sequence, head) units of %d (T=%d each, all %d value rows), %.1f s" % (
-                done, cfg.B * cfg.H, cfg.T, cfg.dv, elapsed)}
+            "sample": "%d (%s, head) units of %d (T=%d each, all %d value rows), %.1f s" % (
+                done, "packed batch of %d sequences" % cfg.n_seqs if cfg.varlen else "sequence",
+                cfg.B * cfg.H, cfg.T, cfg.dv, elapsed)}
 
 
 def main():
@@ -309,26 +338,20 @@ def main():
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     roof_ms = max(t_hbm, t_tc) * 1e3
-    traffic = None
-    prof_json = os.path.join(ROOT, "profiles", "fused_pass_layer_traffic.json")
     kname = "tc" if plan.kernel == gdn.KERNEL_TC else "simt"
-    try:
-        with open(prof_json) as f:
-            pj = json.load(f)
-        if pj.get("kernel") == kname and pj.get("source_sha") == kernel_source_sha(kname):
-            traffic = pj.get("dram_bytes_per_launch")
-    except (OSError, ValueError):
-        pass
+    traffic = recorded_traffic(kname, workload_label(cfg), bool(plan.cp_enabled))
     launches_per_step = 5 + (2 if plan.cp_enabled else 0)
 
     result = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "metric": metric_for(cfg), "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": "GDN fwd layer B=%d T=%d H=%d dk=dv=%d (%s)" % (B, T, H, dk, cfg.name),
+        "config": {"workload": workload_label(cfg),
                    "global_batch": B * ws, "seq_len": T, "heads": H, "head_dim": dk,
                    "parallelism": "replicas" if ws > 1 else "single GPU",
-                   "l2": "flushed between timed steps (512 MB write) and inputs (805 MB) exceed L2",
+                   "l2": "flushed between timed steps (%d MB write); inputs %d MB (%s L2)" % (
+                       FLUSH_BYTES >> 20, input_bytes(cfg) // 10 ** 6,
+                       "exceed" if input_bytes(cfg) > 129 * 10 ** 6 else "fit in"),
                    "fused_kernel": kname, "cp": bool(plan.cp_enabled)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
@@ -362,6 +385,27 @@ def ctypes_ptr(t):
 def ctypes_ptr_stream(s):
     import ctypes
     return ctypes.c_void_p(s.cuda_stream)
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_pass_traffic.json")
+
+
+def recorded_traffic(kname, workload, cp):
+    """DRAM bytes per launch of the fused output pass from an ncu capture of
+    this exact kernel source on this workload (profiles/fused_pass_traffic.json,
+    one record per (kernel, source, workload)); None when no such capture
+    exists, e.g. after the kernel changed."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            records = json.load(f)
+    except (OSError, ValueError):
+        return None
+    sha = kernel_source_sha(kname)
+    for r in records:
+        if (r.get("kernel") == kname and r.get("source_sha") == sha and r.get("workload") == workload
+                and bool(r.get("cp", False)) == cp):
+            return r.get("dram_bytes_per_launch")
+    return None
 
 
 def kernel_source_sha(kname):
@@ -497,9 +541,63 @@ def e2e_measure(gdn, torch, inp, cfg, opts, dev, args):
     if host["cu_seqlens"] is not None:
         h2d += host["cu_seqlens"].numel() * 4
     d2h = o.numel() * el + fs.numel() * 4
+    link = host_link_rates(torch, dev, max(h2d, d2h))
+    copy_ms = (h2d / link["h2d_gbs"] + d2h / link["d2h_gbs"]) / 1e6
     return {"value": cfg.total_tokens / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps,
-            "api": "gdn_chunk_fwd_host (pinned host buffers, synchronous per step)"}
+            "api": "gdn_chunk_fwd_host (pinned host buffers, synchronous per step)",
+            "link_gbs_h2d": link["h2d_gbs"], "link_gbs_d2h": link["d2h_gbs"],
+            "link_gbs_both": link["both_gbs"],
+            "copy_floor_ms_serial": copy_ms,
+            "copy_floor_ms_overlapped": (h2d + d2h) / link["both_gbs"] / 1e6,
+            "link_note": "one pinned cudaMemcpyAsync of %d MB each way (and both at once on two streams), CUDA "
+                         "events, best of %d" % (link["bytes"] // 10 ** 6, link["reps"])}
+
+
+def host_link_rates(torch, dev, nbytes, reps=5):
+    """Plain pinned host<->device copy rates on this machine: one large
+    cudaMemcpyAsync each way (torch copy_), timed with CUDA events, best of
+    `reps`; and both directions at once on two streams (bytes of both / time)."""
+    nbytes = int(min(max(nbytes, 64 << 20), 1 << 30))
+    h_src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_dst = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1 = torch.cuda.Stream(dev)
+    s2 = torch.cuda.Stream(dev)
+
+    def timed(fn, stream):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            best = min(best, a.elapsed_time(b))
+        return best
+
+    with torch.cuda.stream(s1):
+        h2d_ms = timed(lambda: d_a.copy_(h_src, non_blocking=True), s1)
+        d2h_ms = timed(lambda: h_dst.copy_(d_a, non_blocking=True), s1)
+
+    def both():
+        ev = torch.cuda.Event()
+        ev.record(s1)
+        s2.wait_event(ev)
+        with torch.cuda.stream(s2):
+            h_dst.copy_(d_b, non_blocking=True)
+        d_a.copy_(h_src, non_blocking=True)
+        ev2 = torch.cuda.Event()
+        ev2.record(s2)
+        s1.wait_event(ev2)
+
+    with torch.cuda.stream(s1):
+        both_ms = timed(both, s1)
+    return {"h2d_gbs": nbytes / h2d_ms / 1e6, "d2h_gbs": nbytes / d2h_ms / 1e6,
+            "both_gbs": 2 * nbytes / both_ms / 1e6, "bytes": nbytes, "reps": reps}
 
 
 if __name__ == "__main__":
