@@ -25,7 +25,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "GdnOptions", "GdnPlanInfo", "GdnWorkspaceLayout", "WORK_ITEM_DTYPE",
+    "GdnOptions", "GdnPlanInfo", "GdnPlanCosts", "GdnWorkspaceLayout", "WORK_ITEM_DTYPE",
+    "gdn_set_plan_costs", "gdn_get_plan_costs", "gdn_auto_cp_min_chunks",
     "load_library", "library_path", "default_options",
     "gdn_default_options", "gdn_plan_query", "gdn_chunk_fwd_workspace_size", "gdn_workspace_query",
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
@@ -70,6 +71,11 @@ class GdnPlanInfo(ctypes.Structure):
                 ("max_items", ctypes.c_int32), ("max_cp_slots", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("grid_fused", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_size_t)]
+
+
+class GdnPlanCosts(ctypes.Structure):
+    _fields_ = [("chunk_step_us", ctypes.c_float), ("state_step_us", ctypes.c_float),
+                ("scan_step_us", ctypes.c_float), ("pass_us", ctypes.c_float)]
 
 
 class GdnWorkspaceLayout(ctypes.Structure):
@@ -131,6 +137,12 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_chunk_bwd.restype = i32
     lib.gdn_chunk_bwd_check.argtypes = [vp, vp]
     lib.gdn_chunk_bwd_check.restype = i32
+    lib.gdn_set_plan_costs.argtypes = [ctypes.POINTER(GdnPlanCosts)]
+    lib.gdn_set_plan_costs.restype = i32
+    lib.gdn_get_plan_costs.argtypes = [ctypes.POINTER(GdnPlanCosts)]
+    lib.gdn_get_plan_costs.restype = None
+    lib.gdn_auto_cp_min_chunks.argtypes = [i32, i32]
+    lib.gdn_auto_cp_min_chunks.restype = i32
     lib.gdn_status_string.argtypes = [i32]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_version.argtypes = []
@@ -138,7 +150,26 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_last_error_detail.argtypes = []
     lib.gdn_last_error_detail.restype = ctypes.c_char_p
     _lib = lib
+    _apply_measured_costs(lib)
     return lib
+
+
+PLAN_COSTS_FILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "plan_costs.json")
+
+
+def _apply_measured_costs(lib):
+    """The planner's step costs measured by the calibrate module on this kind
+    of GPU (plan_costs.json next to this file), when present; the library's
+    built-in table otherwise."""
+    if not os.path.exists(PLAN_COSTS_FILE):
+        return
+    import json
+    with open(PLAN_COSTS_FILE) as f:
+        c = json.load(f)["costs"]
+    costs = GdnPlanCosts(*(float(c[k]) for k in ("chunk_step_us", "state_step_us", "scan_step_us", "pass_us")))
+    st = lib.gdn_set_plan_costs(ctypes.byref(costs))
+    if st != 0:
+        raise GdnError(st, "gdn_set_plan_costs (%s)" % PLAN_COSTS_FILE)
 
 
 def default_options(**kw) -> GdnOptions:
@@ -220,6 +251,22 @@ def gdn_chunk_bwd(*args) -> int:
 
 def gdn_chunk_bwd_check(workspace_ptr, stream_ptr) -> int:
     return int(load_library().gdn_chunk_bwd_check(workspace_ptr, stream_ptr))
+
+
+def gdn_set_plan_costs(costs: Optional[GdnPlanCosts]) -> None:
+    st = load_library().gdn_set_plan_costs(ctypes.byref(costs) if costs is not None else None)
+    if st != 0:
+        raise GdnError(st, "gdn_set_plan_costs")
+
+
+def gdn_get_plan_costs() -> GdnPlanCosts:
+    c = GdnPlanCosts()
+    load_library().gdn_get_plan_costs(ctypes.byref(c))
+    return c
+
+
+def gdn_auto_cp_min_chunks(units: int, sms: int) -> int:
+    return int(load_library().gdn_auto_cp_min_chunks(units, sms))
 
 
 def gdn_status_string(status: int) -> str:

@@ -206,24 +206,25 @@ constexpr int kMaxLookbackChunks = 256;
 
 // Segments per unit for the units that need correction matrices, when every
 // unit has nc chunks and the planner's segment length gives NS0 segments.
-// Per-pass cost model in chunk steps of the persistent passes on `grid` CTAs
-// (the talk's auto-CP paragraph: one-wave model T = lambda1 L + lambda2 N / L,
-// refined per pass): pass 1 runs 2 NS - 3 items per such unit (S* and M of
-// every segment but the last, S* of the first), pass 2 one item per segment of
-// every unit (n_s units keep NS0 segments and re-run a look-back of about four
-// chunks), the scan about half a chunk step per segment; a pass takes as many
-// waves as its items need, each as long as its longest item.  Fewer, longer
-// segments can save a whole wave of pass 1.  Returns 0 to keep NS0 (unless
-// another count is at least 5% cheaper).
-__device__ int correction_segments(int nc, int NS0, int n_m, int n_s, int grid) {
+// Per-pass cost model in output chunk steps of the persistent passes on `grid`
+// CTAs (the talk's auto-CP paragraph: one-wave model T = lambda1 L +
+// lambda2 N / L, refined per pass, with the measured step costs): pass 1 runs
+// 2 NS - 3 state-only items per such unit (S* and M of every segment but the
+// last, S* of the first), pass 2 one item per segment of every unit (n_s units
+// keep NS0 segments and re-run a look-back of about four chunks), the scan one
+// step per segment; a pass takes as many waves as its items need, each as long
+// as its longest item.  Fewer, longer segments can save a whole wave of pass
+// 1.  Returns 0 to keep NS0 (unless another count is at least 5% cheaper).
+__device__ int correction_segments(int nc, int NS0, int n_m, int n_s, int grid, float state_ratio,
+                                   float scan_ratio) {
     if (n_m <= 0 || NS0 <= 2 || grid <= 0) return 0;
     const int Ls = (nc + NS0 - 1) / NS0 + (n_s > 0 ? 4 : 0);
     auto cost = [&](int ns) {
         const int Lm = (nc + ns - 1) / ns;
         const long long it1 = (long long)n_m * (2 * ns - 3);
         const long long it2 = (long long)n_m * ns + (long long)n_s * NS0;
-        return (double)((it1 + grid - 1) / grid) * Lm + (double)((it2 + grid - 1) / grid) * max(Lm, n_s > 0 ? Ls : 0) +
-               0.5 * ns;
+        return (double)((it1 + grid - 1) / grid) * Lm * state_ratio +
+               (double)((it2 + grid - 1) / grid) * max(Lm, n_s > 0 ? Ls : 0) + (double)scan_ratio * ns;
     };
     const double c0 = cost(NS0);
     int best = NS0;
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Prob
                 if (!(w.flags[u] != 0 && pp.sliding)) ++mine;      // flags are [N, H]: unit u = (u / H, u % H)
             if (mine) atomicAdd(&s_nm, mine);
             __syncthreads();
-            if (tid == 0) s_ns_m = correction_segments(nc, NS0, s_nm, units - s_nm, pp.grid);
+            if (tid == 0) s_ns_m = correction_segments(nc, NS0, s_nm, units - s_nm, pp.grid, pp.state_ratio, pp.scan_ratio);
             __syncthreads();
         }
     }

@@ -18,13 +18,26 @@ namespace {
 
 constexpr int kDefaultSMs = 152;        // GB300
 constexpr int kMinSegmentChunks = 8;
-// Cost-model constants of the auto-CP planner, in units of one chunk step of the
-// fused kernel (the talk's one-wave model T = lambda1 L + lambda2 N / L, made
-// wave-aware): a scan step, the expected look-back of a split segment, and the
-// share of split heads expected to need the correction pass.
-constexpr double kScanStepChunks = 0.5;
+// Priors of the host planner about the gates, which only the device sees (it
+// refines the plan per pass once the head flags are known): the look-back a
+// split segment of a decaying head re-runs, and the share of split heads that
+// need correction matrices (alpha == 1).  They describe the workload, not the
+// hardware; the hardware enters through the measured step costs below.
 constexpr double kLookbackChunks = 4.0;
 constexpr double kCorrectionShare = 0.5;
+
+// Measured step costs of the auto-CP planner (the talk's one-wave model
+// T = lambda1 L + lambda2 N / L, made wave-aware): gdn_plan_costs.  The
+// defaults were measured on a GB300 (152 SMs, 2.07 GHz) with the package's
+// calibrate module; gdn_set_plan_costs() replaces them.
+constexpr gdn_plan_costs kDefaultCosts = {1.80f, 1.50f, 0.90f, 8.0f};
+std::mutex g_costs_mu;
+gdn_plan_costs g_costs = kDefaultCosts;
+
+gdn_plan_costs current_costs() {
+    std::lock_guard<std::mutex> lock(g_costs_mu);
+    return g_costs;
+}
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -71,20 +84,27 @@ void default_options(gdn_options *o) {
     o->sm_count = 0;
 }
 
-// Segments per unit for B equal sequences of nc chunks: minimise the waves of
-// the persistent grid times the longest segment, plus the scan and the expected
-// correction pass.  One segment unless splitting wins by 10%.
+// Modelled time (microseconds) of B equal sequences of nc chunks split into
+// ns segments, on `sms` CTAs of the persistent passes: the output pass takes
+// as many waves as its items need, each as long as a segment (plus the
+// look-back a decaying head re-runs); the correction pass likewise for the
+// expected share of heads that need correction matrices (2 ns - 3 items each),
+// then the serial scan over segments and the fixed cost of the two launches.
+double split_cost(int units, int nc, int ns, int sms, const gdn_plan_costs &c) {
+    if (ns <= 1) return ceil((double)units / sms) * nc * c.chunk_step_us;
+    const int L = (nc + ns - 1) / ns;
+    const double w2 = ceil((double)units * ns / sms);
+    double t = w2 * (L * (double)c.chunk_step_us + kLookbackChunks * c.state_step_us);
+    const double w1 = ceil(kCorrectionShare * units * (2.0 * ns - 3.0) / sms);
+    t += w1 * L * (double)c.state_step_us + (ns - 1) * (double)c.scan_step_us + c.pass_us;
+    return t;
+}
+
+// Segments per unit for B equal sequences of nc chunks: the count with the
+// least modelled time; one segment unless splitting wins by 10%.
 int choose_segments(int units, int nc, int sms) {
-    auto cost = [&](int ns) {
-        const int L = (nc + ns - 1) / ns;
-        const double waves = ceil((double)units * ns / sms);
-        double c = waves * (L + (ns > 1 ? kLookbackChunks : 0.0));
-        if (ns > 1) {
-            const double w1 = ceil(kCorrectionShare * 2.0 * units * (ns - 1) / sms);
-            c += kCorrectionShare * w1 * L + kScanStepChunks * (ns - 2);
-        }
-        return c;
-    };
+    const gdn_plan_costs costs = current_costs();
+    auto cost = [&](int ns) { return split_cost(units, nc, ns, sms, costs); };
     int best = 1;
     double best_cost = cost(1);
     const int max_ns = std::max(1, std::min(nc / kMinSegmentChunks, 4 * sms));
@@ -218,6 +238,42 @@ void gdn_default_options(gdn_options *opts) {
     if (opts) default_options(opts);
 }
 
+gdn_status gdn_set_plan_costs(const gdn_plan_costs *costs) {
+    gdn_plan_costs c = costs ? *costs : kDefaultCosts;
+    auto ok = [](float x, float lo) { return x == x && x >= lo && x < 1e6f; };
+    if (!ok(c.chunk_step_us, 1e-3f) || !ok(c.state_step_us, 1e-3f) || !ok(c.scan_step_us, 0.f) ||
+        !ok(c.pass_us, 0.f))
+        return GDN_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_costs_mu);
+    g_costs = c;
+    return GDN_OK;
+}
+
+void gdn_get_plan_costs(gdn_plan_costs *costs) {
+    if (costs) *costs = current_costs();
+}
+
+int gdn_auto_cp_min_chunks(int units, int sms) {
+    if (units < 1 || sms < 1 || units >= sms) return 0;
+    constexpr int kMax = 1 << 20;
+    // the first length on a geometric grid where the planner splits, then the
+    // exact boundary by bisection below it
+    int lo = kMinSegmentChunks, hi = 0;
+    for (int nc = kMinSegmentChunks; nc <= kMax; nc = std::max(nc + 1, nc + nc / 16)) {
+        if (choose_segments(units, nc, sms) > 1) {
+            hi = nc;
+            break;
+        }
+        lo = nc;
+    }
+    if (hi == 0) return 0;
+    while (hi - lo > 1) {
+        const int mid = lo + (hi - lo) / 2;
+        if (choose_segments(units, mid, sms) > 1) hi = mid; else lo = mid;
+    }
+    return hi;
+}
+
 gdn_status gdn_plan_query(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, gdn_dtype dtype,
                           const gdn_options *opts, gdn_plan_info *out) {
     if (!out) return GDN_ERR_INVALID_ARG;
@@ -323,6 +379,11 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
     pp.sliding = opts.sliding ? 1 : 0;
     pp.ln_eps = logf(opts.sw_eps);
     pp.grid = hp.grid;
+    {
+        const gdn_plan_costs c = current_costs();
+        pp.state_ratio = c.state_step_us / c.chunk_step_us;
+        pp.scan_ratio = c.scan_step_us / c.chunk_step_us;
+    }
 
     const int stages = opts.stages ? opts.stages : (GDN_STAGE_PREP | GDN_STAGE_INVERSE | GDN_STAGE_CORRECTION |
                                                     GDN_STAGE_FUSED);

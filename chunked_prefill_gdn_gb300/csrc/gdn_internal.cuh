@@ -52,6 +52,8 @@ struct PlanParams {
     int sliding;
     float ln_eps;
     int grid;         // CTAs of the persistent fused passes
+    float state_ratio;  // measured: a state-only chunk step / an output chunk step
+    float scan_ratio;   // measured: a scan step / an output chunk step
 };
 
 // Host-side layout of the workspace for one problem.

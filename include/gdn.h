@@ -175,6 +175,47 @@ enum {
 /* Fill *opts with the defaults (AUTO everywhere, sliding on, sw_eps 2^-24). */
 void gdn_default_options(gdn_options *opts);
 
+/*
+ * Cost model of the auto-CP planner.  The intra-card sequence-parallel
+ * paragraph of the FlashQLA talk "Qwen系列模型线性注意力高性能优化实践" models the
+ * time of a split sequence as T = lambda1 L + lambda2 N / L (L chunks per
+ * segment, N / L segments) with lambda measured on the hardware; the planner
+ * here is the wave-aware form of that model and takes its lambdas from this
+ * table, in microseconds on the target GPU with every SM busy:
+ *   chunk_step_us  one chunk step of the fused output pass (lambda1, pass 2)
+ *   state_step_us  one chunk step of a state-only correction item (lambda1, pass 1)
+ *   scan_step_us   one segment step of the segment scan (lambda2)
+ *   pass_us        the fixed cost of the correction pass and the scan launches
+ * The library starts with values measured on a GB300; gdn_set_plan_costs()
+ * replaces them for the whole process (NULL restores those defaults; a
+ * non-finite, negative or zero step cost is GDN_ERR_INVALID_ARG) and
+ * gdn_get_plan_costs() reads the current table.  The Python package's
+ * `calibrate` module measures the table on the GPU at hand by timing this
+ * library's own passes.  Plans made before a change keep the costs they were
+ * made with; nothing else depends on the table (every plan is exact).
+ */
+typedef struct {
+    float chunk_step_us;
+    float state_step_us;
+    float scan_step_us;
+    float pass_us;
+} gdn_plan_costs;
+
+gdn_status gdn_set_plan_costs(const gdn_plan_costs *costs);
+void gdn_get_plan_costs(gdn_plan_costs *costs);
+
+/*
+ * The enabling boundary of auto CP for batches of equal sequences: the least
+ * sequence length, in chunks of 64 tokens, at which GDN_CP_AUTO splits
+ * sequences when there are `units` = B x H (sequence, head) units on `sms`
+ * SMs, under the current cost table; 0 when no length up to 2^20 chunks does
+ * (always for units >= sms).  The talk's enabling-condition paragraph notes
+ * that the boundary in the (B x H, length) plane is a curve rather than a
+ * threshold on either axis: more units leave fewer idle SMs, so a longer
+ * sequence is needed before splitting pays.  Host-only.
+ */
+int gdn_auto_cp_min_chunks(int units, int sms);
+
 /* Host-only planning: which kernel, whether CP is on, the segment length and
  * the workspace size.  `total_T` is B*T for batched input or the packed token
  * count with cu_seqlens (then B must be 1 and n_seqs = N).  opts may be NULL. */

@@ -294,3 +294,56 @@ def test_binding_placement_check():
         gdn.chunk_fwd_host(q, q, v, g, g, initial_state=torch.empty(1, 2, 32, 64, device="meta"))
     with pytest.raises(ValueError, match="device_buffer must be a contiguous CUDA tensor"):
         gdn.chunk_fwd_host(q, q, v, g, g, device_buffer=torch.zeros(16, dtype=torch.uint8))
+
+
+def test_plan_costs_roundtrip_and_validation(lib):
+    """The planner's measured step costs can be read, replaced and restored;
+    bad tables are refused without touching the current one."""
+    orig = gdn.gdn_get_plan_costs()
+    try:
+        c = gdn.GdnPlanCosts(2.0, 1.0, 0.5, 10.0)
+        gdn.gdn_set_plan_costs(c)
+        got = gdn.gdn_get_plan_costs()
+        assert (got.chunk_step_us, got.state_step_us, got.scan_step_us, got.pass_us) == (2.0, 1.0, 0.5, 10.0)
+        for bad in (gdn.GdnPlanCosts(0.0, 1.0, 0.5, 1.0), gdn.GdnPlanCosts(1.0, -1.0, 0.5, 1.0),
+                    gdn.GdnPlanCosts(float("nan"), 1.0, 0.5, 1.0), gdn.GdnPlanCosts(1.0, 1.0, -0.1, 1.0)):
+            with pytest.raises(gdn.GdnError):
+                gdn.gdn_set_plan_costs(bad)
+        assert gdn.gdn_get_plan_costs().chunk_step_us == 2.0
+        gdn.gdn_set_plan_costs(None)                     # the library's built-in table
+        d = gdn.gdn_get_plan_costs()
+        assert d.chunk_step_us > 0 and d.state_step_us > 0 and d.scan_step_us >= 0
+    finally:
+        gdn.gdn_set_plan_costs(orig)
+
+
+def test_auto_cp_boundary_is_a_curve(lib):
+    """The talk's enabling-condition paragraph: in the plane of (sequence, head)
+    units and sequence length, the region where auto CP pays is bounded by a
+    curve, not by a threshold on either axis.  The planner's boundary: more
+    units leave fewer idle SMs, so the least length that splits grows with the
+    unit count and no length does once the units fill the SMs; and the plan
+    query agrees with the boundary on both sides of it."""
+    sms = 152
+    mins = {u: gdn.gdn_auto_cp_min_chunks(u, sms) for u in (1, 2, 4, 8, 16, 24, 32, 48, 64, 96, 128, 151, 152, 300)}
+    assert mins[152] == 0 and mins[300] == 0
+    on = [u for u, m in sorted(mins.items()) if m > 0]
+    assert on and on[0] == 1
+    assert all(mins[a] <= mins[b] for a, b in zip(on, on[1:])), mins
+    assert mins[on[-1]] > mins[1]                        # the curve rises before it ends
+    for u in (1, 8, 32):
+        nc = mins[u]
+        H = 8 if u % 8 == 0 else u
+        B = u // H
+        p_on = gdn.gdn_plan_query(B, 64 * nc, H, 128, 128, B, 0, gdn.BF16, gdn.default_options(sm_count=sms))
+        p_off = gdn.gdn_plan_query(B, 64 * (nc - 1), H, 128, 128, B, 0, gdn.BF16,
+                                   gdn.default_options(sm_count=sms))
+        assert p_on.cp_enabled == 1 and p_off.cp_enabled == 0, (u, nc)
+    # a dearer scan (lambda2) pushes the boundary to longer sequences
+    orig = gdn.gdn_get_plan_costs()
+    try:
+        gdn.gdn_set_plan_costs(gdn.GdnPlanCosts(orig.chunk_step_us, orig.state_step_us, 20 * orig.scan_step_us + 5,
+                                                orig.pass_us))
+        assert gdn.gdn_auto_cp_min_chunks(8, sms) > mins[8]
+    finally:
+        gdn.gdn_set_plan_costs(orig)
