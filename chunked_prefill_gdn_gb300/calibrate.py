@@ -72,6 +72,8 @@ def _num_items(inp, ws, opts):
 
 def measure(device="cuda", reps=5, verbose=False):
     dev = torch.device(device)
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     torch.cuda.set_device(dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)

@@ -4,6 +4,8 @@ against a sweep of forced segment counts on the two workloads that split
 heads).  The talk's auto-CP paragraph derives the segment length from a cost
 model with lambdas measured on the hardware; the bar here is that the plan it
 picks runs within 5% of the best segment count in the sweep."""
+import json
+import os
 import statistics
 
 import pytest
@@ -58,6 +60,14 @@ def test_auto_plan_within_5pct_of_the_best_swept(idx):
         L = -(-nc // ns)
         results[ns] = timed_ms(inp, gdn.default_options(cp_mode=gdn.CP_FORCE, chunks_per_segment=L), flush)
     best_ns = min(results, key=results.get)
+    path = os.environ.get("GDN_PLANNER_SWEEP")
+    if path:
+        c = gdn.gdn_get_plan_costs()
+        with open(path, "a") as f:
+            f.write(json.dumps({"workload": idx, "name": cfg.name, "auto_segments": ns_auto,
+                                "auto_chunks_per_segment": info.chunks_per_segment, "auto_ms": t_auto,
+                                "sweep_ms": {str(k): v for k, v in results.items()}, "best_segments": best_ns,
+                                "costs_us": [c.chunk_step_us, c.state_step_us, c.scan_step_us, c.pass_us]}) + "\n")
     assert t_auto <= 1.05 * results[best_ns], (
         "auto plan (%d segments of %d chunks) %.3f ms; best swept %d segments %.3f ms; sweep %s" % (
             ns_auto, info.chunks_per_segment, t_auto, best_ns, results[best_ns],
