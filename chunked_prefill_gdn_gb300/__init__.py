@@ -27,6 +27,8 @@ from . import build as _build
 __all__ = [
     "GdnOptions", "GdnPlanInfo", "GdnPlanCosts", "GdnWorkspaceLayout", "WORK_ITEM_DTYPE",
     "gdn_set_plan_costs", "gdn_get_plan_costs", "gdn_auto_cp_min_chunks",
+    "gdn_chunk_transition_workspace_size", "gdn_chunk_transition", "gdn_state_scan", "chunk_transition",
+    "state_scan",
     "load_library", "library_path", "default_options",
     "gdn_default_options", "gdn_plan_query", "gdn_chunk_fwd_workspace_size", "gdn_workspace_query",
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
@@ -137,6 +139,12 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_chunk_bwd.restype = i32
     lib.gdn_chunk_bwd_check.argtypes = [vp, vp]
     lib.gdn_chunk_bwd_check.restype = i32
+    lib.gdn_chunk_transition_workspace_size.argtypes = [i32] * 8
+    lib.gdn_chunk_transition_workspace_size.restype = sz
+    lib.gdn_chunk_transition.argtypes = [vp, vp, vp, vp, vp, i32] + [i32] * 6 + [vp, vp, vp, sz, vp]
+    lib.gdn_chunk_transition.restype = i32
+    lib.gdn_state_scan.argtypes = [vp, vp, vp] + [i32] * 5 + [vp, vp]
+    lib.gdn_state_scan.restype = i32
     lib.gdn_set_plan_costs.argtypes = [ctypes.POINTER(GdnPlanCosts)]
     lib.gdn_set_plan_costs.restype = i32
     lib.gdn_get_plan_costs.argtypes = [ctypes.POINTER(GdnPlanCosts)]
@@ -251,6 +259,18 @@ def gdn_chunk_bwd(*args) -> int:
 
 def gdn_chunk_bwd_check(workspace_ptr, stream_ptr) -> int:
     return int(load_library().gdn_chunk_bwd_check(workspace_ptr, stream_ptr))
+
+
+def gdn_chunk_transition_workspace_size(B, T, H, dk, dv, n_seqs, varlen, dtype) -> int:
+    return int(load_library().gdn_chunk_transition_workspace_size(B, T, H, dk, dv, n_seqs, int(varlen), dtype))
+
+
+def gdn_chunk_transition(*args) -> int:
+    return int(load_library().gdn_chunk_transition(*args))
+
+
+def gdn_state_scan(*args) -> int:
+    return int(load_library().gdn_state_scan(*args))
 
 
 def gdn_set_plan_costs(costs: Optional[GdnPlanCosts]) -> None:
@@ -401,6 +421,62 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
             if st != 0:
                 raise GdnError(st, "device check")
     return out, final_state
+
+
+def chunk_transition(k, v, g, beta, cu_seqlens=None, workspace=None, stream: Optional[torch.cuda.Stream] = None,
+                     check: bool = False):
+    """The affine map of each (sequence, head) of this slice on the state,
+    S_end = S_start M + S*, through gdn_chunk_transition; returns fp32
+    (s_star [N, H, dk, dv], m [N, H, dk, dk]) in the library's state layout."""
+    B, T, H, dk, dv, N = _check_shapes(k, k, v, g, beta, None, cu_seqlens)
+    dt = _dtype_code(k)
+    f32 = torch.float32
+    _check_dtypes(dict(v=v, g=g, beta=beta, cu_seqlens=cu_seqlens, workspace=workspace),
+                  dict(v=k.dtype, g=f32, beta=f32, cu_seqlens=torch.int32, workspace=torch.uint8))
+    _check_placement("cuda", None, dict(k=k))
+    _check_placement("cuda", k.device, dict(v=v, g=g, beta=beta, cu_seqlens=cu_seqlens, workspace=workspace))
+    with torch.cuda.device(k.device):
+        s_star = torch.empty(N, H, dk, dv, dtype=f32, device=k.device)
+        m = torch.empty(N, H, dk, dk, dtype=f32, device=k.device)
+        if workspace is None:
+            n = gdn_chunk_transition_workspace_size(B, T, H, dk, dv, N, cu_seqlens is not None, dt)
+            if n == 0:
+                raise GdnError(1, "gdn_chunk_transition_workspace_size")
+            workspace = torch.empty(n, dtype=torch.uint8, device=k.device)
+        stream = stream if stream is not None else torch.cuda.current_stream(k.device)
+        st = gdn_chunk_transition(_ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, B, T, H, dk, dv, dt,
+                                  _ptr(s_star), _ptr(m), _ptr(workspace), workspace.numel(),
+                                  ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise GdnError(st, "gdn_chunk_transition")
+        if check:
+            st = gdn_chunk_fwd_check(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream))
+            if st != 0:
+                raise GdnError(st, "device check")
+    return s_star, m
+
+
+def state_scan(s_star, m, s0=None, stream: Optional[torch.cuda.Stream] = None):
+    """Start states of R consecutive slices from their maps (s_star
+    [R, N, H, dk, dv], m [R, N, H, dk, dk], rank-major) through gdn_state_scan:
+    out[0] = s0 (or zero), out[r + 1] = out[r] M_r + S*_r."""
+    if s_star.dim() != 5 or m.dim() != 5:
+        raise ValueError("s_star must be [R, N, H, dk, dv] and m [R, N, H, dk, dk]")
+    R, N, H, dk, dv = s_star.shape
+    _expect("m", m, (R, N, H, dk, dk))
+    _expect("s0", s0, (N, H, dk, dv))
+    f32 = torch.float32
+    _check_dtypes(dict(s_star=s_star, m=m, s0=s0), dict(s_star=f32, m=f32, s0=f32))
+    _check_placement("cuda", None, dict(s_star=s_star))
+    _check_placement("cuda", s_star.device, dict(m=m, s0=s0))
+    with torch.cuda.device(s_star.device):
+        out = torch.empty_like(s_star)
+        stream = stream if stream is not None else torch.cuda.current_stream(s_star.device)
+        st = gdn_state_scan(_ptr(s0), _ptr(s_star), _ptr(m), R, N, H, dk, dv, _ptr(out),
+                            ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise GdnError(st, "gdn_state_scan")
+    return out
 
 
 def qk_l2norm(q=None, k=None, q_out=None, k_out=None, eps: float = 0.0,

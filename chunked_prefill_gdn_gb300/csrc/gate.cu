@@ -263,6 +263,32 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Prob
     }
     if (tid < 4) s_base[tid] = 0;
     const int units = N * H;
+    if (pp.transition) {
+        // the affine map of every (sequence, head) over its whole sequence:
+        // S* (values, from zero) and M (no values, from the identity), written
+        // to slot n H + h of the caller's outputs; sequences longest first
+        __syncthreads();
+        for (int u = tid; u < units; u += blockDim.x) {
+            const int seq = w.seq_order[u / H], h = u % H;
+            gdn_work_item it;
+            it.seq = seq;
+            it.head = h;
+            it.c_begin = it.c_start = 0;
+            it.c_end = w.seqinfo[seq].w;
+            it.slot = seq * H + h;
+            it.pad = 0;
+            it.flags = GDN_ITEM_FROM_ZERO | GDN_ITEM_WRITE_SLOT;
+            w.items1[2 * u] = it;
+            it.flags = GDN_ITEM_FROM_IDENTITY | GDN_ITEM_WRITE_M;
+            w.items1[2 * u + 1] = it;
+        }
+        if (tid == 0) {
+            w.num_items[0] = 0;
+            w.num_items[1] = 2 * units;
+            w.num_items[2] = 0;
+        }
+        return;
+    }
     // 2. segment count of the units that need correction matrices (heads with
     //    alpha identically 1, or every split head without sliding); batched
     //    inputs only, where every sequence has the same chunk count

@@ -386,6 +386,7 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
         pp.state_ratio = c.state_step_us / c.chunk_step_us;
         pp.scan_ratio = c.scan_step_us / c.chunk_step_us;
     }
+    pp.transition = 0;
 
     const int stages = opts.stages ? opts.stages : (GDN_STAGE_PREP | GDN_STAGE_INVERSE | GDN_STAGE_CORRECTION |
                                                     GDN_STAGE_FUSED);
@@ -426,6 +427,137 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
         if (opts.prof_end && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts.prof_end), stream)) != cudaSuccess)
             return cuda_fail("record prof_end", e);
     }
+    return GDN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Inter-card sequence parallelism: the affine map of a slice, and the scan of
+// start states over the ranks' maps.
+
+namespace {
+
+// The forward pass's layout (no CP) plus a correction-item list of two items
+// per (sequence, head); the maps go straight to the caller's outputs.
+gdn_status transition_plan(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, int dtype, HostPlan *hp) {
+    gdn_options o;
+    default_options(&o);
+    o.cp_mode = GDN_CP_OFF;
+    gdn_status st = make_plan(B, T, H, dk, dv, n_seqs, varlen, dtype, &o, device_sm_count(), hp);
+    if (st != GDN_OK) return st;
+    Layout &L = hp->lay;
+    const long long pairs = 2LL * hp->N * H;
+    if (pairs >= (1LL << 30)) return GDN_ERR_UNSUPPORTED;
+    L.items1 = align_up(L.total, 256);
+    L.max_items1 = (int)pairs;
+    L.total = align_up(L.items1 + (size_t)pairs * sizeof(gdn_work_item), 256);
+    return GDN_OK;
+}
+
+}  // namespace
+
+size_t gdn_chunk_transition_workspace_size(int B, int T, int H, int dk, int dv, int n_seqs, int varlen,
+                                           gdn_dtype dtype) {
+    HostPlan hp;
+    if (transition_plan(B, T, H, dk, dv, n_seqs, varlen, dtype, &hp) != GDN_OK) return 0;
+    return hp.lay.total;
+}
+
+gdn_status gdn_chunk_transition(const void *k, const void *v, const float *g, const float *beta,
+                                const int32_t *cu_seqlens, int n_seqs, int B, int T, int H, int dk, int dv,
+                                gdn_dtype dtype, float *s_star, float *m, void *workspace, size_t workspace_bytes,
+                                gdn_stream_t stream_in) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_in);
+    const int varlen = cu_seqlens != nullptr;
+    HostPlan hp;
+    gdn_status st = transition_plan(B, T, H, dk, dv, n_seqs, varlen, dtype, &hp);
+    if (st != GDN_OK) return st;
+    if (!workspace || !s_star || !m) return GDN_ERR_INVALID_ARG;
+    if (hp.total_T > 0 && (!k || !v || !g || !beta)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {k, v, g, beta, s_star, m, workspace};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    if (workspace_bytes < hp.lay.total) return GDN_ERR_WORKSPACE;
+
+    Problem p;
+    memset(&p, 0, sizeof(p));
+    p.q = k;   // the correction items read no queries; any tile of the right shape will do
+    p.k = k; p.v = v; p.g = g; p.beta = beta; p.s0 = nullptr; p.cu = cu_seqlens;
+    p.o = nullptr; p.sf = nullptr;
+    p.B = B; p.T = T; p.H = H; p.dk = dk; p.dv = dv; p.N = hp.N; p.total_T = (int)hp.total_T;
+    p.varlen = varlen; p.dtype = dtype;
+    p.scale = 1.0f / sqrtf((float)dk);
+    p.timeout_probe = 0;
+
+    char *base = static_cast<char *>(workspace);
+    const Layout &L = hp.lay;
+    Workspace w;
+    memset(&w, 0, sizeof(w));
+    w.err = reinterpret_cast<int *>(base + L.err);
+    w.counters = reinterpret_cast<int *>(base + L.counters);
+    w.num_chunks = reinterpret_cast<int *>(base + L.num_chunks);
+    w.num_items = reinterpret_cast<int *>(base + L.num_items);
+    w.seqinfo = reinterpret_cast<int4 *>(base + L.seqinfo);
+    w.chunks = reinterpret_cast<int4 *>(base + L.chunks);
+    w.flags = reinterpret_cast<int *>(base + L.flags);
+    w.G = reinterpret_cast<float *>(base + L.G);
+    w.totals = reinterpret_cast<float *>(base + L.totals);
+    w.tprime = base + L.tprime;
+    w.items2 = reinterpret_cast<gdn_work_item *>(base + L.items2);
+    w.items1 = reinterpret_cast<gdn_work_item *>(base + L.items1);
+    w.scan_units = reinterpret_cast<int4 *>(base + L.scan_units);
+    w.seq_order = reinterpret_cast<int *>(base + L.seq_order);
+    w.cp_s = s_star;   // slot n H + h of the correction pass is unit (n, h) of the outputs
+    w.cp_m = m;
+    w.max_chunks = L.max_chunks;
+    w.max_items = L.max_items;
+    w.max_items1 = L.max_items1;
+    w.max_cp_slots = hp.N * H;
+
+    PlanParams pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.L = hp.L;
+    pp.cp_enabled = 0;
+    pp.sliding = 0;
+    pp.ln_eps = logf(5.9604645e-08f);
+    pp.grid = hp.grid;
+    pp.state_ratio = 1.f;
+    pp.scan_ratio = 1.f;
+    pp.transition = 1;
+
+    cudaGetLastError();
+    cudaError_t e = launch_seqprep(p, w, stream);
+    if (e != cudaSuccess) return cuda_fail("launch seqprep", e);
+    if (L.max_chunks > 0 && (e = launch_gate(p, w, stream)) != cudaSuccess) return cuda_fail("launch gate", e);
+    if ((e = launch_plan(p, w, pp, stream)) != cudaSuccess) return cuda_fail("launch plan", e);
+    const bool tc = hp.kernel == GDN_KERNEL_TC;
+    if (L.max_chunks > 0 && (e = launch_inverse(p, w, tc, stream)) != cudaSuccess)
+        return cuda_fail("launch inverse", e);
+    e = tc ? launch_fused_tc(p, w, 1, hp.grid, stream) : launch_fused_simt(p, w, 1, hp.grid, stream);
+    if (e != cudaSuccess) return cuda_fail(tc ? "launch fused_tc (transition)" : "launch fused_simt (transition)", e);
+    return GDN_OK;
+}
+
+gdn_status gdn_state_scan(const float *s0, const float *s_star, const float *m, int R, int N, int H, int dk, int dv,
+                          float *s_start, gdn_stream_t stream) {
+    if (R < 1 || N < 0 || H < 1 || (long long)N * H >= (1LL << 30)) return GDN_ERR_INVALID_ARG;
+    if (!valid_head_dim(dk) || !valid_head_dim(dv)) return GDN_ERR_UNSUPPORTED;
+    if (!s_start || (R > 1 && (!s_star || !m))) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {s0, s_star, m, s_start};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    // the output must not overlap an input (the walk reads the maps while it writes)
+    const size_t out_bytes = (size_t)R * N * H * dk * dv * 4;
+    auto overlaps = [&](const void *a, size_t bytes) {
+        if (!a) return false;
+        const char *x = static_cast<const char *>(a), *y = reinterpret_cast<const char *>(s_start);
+        return x < y + out_bytes && y < x + bytes;
+    };
+    if (overlaps(s0, (size_t)N * H * dk * dv * 4) || overlaps(s_star, out_bytes) ||
+        overlaps(m, (size_t)R * N * H * dk * dk * 4))
+        return GDN_ERR_INVALID_ARG;
+    cudaGetLastError();
+    cudaError_t e = launch_rank_scan(s0, s_star, m, R, N, H, dk, dv, s_start, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("launch rank scan", e);
     return GDN_OK;
 }
 

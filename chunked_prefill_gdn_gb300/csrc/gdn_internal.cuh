@@ -54,6 +54,9 @@ struct PlanParams {
     int grid;         // CTAs of the persistent fused passes
     float state_ratio;  // measured: a state-only chunk step / an output chunk step
     float scan_ratio;   // measured: a scan step / an output chunk step
+    int transition;     // 1: list, per (sequence, head), the two whole-sequence
+                        // items of its affine map (S* from zero, M from the
+                        // identity) for the correction pass, and nothing else
 };
 
 // Host-side layout of the workspace for one problem.
@@ -76,6 +79,9 @@ cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &
 // (the gate-scaled form that kernel multiplies by) instead of T' itself
 cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s);
 cudaError_t launch_scan(const Problem &p, const Workspace &w, cudaStream_t s);
+// start states of R consecutive slices: out[0] = s0 (or 0), out[r+1] = out[r] M_r + S*_r
+cudaError_t launch_rank_scan(const float *s0, const float *s_star, const float *m, int R, int N, int H, int dk,
+                             int dv, float *out, cudaStream_t s);
 // q and k rows ([rows][dk] each, either may be NULL) scaled to unit L2 norm
 // into qo / ko (which may alias q / k)
 constexpr float kQkNormEps = 1e-6f;

@@ -151,7 +151,84 @@ cudaError_t launch_scan_dk(const Problem &p, const Workspace &w, cudaStream_t s)
     return cudaGetLastError();
 }
 
+// Start states of R consecutive slices (inter-card sequence parallelism): the
+// same step as above, X_start(r+1) = X_M(r) X_start(r) + X*(r), over maps laid
+// out rank-major ([R][N][H][...]), as an all-gather delivers them.  One CTA
+// per (unit, kScanCols value rows) walks the ranks in order; X_M(r) is staged
+// in shared memory by plain 16-byte loads (R is the rank count: a handful of
+// steps, so no copy pipeline).
+template <int DK>
+__global__ void __launch_bounds__(kScanThreads) rank_scan_kernel(const float *__restrict__ s0,
+                                                                 const float *__restrict__ s_star,
+                                                                 const float *__restrict__ m, int R, int units,
+                                                                 int dv, float *__restrict__ out) {
+    extern __shared__ __align__(16) float rs_smem[];
+    float *XM = rs_smem;                   // [DK][DK]
+    float *X = rs_smem + DK * DK;          // [DK][kScanCols]
+    constexpr int kRows = DK * kScanCols / kScanThreads;
+    const int u = blockIdx.x, i0 = blockIdx.y * kScanCols;
+    if (u >= units || i0 >= dv) return;
+    const int tid = threadIdx.x;
+    const int ii = tid % kScanCols, jr0 = tid / kScanCols;
+    const size_t sstride = (size_t)units * DK * dv, mstride = (size_t)units * DK * DK;
+    const size_t ubase = (size_t)u * DK * dv;
+    for (int idx = tid; idx < DK * kScanCols; idx += kScanThreads) {
+        const int jr = idx / kScanCols, c = idx % kScanCols;
+        const float x = (s0 && i0 + c < dv) ? s0[ubase + (size_t)jr * dv + i0 + c] : 0.f;
+        X[idx] = x;
+        if (i0 + c < dv) out[ubase + (size_t)jr * dv + i0 + c] = x;
+    }
+    for (int r = 0; r + 1 < R; ++r) {
+        const float4 *src = reinterpret_cast<const float4 *>(m + r * mstride + (size_t)u * DK * DK);
+        for (int idx = tid; idx < DK * DK / 4; idx += kScanThreads) reinterpret_cast<float4 *>(XM)[idx] = src[idx];
+        __syncthreads();
+        float acc[kRows];
+        const float *xs = s_star + r * sstride + ubase;
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+            const int jr = jr0 + q * (kScanThreads / kScanCols);
+            acc[q] = i0 + ii < dv ? xs[(size_t)jr * dv + i0 + ii] : 0.f;
+        }
+#pragma unroll 4
+        for (int mm = 0; mm < DK; ++mm) {
+            const float xv = X[mm * kScanCols + ii];
+#pragma unroll
+            for (int q = 0; q < kRows; ++q) acc[q] = fmaf(XM[(jr0 + q * (kScanThreads / kScanCols)) * DK + mm], xv, acc[q]);
+        }
+        __syncthreads();                   // every read of X and XM is done
+        float *o = out + (r + 1) * sstride + ubase;
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+            const int jr = jr0 + q * (kScanThreads / kScanCols);
+            X[jr * kScanCols + ii] = acc[q];
+            if (i0 + ii < dv) o[(size_t)jr * dv + i0 + ii] = acc[q];
+        }
+        __syncthreads();
+    }
+}
+
+template <int DK>
+cudaError_t launch_rank_scan_dk(const float *s0, const float *s_star, const float *m, int R, int units, int dv,
+                                float *out, cudaStream_t s) {
+    const size_t smem = ((size_t)DK * DK + (size_t)DK * kScanCols) * 4;
+    cudaError_t e =
+        cudaFuncSetAttribute(rank_scan_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(units, (dv + kScanCols - 1) / kScanCols);
+    rank_scan_kernel<DK><<<grid, kScanThreads, smem, s>>>(s0, s_star, m, R, units, dv, out);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_rank_scan(const float *s0, const float *s_star, const float *m, int R, int N, int H, int dk,
+                             int dv, float *out, cudaStream_t s) {
+    const int units = N * H;
+    if (units == 0 || R == 0) return cudaSuccess;
+    if (dk == 32) return launch_rank_scan_dk<32>(s0, s_star, m, R, units, dv, out, s);
+    if (dk == 64) return launch_rank_scan_dk<64>(s0, s_star, m, R, units, dv, out, s);
+    return launch_rank_scan_dk<128>(s0, s_star, m, R, units, dv, out, s);
+}
 
 cudaError_t launch_scan(const Problem &p, const Workspace &w, cudaStream_t s) {
     if (w.max_cp_slots <= 0) return cudaSuccess;

@@ -289,6 +289,52 @@ gdn_status gdn_chunk_fwd_host(const void *q, const void *k, const void *v,
                               const gdn_options *opts, gdn_stream_t stream);
 
 /*
+ * Inter-card sequence parallelism (the talk's difference and compute-for-memory
+ * paragraphs, and its timeline paragraph's "inter-card sequence parallelism":
+ * the three steps of intra-card CP with the segments on different GPUs).  A
+ * batch of sequences is split along time into R slices, one per rank; every
+ * rank holds the same (sequence, head) units.  Step one, on every rank:
+ *
+ *   gdn_chunk_transition: for each (sequence, head) of the local slice, the
+ *   affine map the slice applies to the state, S_end = S_start M + S*:
+ *   S* is the slice's end state from S_start = 0 with the slice's values, and
+ *   M (dk x dk) the end state from S_start = I with zero values, i.e. the
+ *   product of the slice's token transitions alpha_t (I - beta_t k_t k_t^T).
+ *
+ * q is not read (the map does not depend on the queries).  k, v, g, beta,
+ * cu_seqlens, B, T, H, dk, dv, dtype as for gdn_chunk_fwd.  Outputs (device,
+ * fp32, 16-byte aligned): s_star [N, H, dk, dv] in the state layout of
+ * final_state, m [N, H, dk, dk] in the same transposed layout
+ * (m[n][h][b][a] = M[a][b]).  An empty sequence maps to S* = 0, M = I.  The
+ * workspace holds gdn_chunk_transition_workspace_size() bytes.  Nothing syncs;
+ * device-side errors (bad cu_seqlens, timeout) land in the workspace's error
+ * word: read them with gdn_chunk_fwd_check(workspace, stream).
+ *
+ * Step two is an all-gather of (S*, M) over the ranks (the caller's
+ * collective), step three gdn_state_scan below, step four gdn_chunk_fwd on the
+ * local slice from the rank's start state.
+ */
+size_t gdn_chunk_transition_workspace_size(int B, int T, int H, int dk, int dv, int n_seqs, int varlen,
+                                           gdn_dtype dtype);
+gdn_status gdn_chunk_transition(const void *k, const void *v, const float *g, const float *beta,
+                                const int32_t *cu_seqlens, int n_seqs,
+                                int B, int T, int H, int dk, int dv, gdn_dtype dtype,
+                                float *s_star, float *m,
+                                void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/*
+ * Start states of R consecutive slices of the same sequences from their maps:
+ * s_start[0] = s0 (NULL: zero) and s_start[r + 1] = s_start[r] M_r + S*_r.
+ * s_star [R, N, H, dk, dv], m [R, N, H, dk, dk] as gdn_chunk_transition writes
+ * them (rank-major, e.g. the result of an all-gather), s0 [N, H, dk, dv] or
+ * NULL, s_start [R, N, H, dk, dv]; device fp32, 16-byte aligned; s_start must
+ * not overlap the inputs.  The last map (r = R - 1) is not used.  fp32
+ * arithmetic, one CUDA kernel, nothing syncs.
+ */
+gdn_status gdn_state_scan(const float *s0, const float *s_star, const float *m, int R, int N, int H, int dk,
+                          int dv, float *s_start, gdn_stream_t stream);
+
+/*
  * The same forward pass for callers that cannot allocate device memory while
  * they run: a server that hands all of HBM to its own pool at start-up and
  * forbids allocation on the request path, or a plugin that receives tensors

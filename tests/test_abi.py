@@ -347,3 +347,36 @@ def test_auto_cp_boundary_is_a_curve(lib):
         assert gdn.gdn_auto_cp_min_chunks(8, sms) > mins[8]
     finally:
         gdn.gdn_set_plan_costs(orig)
+
+
+def test_transition_and_scan_argument_errors_before_launch(lib):
+    """gdn_chunk_transition and gdn_state_scan reject bad sizes, NULL or
+    misaligned pointers, a short workspace and an output that overlaps an
+    input on the host; none of these calls reaches the GPU."""
+    fake = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    ws = gdn.gdn_chunk_transition_workspace_size(1, 256, 2, 32, 32, 1, 0, gdn.F32)
+    assert ws > 0
+    assert gdn.gdn_chunk_transition_workspace_size(1, 256, 2, 48, 32, 1, 0, gdn.F32) == 0
+
+    def tr(k=fake, s=fake, m=fake, wsp=fake, wsb=ws, dk=32):
+        return gdn.gdn_chunk_transition(k, fake, fake, fake, None, 1, 1, 256, 2, dk, 32, gdn.F32, s, m, wsp, wsb,
+                                        None)
+    assert tr(k=None) == 1
+    assert tr(k=mis) == 1
+    assert tr(s=None) == 1
+    assert tr(m=mis) == 1
+    assert tr(wsp=None) == 1
+    assert tr(wsb=ws - 1) == 3
+    assert tr(dk=48) == 2
+    sc = gdn.gdn_state_scan
+    base = 1 << 24
+    p = lambda off: ctypes.c_void_p(base + off)
+    n = 3 * 1 * 2 * 32 * 32 * 4                    # bytes of the s_star / s_start stacks (R=3, N=1, H=2, d=32)
+    assert sc(None, p(0), p(n), 0, 1, 2, 32, 32, p(2 * n), None) == 1           # R
+    assert sc(None, p(0), p(n), 3, 1, 2, 48, 32, p(2 * n), None) == 2           # dk
+    assert sc(None, None, p(n), 3, 1, 2, 32, 32, p(2 * n), None) == 1           # s_star NULL
+    assert sc(None, p(0), p(n), 3, 1, 2, 32, 32, None, None) == 1               # out NULL
+    assert sc(None, p(4), p(n), 3, 1, 2, 32, 32, p(2 * n), None) == 1           # misaligned
+    assert sc(None, p(0), p(n), 3, 1, 2, 32, 32, p(n // 2), None) == 1          # out overlaps s_star
+    assert sc(p(2 * n + 64), p(0), p(n), 3, 1, 2, 32, 32, p(2 * n), None) == 1  # out overlaps s0
