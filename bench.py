@@ -458,27 +458,23 @@ def backward_flops(dk, dv, chunks, H):
 
 
 def backward_measure(gdn, torch, inp, cfg, flush, stream, iters=3):
-    """The backward pass (gdn_chunk_bwd) on this workload with seeded upstream
-    gradients: CUDA events around each launch sequence (the main kernel and the
-    slice reduction), L2 flushed before each.  Reported against the FP32
-    CUDA-core peak (all but its two Gram products run on CUDA cores)."""
+    """The backward pass (chunk_bwd: gdn_chunk_bwd, with the automatic
+    sequence-parallel plan) on this workload with seeded upstream gradients:
+    CUDA events around each call, L2 flushed before each.  Reported against the
+    FP32 CUDA-core peak (all but its two Gram products run on CUDA cores)."""
     from chunked_prefill_gdn_gb300.inputs import make_grad_inputs
     grads = make_grad_inputs(cfg, inp["q"].device)
     do, dsf = grads["do"], grads["d_final_state"]
     q = inp["q"]
     B, T, H, dk = q.shape
     dv = inp["v"].shape[-1]
-    dt = gdn.BF16 if q.dtype == torch.bfloat16 else gdn.F32
-    ws = torch.empty(gdn.gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, cfg.num_seqs, inp["cu_seqlens"] is not None,
-                                                      dt), dtype=torch.uint8, device=q.device)
+    from chunked_prefill_gdn_gb300.seqpar import backward_segments
+    segments = backward_segments(q, inp["v"]) if inp["cu_seqlens"] is None else 1
 
-    def run():
+    def run(check=False):
         return gdn.chunk_bwd(q, inp["k"], inp["v"], inp["g"], inp["beta"], do, inp["initial_state"],
-                             inp["cu_seqlens"], inp["scale"], dsf, workspace=ws, stream=stream)
-    run()
-    st = gdn.gdn_chunk_bwd_check(ctypes_ptr(ws), ctypes_ptr_stream(stream))
-    if st != 0:
-        raise SystemExit("backward device check failed: %s" % gdn.gdn_status_string(st))
+                             inp["cu_seqlens"], inp["scale"], dsf, stream=stream, check=check)
+    run(check=True)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
     for i, (a, b) in enumerate(evs):
         flush.fill_((i + 11) & 0xFF)
@@ -495,13 +491,16 @@ def backward_measure(gdn, torch, inp, cfg, flush, stream, iters=3):
     flops = backward_flops(dk, dv, chunks, H)
     achieved = flops / (ms * 1e-3) / 1e12
     slices = dv // 32
-    return {"kernel": "bwd_kernel + bwd_reduce_kernel (gdn_chunk_bwd)", "ms": ms,
+    return {"kernel": "bwd_kernel + bwd_reduce_kernel (gdn_chunk_bwd)", "ms": ms, "segments": segments,
             "tokens_per_s": cfg.total_tokens / (ms * 1e-3), "bound": "alu", "achieved": achieved,
             "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": achieved / FP32_ALU_TFLOPS,
-            "alg_flops": flops, "launches": iters * (1 + (4 if slices > 1 else 0)),
+            "alg_flops": flops,
+            "launches": iters * ((1 + (4 if slices > 1 else 0)) * (1 if segments == 1 else 2) + (0 if segments == 1 else 7)),
             "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
             "note": "Gram products on tcgen05 (bf16, d=128), the other products fp32 on CUDA cores; one CTA per "
-                    "(32 value columns, head, sequence); not inside the timed step"}
+                    "(32 value columns, head, sequence or segment); with segments > 1 each sequence is cut into "
+                    "that many segments (forward maps and scan, a local backward, the reverse gradient scan, the "
+                    "backward per segment: two backward passes); not inside the timed step"}
 
 
 def e2e_measure(gdn, torch, inp, cfg, opts, dev, args):

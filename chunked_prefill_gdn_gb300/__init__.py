@@ -28,7 +28,7 @@ __all__ = [
     "GdnOptions", "GdnPlanInfo", "GdnPlanCosts", "GdnWorkspaceLayout", "WORK_ITEM_DTYPE",
     "gdn_set_plan_costs", "gdn_get_plan_costs", "gdn_auto_cp_min_chunks",
     "gdn_chunk_transition_workspace_size", "gdn_chunk_transition", "gdn_state_scan", "chunk_transition",
-    "state_scan",
+    "state_scan", "gdn_state_grad_scan", "state_grad_scan",
     "load_library", "library_path", "default_options",
     "gdn_default_options", "gdn_plan_query", "gdn_chunk_fwd_workspace_size", "gdn_workspace_query",
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
@@ -145,6 +145,8 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_chunk_transition.restype = i32
     lib.gdn_state_scan.argtypes = [vp, vp, vp] + [i32] * 5 + [vp, vp]
     lib.gdn_state_scan.restype = i32
+    lib.gdn_state_grad_scan.argtypes = [vp, vp, vp] + [i32] * 5 + [vp, vp]
+    lib.gdn_state_grad_scan.restype = i32
     lib.gdn_set_plan_costs.argtypes = [ctypes.POINTER(GdnPlanCosts)]
     lib.gdn_set_plan_costs.restype = i32
     lib.gdn_get_plan_costs.argtypes = [ctypes.POINTER(GdnPlanCosts)]
@@ -271,6 +273,10 @@ def gdn_chunk_transition(*args) -> int:
 
 def gdn_state_scan(*args) -> int:
     return int(load_library().gdn_state_scan(*args))
+
+
+def gdn_state_grad_scan(*args) -> int:
+    return int(load_library().gdn_state_grad_scan(*args))
 
 
 def gdn_set_plan_costs(costs: Optional[GdnPlanCosts]) -> None:
@@ -479,6 +485,30 @@ def state_scan(s_star, m, s0=None, stream: Optional[torch.cuda.Stream] = None):
     return out
 
 
+def state_grad_scan(ds_star, m, ds_last=None, stream: Optional[torch.cuda.Stream] = None):
+    """End-state gradients of R consecutive slices from each slice's own
+    start-state gradient (ds_star [R, N, H, dk, dv]) and map (m [R, N, H, dk,
+    dk]) through gdn_state_grad_scan: out[R - 1] = ds_last (or zero),
+    out[r] = out[r + 1] M_{r+1}^T + ds_star[r + 1]."""
+    if ds_star.dim() != 5 or m.dim() != 5:
+        raise ValueError("ds_star must be [R, N, H, dk, dv] and m [R, N, H, dk, dk]")
+    R, N, H, dk, dv = ds_star.shape
+    _expect("m", m, (R, N, H, dk, dk))
+    _expect("ds_last", ds_last, (N, H, dk, dv))
+    f32 = torch.float32
+    _check_dtypes(dict(ds_star=ds_star, m=m, ds_last=ds_last), dict(ds_star=f32, m=f32, ds_last=f32))
+    _check_placement("cuda", None, dict(ds_star=ds_star))
+    _check_placement("cuda", ds_star.device, dict(m=m, ds_last=ds_last))
+    with torch.cuda.device(ds_star.device):
+        out = torch.empty_like(ds_star)
+        stream = stream if stream is not None else torch.cuda.current_stream(ds_star.device)
+        st = gdn_state_grad_scan(_ptr(ds_last), _ptr(ds_star), _ptr(m), R, N, H, dk, dv, _ptr(out),
+                                 ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise GdnError(st, "gdn_state_grad_scan")
+    return out
+
+
 def qk_l2norm(q=None, k=None, q_out=None, k_out=None, eps: float = 0.0,
               stream: Optional[torch.cuda.Stream] = None):
     """Unit-L2-norm rows of q and/or k ([..., dk], contiguous CUDA tensors of one
@@ -577,9 +607,18 @@ def chunk_fwd_host(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=
 
 
 def chunk_bwd(q, k, v, g, beta, do, initial_state=None, cu_seqlens=None, scale=None, d_final_state=None,
-              workspace=None, stream: Optional[torch.cuda.Stream] = None, check: bool = False):
+              workspace=None, stream: Optional[torch.cuda.Stream] = None, check: bool = False, segments=None):
     """Gradients of sum <o, do> + <final_state, d_final_state> through
-    gdn_chunk_bwd; returns fp32 (dq, dk, dv, dg, dbeta, d_initial_state)."""
+    gdn_chunk_bwd; returns fp32 (dq, dk, dv, dg, dbeta, d_initial_state).
+    segments: None lets the backward's sequence-parallel plan decide how many
+    segments each sequence is cut into (batched input only; see seqpar), 1
+    runs each (sequence, head) whole, n > 1 forces n segments."""
+    if workspace is None and cu_seqlens is None and segments != 1:
+        from .seqpar import backward_segments, chunk_bwd_segmented
+        ns = segments if segments is not None else backward_segments(q, v)
+        if ns > 1:
+            return chunk_bwd_segmented(q, k, v, g, beta, do, initial_state, scale, d_final_state, ns,
+                                       stream=stream, check=check)
     B, T, H, dk, dv, N = _check_shapes(q, k, v, g, beta, initial_state, cu_seqlens)
     _expect("do", do, (B, T, H, dv))
     _expect("d_final_state", d_final_state, (N, H, dk, dv))

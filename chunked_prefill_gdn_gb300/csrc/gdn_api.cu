@@ -537,8 +537,10 @@ gdn_status gdn_chunk_transition(const void *k, const void *v, const float *g, co
     return GDN_OK;
 }
 
-gdn_status gdn_state_scan(const float *s0, const float *s_star, const float *m, int R, int N, int H, int dk, int dv,
-                          float *s_start, gdn_stream_t stream) {
+namespace {
+
+gdn_status state_scan_any(const float *s0, const float *s_star, const float *m, int R, int N, int H, int dk, int dv,
+                          float *s_start, bool grad, gdn_stream_t stream) {
     if (R < 1 || N < 0 || H < 1 || (long long)N * H >= (1LL << 30)) return GDN_ERR_INVALID_ARG;
     if (!valid_head_dim(dk) || !valid_head_dim(dv)) return GDN_ERR_UNSUPPORTED;
     if (!s_start || (R > 1 && (!s_star || !m))) return GDN_ERR_INVALID_ARG;
@@ -556,9 +558,22 @@ gdn_status gdn_state_scan(const float *s0, const float *s_star, const float *m, 
         overlaps(m, (size_t)R * N * H * dk * dk * 4))
         return GDN_ERR_INVALID_ARG;
     cudaGetLastError();
-    cudaError_t e = launch_rank_scan(s0, s_star, m, R, N, H, dk, dv, s_start, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e =
+        launch_rank_scan(s0, s_star, m, R, N, H, dk, dv, s_start, grad, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail("launch rank scan", e);
     return GDN_OK;
+}
+
+}  // namespace
+
+gdn_status gdn_state_scan(const float *s0, const float *s_star, const float *m, int R, int N, int H, int dk, int dv,
+                          float *s_start, gdn_stream_t stream) {
+    return state_scan_any(s0, s_star, m, R, N, H, dk, dv, s_start, false, stream);
+}
+
+gdn_status gdn_state_grad_scan(const float *ds_last, const float *ds_star, const float *m, int R, int N, int H,
+                               int dk, int dv, float *ds_end, gdn_stream_t stream) {
+    return state_scan_any(ds_last, ds_star, m, R, N, H, dk, dv, ds_end, true, stream);
 }
 
 gdn_status gdn_chunk_fwd_check(const void *workspace, gdn_stream_t stream) {

@@ -79,9 +79,10 @@ cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &
 // (the gate-scaled form that kernel multiplies by) instead of T' itself
 cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s);
 cudaError_t launch_scan(const Problem &p, const Workspace &w, cudaStream_t s);
-// start states of R consecutive slices: out[0] = s0 (or 0), out[r+1] = out[r] M_r + S*_r
+// start states of R consecutive slices: out[0] = s0 (or 0), out[r+1] = out[r] M_r + S*_r;
+// grad: end gradients, out[R-1] = s0 (or 0), out[r] = out[r+1] M_{r+1}^T + S*_{r+1}
 cudaError_t launch_rank_scan(const float *s0, const float *s_star, const float *m, int R, int N, int H, int dk,
-                             int dv, float *out, cudaStream_t s);
+                             int dv, float *out, bool grad, cudaStream_t s);
 // q and k rows ([rows][dk] each, either may be NULL) scaled to unit L2 norm
 // into qo / ko (which may alias q / k)
 constexpr float kQkNormEps = 1e-6f;

@@ -157,7 +157,13 @@ cudaError_t launch_scan_dk(const Problem &p, const Workspace &w, cudaStream_t s)
 // per (unit, kScanCols value rows) walks the ranks in order; X_M(r) is staged
 // in shared memory by plain 16-byte loads (R is the rank count: a handful of
 // steps, so no copy pipeline).
-template <int DK>
+//
+// GRAD: the gradient of the state walks the other way, dS_end(r) =
+// dS_end(r+1) M(r+1)^T + dS*(r+1) (S_end = S_start M + S* gives
+// dL/dS_start = dL/dS_end M^T plus the slice's own term), which in the stored
+// layout reads Y(r) = X_M(r+1)^T Y(r+1) + Y*(r+1): the same walk from the last
+// slice down, with X_M read transposed.
+template <int DK, bool GRAD>
 __global__ void __launch_bounds__(kScanThreads) rank_scan_kernel(const float *__restrict__ s0,
                                                                  const float *__restrict__ s_star,
                                                                  const float *__restrict__ m, int R, int units,
@@ -172,13 +178,16 @@ __global__ void __launch_bounds__(kScanThreads) rank_scan_kernel(const float *__
     const int ii = tid % kScanCols, jr0 = tid / kScanCols;
     const size_t sstride = (size_t)units * DK * dv, mstride = (size_t)units * DK * DK;
     const size_t ubase = (size_t)u * DK * dv;
+    const int first = GRAD ? R - 1 : 0;
     for (int idx = tid; idx < DK * kScanCols; idx += kScanThreads) {
         const int jr = idx / kScanCols, c = idx % kScanCols;
         const float x = (s0 && i0 + c < dv) ? s0[ubase + (size_t)jr * dv + i0 + c] : 0.f;
         X[idx] = x;
-        if (i0 + c < dv) out[ubase + (size_t)jr * dv + i0 + c] = x;
+        if (i0 + c < dv) out[first * sstride + ubase + (size_t)jr * dv + i0 + c] = x;
     }
-    for (int r = 0; r + 1 < R; ++r) {
+    for (int step = 0; step + 1 < R; ++step) {
+        const int r = GRAD ? R - 1 - step : step;     // the map applied in this step
+        const int dst = GRAD ? r - 1 : r + 1;         // the slice whose value it gives
         const float4 *src = reinterpret_cast<const float4 *>(m + r * mstride + (size_t)u * DK * DK);
         for (int idx = tid; idx < DK * DK / 4; idx += kScanThreads) reinterpret_cast<float4 *>(XM)[idx] = src[idx];
         __syncthreads();
@@ -193,10 +202,13 @@ __global__ void __launch_bounds__(kScanThreads) rank_scan_kernel(const float *__
         for (int mm = 0; mm < DK; ++mm) {
             const float xv = X[mm * kScanCols + ii];
 #pragma unroll
-            for (int q = 0; q < kRows; ++q) acc[q] = fmaf(XM[(jr0 + q * (kScanThreads / kScanCols)) * DK + mm], xv, acc[q]);
+            for (int q = 0; q < kRows; ++q) {
+                const int jr = jr0 + q * (kScanThreads / kScanCols);
+                acc[q] = fmaf(GRAD ? XM[mm * DK + jr] : XM[jr * DK + mm], xv, acc[q]);
+            }
         }
         __syncthreads();                   // every read of X and XM is done
-        float *o = out + (r + 1) * sstride + ubase;
+        float *o = out + dst * sstride + ubase;
 #pragma unroll
         for (int q = 0; q < kRows; ++q) {
             const int jr = jr0 + q * (kScanThreads / kScanCols);
@@ -207,27 +219,34 @@ __global__ void __launch_bounds__(kScanThreads) rank_scan_kernel(const float *__
     }
 }
 
-template <int DK>
+template <int DK, bool GRAD>
 cudaError_t launch_rank_scan_dk(const float *s0, const float *s_star, const float *m, int R, int units, int dv,
                                 float *out, cudaStream_t s) {
     const size_t smem = ((size_t)DK * DK + (size_t)DK * kScanCols) * 4;
     cudaError_t e =
-        cudaFuncSetAttribute(rank_scan_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(rank_scan_kernel<DK, GRAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(units, (dv + kScanCols - 1) / kScanCols);
-    rank_scan_kernel<DK><<<grid, kScanThreads, smem, s>>>(s0, s_star, m, R, units, dv, out);
+    rank_scan_kernel<DK, GRAD><<<grid, kScanThreads, smem, s>>>(s0, s_star, m, R, units, dv, out);
     return cudaGetLastError();
+}
+
+template <bool GRAD>
+cudaError_t launch_rank_scan_any(const float *s0, const float *s_star, const float *m, int R, int units, int dk,
+                                 int dv, float *out, cudaStream_t s) {
+    if (dk == 32) return launch_rank_scan_dk<32, GRAD>(s0, s_star, m, R, units, dv, out, s);
+    if (dk == 64) return launch_rank_scan_dk<64, GRAD>(s0, s_star, m, R, units, dv, out, s);
+    return launch_rank_scan_dk<128, GRAD>(s0, s_star, m, R, units, dv, out, s);
 }
 
 }  // namespace
 
 cudaError_t launch_rank_scan(const float *s0, const float *s_star, const float *m, int R, int N, int H, int dk,
-                             int dv, float *out, cudaStream_t s) {
+                             int dv, float *out, bool grad, cudaStream_t s) {
     const int units = N * H;
     if (units == 0 || R == 0) return cudaSuccess;
-    if (dk == 32) return launch_rank_scan_dk<32>(s0, s_star, m, R, units, dv, out, s);
-    if (dk == 64) return launch_rank_scan_dk<64>(s0, s_star, m, R, units, dv, out, s);
-    return launch_rank_scan_dk<128>(s0, s_star, m, R, units, dv, out, s);
+    return grad ? launch_rank_scan_any<true>(s0, s_star, m, R, units, dk, dv, out, s)
+                : launch_rank_scan_any<false>(s0, s_star, m, R, units, dk, dv, out, s);
 }
 
 cudaError_t launch_scan(const Problem &p, const Workspace &w, cudaStream_t s) {

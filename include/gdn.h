@@ -335,6 +335,25 @@ gdn_status gdn_state_scan(const float *s0, const float *s_star, const float *m, 
                           int dv, float *s_start, gdn_stream_t stream);
 
 /*
+ * The same walk for the gradient of the state, from the last slice down
+ * (sequence parallelism in the backward pass: the results paragraph of the
+ * talk has the backward split with the same sliding-window / correction
+ * scheme).  With S_end = S_start M + S* per slice, the gradient of the loss
+ * with respect to a slice's start state is that of its end state times M^T
+ * plus the slice's own term ds_star (its backward run with a zero end
+ * gradient), so
+ *
+ *   ds_end[R - 1] = ds_last (NULL: zero),
+ *   ds_end[r] = ds_end[r + 1] M_{r+1}^T + ds_star[r + 1].
+ *
+ * Layouts, alignment and errors as gdn_state_scan (ds_star in the state
+ * layout, m as gdn_chunk_transition writes it); ds_star[0] and m[0] are not
+ * used.
+ */
+gdn_status gdn_state_grad_scan(const float *ds_last, const float *ds_star, const float *m, int R, int N, int H,
+                               int dk, int dv, float *ds_end, gdn_stream_t stream);
+
+/*
  * The same forward pass for callers that cannot allocate device memory while
  * they run: a server that hands all of HBM to its own pool at start-up and
  * forbids allocation on the request path, or a plugin that receives tensors
