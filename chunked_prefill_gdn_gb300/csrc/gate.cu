@@ -19,9 +19,13 @@ namespace gdn {
 
 // ---------------------------------------------------------------------------
 // Sequence preparation: validate cu_seqlens, build the per-sequence table and
-// the chunk table, zero the counters and head flags.  One CTA.
+// the chunk table, zero the counters and head flags.  One CTA.  With
+// emit_items (equal sequences, no split) it also writes the output pass's work
+// list, one whole-sequence item per (sequence, head), so that no planner
+// launch is needed.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) seqprep_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w) {
+__global__ void __launch_bounds__(1024) seqprep_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w,
+                                                       int emit_items) {
     grid_dependency_wait();
     __shared__ int s_bad;
     __shared__ int s_carry;
@@ -106,6 +110,27 @@ __global__ void __launch_bounds__(1024) seqprep_kernel(const __grid_constant__ P
         int len = min(kChunk, si.x + si.y - t0);
         w.chunks[c] = make_int4(lo, t0, len, ci);
     }
+    if (emit_items) {
+        const int units = N * p.H;
+        for (int u = tid; u < units && u < w.max_items; u += blockDim.x) {
+            gdn_work_item it;
+            it.seq = u / p.H;
+            it.head = u % p.H;
+            it.c_begin = it.c_start = 0;
+            it.c_end = w.seqinfo[it.seq].w;
+            it.flags = GDN_ITEM_OUTPUT | GDN_ITEM_FROM_INITIAL | GDN_ITEM_WRITE_FINAL;
+            it.slot = -1;
+            it.pad = 0;
+            w.items2[u] = it;
+        }
+        if (tid == 0) {
+            const bool fits = units <= w.max_items;
+            if (!fits) report_error(w.err, GDN_ERR_DEVICE_CHECK);
+            w.num_items[0] = fits ? units : 0;
+            w.num_items[1] = 0;
+            w.num_items[2] = 0;
+        }
+    }
     if (tid == 0) *w.num_chunks = total;
 }
 
@@ -115,12 +140,22 @@ __global__ void __launch_bounds__(1024) seqprep_kernel(const __grid_constant__ P
 constexpr int kGateHeads = 64;
 
 __global__ void __launch_bounds__(256) gate_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w) {
-    grid_dependency_wait();
     __shared__ float tile[kChunk][kGateHeads + 1];
     __shared__ int s_nz[kGateHeads];
     const int cid = blockIdx.x;
-    if (cid >= *w.num_chunks) return;
-    const int4 ci = w.chunks[cid];
+    int4 ci;
+    if (!p.varlen) {
+        // equal sequences: the chunk's place follows from its index, so the
+        // gate values are read while the sequence-prep kernel still runs
+        // (programmatic dependent launch), and only the writes wait for it
+        const int ncs = (p.T + kChunk - 1) / kChunk;
+        const int seq = cid / ncs, c = cid - seq * ncs;
+        ci = make_int4(seq, seq * p.T + c * kChunk, min(kChunk, p.T - c * kChunk), c);
+    } else {
+        grid_dependency_wait();
+        if (cid >= *w.num_chunks) return;
+        ci = w.chunks[cid];
+    }
     const int t0 = ci.y, len = ci.z;
     const int h0 = blockIdx.y * kGateHeads;
     const int nh = min(kGateHeads, p.H - h0);
@@ -128,6 +163,7 @@ __global__ void __launch_bounds__(256) gate_kernel(const __grid_constant__ Probl
         int r = idx / nh, hh = idx % nh;
         tile[r][hh] = r < len ? p.g[(size_t)(t0 + r) * p.H + h0 + hh] : 0.f;
     }
+    if (!p.varlen) grid_dependency_wait();   // the head flags are zeroed by the sequence-prep kernel
     __syncthreads();
     // one warp per head: lane l holds rows 2l and 2l+1; a shuffle scan of the
     // pair sums gives the inclusive cumsum (rows past the end are zero in the
@@ -404,8 +440,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Prob
     }
 }
 
-cudaError_t launch_seqprep(const Problem &p, const Workspace &w, cudaStream_t s) {
-    seqprep_kernel<<<1, 1024, 0, s>>>(p, w);
+cudaError_t launch_seqprep(const Problem &p, const Workspace &w, bool emit_items, cudaStream_t s) {
+    seqprep_kernel<<<1, 1024, 0, s>>>(p, w, emit_items ? 1 : 0);
     return cudaGetLastError();
 }
 

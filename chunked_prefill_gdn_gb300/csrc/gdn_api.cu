@@ -402,10 +402,13 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
         p.k = kn;
     }
     if (stages & GDN_STAGE_PREP) {
-        cudaError_t e = launch_seqprep(p, w, stream);
+        // equal sequences without a split: every (sequence, head) is one whole
+        // item, which the sequence-prep kernel lists itself
+        const bool direct = !varlen && !hp.cp;
+        cudaError_t e = launch_seqprep(p, w, direct, stream);
         if (e != cudaSuccess) return cuda_fail("launch seqprep", e);
         if (L.max_chunks > 0 && (e = launch_gate(p, w, stream)) != cudaSuccess) return cuda_fail("launch gate", e);
-        if ((e = launch_plan(p, w, pp, stream)) != cudaSuccess) return cuda_fail("launch plan", e);
+        if (!direct && (e = launch_plan(p, w, pp, stream)) != cudaSuccess) return cuda_fail("launch plan", e);
     }
     if ((stages & GDN_STAGE_INVERSE) && L.max_chunks > 0) {
         cudaError_t e = launch_inverse(p, w, hp.kernel == GDN_KERNEL_TC, stream);
@@ -525,7 +528,7 @@ gdn_status gdn_chunk_transition(const void *k, const void *v, const float *g, co
     pp.transition = 1;
 
     cudaGetLastError();
-    cudaError_t e = launch_seqprep(p, w, stream);
+    cudaError_t e = launch_seqprep(p, w, false, stream);
     if (e != cudaSuccess) return cuda_fail("launch seqprep", e);
     if (L.max_chunks > 0 && (e = launch_gate(p, w, stream)) != cudaSuccess) return cuda_fail("launch gate", e);
     if ((e = launch_plan(p, w, pp, stream)) != cudaSuccess) return cuda_fail("launch plan", e);

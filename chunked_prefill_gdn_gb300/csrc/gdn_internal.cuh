@@ -72,7 +72,9 @@ void set_error_detail(const char *where, cudaError_t e, int driver_result = 0);
 void set_error_text(const char *text);
 
 // Launchers (each returns cudaGetLastError() of its launch).
-cudaError_t launch_seqprep(const Problem &p, const Workspace &w, cudaStream_t s);
+// emit_items: also write the output pass's work list (equal sequences, no split), so
+// that the planner need not run
+cudaError_t launch_seqprep(const Problem &p, const Workspace &w, bool emit_items, cudaStream_t s);
 cudaError_t launch_gate(const Problem &p, const Workspace &w, cudaStream_t s);
 cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &pp, cudaStream_t s);
 // for_tc: the tcgen05 fused kernel consumes the result, which is then T' diag(c1)
