@@ -15,7 +15,8 @@
 //
 //   P0     Q K^T                                 into the U' columns, masked
 //                                                (times exp(-G*)) by the side warps
-//   MMA1   P    = S [K;Q]^T                      A = bf16(S) (TMEM), N = 128
+//   MMA1   P    = S [K;Q]^T                      A = bf16(S) (TMEM); P_K (N = 64) first,
+//                                                then P_Q (N = 64) under E2
 //   MMA2a  U'   = V^T T1^T                       A = the V tile (smem, MN-major)
 //   E2     W2   = -gamma P_K                     (forward merge: "V - S first";
 //   MMA2b  U'  += W2 T1^T                         c1 gamma = b beta gamma), U = D_a U'
@@ -71,6 +72,13 @@ constexpr uint32_t kOffT1 = kOffTP;
 constexpr uint32_t kStageBytes = kOffTP + kTPBytes;
 constexpr uint32_t kTxBytes = kKQBytes + kVBytes + kTPBytes;  // bytes TMA brings per stage
 constexpr int kStages = 3;
+// Gate coefficients live in a ring of their own: a data stage is read only by
+// the MMAs and is refilled as soon as MMA3 of its chunk completes, while the
+// coefficients of a chunk stay in use until its output is written, one chunk
+// later.  (When the data waited for the output as well, the next tiles were
+// requested only ~1.7 us before they were needed and every role of the CTA
+// waited on them each chunk.)
+constexpr int kCoefSlots = 6;
 constexpr uint32_t kOffQM = kStages * kStageBytes;  // two tril(Q K^T) tiles (chunk parity), [64][128 B]
 constexpr uint32_t kOffSmall = kOffQM + 16384;
 
@@ -95,8 +103,9 @@ struct Coef {
 };
 
 struct Small {
-    Coef coef[kStages];
-    uint64_t full[kStages], empty[kStages];
+    Coef coef[kCoefSlots];
+    uint64_t full[kStages], empty[kStages];  // empty: MMA3 of the stage's chunk is done
+    uint64_t cempty[kCoefSlots];             // the chain and the side warps are done with the slot
     uint64_t e1, e2, e3, e4, qm;
     // by chunk parity (chunk n: [n & 1], phase n >> 1)
     uint64_t oepi[2];  // output of chunk n done
@@ -144,7 +153,7 @@ __device__ __forceinline__ bool ewait(const Ctx &cx, uint64_t *bar, uint32_t par
     return __all_sync(0xffffffffu, r);
 }
 
-// Shared-space address of coefficient array `field` of stage s.
+// Shared-space address of coefficient array `field` of coefficient slot s.
 #define COEF_ADDR(cx, s, field) ((cx).sbase + kOffSmall + (s) * sizeof(Coef) + offsetof(Coef, field))
 
 // Items of this CTA: round r takes item r G + c in even rounds and
@@ -159,6 +168,7 @@ __device__ __forceinline__ int cta_item(int r) {
 
 // Stage ring: chunk n uses stage n % kStages; its use index is n / kStages.
 __device__ __forceinline__ int stage_of(uint32_t n) { return static_cast<int>(n % kStages); }
+__device__ __forceinline__ int coef_of(uint32_t n) { return static_cast<int>(n % kCoefSlots); }
 __device__ __forceinline__ uint32_t use_parity(uint32_t n) { return (n / kStages) & 1u; }
 
 // ---------------------------------------------------------------- producer
@@ -212,8 +222,9 @@ __device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps,
         const int h = ph, t0 = pt0;
         more = advance();
         if (more) fetch();
-        const int s = stage_of(n);
+        const int s = stage_of(n), cs = coef_of(n);
         if (n >= kStages && !wait_or_abort(cx, &sm.empty[s], ((n / kStages) - 1) & 1)) break;
+        if (n >= kCoefSlots && !wait_or_abort(cx, &sm.cempty[cs], ((n / kCoefSlots) - 1) & 1)) break;
         {
             const float Gfirst = __shfl_sync(0xffffffffu, g0, 0);
             const float Glast = __shfl_sync(0xffffffffu, g1, 31);  // row 63 repeats row len-1
@@ -222,7 +233,7 @@ __device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps,
             // used (the inverse kernel takes the same decision from the same G)
             const bool exact = Glast < -80.f;
             const float Gs = 0.5f * (Gfirst + Glast);
-            Coef &cf = sm.coef[s];
+            Coef &cf = sm.coef[cs];
             const float gg[2] = {g0, g1};
             const float fN = __expf(-Gs), eN = __expf(Glast - Gs);
 #pragma unroll
@@ -317,7 +328,7 @@ __device__ __forceinline__ void mma_role(const Ctx &cx) {
     Small &sm = *cx.sm;
     const uint32_t t = cx.tbase;
     const uint32_t smem0 = smem_u32(cx.smem);
-    constexpr uint32_t I1 = idesc_bf16_f32(128, 128, 0, 0);   // P = S16 [K;Q]^T
+    constexpr uint32_t I1h = idesc_bf16_f32(128, 64, 0, 0);   // P_K = S16 K^T, then P_Q = S16 Q^T
     constexpr uint32_t I0 = idesc_bf16_f32(128, 64, 0, 0);    // [K;Q] K^T
     constexpr uint32_t I2a = idesc_bf16_f32(128, 64, 1, 0);   // U' = V^T (T' D_c1)^T, V^T MN-major
     constexpr uint32_t I2b = idesc_bf16_f32(128, 64, 0, 0);   // U' += W2 T1^T
@@ -381,7 +392,7 @@ __device__ __forceinline__ void mma_role(const Ctx &cx) {
         const bool zero_v = cu.flags & GDN_ITEM_FROM_IDENTITY;  // correction items: no V term
         const uint32_t st = smem0 + s * kStageBytes;
         const uint32_t pc = t + kColP + (n & 1) * 128;        // this chunk's P buffer
-        const bool exact = cx.sm->coef[s].exact;
+        const bool exact = cx.sm->coef[coef_of(n)].exact;
         const uint64_t dKQ = smem_desc_sw128(st, 16, 1024);             // K|Q rows, K-major
         const uint64_t dV = smem_desc_sw128(st + kOffV, 8192, 1024);    // V^T, MN-major
         const uint64_t dT1 = smem_desc_sw128(st + kOffT1, 16, 1024);
@@ -393,10 +404,16 @@ __device__ __forceinline__ void mma_role(const Ctx &cx) {
         if (!wait_or_abort(cx, &sm.e1, par)) break;
         tc_fence_after();
         if (leader) {
+            // P_K first (N = 64, the K rows of the tile): E2 needs only P_K, so
+            // P_Q (the Q rows, 8 KB further) runs on the tensor pipe under E2
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_ts(pc, t + kColS16 + 8 * kk, dKQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), I1, kk > 0);
+                mma_ts(pc, t + kColS16 + 8 * kk, dKQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), I1h, kk > 0);
             tc_commit(&sm.m1);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_ts(pc + 64, t + kColS16 + 8 * kk, dKQ + (((kk >> 2) * 16384 + (kk & 3) * 32 + 8192) >> 4), I1h,
+                       kk > 0);
         }
         __syncwarp();
         if (pend4 && !issue_mma4(n - 1, pend4_out, false)) break;
@@ -463,18 +480,29 @@ __device__ __forceinline__ void load_tile32(const Ctx &cx, const EpiThread &e, u
 }
 
 // Stores 32 state columns j0 .. j0+31 (key index) of this thread's value row.
+// The destinations are formed once, before any store: a float store could
+// alias the parameter blocks as far as the compiler can tell, and re-reading
+// their fields after every store made the 64 KB flush of a CTA take ~9 us.
 __device__ __noinline__ void write_state32(const Ctx cx, const EpiThread e, const gdn_work_item it, int j0,
                                            const float *sv) {
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
-    const int i = e.i;
+    const size_t col = (size_t)j0 * kD + e.i;
+    float *const df = (it.flags & GDN_ITEM_WRITE_FINAL)
+                          ? p.sf + ((size_t)it.seq * p.H + it.head) * kD * kD + col : nullptr;
+    float *const ds = (it.flags & GDN_ITEM_WRITE_SLOT) ? w.cp_s + (size_t)it.slot * kD * kD + col : nullptr;
+    float *const dm = (it.flags & GDN_ITEM_WRITE_M) ? w.cp_m + (size_t)it.slot * kD * kD + col : nullptr;
+    if (df) {
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-        const int j = j0 + jj;
-        if (it.flags & GDN_ITEM_WRITE_FINAL)
-            p.sf[(((size_t)it.seq * p.H + it.head) * kD + j) * kD + i] = sv[jj];
-        if (it.flags & GDN_ITEM_WRITE_SLOT) w.cp_s[((size_t)it.slot * kD + j) * kD + i] = sv[jj];
-        if (it.flags & GDN_ITEM_WRITE_M) w.cp_m[((size_t)it.slot * kD + j) * kD + i] = sv[jj];
+        for (int jj = 0; jj < 32; ++jj) df[jj * kD] = sv[jj];
+    }
+    if (ds) {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) ds[jj * kD] = sv[jj];
+    }
+    if (dm) {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) dm[jj * kD] = sv[jj];
     }
 }
 
@@ -484,19 +512,15 @@ __device__ __noinline__ void load_start_state32(const Ctx cx, const EpiThread e,
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
     const int i = e.i;
+    const size_t col = (size_t)j0 * kD + i;
+    const float *src = nullptr;
+    if (it.flags & GDN_ITEM_FROM_INITIAL)
+        src = p.s0 ? p.s0 + ((size_t)it.seq * p.H + it.head) * kD * kD + col : nullptr;
+    else if (!(it.flags & GDN_ITEM_FROM_IDENTITY) && (it.flags & GDN_ITEM_FROM_SLOT))
+        src = w.cp_s + (size_t)it.slot * kD * kD + col;
+    const bool ident = !(it.flags & GDN_ITEM_FROM_INITIAL) && (it.flags & GDN_ITEM_FROM_IDENTITY);
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-        const int j = j0 + jj;
-        float x = 0.f;
-        if (it.flags & GDN_ITEM_FROM_INITIAL) {
-            if (p.s0) x = p.s0[(((size_t)it.seq * p.H + it.head) * kD + j) * kD + i];
-        } else if (it.flags & GDN_ITEM_FROM_IDENTITY) {
-            x = (i == j) ? 1.f : 0.f;
-        } else if (it.flags & GDN_ITEM_FROM_SLOT) {
-            x = w.cp_s[((size_t)it.slot * kD + j) * kD + i];
-        }
-        sv[jj] = x;
-    }
+    for (int jj = 0; jj < 32; ++jj) sv[jj] = src ? src[jj * kD] : (ident && i == j0 + jj) ? 1.f : 0.f;
 }
 
 // Writes the state held in TMEM (this thread's row, its 64 columns) for `it`.
@@ -560,11 +584,11 @@ __device__ __forceinline__ void chain_role(const Ctx &cx, int warp, int lane) {
             continue;
         }
         for (int c = it.c_start; c < it.c_end; ++c, ++n) {
-            const int s = stage_of(n);
+            const int s = stage_of(n), cs = coef_of(n);
             const uint32_t par = n & 1;
             const int len = w.chunks[si.z + c].z;
             const uint32_t pcol = kColP + (n & 1) * 128;
-            const Coef &cf = sm.coef[s];
+            const Coef &cf = sm.coef[cs];
             if (!ewait(cx, &sm.full[s], use_parity(n))) { ok = false; break; }
 
             // ---- E1: S16 = bf16(S), S32 = gamma_C S   (after MMA3 of the last chunk)
@@ -616,7 +640,7 @@ __device__ __forceinline__ void chain_role(const Ctx &cx, int warp, int lane) {
             {
                 float pk[32];
                 load_tile32(cx, e, pcol + 32 * ch, pk);
-                const uint32_t c2a = COEF_ADDR(cx, s, gam) + 128 * ch;
+                const uint32_t c2a = COEF_ADDR(cx, cs, gam) + 128 * ch;
                 uint32_t w2[16];
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
@@ -642,7 +666,7 @@ __device__ __forceinline__ void chain_role(const Ctx &cx, int warp, int lane) {
                     for (int j = 0; j < 32; ++j)
                         if (32 * ch + j >= len) u[j] = 0.f;
                 }
-                const uint32_t ea = COEF_ADDR(cx, s, e) + 128 * ch;
+                const uint32_t ea = COEF_ADDR(cx, cs, e) + 128 * ch;
                 uint32_t ut[16];
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
@@ -661,7 +685,7 @@ __device__ __forceinline__ void chain_role(const Ctx &cx, int warp, int lane) {
             }
             tc_fence_before();
             mbar_arrive(&sm.e4);
-            mbar_arrive(&sm.empty[s]);
+            mbar_arrive(&sm.cempty[cs]);
         }
         if (!ok) break;
         prev_item = it;
@@ -789,13 +813,13 @@ __device__ __forceinline__ void side_role(const Ctx &cx, int warp, int lane) {
         const gdn_work_item it = cx.items[cta_item(r)];
         const int4 si = w.seqinfo[it.seq];
         for (int c = it.c_start; c < it.c_end; ++c, ++n) {
-            const int s = stage_of(n);
+            const int s = stage_of(n), cs = coef_of(n);
             const uint32_t par = n & 1;
             const int4 ci = w.chunks[si.z + c];
             const int t0 = ci.y, len = ci.z;
             const bool out = (it.flags & GDN_ITEM_OUTPUT) && c >= it.c_begin;
             const uint32_t pcol = kColP + (n & 1) * 128, ocol = kColP + ((n + 1) & 1) * 128;
-            const Coef &cf = sm.coef[s];
+            const Coef &cf = sm.coef[cs];
             if (!ewait(cx, &sm.full[s], use_parity(n))) { ok = false; break; }
             const bool exact = cf.exact;
 
@@ -822,14 +846,14 @@ __device__ __forceinline__ void side_role(const Ctx &cx, int warp, int lane) {
                 if (pv_out) output_chunk(cx, e, pv_s, pv_exact, pv_pcol + 64, pv_ocol, pv_t0, pv_len, pv_h);
                 tc_fence_before();
                 mbar_arrive(&sm.oepi[(n - 1) & 1]);
-                mbar_arrive(&sm.empty[pv_s]);
+                mbar_arrive(&sm.cempty[pv_s]);
             }
 
             pv_out = out;
             pv_t0 = t0;
             pv_len = len;
             pv_h = it.head;
-            pv_s = s;
+            pv_s = cs;
             pv_exact = exact;
             pv_pcol = pcol;
             pv_ocol = ocol;
@@ -857,8 +881,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.full[s], 32);
-            mbar_init(&sm.empty[s], 1 + kEpiThreads);
+            mbar_init(&sm.empty[s], 1);
         }
+        for (int c = 0; c < kCoefSlots; ++c) mbar_init(&sm.cempty[c], kEpiThreads);
         mbar_init(&sm.e1, kChainThreads);
         mbar_init(&sm.e2, kChainThreads);
         mbar_init(&sm.e3, kChainThreads);
