@@ -64,7 +64,8 @@ class GdnOptions(ctypes.Structure):
                 ("sw_eps", ctypes.c_float), ("sm_count", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("debug_checks", ctypes.c_int32),
                 ("prof_begin", ctypes.c_void_p), ("prof_end", ctypes.c_void_p),
-                ("qk_l2norm", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("qk_l2norm", ctypes.c_int32), ("inverse_overlap", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 class GdnPlanInfo(ctypes.Structure):
@@ -72,7 +73,7 @@ class GdnPlanInfo(ctypes.Structure):
                 ("chunks_per_segment", ctypes.c_int32), ("max_chunks", ctypes.c_int32),
                 ("max_items", ctypes.c_int32), ("max_cp_slots", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("grid_fused", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("overlap_columns", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class GdnPlanCosts(ctypes.Structure):

@@ -39,12 +39,15 @@
 // E2, MMA2b, E3, MMA3 free of work off it.  Every wait is bounded: on timeout
 // the kernel records GDN_ERR_TIMEOUT, waits for its own copies in flight, frees
 // TMEM and returns.
+#include <limits.h>
 #include <stddef.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "gdn_internal.cuh"
+#include "inverse_tc.cuh"
 #include "tc_ptx.cuh"
 
 namespace gdn {
@@ -131,7 +134,12 @@ struct Ctx {
     const gdn_work_item *items;
     int n_items;
     uint32_t tbase;
+    int G;               // CTAs that run work items (the chain CTAs)
+    int ov_c0;           // chunk columns from ov_c0 on are computed during this pass
+    int ov_expected;     // units per column then
+    int *ov_ready;       // [columns]: units of a column whose T1 rows are in memory
 };
+
 
 // Slow path of a wait, out of line so the per-chunk code stays small enough
 // for the instruction cache: bounded spin, then GDN_ERR_TIMEOUT.
@@ -161,8 +169,8 @@ __device__ __forceinline__ bool ewait(const Ctx &cx, uint64_t *bar, uint32_t par
 // lists items longest first, so the rounds snake the long ones over the CTAs
 // instead of stacking them on the first ones.  Every role of the CTA walks the
 // same sequence; it ends at the first index past the list.
-__device__ __forceinline__ int cta_item(int r) {
-    const int G = gridDim.x, c = blockIdx.x;
+__device__ __forceinline__ int cta_item(int r, int G) {
+    const int c = blockIdx.x;
     return r * G + ((r & 1) ? G - 1 - c : c);
 }
 
@@ -170,6 +178,29 @@ __device__ __forceinline__ int cta_item(int r) {
 __device__ __forceinline__ int stage_of(uint32_t n) { return static_cast<int>(n % kStages); }
 __device__ __forceinline__ int coef_of(uint32_t n) { return static_cast<int>(n % kCoefSlots); }
 __device__ __forceinline__ uint32_t use_parity(uint32_t n) { return (n / kStages) & 1u; }
+
+// Bounded wait for every unit of chunk column `col` (see FusedOverlap).
+__device__ __noinline__ bool wait_column(const Ctx cx, int col) {
+    const int *cnt = cx.ov_ready + col;
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    if (v < cx.ov_expected) {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t it = 1;; ++it) {
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+            if (v >= cx.ov_expected) break;
+            if ((it & 63u) == 0u) {
+                if (*(volatile int *)&cx.sm->abort) return false;
+                if (global_timer_ns() - t0 > kTimeoutNs) {
+                    if (atomicExch(&cx.sm->abort, 1) == 0) report_error(cx.w->err, GDN_ERR_TIMEOUT);
+                    return false;
+                }
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
 
 // ---------------------------------------------------------------- producer
 __device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps, int lane) {
@@ -189,8 +220,8 @@ __device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps,
         }
         if (started) ++r;
         started = true;
-        for (; cta_item(r) < cx.n_items; ++r) {
-            const gdn_work_item it = cx.items[cta_item(r)];
+        for (; cta_item(r, cx.G) < cx.n_items; ++r) {
+            const gdn_work_item it = cx.items[cta_item(r, cx.G)];
             if (it.c_start < it.c_end) {
                 c = it.c_start;
                 cend = it.c_end;
@@ -204,11 +235,12 @@ __device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps,
     // the gate values of the next chunk are fetched one step ahead, so their
     // latency overlaps the wait for a free stage
     float pg0 = 0.f, pg1 = 0.f;
-    int ph = 0, pt0 = 0, plen = 1;
+    int ph = 0, pt0 = 0, plen = 1, pcol = 0;
     auto fetch = [&]() {
         const int4 ci = w.chunks[chunk0 + c];
         pt0 = ci.y;
         plen = ci.z;
+        pcol = c;
         ph = head;
         const size_t gb = (size_t)ph * p.total_T + pt0;
         pg0 = w.G[gb + min(lane, plen - 1)];
@@ -219,7 +251,7 @@ __device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps,
     uint32_t n = 0;
     while (more) {
         const float g0 = pg0, g1 = pg1;
-        const int h = ph, t0 = pt0;
+        const int h = ph, t0 = pt0, col = pcol;
         more = advance();
         if (more) fetch();
         const int s = stage_of(n), cs = coef_of(n);
@@ -251,6 +283,11 @@ __device__ __forceinline__ void producer_role(const Ctx &cx, const TcMaps &maps,
                 cf.gC = __expf(Glast);
                 cf.exact = exact;
             }
+        }
+        if (col >= cx.ov_c0) {
+            bool ready = true;
+            if (lane == 0) ready = wait_column(cx, col);
+            if (!__shfl_sync(0xffffffffu, ready, 0)) break;
         }
         uint8_t *st = cx.smem + s * kStageBytes;
         if (lane == 0) {
@@ -287,8 +324,8 @@ struct MmaCursor {
 
 __device__ __forceinline__ void cursor_start(const Ctx &cx, MmaCursor &cu) {
     cu.valid = false;
-    for (cu.r = 0; cta_item(cu.r) < cx.n_items; ++cu.r) {
-        const gdn_work_item it = cx.items[cta_item(cu.r)];
+    for (cu.r = 0; cta_item(cu.r, cx.G) < cx.n_items; ++cu.r) {
+        const gdn_work_item it = cx.items[cta_item(cu.r, cx.G)];
         if (it.c_start < it.c_end) {
             cu.c = it.c_start;
             cu.cend = it.c_end;
@@ -303,8 +340,8 @@ __device__ __forceinline__ void cursor_start(const Ctx &cx, MmaCursor &cu) {
 __device__ __forceinline__ void cursor_next(const Ctx &cx, MmaCursor &cu) {
     if (++cu.c < cu.cend) return;
     cu.valid = false;
-    for (++cu.r; cta_item(cu.r) < cx.n_items; ++cu.r) {
-        const gdn_work_item it = cx.items[cta_item(cu.r)];
+    for (++cu.r; cta_item(cu.r, cx.G) < cx.n_items; ++cu.r) {
+        const gdn_work_item it = cx.items[cta_item(cu.r, cx.G)];
         if (it.c_start < it.c_end) {
             cu.c = it.c_start;
             cu.cend = it.c_end;
@@ -564,8 +601,8 @@ __device__ __forceinline__ void chain_role(const Ctx &cx, int warp, int lane) {
     prev_item.flags = 0;
     bool ok = true;
 
-    for (int r = 0; cta_item(r) < cx.n_items && ok; ++r) {
-        const gdn_work_item it = cx.items[cta_item(r)];
+    for (int r = 0; cta_item(r, cx.G) < cx.n_items && ok; ++r) {
+        const gdn_work_item it = cx.items[cta_item(r, cx.G)];
         const int4 si = w.seqinfo[it.seq];
         if (it.c_start >= it.c_end) {
             // an empty sequence: its end state is its start state
@@ -809,8 +846,8 @@ __device__ __forceinline__ void side_role(const Ctx &cx, int warp, int lane) {
     uint32_t pv_pcol = 0, pv_ocol = 0;
     bool ok = true;
 
-    for (int r = 0; cta_item(r) < cx.n_items && ok; ++r) {
-        const gdn_work_item it = cx.items[cta_item(r)];
+    for (int r = 0; cta_item(r, cx.G) < cx.n_items && ok; ++r) {
+        const gdn_work_item it = cx.items[cta_item(r, cx.G)];
         const int4 si = w.seqinfo[it.seq];
         for (int c = it.c_start; c < it.c_end; ++c, ++n) {
             const int s = stage_of(n), cs = coef_of(n);
@@ -867,14 +904,35 @@ __device__ __forceinline__ void side_role(const Ctx &cx, int warp, int lane) {
     }
 }
 
+// The inverse role of the overlap launch, out of line so that its register
+// needs do not shape the allocation of the state chain's code.
+__device__ __noinline__ void inverse_role(const CUtensorMap *kmap, const Problem &p, const Workspace &w,
+                                          const FusedOverlap &ov, uint8_t *smem_raw) {
+    InvSel sel;
+    sel.mode = 2;
+    sel.nc = ov.nc;
+    sel.c0 = ov.c0;
+    sel.cta = (int)blockIdx.x - ov.chain_ctas;
+    sel.ctas = (int)gridDim.x - ov.chain_ctas;
+    sel.ready = ov.ready;
+    inverse_tc_body(kmap, p, w, ov.gate_scaled, sel, smem_raw);
+}
+
 // ---------------------------------------------------------------- kernel
 // 14 warps share the 4 SM sub-partitions 4/4/3/3, so a thread may hold at most
-// 16384 / (4 * 32) = 128 registers.
-__global__ void __launch_bounds__(kThreads, 1)
+// 16384 / (4 * 32) = 128 registers.  OVL: the launch also has CTAs past the
+// chain CTAs, which compute the T1 tiles of the last chunk columns (the
+// inverse's 16 warps; the chain CTAs leave warps 14 and 15 idle).
+template <bool OVL>
+__global__ void __launch_bounds__(OVL ? kInvThreads : kThreads, 1)
     fused_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ Problem p,
-                    const __grid_constant__ Workspace w, const int pass) {
+                    const __grid_constant__ Workspace w, const int pass, const __grid_constant__ FusedOverlap ov) {
     grid_dependency_wait();
     extern __shared__ uint8_t smem_raw[];
+    if (OVL && (int)blockIdx.x >= ov.chain_ctas) {
+        inverse_role(&maps.k, p, w, ov, smem_raw);
+        return;
+    }
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Small &sm = *reinterpret_cast<Small *>(smem + kOffSmall);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -925,6 +983,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     cx.items = pass == 2 ? w.items2 : w.items1;
     cx.n_items = *(volatile const int *)&w.num_items[pass == 2 ? 0 : 1];
     cx.tbase = sm.tmem_base;
+    cx.G = OVL ? ov.chain_ctas : (int)gridDim.x;
+    cx.ov_c0 = OVL ? ov.c0 : INT_MAX;
+    cx.ov_expected = ov.expected;
+    cx.ov_ready = ov.ready;
 
     if (warp == kProducerWarp) {
         producer_role(cx, maps, lane);
@@ -932,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_role(cx);
     } else if (warp < 8) {
         chain_role(cx, warp, lane);
-    } else {
+    } else if (warp < 12) {
         side_role(cx, warp, lane);
     }
 
@@ -980,7 +1042,8 @@ int encode_rows(EncodeTiledFn fn, CUtensorMap *m, const void *base, int H, int t
 
 bool fused_tc_supported(int dtype, int dk, int dv) { return dtype == GDN_BF16 && dk == kD && dv == kD; }
 
-cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s) {
+cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s,
+                            const FusedOverlap *ov) {
     if (!fused_tc_supported(p.dtype, p.dk, p.dv)) return cudaErrorNotSupported;
     if (p.total_T == 0) return launch_fused_simt(p, w, pass, grid, s);  // only empty sequences: nothing to tile
     EncodeTiledFn fn = encode_fn();
@@ -1004,9 +1067,41 @@ cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int 
         set_error_detail("encode tensor map", cudaErrorInvalidValue, r);
         return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    FusedOverlap none = {};
+    const FusedOverlap *o = ov && ov->c0 < ov->nc ? ov : nullptr;
+    if (!o) {
+        cudaError_t e =
+            cudaFuncSetAttribute(fused_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = launch_dependent(fused_tc_kernel<false>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, p, w,
+                             pass, none);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+    // one cooperative launch, so that the chain CTAs, which wait on the
+    // inverse CTAs, are guaranteed to run alongside them
+    const size_t smem = std::max<size_t>(kSmemBytes, kInvSmem);
+    cudaError_t e = cudaFuncSetAttribute(fused_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(fused_tc_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, s, maps, p, w, pass);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kInvThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, fused_tc_kernel<true>, maps, p, w, pass, *o);
+    if (e != cudaSuccess && e != cudaErrorCooperativeLaunchTooLarge) {
+        // without the overlap with the previous kernel's tail
+        cudaGetLastError();
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, fused_tc_kernel<true>, maps, p, w, pass, *o);
+    }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

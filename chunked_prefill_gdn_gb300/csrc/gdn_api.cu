@@ -71,6 +71,10 @@ struct HostPlan {
     int L;
     int sms;
     int grid;
+    int nc;             // chunks per sequence (equal sequences)
+    int ov_cols;        // chunk columns whose inverse runs inside the fused pass
+    int ov_ctas;        // CTAs of the fused launch that run it
+    int units;          // (sequence, head) units
     int N;
     long long total_T;
     Layout lay;
@@ -168,6 +172,13 @@ gdn_status make_plan(int B, int T, int H, int dk, int dv, int n_seqs, int varlen
             L = std::max(kMinSegmentChunks, (int)(((long long)max_chunks * H + sms - 1) / sms));
         }
     }
+    // the inverse of the last chunk columns inside the fused pass (equal
+    // sequences without a split, tcgen05 kernels, idle SMs)
+    int ov_cols = 0, ov_ctas = 0;
+    if (kernel == GDN_KERNEL_TC && !cp && !varlen && opts.inverse_overlap > 0 && units < sms && nc_seq > 0) {
+        ov_cols = (int)std::min<long long>(opts.inverse_overlap, nc_seq);
+        ov_ctas = sms - units;
+    }
     const int segs_bound = cp ? (int)(((long long)max_chunks + L - 1) / L) : 0;
     Layout &lay = hp->lay;
     lay.max_chunks = max_chunks;
@@ -200,12 +211,17 @@ gdn_status make_plan(int B, int T, int H, int dk, int dv, int n_seqs, int varlen
     const size_t qk_bytes = opts.qk_l2norm ? (size_t)total_T * H * dk * (dtype == GDN_BF16 ? 2 : 4) : 0;
     lay.qn = take(qk_bytes);
     lay.kn = take(qk_bytes);
+    lay.ready = take(ov_cols > 0 ? (size_t)nc_seq * 4 : 0);
     lay.total = off;
     hp->kernel = kernel;
     hp->cp = cp;
     hp->L = L;
     hp->sms = sms;
     hp->grid = sms;
+    hp->nc = (int)nc_seq;
+    hp->ov_cols = ov_cols;
+    hp->ov_ctas = ov_ctas;
+    hp->units = units;
     hp->N = N;
     hp->total_T = total_T;
     return GDN_OK;
@@ -290,7 +306,8 @@ gdn_status gdn_plan_query(int B, int T, int H, int dk, int dv, int n_seqs, int v
     out->max_items = hp.lay.max_items;
     out->max_cp_slots = hp.lay.max_cp_slots;
     out->sm_count = hp.sms;
-    out->grid_fused = hp.grid;
+    out->grid_fused = hp.ov_cols > 0 ? hp.units + hp.ov_ctas : hp.grid;
+    out->overlap_columns = hp.ov_cols;
     out->workspace_bytes = hp.lay.total;
     return GDN_OK;
 }
@@ -410,8 +427,25 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
         if (L.max_chunks > 0 && (e = launch_gate(p, w, stream)) != cudaSuccess) return cuda_fail("launch gate", e);
         if (!direct && (e = launch_plan(p, w, pp, stream)) != cudaSuccess) return cuda_fail("launch plan", e);
     }
+    // with the overlap, the fused pass computes the inverse of chunk columns
+    // [ov_c0, nc) and counts each column's finished units in `ready`
+    const int ov_c0 = hp.nc - hp.ov_cols;
+    FusedOverlap ov = {};
+    if (hp.ov_cols > 0) {
+        ov.chain_ctas = hp.units;
+        ov.c0 = ov_c0;
+        ov.nc = hp.nc;
+        ov.expected = hp.units;
+        ov.ready = reinterpret_cast<int *>(base + L.ready);
+        ov.gate_scaled = 1;
+        if (stages & GDN_STAGE_PREP) {
+            cudaError_t e = cudaMemsetAsync(ov.ready, 0, (size_t)hp.nc * sizeof(int), stream);
+            if (e != cudaSuccess) return cuda_fail("clear column counts", e);
+        }
+    }
     if ((stages & GDN_STAGE_INVERSE) && L.max_chunks > 0) {
-        cudaError_t e = launch_inverse(p, w, hp.kernel == GDN_KERNEL_TC, stream);
+        cudaError_t e = hp.ov_cols > 0 ? launch_inverse(p, w, true, stream, ov_c0, hp.nc)
+                                       : launch_inverse(p, w, hp.kernel == GDN_KERNEL_TC, stream);
         if (e != cudaSuccess) return cuda_fail("launch inverse", e);
     }
     const bool tc = hp.kernel == GDN_KERNEL_TC;
@@ -425,7 +459,19 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
         if (opts.prof_begin &&
             (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts.prof_begin), stream)) != cudaSuccess)
             return cuda_fail("record prof_begin", e);
-        e = tc ? launch_fused_tc(p, w, 2, hp.grid, stream) : launch_fused_simt(p, w, 2, hp.grid, stream);
+        if (!tc) {
+            e = launch_fused_simt(p, w, 2, hp.grid, stream);
+        } else if (hp.ov_cols > 0) {
+            e = launch_fused_tc(p, w, 2, hp.units + hp.ov_ctas, stream, &ov);
+            if (e == cudaErrorCooperativeLaunchTooLarge) {
+                // the SMs are not all free: the whole inverse first, then the plain pass
+                cudaGetLastError();
+                if ((e = launch_inverse(p, w, true, stream)) == cudaSuccess)
+                    e = launch_fused_tc(p, w, 2, hp.grid, stream);
+            }
+        } else {
+            e = launch_fused_tc(p, w, 2, hp.grid, stream);
+        }
         if (e != cudaSuccess) return cuda_fail(tc ? "launch fused_tc pass 2" : "launch fused_simt pass 2", e);
         if (opts.prof_end && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(opts.prof_end), stream)) != cudaSuccess)
             return cuda_fail("record prof_end", e);

@@ -62,7 +62,7 @@ struct PlanParams {
 // Host-side layout of the workspace for one problem.
 struct Layout {
     size_t err, counters, num_chunks, num_items, seqinfo, chunks, flags, G, totals, tprime,
-        items2, items1, scan_units, seq_order, cp_s, cp_m, qn, kn, total;
+        items2, items1, scan_units, seq_order, cp_s, cp_m, qn, kn, ready, total;
     int max_chunks, max_items, max_items1, max_cp_slots;
 };
 
@@ -79,7 +79,9 @@ cudaError_t launch_gate(const Problem &p, const Workspace &w, cudaStream_t s);
 cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &pp, cudaStream_t s);
 // for_tc: the tcgen05 fused kernel consumes the result, which is then T' diag(c1)
 // (the gate-scaled form that kernel multiplies by) instead of T' itself
-cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s);
+// cols < nc (equal sequences of nc chunks, tcgen05 inverse only): chunk
+// columns [0, cols) only, the fused kernel computing the others
+cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s, int cols = 0, int nc = 0);
 cudaError_t launch_scan(const Problem &p, const Workspace &w, cudaStream_t s);
 // start states of R consecutive slices: out[0] = s0 (or 0), out[r+1] = out[r] M_r + S*_r;
 // grad: end gradients, out[R-1] = s0 (or 0), out[r] = out[r+1] M_{r+1}^T + S*_{r+1}
@@ -93,7 +95,22 @@ cudaError_t launch_qk_l2norm(const void *q, const void *k, void *qo, void *ko, l
 // pass 1 (state-only correction items) or pass 2 (output items) on the CUDA-core kernel
 cudaError_t launch_fused_simt(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s);
 // the tcgen05 kernel; returns cudaErrorNotSupported when the compiled library or the device cannot run it
-cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s);
+// The fused kernel can compute the T1 tiles of the last chunk columns itself:
+// CTAs past the chain CTAs run the tcgen05 inverse on SMs the (sequence, head)
+// units leave idle, column by column, in one cooperative launch.  Before
+// loading the T1 tile of such a column the tile producer waits, bounded,
+// until every unit of the column is in memory (an acquire of the column's
+// count, then a proxy fence before the TMA read).
+struct FusedOverlap {
+    int chain_ctas;      // CTAs that run work items; the rest run the inverse
+    int c0, nc;          // chunk columns [c0, nc) of nc-chunk equal sequences
+    int expected;        // units per column (sequences x heads)
+    int *ready;          // [nc] per-column counts, zero before the pass
+    int gate_scaled;     // 1: T1 = T' diag(c1) as the tcgen05 fused kernel reads it
+};
+
+cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s,
+                            const FusedOverlap *ov = nullptr);
 bool fused_tc_supported(int dtype, int dk, int dv);
 int fused_simt_smem_bytes(int dk, int dv);
 

@@ -101,7 +101,18 @@ typedef struct {
                                    (gdn_qk_l2norm with eps 1e-6) into workspace copies
                                    before the pass; 0 (default): the caller's rows are
                                    used as they are (they should be unit-norm already) */
-    int32_t reserved[3];
+    int32_t inverse_overlap;    /* the tcgen05 path on equal sequences without a split, when
+                                   the (sequence, head) units leave SMs idle: k > 0 lets the
+                                   fused pass run the per-chunk inverse of the last k chunk
+                                   columns (at most all) on those SMs while the other CTAs
+                                   run the state recurrence (one cooperative launch; each
+                                   such column is loaded only once all its units are in
+                                   memory; the results are bitwise those of the separate
+                                   inverse).  0 (default) and -1: off.  On a GB300 at
+                                   B=4, T=8192, H=32 it moved the step by -6..+3 us (the
+                                   24 idle SMs' inverse traffic slows the chain about as
+                                   much as it hides), so it is not on by default */
+    int32_t reserved[2];
 } gdn_options;
 
 /* GDN_DEBUG_TIMEOUT_PROBE: the tile producer of the tcgen05 fused pass signals
@@ -128,6 +139,8 @@ typedef struct {
     int32_t max_cp_slots;       /* capacity of the correction-matrix buffers */
     int32_t sm_count;           /* SMs the plan was made for */
     int32_t grid_fused;         /* CTAs of the persistent fused kernel */
+    int32_t overlap_columns;    /* chunk columns whose inverse runs inside the fused pass
+                                   (see gdn_options.inverse_overlap); 0: none */
     size_t workspace_bytes;     /* bytes gdn_chunk_fwd needs */
 } gdn_plan_info;
 

@@ -76,6 +76,23 @@ def test_plan_cp_modes(lib):
     assert force.max_items >= 4 * 32 * 8
 
 
+def test_plan_inverse_overlap(lib):
+    """The fused pass takes over the inverse of the last chunk columns only
+    when asked (inverse_overlap = k > 0), and only for equal sequences without
+    a split on the tcgen05 kernels with idle SMs; k is capped at the columns."""
+    q = lambda B, T, H, **kw: plan(B, T, H, 128, 128, B, 0, gdn.BF16, sm_count=152, **kw)
+    assert q(4, 8192, 32).overlap_columns == 0                               # off by default
+    assert q(4, 8192, 32, inverse_overlap=-1).overlap_columns == 0
+    on = q(4, 8192, 32, inverse_overlap=7)
+    assert on.overlap_columns == 7 and on.grid_fused == 152
+    assert q(4, 8192, 32, inverse_overlap=500).overlap_columns == 128
+    assert q(8, 8192, 32, inverse_overlap=7).overlap_columns == 0           # no idle SM
+    assert q(4, 8192, 32, inverse_overlap=7, cp_mode=gdn.CP_FORCE).overlap_columns == 0
+    assert q(4, 8192, 32, inverse_overlap=7, kernel=gdn.KERNEL_SIMT).overlap_columns == 0
+    assert plan(1, 8192, 32, 128, 128, 4, 1, gdn.BF16, sm_count=152, inverse_overlap=7).overlap_columns == 0
+    assert plan(4, 8192, 32, 128, 128, 4, 0, gdn.F32, sm_count=152, inverse_overlap=7).overlap_columns == 0
+
+
 def test_plan_varlen_capacity_bounds(lib):
     p = plan(1, 262144, 16, 128, 128, 64, 1, gdn.BF16, sm_count=152)
     assert p.max_chunks == 262144 // 64 + 64

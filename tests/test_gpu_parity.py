@@ -127,6 +127,26 @@ def test_cp_off_is_deterministic():
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
+@pytest.mark.parametrize("cols", [1, 6, 16])
+def test_inverse_overlap_is_bit_identical(cols):
+    """The fused pass computing the inverse of the last `cols` chunk columns on
+    the SMs its units leave idle (one cooperative launch; each such column's T1
+    is loaded once its ready count says all units are in memory) gives the
+    same bits as the separate inverse launch; 16 columns is every column of
+    these sequences, including the ragged last one."""
+    inp = to_device(make_inputs(CONFIGS[1].scaled(B=2, T=1000, H=8), "cpu"))
+    B, T, H, dk = inp["q"].shape
+    info = gdn.gdn_plan_query(B, T, H, dk, dk, B, 0, gdn.BF16, opts_for(cp_mode=gdn.CP_OFF, inverse_overlap=cols))
+    assert info.overlap_columns == min(cols, 16)
+    o0, s0 = gpu_run(inp, opts_for(cp_mode=gdn.CP_OFF, inverse_overlap=-1))
+    o1, s1 = gpu_run(inp, opts_for(cp_mode=gdn.CP_OFF, inverse_overlap=cols))
+    assert torch.equal(o0, o1) and torch.equal(s0, s1)
+    if cols == 16:
+        o_ref, sf_ref = full_reference(inp)
+        assert_close("o", oracle.to_f64(o1).reshape(B * T, H, -1), o_ref)
+        assert_close("final_state", oracle.to_f64(s1), sf_ref)
+
+
 # ----------------------------------------------------------- intermediates
 
 def _workspace_views(inp, ws, opts=None):
