@@ -904,20 +904,6 @@ __device__ __forceinline__ void side_role(const Ctx &cx, int warp, int lane) {
     }
 }
 
-// The inverse role of the overlap launch, out of line so that its register
-// needs do not shape the allocation of the state chain's code.
-__device__ __noinline__ void inverse_role(const CUtensorMap *kmap, const Problem &p, const Workspace &w,
-                                          const FusedOverlap &ov, uint8_t *smem_raw) {
-    InvSel sel;
-    sel.mode = 2;
-    sel.nc = ov.nc;
-    sel.c0 = ov.c0;
-    sel.cta = (int)blockIdx.x - ov.chain_ctas;
-    sel.ctas = (int)gridDim.x - ov.chain_ctas;
-    sel.ready = ov.ready;
-    inverse_tc_body(kmap, p, w, ov.gate_scaled, sel, smem_raw);
-}
-
 // ---------------------------------------------------------------- kernel
 // 14 warps share the 4 SM sub-partitions 4/4/3/3, so a thread may hold at most
 // 16384 / (4 * 32) = 128 registers.  OVL: the launch also has CTAs past the
@@ -930,7 +916,15 @@ __global__ void __launch_bounds__(OVL ? kInvThreads : kThreads, 1)
     grid_dependency_wait();
     extern __shared__ uint8_t smem_raw[];
     if (OVL && (int)blockIdx.x >= ov.chain_ctas) {
-        inverse_role(&maps.k, p, w, ov, smem_raw);
+        // (inline: the tensor map must be addressed in the kernel's parameter space)
+        InvSel sel = {};
+        sel.mode = 2;
+        sel.nc = ov.nc;
+        sel.c0 = ov.c0;
+        sel.cta = (int)blockIdx.x - ov.chain_ctas;
+        sel.ctas = (int)gridDim.x - ov.chain_ctas;
+        sel.ready = ov.ready;
+        inverse_tc_body(&maps.k, p, w, ov.gate_scaled, sel, smem_raw);
         return;
     }
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

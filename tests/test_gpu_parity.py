@@ -216,27 +216,36 @@ def test_planner_gives_correction_heads_fewer_segments_when_a_wave_is_saved():
     assert_close("final_state", oracle.to_f64(sf), sf_ref)
 
 
-def test_gate_and_inverse_intermediates():
-    cfg = CONFIGS[3].scaled(T=3000, H=3, n_seqs=5, zero_gate_heads=(1,))
+@pytest.mark.parametrize("case", ["varlen", "equal"])
+def test_gate_and_inverse_intermediates(case):
+    """G, chunk totals, head flags and T1 in the workspace after a call, for
+    packed sequences and for equal ones without a split (whose work list the
+    sequence-prep kernel writes itself)."""
+    if case == "varlen":
+        cfg = CONFIGS[3].scaled(T=3000, H=3, n_seqs=5, zero_gate_heads=(1,))
+    else:
+        cfg = CONFIGS[1].scaled(B=3, T=1000, H=3)
     inp = to_device(make_inputs(cfg, "cpu"))
-    ws = gdn.workspace_for(inp["q"], inp["v"], inp["cu_seqlens"])
-    gpu_run(inp, workspace=ws)
-    views = _workspace_views(inp, ws)
+    H = inp["q"].shape[2]
+    opts = gdn.default_options(cp_mode=gdn.CP_OFF) if case == "equal" else None
+    ws = gdn.workspace_for(inp["q"], inp["v"], inp["cu_seqlens"], opts)
+    gpu_run(inp, opts, workspace=ws)
+    views = _workspace_views(inp, ws, opts)
     cu = seq_bounds(inp)
-    g = oracle.to_f64(inp["g"]).reshape(-1, 3)
+    g = oracle.to_f64(inp["g"]).reshape(-1, H)
     # chunk-local cumsum of the gate
     G_ref = gate.chunk_local_cumsum(g, cu, 64)
     assert np.abs(oracle.to_f64(views["G"]).T - G_ref).max() < 1e-4
-    # chunk totals and head flags
-    tot_ref = gate.chunk_totals(g, cu, 64)
     nck = views["num_chunks"]
     assert nck == len(gate.chunk_table(cu, 64))
+    # chunk totals and head flags
+    tot_ref = gate.chunk_totals(g, cu, 64)
     assert np.abs(oracle.to_f64(views["totals"][:, :nck]).T - tot_ref).max() < 1e-4
     assert views["flags"].cpu().numpy().tolist() == gate.head_flags(g, cu).tolist()
     # T' rows against the fp64 inverse (bf16 storage).  The tcgen05 path stores
     # the gate-scaled T1 = T' diag(c1) that its fused kernel multiplies by.
-    beta = oracle.to_f64(inp["beta"]).reshape(-1, 3)
-    Tp_ref = chunked.inverse_rows(oracle.to_f64(inp["k"]).reshape(-1, 3, 128), beta, cu, 64)
+    beta = oracle.to_f64(inp["beta"]).reshape(-1, H)
+    Tp_ref = chunked.inverse_rows(oracle.to_f64(inp["k"]).reshape(-1, H, 128), beta, cu, 64)
     Tp_ref = gate_scaled_tprime(Tp_ref, G_ref, beta, cu, 64)
     Tp = oracle.to_f64(views["tprime"]).transpose(1, 0, 2)
     # element-wise: bf16 storage of entries that the gate scaling can make large
