@@ -8,6 +8,9 @@ max(1, max |reference|) for every gradient — the gradients reach tens, so the
 forward's absolute 2e-2 is applied relative to their scale.  Inputs are
 bf16- or fp32-exact on both sides and the device computes in fp32, so the
 expected error is ~1e-5 relative."""
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -38,6 +41,12 @@ def check(name, got, ref):
     assert np.isfinite(got).all(), "%s has non-finite values" % name
     rel, mab = errors(got, ref)
     bound = MAX_ABS_REL * max(1.0, float(np.abs(ref).max()))
+    path = os.environ.get("GDN_BWD_MARGINS")
+    if path:   # the margins of every checked gradient, absolute error included
+        with open(path, "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], "grad": name,
+                                "rel_l2": rel, "max_abs": mab, "max_ref": float(np.abs(ref).max()),
+                                "max_abs_bound": bound}) + "\n")
     assert rel <= REL_L2 and mab <= bound, "%s: rel-L2 %.3e (tol %.1e), max-abs %.3e (tol %.2e)" % (
         name, rel, REL_L2, mab, bound)
 
