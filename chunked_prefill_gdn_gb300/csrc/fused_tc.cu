@@ -520,26 +520,34 @@ __device__ __forceinline__ void load_tile32(const Ctx &cx, const EpiThread &e, u
 // The destinations are formed once, before any store: a float store could
 // alias the parameter blocks as far as the compiler can tell, and re-reading
 // their fields after every store made the 64 KB flush of a CTA take ~9 us.
+// With head sizes below 128 the tiles are zero-padded to 128 (the TMA fills
+// features past dk / dv with zeros), which leaves the real rows and columns
+// of the state exact; only those are stored: value rows i < dv (i < dk for a
+// correction matrix, whose rows are key indices) and key columns j < dk.
 __device__ __noinline__ void write_state32(const Ctx cx, const EpiThread e, const gdn_work_item it, int j0,
                                            const float *sv) {
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
-    const size_t col = (size_t)j0 * kD + e.i;
-    float *const df = (it.flags & GDN_ITEM_WRITE_FINAL)
-                          ? p.sf + ((size_t)it.seq * p.H + it.head) * kD * kD + col : nullptr;
-    float *const ds = (it.flags & GDN_ITEM_WRITE_SLOT) ? w.cp_s + (size_t)it.slot * kD * kD + col : nullptr;
-    float *const dm = (it.flags & GDN_ITEM_WRITE_M) ? w.cp_m + (size_t)it.slot * kD * kD + col : nullptr;
+    const int dk = p.dk, dv = p.dv;
+    if (j0 >= dk) return;
+    const bool row_v = e.i < dv, row_k = e.i < dk;
+    float *const df = (it.flags & GDN_ITEM_WRITE_FINAL) && row_v
+                          ? p.sf + ((size_t)it.seq * p.H + it.head) * dk * dv + (size_t)j0 * dv + e.i : nullptr;
+    float *const ds = (it.flags & GDN_ITEM_WRITE_SLOT) && row_v
+                          ? w.cp_s + (size_t)it.slot * dk * dv + (size_t)j0 * dv + e.i : nullptr;
+    float *const dm = (it.flags & GDN_ITEM_WRITE_M) && row_k
+                          ? w.cp_m + (size_t)it.slot * dk * dk + (size_t)j0 * dk + e.i : nullptr;
     if (df) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) df[jj * kD] = sv[jj];
+        for (int jj = 0; jj < 32; ++jj) df[jj * dv] = sv[jj];
     }
     if (ds) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) ds[jj * kD] = sv[jj];
+        for (int jj = 0; jj < 32; ++jj) ds[jj * dv] = sv[jj];
     }
     if (dm) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) dm[jj * kD] = sv[jj];
+        for (int jj = 0; jj < 32; ++jj) dm[jj * dk] = sv[jj];
     }
 }
 
@@ -548,16 +556,17 @@ __device__ __noinline__ void load_start_state32(const Ctx cx, const EpiThread e,
                                                 float *sv) {
     const Problem &p = *cx.p;
     const Workspace &w = *cx.w;
-    const int i = e.i;
-    const size_t col = (size_t)j0 * kD + i;
+    const int i = e.i, dk = p.dk, dv = p.dv;
+    const size_t col = (size_t)j0 * dv + i;
     const float *src = nullptr;
+    const bool real = i < dv && j0 < dk;   // padded rows and columns start at zero
     if (it.flags & GDN_ITEM_FROM_INITIAL)
-        src = p.s0 ? p.s0 + ((size_t)it.seq * p.H + it.head) * kD * kD + col : nullptr;
+        src = p.s0 && real ? p.s0 + ((size_t)it.seq * p.H + it.head) * dk * dv + col : nullptr;
     else if (!(it.flags & GDN_ITEM_FROM_IDENTITY) && (it.flags & GDN_ITEM_FROM_SLOT))
-        src = w.cp_s + (size_t)it.slot * kD * kD + col;
+        src = real ? w.cp_s + (size_t)it.slot * dk * dv + col : nullptr;
     const bool ident = !(it.flags & GDN_ITEM_FROM_INITIAL) && (it.flags & GDN_ITEM_FROM_IDENTITY);
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) sv[jj] = src ? src[jj * kD] : (ident && i == j0 + jj) ? 1.f : 0.f;
+    for (int jj = 0; jj < 32; ++jj) sv[jj] = src ? src[jj * dv] : (ident && i == j0 + jj) ? 1.f : 0.f;
 }
 
 // Writes the state held in TMEM (this thread's row, its 64 columns) for `it`.
@@ -799,9 +808,10 @@ __device__ __forceinline__ void add_d4(const Ctx &cx, const EpiThread &e, uint32
 __device__ __forceinline__ void output_chunk(const Ctx &cx, const EpiThread &e, int s, bool exact, uint32_t pq_col,
                              uint32_t d4_col, int t0, int len, int h) {
     const Problem &p = *cx.p;
-    const size_t rs = (size_t)p.H * kD;
-    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.o) + ((size_t)t0 * p.H + h) * kD + e.i;
+    const size_t rs = (size_t)p.H * p.dv;
+    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.o) + ((size_t)t0 * p.H + h) * p.dv + e.i;
     const uint32_t soa = COEF_ADDR(cx, s, so);
+    if (e.i >= p.dv) return;   // a padded value row
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
         float x[32];
@@ -1020,11 +1030,12 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [total_T, H, 128] bf16 rows, boxes of 64 tokens x 64 features, 128-byte swizzle;
-// returns the driver result (0 on success)
-int encode_rows(EncodeTiledFn fn, CUtensorMap *m, const void *base, int H, int total_T) {
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)total_T};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+// [total_T, H, d] bf16 rows, boxes of 64 tokens x 64 features, 128-byte
+// swizzle; with d < 128 the features past d read as zeros (the kernel always
+// loads two 64-feature halves); returns the driver result (0 on success)
+int encode_rows(EncodeTiledFn fn, CUtensorMap *m, const void *base, int H, int total_T, int d) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)total_T};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
     cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
@@ -1034,7 +1045,10 @@ int encode_rows(EncodeTiledFn fn, CUtensorMap *m, const void *base, int H, int t
 
 }  // namespace
 
-bool fused_tc_supported(int dtype, int dk, int dv) { return dtype == GDN_BF16 && dk == kD && dv == kD; }
+bool fused_tc_supported(int dtype, int dk, int dv) {
+    auto ok = [](int d) { return d == 32 || d == 64 || d == kD; };
+    return dtype == GDN_BF16 && ok(dk) && ok(dv);
+}
 
 cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s,
                             const FusedOverlap *ov) {
@@ -1053,8 +1067,8 @@ cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int 
     cuuint32_t box[2] = {64, 64};
     cuuint32_t es[2] = {1, 1};
     int r;
-    if ((r = encode_rows(fn, &maps.q, p.q, p.H, p.total_T)) || (r = encode_rows(fn, &maps.k, p.k, p.H, p.total_T)) ||
-        (r = encode_rows(fn, &maps.v, p.v, p.H, p.total_T)) ||
+    if ((r = encode_rows(fn, &maps.q, p.q, p.H, p.total_T, p.dk)) || (r = encode_rows(fn, &maps.k, p.k, p.H, p.total_T, p.dk)) ||
+        (r = encode_rows(fn, &maps.v, p.v, p.H, p.total_T, p.dv)) ||
         (r = fn(&maps.tp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.tprime, dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE))) {

@@ -145,7 +145,8 @@ cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, int gate_sca
 }  // namespace
 
 cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s, int cols, int nc) {
-    if (p.dtype == GDN_BF16 && p.dk == 128 && p.total_T > 0)
+    // (the tcgen05 inverse pads head sizes 32 and 64 to 128 with zero features)
+    if (p.dtype == GDN_BF16 && (p.dk == 32 || p.dk == 64 || p.dk == 128) && p.total_T > 0)
         return launch_inverse_tc(p, w, for_tc ? 1 : 0, cols, nc, s);
     const int smem = (kChunk * (p.dk + 1) + 2 * kChunk * 65) * (int)sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(inverse_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -76,7 +76,9 @@ typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
 typedef enum { GDN_CP_AUTO = 0, GDN_CP_OFF = 1, GDN_CP_FORCE = 2 } gdn_cp_mode;
 
 /* Which fused kernel runs: AUTO picks the tcgen05 kernel when it supports the
- * shape (bf16, dk = dv = 128) and the CUDA-core kernel otherwise. */
+ * shape (bf16 with dk, dv in {32, 64, 128}; head sizes below 128 run zero-
+ * padded to 128 inside the kernels, which is exact) and the CUDA-core kernel
+ * otherwise (fp32). */
 typedef enum { GDN_KERNEL_AUTO = 0, GDN_KERNEL_TC = 1, GDN_KERNEL_SIMT = 2 } gdn_kernel;
 
 typedef struct {
@@ -152,7 +154,7 @@ typedef struct {
     size_t chunk_totals;   /* fp32 [H, max_chunks]: sum of g per chunk (chunks in sequence order) */
     size_t head_flags;     /* int32 [N, H]: 1 when some g != 0 (alpha not identically 1) */
     size_t tprime;         /* [H, total_T, 64] T' rows by token; bf16 for bf16 inputs, fp32 for fp32.
-                              When the tcgen05 fused kernel runs (bf16, dk = dv = 128) this holds
+                              When the tcgen05 fused kernel runs (bf16) this holds
                               T' diag(c1) instead, c1_m = exp(G* - G_m) beta_m with G* the middle of
                               the chunk's gate cumsum range, or (Gamma ⊙ T') diag(beta) for a chunk
                               whose last cumsum is below -80 */

@@ -93,6 +93,15 @@ def test_plan_inverse_overlap(lib):
     assert plan(4, 8192, 32, 128, 128, 4, 0, gdn.F32, sm_count=152, inverse_overlap=7).overlap_columns == 0
 
 
+def test_plan_kernel_choice_by_head_size(lib):
+    """bf16 with head sizes 32, 64 or 128 (any pair) takes the tcgen05 kernels;
+    fp32 takes the CUDA-core ones."""
+    for dk in (32, 64, 128):
+        for dv in (32, 64, 128):
+            assert plan(2, 256, 2, dk, dv, 2, 0, gdn.BF16).kernel == gdn.KERNEL_TC
+            assert plan(2, 256, 2, dk, dv, 2, 0, gdn.F32).kernel == gdn.KERNEL_SIMT
+
+
 def test_plan_varlen_capacity_bounds(lib):
     p = plan(1, 262144, 16, 128, 128, 64, 1, gdn.BF16, sm_count=152)
     assert p.max_chunks == 262144 // 64 + 64

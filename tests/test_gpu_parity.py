@@ -97,6 +97,25 @@ def test_head_sizes_fp32(d):
     assert_close("final_state", oracle.to_f64(sf), sf_ref)
 
 
+@pytest.mark.parametrize("cp", ["off", "force"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 64), (64, 128), (32, 64), (128, 32)])
+def test_bf16_small_head_sizes_run_on_tcgen05(dk, dv, cp):
+    """bf16 head sizes 32 and 64, and mixed ones, run on the tcgen05 kernels,
+    zero-padded to 128 by the TMA (features past dk or dv read as zeros, which
+    leaves the real rows and columns of the state exact); compared with the
+    oracle.  With CP forced the correction matrices (dk x dk) and segment
+    starts (dk x dv) go through the padded state too."""
+    cfg = CONFIGS[1].scaled(B=2, T=333, H=3, dk=dk, dv=dv, s0_std=0.05)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    info = gdn.gdn_plan_query(2, 333, 3, dk, dv, 2, 0, gdn.BF16, opts_for("auto"))
+    assert info.kernel == gdn.KERNEL_TC
+    kw = dict(cp_mode=gdn.CP_OFF) if cp == "off" else dict(cp_mode=gdn.CP_FORCE, chunks_per_segment=2, sliding=0)
+    o_ref, sf_ref = full_reference(inp)
+    o, sf = gpu_run(inp, opts_for("auto", **kw))
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+
+
 def test_unequal_head_sizes():
     cfg = CONFIGS[1].scaled(B=2, T=150, H=2, dk=128, dv=64, s0_std=0.02)
     inp = to_device(make_inputs(cfg, "cpu"))
