@@ -37,6 +37,12 @@
 // tensor-memory columns, read back by the lane-quadrant warps.  All other
 // products are fp32 on CUDA cores with operands in shared memory (padded
 // strides, conflict-free), the work of each phase spread over the 16 warps.
+// T is not solved here: before the kernel, the sequence-prep kernel builds the
+// chunk table and the library's per-chunk inverse writes T' = (I + A')^-1
+// (A' = diag(beta) strictlower(K K^T), fp32) for every chunk once, and the
+// kernel takes T = Gamma ⊙ T' (the Gamma-extraction identity, exact) — the
+// substitution on two warps, repeated per chunk, value slice and sweep, was
+// ~45% of the kernel's time.
 #include <math.h>
 
 #include <algorithm>
@@ -109,6 +115,7 @@ struct BwdArgs {
     float *gq, *gk, *gv, *gg, *gbeta, *gs0;   // gradients; gq, gk, gg, gbeta: per-slice partials
                                               // when slices > 1
     float *states;                            // [slots][H][DK][dv] chunk start states
+    const float *tp;                          // [H, total_T, C] T' (no gate factors), fp32
     int *err;
     long long part_stride_k;                  // total_T * H * DK: slice stride of the dq / dk partials
     long long part_stride_t;                  // total_T * H: slice stride of the dg / dbeta partials
@@ -332,27 +339,22 @@ __device__ void tc_read_qk(float *sm, uint32_t tbase) {
     }
 }
 
-// T = (I + A)^-1 by forward substitution, one column per thread; called by
-// warps 0-1 only (the other warps work on tiles it does not touch meanwhile).
+// T = Gamma ⊙ T' (the Gamma-extraction identity: T_rm = exp(G_r - G_m) T'_rm,
+// exact) from the T' rows formed before the kernel; rows past the chunk's
+// length are identity rows (their A rows are zero).  Called by warps 0-1 only,
+// after the Gamma tile is formed; one column per thread, each load of a warp
+// 128 contiguous bytes.
 template <int DK, bool W>
-__device__ void chunk_solve(float *sm) {
+__device__ void chunk_load_t(float *sm, const float *tp_rows, int len) {
     using L = BwdSmem<DK, W>;
-    {
-        const int j = threadIdx.x;
-        const float *sA = sm + L::kA;
-        float *sT = sm + L::kT;
-        for (int r = 0; r < C; ++r) {
-            float a0 = (r == j) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-            int i = 0;
-            for (; i + 4 <= r; i += 4) {
-                a0 -= sA[r * CP + i] * sT[i * CP + j];
-                a1 -= sA[r * CP + i + 1] * sT[(i + 1) * CP + j];
-                a2 -= sA[r * CP + i + 2] * sT[(i + 2) * CP + j];
-                a3 -= sA[r * CP + i + 3] * sT[(i + 3) * CP + j];
-            }
-            for (; i < r; ++i) a0 -= sA[r * CP + i] * sT[i * CP + j];
-            sT[r * CP + j] = (a0 + a1) + (a2 + a3);
-        }
+    const int j = threadIdx.x;
+    float *sT = sm + L::kT;
+    const float *sGam = sm + L::kGam;
+#pragma unroll 4
+    for (int r = 0; r < C; ++r) {
+        float t = (r == j) ? 1.f : 0.f;
+        if (r < len && j <= r) t = sGam[r * CP + j] * __ldg(tp_rows + (size_t)r * C + j);
+        sT[r * CP + j] = t;
     }
 }
 
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         __syncthreads();
         if constexpr (TC) tc_gram<DK, TC>(sm, tbase, phase, a.err); else chunk_gram<DK, TC>(sm);
         if (warp < 2) {
-            chunk_solve<DK, TC>(sm);
+            chunk_load_t<DK, TC>(sm, a.tp + ((size_t)h * a.total_T + t0) * C, len);
         } else {
             for (int r = warp - 2; r < C; r += kBwdWarps - 2) {     // Y = K S0
                 float y = 0.f;
@@ -516,7 +518,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         __syncthreads();
         if constexpr (TC) tc_gram<DK, TC>(sm, tbase, phase, a.err); else chunk_gram<DK, TC>(sm);
         if (warp < 2) {
-            chunk_solve<DK, TC>(sm);
+            chunk_load_t<DK, TC>(sm, a.tp + ((size_t)h * a.total_T + t0) * C, len);
         } else {
             // while T is solved: Y = K S0; K dS; scale dO . (Q S0) per row
             for (int r = warp - 2; r < C; r += kBwdWarps - 2) {
@@ -835,8 +837,8 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 size_t round_up(size_t x) { return (x + 255) / 256 * 256; }
 
 struct BwdLayout {
-    size_t err, states, pdq, pdk, pdg, pdb, total;
-    int slices;
+    size_t err, states, pdq, pdk, pdg, pdb, prep, seqinfo, chunks, flags, tp, total;
+    int slices, max_chunks;
     long long total_T;
     int N;
 };
@@ -868,6 +870,21 @@ bool bwd_layout(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, int
         L->pdg = off; off = round_up(off + nt);
         L->pdb = off; off = round_up(off + nt);
     }
+    // the chunk table (sequence prep) and T' of every chunk in fp32, formed
+    // once before the backward kernel instead of a substitution per chunk,
+    // value slice and sweep
+    const long long nc_seq = ((long long)T + C - 1) / C;
+    L->max_chunks = (int)(varlen ? total_T / C + N : (long long)B * nc_seq);
+    L->prep = off;                                   // counters [8], num_chunks, num_items [4]
+    off = round_up(off + 64);
+    L->seqinfo = off;
+    off = round_up(off + (size_t)N * 16);
+    L->chunks = off;
+    off = round_up(off + (size_t)L->max_chunks * 16);
+    L->flags = off;
+    off = round_up(off + (size_t)N * H * 4);
+    L->tp = off;
+    off = round_up(off + (size_t)total_T * H * C * sizeof(float));
     L->total = off;
     return true;
 }
@@ -928,6 +945,33 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
 
     cudaError_t e = cudaMemsetAsync(a.err, 0, sizeof(int), s);
     if (e != cudaSuccess) { set_error_detail("clear error word", e); return GDN_ERR_CUDA; }
+    // the chunk table, then T' of every chunk (the kernel multiplies it by Gamma)
+    a.tp = reinterpret_cast<float *>(base + L.tp);
+    if (L.total_T > 0) {
+        Problem p = {};
+        p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.cu = cu_seqlens;
+        p.B = B; p.T = T; p.H = H; p.dk = dk; p.dv = dv; p.N = L.N; p.total_T = (int)L.total_T;
+        p.varlen = varlen; p.dtype = dtype; p.scale = a.scale;
+        Workspace w = {};
+        w.err = a.err;
+        w.counters = reinterpret_cast<int *>(base + L.prep);
+        w.num_chunks = reinterpret_cast<int *>(base + L.prep + 32);
+        w.num_items = reinterpret_cast<int *>(base + L.prep + 48);
+        w.seqinfo = reinterpret_cast<int4 *>(base + L.seqinfo);
+        w.chunks = reinterpret_cast<int4 *>(base + L.chunks);
+        w.flags = reinterpret_cast<int *>(base + L.flags);
+        w.G = reinterpret_cast<float *>(base + L.tp);   // (not read: no gate factors)
+        w.tprime = base + L.tp;
+        w.max_chunks = L.max_chunks;
+        if ((e = launch_seqprep(p, w, false, s)) != cudaSuccess) {
+            set_error_detail("launch backward sequence prep", e);
+            return GDN_ERR_CUDA;
+        }
+        if ((e = launch_inverse_f32(p, w, s)) != cudaSuccess) {
+            set_error_detail("launch backward inverse", e);
+            return GDN_ERR_CUDA;
+        }
+    }
     const bool bf = dtype == GDN_BF16;
     if (dk == 32) e = bf ? launch_bwd_t<32, __nv_bfloat16>(a, L.slices, s) : launch_bwd_t<32, float>(a, L.slices, s);
     else if (dk == 64) e = bf ? launch_bwd_t<64, __nv_bfloat16>(a, L.slices, s) : launch_bwd_t<64, float>(a, L.slices, s);

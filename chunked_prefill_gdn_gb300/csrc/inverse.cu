@@ -104,7 +104,8 @@ EncodeTiledFnInv inv_encode_fn() {
     return fn;
 }
 
-cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, int gate_scaled, int cols, int nc, cudaStream_t s) {
+cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, int gate_scaled, int cols, int nc, int f32_out,
+                              cudaStream_t s) {
     EncodeTiledFnInv fn = inv_encode_fn();
     if (!fn) {
         set_error_detail("driver entry point cuTensorMapEncodeTiled", cudaErrorNotSupported);
@@ -134,6 +135,7 @@ cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, int gate_sca
     sel.mode = cols < nc ? 1 : 0;
     sel.nc = nc;
     sel.c0 = cols;
+    sel.f32_out = f32_out;
     const long long pairs = (sel.mode ? (long long)p.N * cols : (long long)w.max_chunks) * ((p.H + 1) / 2);
     if (pairs == 0) return cudaSuccess;
     const int grid = (int)std::max(1LL, std::min<long long>(sms, pairs));
@@ -147,7 +149,7 @@ cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, int gate_sca
 cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s, int cols, int nc) {
     // (the tcgen05 inverse pads head sizes 32 and 64 to 128 with zero features)
     if (p.dtype == GDN_BF16 && (p.dk == 32 || p.dk == 64 || p.dk == 128) && p.total_T > 0)
-        return launch_inverse_tc(p, w, for_tc ? 1 : 0, cols, nc, s);
+        return launch_inverse_tc(p, w, for_tc ? 1 : 0, cols, nc, 0, s);
     const int smem = (kChunk * (p.dk + 1) + 2 * kChunk * 65) * (int)sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(inverse_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -155,6 +157,17 @@ cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cu
     e = launch_dependent(inverse_simt_kernel, grid, dim3(128), (size_t)smem, s, p, w);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// T' itself (no gate factors) as fp32 rows [H, total_T, 64], for the
+// backward pass: the tcgen05 inverse for bf16 keys, the CUDA-core one (whose
+// output follows the input type) for fp32 keys.
+cudaError_t launch_inverse_f32(const Problem &p, const Workspace &w, cudaStream_t s) {
+    if (p.total_T == 0) return cudaSuccess;
+    if (p.dtype == GDN_BF16 && (p.dk == 32 || p.dk == 64 || p.dk == 128))
+        return launch_inverse_tc(p, w, 0, 0, 0, 1, s);
+    if (p.dtype != GDN_F32) return cudaErrorNotSupported;
+    return launch_inverse(p, w, false, s);
 }
 
 }  // namespace gdn

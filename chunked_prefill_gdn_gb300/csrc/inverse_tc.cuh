@@ -176,6 +176,7 @@ __device__ __forceinline__ bool inv_wait(InvBars &b, uint64_t *bar, uint32_t par
 struct InvSel {
     int mode, nc, c0, cta, ctas;
     int *ready;
+    int f32_out;   // 1: store T' itself (no gate factors) as fp32 rows [H, total_T, 64]
 };
 
 struct PairInfo {
@@ -323,6 +324,7 @@ __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const P
         };
         // gate cumsum of this row, and the chunk's first and last (for c1)
         auto gate_of = [&](const PairInfo &q) {
+            if (!gate_scaled) return make_float3(0.f, 0.f, 0.f);   // (no gate factors: G unread)
             const int hd = half ? q.h1 : q.h0;
             const float *Gh = w.G + (size_t)hd * p.total_T + q.t0;
             return make_float3(Gh[min(r, q.len - 1)], Gh[0], Gh[q.len - 1]);
@@ -416,6 +418,33 @@ __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const P
             if (exact) {
                 Gc[0] = Gh[min(j, len - 1)];
                 Gc[1] = Gh[min(32 + j, len - 1)];
+            }
+            if (sel.f32_out) {
+                // T' as fp32 rows: column j over rows 0..63, then column 32 + j over
+                // rows 32..63 (zero above); each store of a warp covers 128
+                // contiguous bytes of one row
+                float *rows = reinterpret_cast<float *>(w.tprime) + ((size_t)un.z * p.total_T + un.x) * kChunk;
+                solve_blocked(A, xcol, j, 0);
+                uint32_t v[64];
+                tc::tmem_ld32(xcol, v);
+                tc::tmem_ld32(xcol + 32, v + 32);
+                tc::tmem_wait_ld();
+                if (store) {
+#pragma unroll
+                    for (int r = 0; r < 64; ++r)
+                        if (r < len) rows[(size_t)r * kChunk + j] = __uint_as_float(v[r]);
+                }
+                solve_blocked(A, xcol, 32 + j, 2);
+                tc::tmem_ld32(xcol + 32, v + 32);
+                tc::tmem_wait_ld();
+                if (store) {
+#pragma unroll
+                    for (int r = 0; r < 64; ++r)
+                        if (r < len) rows[(size_t)r * kChunk + 32 + j] = r < 32 ? 0.f : __uint_as_float(v[r]);
+                }
+                __syncwarp();
+                tc::mbar_arrive(&b.aempty[s]);
+                continue;
             }
             // pass A: column j over rows 0..63 -> x in columns xcol .. xcol+63;
             // then scaled and packed to bf16 pairs of rows in columns xcol .. xcol+31
