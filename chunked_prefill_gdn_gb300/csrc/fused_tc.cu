@@ -1047,13 +1047,14 @@ int encode_rows(EncodeTiledFn fn, CUtensorMap *m, const void *base, int H, int t
 
 bool fused_tc_supported(int dtype, int dk, int dv) {
     auto ok = [](int d) { return d == 32 || d == 64 || d == kD; };
-    return dtype == GDN_BF16 && ok(dk) && ok(dv);
+    return (dtype == GDN_BF16 && ok(dk) && ok(dv)) || fused_tf32_supported(dtype, dk, dv);
 }
 
 cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s,
                             const FusedOverlap *ov) {
     if (!fused_tc_supported(p.dtype, p.dk, p.dv)) return cudaErrorNotSupported;
     if (p.total_T == 0) return launch_fused_simt(p, w, pass, grid, s);  // only empty sequences: nothing to tile
+    if (p.dtype == GDN_F32) return launch_fused_tf32(p, w, pass, grid, s);
     EncodeTiledFn fn = encode_fn();
     if (!fn) {
         set_error_detail("driver entry point cuTensorMapEncodeTiled", cudaErrorNotSupported);

@@ -175,7 +175,8 @@ gdn_status make_plan(int B, int T, int H, int dk, int dv, int n_seqs, int varlen
     // the inverse of the last chunk columns inside the fused pass (equal
     // sequences without a split, tcgen05 kernels, idle SMs)
     int ov_cols = 0, ov_ctas = 0;
-    if (kernel == GDN_KERNEL_TC && !cp && !varlen && opts.inverse_overlap > 0 && units < sms && nc_seq > 0) {
+    if (kernel == GDN_KERNEL_TC && dtype == GDN_BF16 && !cp && !varlen && opts.inverse_overlap > 0 && units < sms &&
+        nc_seq > 0) {
         ov_cols = (int)std::min<long long>(opts.inverse_overlap, nc_seq);
         ov_ctas = sms - units;
     }

@@ -114,7 +114,10 @@ struct FusedOverlap {
 
 cudaError_t launch_fused_tc(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s,
                             const FusedOverlap *ov = nullptr);
+// bf16: the kernel above; fp32: the kind::tf32 kernel (launch_fused_tc dispatches)
 bool fused_tc_supported(int dtype, int dk, int dv);
+bool fused_tf32_supported(int dtype, int dk, int dv);
+cudaError_t launch_fused_tf32(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s);
 int fused_simt_smem_bytes(int dk, int dv);
 
 // Called once per CTA of a persistent pass after it found the queue empty: the

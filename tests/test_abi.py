@@ -94,12 +94,13 @@ def test_plan_inverse_overlap(lib):
 
 
 def test_plan_kernel_choice_by_head_size(lib):
-    """bf16 with head sizes 32, 64 or 128 (any pair) takes the tcgen05 kernels;
-    fp32 takes the CUDA-core ones."""
+    """Head sizes 32, 64 or 128 (any pair) take the tcgen05 kernels: kind::f16
+    for bf16, kind::tf32 for fp32; the CUDA-core kernel only when asked."""
     for dk in (32, 64, 128):
         for dv in (32, 64, 128):
             assert plan(2, 256, 2, dk, dv, 2, 0, gdn.BF16).kernel == gdn.KERNEL_TC
-            assert plan(2, 256, 2, dk, dv, 2, 0, gdn.F32).kernel == gdn.KERNEL_SIMT
+            assert plan(2, 256, 2, dk, dv, 2, 0, gdn.F32).kernel == gdn.KERNEL_TC
+            assert plan(2, 256, 2, dk, dv, 2, 0, gdn.F32, kernel=gdn.KERNEL_SIMT).kernel == gdn.KERNEL_SIMT
 
 
 def test_plan_varlen_capacity_bounds(lib):

@@ -116,6 +116,27 @@ def test_bf16_small_head_sizes_run_on_tcgen05(dk, dv, cp):
     assert_close("final_state", oracle.to_f64(sf), sf_ref)
 
 
+@pytest.mark.parametrize("cp", ["off", "force"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 64), (128, 128), (32, 128), (128, 64)])
+def test_fp32_runs_on_tcgen05_tf32(dk, dv, cp):
+    """fp32 inputs run on the kind::tf32 kernel (the plan reports the tcgen05
+    kernel), compared with the oracle over several chunks, a ragged last chunk,
+    an initial state and, with CP forced, the correction matrices and segment
+    starts; and with the CUDA-core kernel on the same inputs."""
+    cfg = CONFIGS[0].scaled(B=2, T=333, H=3, dk=dk, dv=dv, s0_std=0.1)
+    inp = to_device(make_inputs(cfg, "cpu"))
+    info = gdn.gdn_plan_query(2, 333, 3, dk, dv, 2, 0, gdn.F32, opts_for("auto"))
+    assert info.kernel == gdn.KERNEL_TC
+    kw = dict(cp_mode=gdn.CP_OFF) if cp == "off" else dict(cp_mode=gdn.CP_FORCE, chunks_per_segment=2, sliding=0)
+    o_ref, sf_ref = full_reference(inp)
+    o, sf = gpu_run(inp, opts_for("auto", **kw))
+    assert_close("o", oracle.to_f64(o).reshape(o_ref.shape), o_ref)
+    assert_close("final_state", oracle.to_f64(sf), sf_ref)
+    o_si, sf_si = gpu_run(inp, opts_for("simt", **kw))
+    assert_close("o vs CUDA-core", oracle.to_f64(o), oracle.to_f64(o_si))
+    assert_close("final_state vs CUDA-core", oracle.to_f64(sf), oracle.to_f64(sf_si))
+
+
 def test_unequal_head_sizes():
     cfg = CONFIGS[1].scaled(B=2, T=150, H=2, dk=128, dv=64, s0_std=0.02)
     inp = to_device(make_inputs(cfg, "cpu"))
