@@ -34,6 +34,7 @@ __all__ = [
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
     "gdn_chunk_fwd_static", "gdn_qk_l2norm", "qk_l2norm", "gdn_qk_l2norm_bwd", "qk_l2norm_backward",
     "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd", "gdn_chunk_bwd_check", "chunk_bwd",
+    "gdn_set_backward_kernel", "gdn_get_backward_kernel",
     "chunk_gated_delta_rule",
     "gdn_status_string", "gdn_version", "gdn_last_error_detail", "chunk_fwd", "chunk_fwd_host", "workspace_for", "GdnError",
     "CP_AUTO", "CP_OFF", "CP_FORCE", "KERNEL_AUTO", "KERNEL_TC", "KERNEL_SIMT", "BF16", "F32",
@@ -140,6 +141,10 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_chunk_bwd.restype = i32
     lib.gdn_chunk_bwd_check.argtypes = [vp, vp]
     lib.gdn_chunk_bwd_check.restype = i32
+    lib.gdn_set_backward_kernel.argtypes = [i32]
+    lib.gdn_set_backward_kernel.restype = i32
+    lib.gdn_get_backward_kernel.argtypes = []
+    lib.gdn_get_backward_kernel.restype = i32
     lib.gdn_chunk_transition_workspace_size.argtypes = [i32] * 8
     lib.gdn_chunk_transition_workspace_size.restype = sz
     lib.gdn_chunk_transition.argtypes = [vp, vp, vp, vp, vp, i32] + [i32] * 6 + [vp, vp, vp, sz, vp]
@@ -262,6 +267,18 @@ def gdn_chunk_bwd(*args) -> int:
 
 def gdn_chunk_bwd_check(workspace_ptr, stream_ptr) -> int:
     return int(load_library().gdn_chunk_bwd_check(workspace_ptr, stream_ptr))
+
+
+def gdn_set_backward_kernel(kernel) -> None:
+    """KERNEL_AUTO / KERNEL_TC: the tensor-core backward (default);
+    KERNEL_SIMT: the CUDA-core backward.  Process-wide, for later calls."""
+    st = int(load_library().gdn_set_backward_kernel(int(kernel)))
+    if st != 0:
+        raise GdnError(st, "gdn_set_backward_kernel")
+
+
+def gdn_get_backward_kernel() -> int:
+    return int(load_library().gdn_get_backward_kernel())
 
 
 def gdn_chunk_transition_workspace_size(B, T, H, dk, dv, n_seqs, varlen, dtype) -> int:

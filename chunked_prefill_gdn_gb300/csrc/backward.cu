@@ -46,6 +46,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "gdn_internal.cuh"
@@ -832,12 +833,15 @@ cudaError_t launch_reduce(const float *part, float *out, long long n, long long 
     return cudaGetLastError();
 }
 
+std::atomic<int> g_bwd_kernel{GDN_KERNEL_AUTO};
+
 bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 size_t round_up(size_t x) { return (x + 255) / 256 * 256; }
 
 struct BwdLayout {
     size_t err, states, pdq, pdk, pdg, pdb, prep, seqinfo, chunks, flags, tp, total;
+    size_t dst, ry, rqs, ru, rdb, rkds;   // the tensor-core backward's intermediates (over the partials)
     int slices, max_chunks;
     long long total_T;
     int N;
@@ -861,6 +865,9 @@ bool bwd_layout(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, int
     off = round_up(off + sizeof(int));
     L->states = off;
     off = round_up(off + (size_t)slots * H * dk * dv * sizeof(float));
+    // the CUDA-core kernel's per-slice partials and the tensor-core kernels'
+    // intermediates share one region (a call uses one of them)
+    const size_t shared0 = off;
     L->pdq = L->pdk = L->pdg = L->pdb = 0;
     if (L->slices > 1) {
         const size_t nk = (size_t)L->slices * total_T * H * dk * sizeof(float);
@@ -870,6 +877,16 @@ bool bwd_layout(int B, int T, int H, int dk, int dv, int n_seqs, int varlen, int
         L->pdg = off; off = round_up(off + nt);
         L->pdb = off; off = round_up(off + nt);
     }
+    const size_t end_partials = off;
+    off = shared0;
+    L->dst = off; off = round_up(off + (size_t)slots * H * dk * dv * sizeof(float));
+    const size_t rows = (size_t)total_T * H * dv * sizeof(float);
+    L->ry = off; off = round_up(off + rows);
+    L->rqs = off; off = round_up(off + rows);
+    L->ru = off; off = round_up(off + rows);
+    L->rdb = off; off = round_up(off + rows);
+    L->rkds = off; off = round_up(off + rows);
+    off = std::max(off, end_partials);
     // the chunk table (sequence prep) and T' of every chunk in fp32, formed
     // once before the backward kernel instead of a substitution per chunk,
     // value slice and sweep
@@ -973,6 +990,32 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
         }
     }
     const bool bf = dtype == GDN_BF16;
+    if (g_bwd_kernel.load() != GDN_KERNEL_SIMT) {
+        if (L.total_T == 0 && !d_initial_state) return GDN_OK;
+        BwdTcArgs t = {};
+        t.q = q; t.k = k; t.v = v; t.dout = d_o;
+        t.g = g; t.beta = beta; t.s0 = initial_state; t.dsf = d_final_state; t.cu = cu_seqlens;
+        t.tp = a.tp;
+        t.chunks = reinterpret_cast<const int4 *>(base + L.chunks);
+        t.num_chunks = reinterpret_cast<const int *>(base + L.prep + 32);
+        t.s0t = a.states;
+        t.dst = reinterpret_cast<float *>(base + L.dst);
+        t.ry = reinterpret_cast<float *>(base + L.ry);
+        t.rqs = reinterpret_cast<float *>(base + L.rqs);
+        t.ru = reinterpret_cast<float *>(base + L.ru);
+        t.rdb = reinterpret_cast<float *>(base + L.rdb);
+        t.rkds = reinterpret_cast<float *>(base + L.rkds);
+        t.gq = dq; t.gk = dk_out; t.gv = dv_out; t.gg = dg; t.gbeta = dbeta; t.gs0 = d_initial_state;
+        t.err = a.err;
+        t.T = T; t.H = H; t.dk = dk; t.dv = dv; t.N = L.N; t.total_T = (int)L.total_T; t.varlen = varlen;
+        t.dtype = dtype;
+        t.scale = a.scale;
+        if ((e = launch_bwd_tc(t, L.total_T > 0 ? L.max_chunks : 0, s)) != cudaSuccess) {
+            set_error_detail("launch tensor-core backward", e);
+            return GDN_ERR_CUDA;
+        }
+        return GDN_OK;
+    }
     if (dk == 32) e = bf ? launch_bwd_t<32, __nv_bfloat16>(a, L.slices, s) : launch_bwd_t<32, float>(a, L.slices, s);
     else if (dk == 64) e = bf ? launch_bwd_t<64, __nv_bfloat16>(a, L.slices, s) : launch_bwd_t<64, float>(a, L.slices, s);
     else e = bf ? launch_bwd_t<128, __nv_bfloat16>(a, L.slices, s) : launch_bwd_t<128, float>(a, L.slices, s);
@@ -995,6 +1038,14 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
     }
     return GDN_OK;
 }
+
+gdn_status gdn_set_backward_kernel(gdn_kernel kernel) {
+    if (kernel != GDN_KERNEL_AUTO && kernel != GDN_KERNEL_TC && kernel != GDN_KERNEL_SIMT) return GDN_ERR_INVALID_ARG;
+    g_bwd_kernel.store(kernel);
+    return GDN_OK;
+}
+
+gdn_kernel gdn_get_backward_kernel(void) { return static_cast<gdn_kernel>(g_bwd_kernel.load()); }
 
 gdn_status gdn_chunk_bwd_check(const void *workspace, gdn_stream_t stream) {
     return gdn_chunk_fwd_check(workspace, stream);

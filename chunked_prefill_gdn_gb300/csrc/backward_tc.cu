@@ -1,0 +1,978 @@
+// Tensor-core backward of the chunked GDN forward (tcgen05, kind::tf32): the
+// gradients of q, k, v, g, beta and the initial state from those of o and of
+// the final state.  The algebra is the chain rule through one chunk of the WY
+// form (the backward paragraph of the talk "Qwen系列模型线性注意力高性能优化实践";
+// math orientation, S dv x dk, start state S0, end-state gradient dS, chunk-local
+// G = cumsum g, gamma = exp(G), Gamma_rm = exp(G_r - G_m), e = gamma_C / gamma):
+//
+//   forward   Y = K S0^T, X = D_gamma Y, B = diag(beta)(V - X), U = T B,
+//             M = Gamma ⊙ tril(Q K^T), S_C = gamma_C S0 + U^T D_e K
+//   backward  dU = scale M^T dO + D_e K dS^T,  dB = T^T dU,  dv = diag(beta) dB,
+//             dS0 = gamma_C dS + scale dO^T D_gamma Q - dB^T D_gamma diag(beta) K,
+//             dM = scale dO U^T (lower),  dA = -dB U^T (strictly lower),
+//             P = dA ⊙ Gamma ⊙ beta_r,  R = dM ⊙ Gamma,
+//             dK = (P + P^T) K + R^T Q + D_gamma dX S0 + D_e U dS   (dX = -diag(beta) dB)
+//             dQ = R K + scale D_gamma dO S0,
+//             dbeta and dG from every place beta and G enter (dg: the reverse
+//             cumsum of dG inside the chunk)
+//
+// Two kernels.  The chain kernel (one CTA per (head, sequence)) carries the
+// state forward over the chunks (storing each chunk's start state transposed,
+// and the rows of K S0^T, Q S0^T and U), then the state gradient back (storing
+// each chunk's end-state gradient transposed and the rows of dB and K dS^T,
+// and writing dv and the initial state's gradient).  The chunk kernel (one CTA
+// per (chunk, head), all independent) reads those and forms dq, dk, dg, dbeta.
+// Every product is a tcgen05 MMA of M = 128 with fp32 operands read as tf32 and
+// fp32 accumulation; the 128-wide dimension (value rows in the chain kernel, key
+// columns in the chunk kernel) runs along the TMEM lanes, padded with zeros
+// for head sizes 32 and 64.  Operands are staged by the CTA's threads as
+// 128-byte-swizzled K-major fp32 tiles; T = Gamma ⊙ T' comes from the T' of the
+// per-chunk inverse (Gamma-extraction identity).  Every wait on an MMA is
+// bounded: on timeout the kernels record GDN_ERR_TIMEOUT and return.
+#include <math.h>
+
+#include <type_traits>
+
+#include "gdn_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace gdn {
+
+using namespace tc;
+
+namespace {
+
+constexpr int kBT = 256;                      // threads: warps w and w + 4 share TMEM lane quadrant w
+constexpr uint64_t kBtTimeoutNs = 2000000000ull;
+constexpr uint32_t kBlk128 = 16384;           // block stride of a 128-row fp32 tile
+constexpr uint32_t kBlk64 = 8192;             // block stride of a 64-row fp32 tile
+
+struct BtCoef {
+    float G[64], beta[64], gam[64], e[64];    // rows past the chunk: g = beta = 0 (G repeats the last)
+};
+
+template <typename TI>
+__device__ __forceinline__ float4 ld4(const TI *p);
+template <>
+__device__ __forceinline__ float4 ld4<float>(const float *p) {
+    return __ldg(reinterpret_cast<const float4 *>(p));
+}
+template <>
+__device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+    return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+}
+template <typename TI>
+__device__ __forceinline__ float ld1(const TI *p) {
+    if constexpr (std::is_same<TI, float>::value) return __ldg(p);
+    else return __bfloat162float(*p);
+}
+
+__device__ __forceinline__ void sts_f4(uint32_t a, float x, float y, float z, float w) {
+    sts_u4(a, make_uint4(__float_as_uint(x), __float_as_uint(y), __float_as_uint(z), __float_as_uint(w)));
+}
+__device__ __forceinline__ void sts_f32(uint32_t a, float x) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(x) : "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// Gate and beta coefficients of a chunk (warp 0): inclusive scans of g over
+// both halves, rows past len with g = 0.
+__device__ __forceinline__ void chunk_coef(BtCoef *cf, const float *g, const float *b, int t0, int len, int H,
+                                           int h) {
+    const int lane = threadIdx.x & 31;
+    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+    if (lane < len) {
+        g0 = g[(size_t)(t0 + lane) * H + h];
+        b0 = b[(size_t)(t0 + lane) * H + h];
+    }
+    if (32 + lane < len) {
+        g1 = g[(size_t)(t0 + 32 + lane) * H + h];
+        b1 = b[(size_t)(t0 + 32 + lane) * H + h];
+    }
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y0 = __shfl_up_sync(0xffffffffu, g0, off);
+        const float y1 = __shfl_up_sync(0xffffffffu, g1, off);
+        if (lane >= off) { g0 += y0; g1 += y1; }
+    }
+    g1 += __shfl_sync(0xffffffffu, g0, 31);
+    const float glast = __shfl_sync(0xffffffffu, g1, 31);
+    cf->G[lane] = g0;
+    cf->G[32 + lane] = g1;
+    cf->gam[lane] = expf(g0);
+    cf->gam[32 + lane] = expf(g1);
+    cf->e[lane] = expf(glast - g0);
+    cf->e[32 + lane] = expf(glast - g1);
+    cf->beta[lane] = b0;
+    cf->beta[32 + lane] = b1;
+}
+
+// Tile rows row0 + r (r < 64) = f(r) x[t0 + r][0, d); zero past len.
+template <typename TI, typename F>
+__device__ __forceinline__ void tile_rows(uint32_t tile, uint32_t block, int row0, const TI *x, int t0, int len,
+                                          int H, int h, int d, F f) {
+    const int d4 = d >> 2;
+    for (int idx = threadIdx.x; idx < 64 * d4; idx += kBT) {
+        const int r = idx / d4, c4 = idx - r * d4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < len) {
+            v = ld4<TI>(x + ((size_t)(t0 + r) * H + h) * d + 4 * c4);
+            const float s = f(r);
+            v.x *= s; v.y *= s; v.z *= s; v.w *= s;
+        }
+        sts_f4(tile + f32_tile_off(row0 + r, 4 * c4, block), v.x, v.y, v.z, v.w);
+    }
+}
+
+// Tile row j < rows, columns r < 64: f(r) x[t0 + r][j] (zero for j >= d or
+// r >= len).  Lanes take consecutive j, so the reads of a token row coalesce.
+template <typename TI, typename F>
+__device__ __forceinline__ void tile_cols(uint32_t tile, uint32_t block, int rows, const TI *x, int t0, int len,
+                                          int H, int h, int d, F f) {
+    for (int idx = threadIdx.x; idx < rows * 16; idx += kBT) {
+        const int r4 = idx / rows, j = idx - r4 * rows;
+        float e[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = 4 * r4 + u;
+            e[u] = (j < d && r < len) ? f(r) * ld1<TI>(x + ((size_t)(t0 + r) * H + h) * d + j) : 0.f;
+        }
+        sts_f4(tile + f32_tile_off(j, 4 * r4, block), e[0], e[1], e[2], e[3]);
+    }
+}
+
+// T = Gamma ⊙ T' rows [n][m] (fwd) or transposed [r][n] = T[n][r] (rev), from
+// T' rows (row n at tp + 64 n, entries past the chunk not read).
+__device__ __forceinline__ void tile_t(uint32_t tile, const float *tp, int len, const float *G) {
+    for (int idx = threadIdx.x; idx < 64 * 16; idx += kBT) {
+        const int n = idx >> 4, m4 = (idx & 15) * 4;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (n < len && m4 <= n) {
+            const float4 t = __ldg(reinterpret_cast<const float4 *>(tp + (size_t)n * 64 + m4));
+            const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (m4 + u <= n) x[u] = tv[u] * expf(G[n] - G[m4 + u]);
+        }
+        sts_f4(tile + f32_tile_off(n, m4, kBlk64), x[0], x[1], x[2], x[3]);
+    }
+}
+__device__ __forceinline__ void tile_t_transposed(uint32_t tile, const float *tp, int len, const float *G) {
+    for (int idx = threadIdx.x; idx < 64 * 16; idx += kBT) {
+        const int n4 = idx >> 6, r = idx & 63;
+        float x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int n = 4 * n4 + u;
+            x[u] = (n < len && r <= n) ? __ldg(tp + (size_t)n * 64 + r) * expf(G[n] - G[r]) : 0.f;
+        }
+        sts_f4(tile + f32_tile_off(r, 4 * n4, kBlk64), x[0], x[1], x[2], x[3]);
+    }
+}
+
+struct One {
+    __device__ float operator()(int) const { return 1.f; }
+};
+
+__device__ __forceinline__ bool bt_wait(uint64_t *bar, uint32_t parity, int *abort) {
+    const bool ok = mbar_wait(bar, parity, abort, kBtTimeoutNs);
+    return !__syncthreads_or(!ok);
+}
+
+// Sequence bounds of sequence n; false (and the error recorded) for bad cu_seqlens.
+__device__ __forceinline__ bool seq_bounds(const BwdTcArgs &a, int n, int &t_begin, int &len_seq) {
+    if (a.varlen) {
+        const int c0 = a.cu[n], c1 = a.cu[n + 1];
+        if (c0 < 0 || c1 < c0 || c1 > a.total_T || (n == 0 && c0 != 0) || (n == a.N - 1 && c1 != a.total_T)) {
+            if (threadIdx.x == 0) report_error(a.err, GDN_ERR_DEVICE_CHECK);
+            return false;
+        }
+        t_begin = c0;
+        len_seq = c1 - c0;
+    } else {
+        t_begin = n * a.T;
+        len_seq = a.T;
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ chain kernel
+// shared memory (1024-byte aligned offsets)
+constexpr uint32_t kA_KQ = 0;         // [K;Q] rows (64 KB); reverse: scale gamma Q^T, then -gamma beta K^T (32 KB each)
+constexpr uint32_t kA_AV = 65536;     // A tile [128 value rows][64]: B^T, U^T / dU^T, dB^T
+constexpr uint32_t kA_TT = 98304;     // T [n][m] (forward), T^T [r][n] (reverse)
+constexpr uint32_t kA_MT = 114688;    // M^T [n][r] (reverse)
+constexpr uint32_t kA_X = 131072;     // decay-scaled K^T [j][r] (forward), dO^T [i][r] (reverse)
+constexpr uint32_t kA_Small = 163840;
+
+struct ChainSmall {
+    BtCoef cf;
+    uint64_t bar[4];
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr uint32_t kChainSmem = kA_Small + sizeof(ChainSmall) + 1024;
+
+// TMEM columns
+constexpr uint32_t tS = 0;     // state (forward), state gradient (reverse): [value row][key column]
+constexpr uint32_t tP = 128;   // [S K^T | S Q^T]
+constexpr uint32_t tU = 256;   // U^T (forward), dS K^T (reverse)
+constexpr uint32_t tQK = 320;  // [K K^T; Q K^T]
+constexpr uint32_t tDU = 384;  // dO^T M
+constexpr uint32_t tDB = 448;  // dB^T
+
+template <typename TI>
+__global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_constant__ BwdTcArgs a) {
+    const int h = blockIdx.x, n = blockIdx.y;
+    int t_begin, len_seq;
+    if (!seq_bounds(a, n, t_begin, len_seq)) return;   // uniform over the CTA
+    extern __shared__ uint8_t bt_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(bt_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    ChainSmall *sm = reinterpret_cast<ChainSmall *>(smem + kA_Small);
+    BtCoef *cf = &sm->cf;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int li = quad * 32 + lane;
+    if (warp == 0) {
+        tmem_alloc(&sm->tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        for (int b = 0; b < 4; ++b) mbar_init(&sm->bar[b], 1);
+        sm->abort = 0;
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = sm->tmem_base;
+    const uint32_t tl = tb + ((uint32_t)(quad * 32) << 16);
+    const int H = a.H, dk = a.dk, dv = a.dv;
+    const TI *qg = static_cast<const TI *>(a.q);
+    const TI *kg = static_cast<const TI *>(a.k);
+    const TI *vg = static_cast<const TI *>(a.v);
+    const TI *og = static_cast<const TI *>(a.dout);
+    const uint64_t dKQ = smem_desc_sw128(sb + kA_KQ, 16, 1024);
+    const uint64_t dKT2 = smem_desc_sw128(sb + kA_KQ + 32768, 16, 1024);
+    const uint64_t dAV = smem_desc_sw128(sb + kA_AV, 16, 1024);
+    const uint64_t dTT = smem_desc_sw128(sb + kA_TT, 16, 1024);
+    const uint64_t dMT = smem_desc_sw128(sb + kA_MT, 16, 1024);
+    const uint64_t dX = smem_desc_sw128(sb + kA_X, 16, 1024);
+    const uint32_t I64 = idesc_tf32_f32(128, 64), I128 = idesc_tf32_f32(128, 128), IDK = idesc_tf32_f32(128, dk);
+    uint32_t ph[4] = {0u, 0u, 0u, 0u};
+    bool failed = false;
+    const int nc = (len_seq + kChunk - 1) / kChunk;
+    const float scale = a.scale;
+
+    // ---------------- forward sweep: the start state of every chunk ----------------
+    for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+        uint32_t r[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int j = c0 + u;
+            const float x = (a.s0 && li < dv && j < dk) ? a.s0[(((size_t)n * H + h) * dk + j) * dv + li] : 0.f;
+            r[u] = __float_as_uint(x);
+        }
+        tmem_st32(tl + tS + c0, r);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    for (int c = 0; c < nc; ++c) {
+        const int t0 = t_begin + c * kChunk, len = min(kChunk, t_begin + len_seq - t0);
+        const size_t slot = (size_t)(t0 / kChunk + n);
+        if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
+        {   // this chunk's start state, transposed ([key][value]), to the workspace
+            float *dst = a.s0t + (slot * H + h) * (size_t)dk * dv;
+            for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tl + tS + c0, r);
+                tmem_wait_ld();
+                if (li < dv) {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u)
+                        if (c0 + u < dk) dst[(size_t)(c0 + u) * dv + li] = __uint_as_float(r[u]);
+                }
+            }
+        }
+        tile_rows<TI>(sb + kA_KQ, kBlk128, 0, kg, t0, len, H, h, dk, One());
+        tile_rows<TI>(sb + kA_KQ, kBlk128, 64, qg, t0, len, H, h, dk, One());
+        __syncthreads();  // coefficients
+        tile_t(sb + kA_TT, a.tp + ((size_t)h * a.total_T + t0) * kChunk, len, cf->G);
+        tile_cols<TI>(sb + kA_X, kBlk128, dk, kg, t0, len, H, h, dk, [cf](int r) { return cf->e[r]; });
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < dk / 8; ++kk)
+                    mma_ts_tf32(tb + tP, tb + tS + 8 * kk, f32_desc_kstep(dKQ, kk, kBlk128), I128, kk > 0);
+                tc_commit(&sm->bar[0]);
+            }
+            __syncwarp();
+        }
+        float vv[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int r = 32 * half + u;
+            vv[u] = (li < dv && r < len) ? ld1<TI>(vg + ((size_t)(t0 + r) * H + h) * dv + li) : 0.f;
+        }
+        if (!bt_wait(&sm->bar[0], ph[0] & 1u, &sm->abort)) { failed = true; break; }
+        ++ph[0];
+        tc_fence_after();
+        {
+            uint32_t pk[32], pq[32];
+            tmem_ld32(tl + tP + 32 * half, pk);
+            tmem_ld32(tl + tP + 64 + 32 * half, pq);
+            tmem_wait_ld();
+            if (li < dv) {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int r = 32 * half + u;
+                    if (r < len) {
+                        const size_t o = ((size_t)(t0 + r) * H + h) * dv + li;
+                        a.ry[o] = __uint_as_float(pk[u]);
+                        a.rqs[o] = __uint_as_float(pq[u]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                float x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int r = 32 * half + 4 * c4 + u;
+                    x[u] = cf->beta[r] * (vv[4 * c4 + u] - cf->gam[r] * __uint_as_float(pk[4 * c4 + u]));
+                }
+                sts_f4(sb + kA_AV + f32_tile_off(li, 32 * half + 4 * c4, kBlk128), x[0], x[1], x[2], x[3]);
+            }
+        }
+        {   // S <- gamma_C S (the MMA that read S is complete)
+            const float gC = cf->gam[len - 1];
+            for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tl + tS + c0, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(gC * __uint_as_float(r[u]));
+                tmem_st32(tl + tS + c0, r);
+            }
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss_tf32(tb + tU, f32_desc_kstep(dAV, kk, kBlk128), f32_desc_kstep(dTT, kk, kBlk64), I64,
+                                kk > 0);
+                tc_commit(&sm->bar[1]);
+            }
+            __syncwarp();
+        }
+        if (!bt_wait(&sm->bar[1], ph[1] & 1u, &sm->abort)) { failed = true; break; }
+        ++ph[1];
+        tc_fence_after();
+        {
+            uint32_t u32[32];
+            tmem_ld32(tl + tU + 32 * half, u32);
+            tmem_wait_ld();
+            if (li < dv) {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int r = 32 * half + u;
+                    if (r < len) a.ru[((size_t)(t0 + r) * H + h) * dv + li] = __uint_as_float(u32[u]);
+                }
+            }
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+                sts_u4(sb + kA_AV + f32_tile_off(li, 32 * half + 4 * c4, kBlk128),
+                       make_uint4(u32[4 * c4], u32[4 * c4 + 1], u32[4 * c4 + 2], u32[4 * c4 + 3]));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss_tf32(tb + tS, f32_desc_kstep(dAV, kk, kBlk128), f32_desc_kstep(dX, kk, kBlk128), IDK, 1);
+                tc_commit(&sm->bar[2]);
+            }
+            __syncwarp();
+        }
+        if (!bt_wait(&sm->bar[2], ph[2] & 1u, &sm->abort)) { failed = true; break; }
+        ++ph[2];
+        tc_fence_after();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+
+    // ---------------- reverse sweep: the state gradient back to the start ----------------
+    if (!failed) {
+        for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+            uint32_t r[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int j = c0 + u;
+                const float x = (a.dsf && li < dv && j < dk) ? a.dsf[(((size_t)n * H + h) * dk + j) * dv + li] : 0.f;
+                r[u] = __float_as_uint(x);
+            }
+            tmem_st32(tl + tS + c0, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    for (int c = nc - 1; c >= 0 && !failed; --c) {
+        const int t0 = t_begin + c * kChunk, len = min(kChunk, t_begin + len_seq - t0);
+        const size_t slot = (size_t)(t0 / kChunk + n);
+        if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
+        {   // this chunk's end-state gradient, transposed, to the workspace
+            float *dst = a.dst + (slot * H + h) * (size_t)dk * dv;
+            for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tl + tS + c0, r);
+                tmem_wait_ld();
+                if (li < dv) {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u)
+                        if (c0 + u < dk) dst[(size_t)(c0 + u) * dv + li] = __uint_as_float(r[u]);
+                }
+            }
+        }
+        tile_rows<TI>(sb + kA_KQ, kBlk128, 0, kg, t0, len, H, h, dk, One());
+        tile_rows<TI>(sb + kA_KQ, kBlk128, 64, qg, t0, len, H, h, dk, One());
+        tile_cols<TI>(sb + kA_X, kBlk128, 128, og, t0, len, H, h, dv, One());   // dO^T, rows past dv zero
+        __syncthreads();  // coefficients
+        tile_t_transposed(sb + kA_TT, a.tp + ((size_t)h * a.total_T + t0) * kChunk, len, cf->G);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < dk / 8; ++kk)      // dS K^T
+                    mma_ts_tf32(tb + tU, tb + tS + 8 * kk, f32_desc_kstep(dKQ, kk, kBlk128), I64, kk > 0);
+                for (int kk = 0; kk < dk / 8; ++kk)      // [K;Q] K^T
+                    mma_ss_tf32(tb + tQK, f32_desc_kstep(dKQ, kk, kBlk128), f32_desc_kstep(dKQ, kk, kBlk128), I64,
+                                kk > 0);
+                tc_commit(&sm->bar[0]);
+            }
+            __syncwarp();
+        }
+        if (!bt_wait(&sm->bar[0], ph[0] & 1u, &sm->abort)) { failed = true; break; }
+        ++ph[0];
+        tc_fence_after();
+        {
+            uint32_t x[32];
+            tmem_ld32(tl + tU + 32 * half, x);
+            tmem_wait_ld();
+            if (li < dv) {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int r = 32 * half + u;
+                    if (r < len) a.rkds[((size_t)(t0 + r) * H + h) * dv + li] = __uint_as_float(x[u]);
+                }
+            }
+        }
+        if (quad >= 2) {   // M^T [m][r] = Gamma ⊙ tril(Q K^T) [r][m], row r = lane - 64 of Q K^T
+            uint32_t qk[32];
+            tmem_ld32(tl + tQK + 32 * half, qk);
+            tmem_wait_ld();
+            const int r = li - 64;
+            const float Gr = cf->G[r];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int m = 32 * half + u;
+                const float x = (r < len && m <= r) ? __uint_as_float(qk[u]) * expf(Gr - cf->G[m]) : 0.f;
+                sts_f32(sb + kA_MT + f32_tile_off(m, r, kBlk64), x);
+            }
+        }
+        {   // dS <- gamma_C dS (the MMA that read it is complete)
+            const float gC = cf->gam[len - 1];
+            for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tl + tS + c0, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(gC * __uint_as_float(r[u]));
+                tmem_st32(tl + tS + c0, r);
+            }
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)           // dO^T M = (M^T dO)^T
+                    mma_ss_tf32(tb + tDU, f32_desc_kstep(dX, kk, kBlk128), f32_desc_kstep(dMT, kk, kBlk64), I64,
+                                kk > 0);
+                tc_commit(&sm->bar[1]);
+            }
+            __syncwarp();
+        }
+        if (!bt_wait(&sm->bar[1], ph[1] & 1u, &sm->abort)) { failed = true; break; }
+        ++ph[1];
+        tc_fence_after();
+        {   // dU^T = scale dO^T M + (dS K^T) D_e into the A tile
+            uint32_t du[32], x[32];
+            tmem_ld32(tl + tDU + 32 * half, du);
+            tmem_ld32(tl + tU + 32 * half, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                float y[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int m = 32 * half + 4 * c4 + u;
+                    y[u] = scale * __uint_as_float(du[4 * c4 + u]) + cf->e[m] * __uint_as_float(x[4 * c4 + u]);
+                }
+                sts_f4(sb + kA_AV + f32_tile_off(li, 32 * half + 4 * c4, kBlk128), y[0], y[1], y[2], y[3]);
+            }
+        }
+        // B operands of the state-gradient update, over the [K;Q] tile (its MMAs are done)
+        tile_cols<TI>(sb + kA_KQ, kBlk128, dk, qg, t0, len, H, h, dk,
+                      [cf, scale](int r) { return scale * cf->gam[r]; });
+        tile_cols<TI>(sb + kA_KQ + 32768, kBlk128, dk, kg, t0, len, H, h, dk,
+                      [cf](int r) { return -cf->gam[r] * cf->beta[r]; });
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)           // dB^T = dU^T T
+                    mma_ss_tf32(tb + tDB, f32_desc_kstep(dAV, kk, kBlk128), f32_desc_kstep(dTT, kk, kBlk64), I64,
+                                kk > 0);
+                tc_commit(&sm->bar[2]);
+            }
+            __syncwarp();
+        }
+        if (!bt_wait(&sm->bar[2], ph[2] & 1u, &sm->abort)) { failed = true; break; }
+        ++ph[2];
+        tc_fence_after();
+        {
+            uint32_t db[32];
+            tmem_ld32(tl + tDB + 32 * half, db);
+            tmem_wait_ld();
+            if (li < dv) {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int r = 32 * half + u;
+                    if (r < len) {
+                        const size_t o = ((size_t)(t0 + r) * H + h) * dv + li;
+                        a.gv[o] = cf->beta[r] * __uint_as_float(db[u]);
+                        a.rdb[o] = __uint_as_float(db[u]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+                sts_u4(sb + kA_AV + f32_tile_off(li, 32 * half + 4 * c4, kBlk128),
+                       make_uint4(db[4 * c4], db[4 * c4 + 1], db[4 * c4 + 2], db[4 * c4 + 3]));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)           // dS += dO^T (scale D_gamma Q)
+                    mma_ss_tf32(tb + tS, f32_desc_kstep(dX, kk, kBlk128), f32_desc_kstep(dKQ, kk, kBlk128), IDK, 1);
+                for (int kk = 0; kk < 8; ++kk)           // dS += dB^T (-D_gamma diag(beta) K)
+                    mma_ss_tf32(tb + tS, f32_desc_kstep(dAV, kk, kBlk128), f32_desc_kstep(dKT2, kk, kBlk128), IDK, 1);
+                tc_commit(&sm->bar[3]);
+            }
+            __syncwarp();
+        }
+        if (!bt_wait(&sm->bar[3], ph[3] & 1u, &sm->abort)) { failed = true; break; }
+        ++ph[3];
+        tc_fence_after();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (!failed && a.gs0) {
+        for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tl + tS + c0, r);
+            tmem_wait_ld();
+            if (li < dv) {
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    if (c0 + u < dk) a.gs0[(((size_t)n * H + h) * dk + c0 + u) * dv + li] = __uint_as_float(r[u]);
+            }
+        }
+    }
+    if (failed && tid == 0) {
+        report_error(a.err, GDN_ERR_TIMEOUT);
+        sm->abort = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+}
+
+// ------------------------------------------------------------------ chunk kernel
+constexpr uint32_t kB_R0 = 0;          // [K;Q] rows; then K^T | Q^T; then dS^T
+constexpr uint32_t kB_R1 = 65536;      // [dO;dB] rows; then the C x C work arrays (into R2); then S0^T
+constexpr uint32_t kB_R2 = 131072;     // U rows; then -gamma beta dB rows; then e U rows
+constexpr uint32_t kB_R3 = 163840;     // P + P^T | R | R^T (16 KB each); then scale gamma dO rows
+constexpr uint32_t kB_Small = 212992;
+
+struct ChunkSmall {
+    BtCoef cf;
+    float dG[64], db[64], de[64];
+    float red[8];
+    uint64_t bar;
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr uint32_t kChunkSmem = kB_Small + sizeof(ChunkSmall) + 1024;
+constexpr int kCP = 65;  // row stride of the C x C work arrays
+
+// TMEM columns
+constexpr uint32_t tG = 0;     // [K K^T; Q K^T]
+constexpr uint32_t tH = 64;    // [dO U^T; dB U^T]
+constexpr uint32_t tDK = 128;  // dK^T [key][row]
+constexpr uint32_t tDQ = 192;  // dQ^T
+
+template <typename TI>
+__global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_constant__ BwdTcArgs a) {
+    const int ci = blockIdx.x, h = blockIdx.y;
+    if (ci >= *a.num_chunks) return;
+    extern __shared__ uint8_t bt_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(bt_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    ChunkSmall *sm = reinterpret_cast<ChunkSmall *>(smem + kB_Small);
+    BtCoef *cf = &sm->cf;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int li = quad * 32 + lane;
+    if (warp == 0) {
+        tmem_alloc(&sm->tmem_base, 256);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        mbar_init(&sm->bar, 1);
+        sm->abort = 0;
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = sm->tmem_base;
+    const uint32_t tl = tb + ((uint32_t)(quad * 32) << 16);
+    const int H = a.H, dk = a.dk, dv = a.dv;
+    const TI *qg = static_cast<const TI *>(a.q);
+    const TI *kg = static_cast<const TI *>(a.k);
+    const TI *vg = static_cast<const TI *>(a.v);
+    const TI *og = static_cast<const TI *>(a.dout);
+    const int4 ch = a.chunks[ci];
+    const int seq = ch.x, t0 = ch.y, len = ch.z;
+    const size_t slot = (size_t)(t0 / kChunk + seq);
+    const float scale = a.scale;
+    const uint64_t dR0 = smem_desc_sw128(sb + kB_R0, 16, 1024);
+    const uint64_t dR0q = smem_desc_sw128(sb + kB_R0 + 32768, 16, 1024);
+    const uint64_t dR1 = smem_desc_sw128(sb + kB_R1, 16, 1024);
+    const uint64_t dR2 = smem_desc_sw128(sb + kB_R2, 16, 1024);
+    const uint64_t dR3 = smem_desc_sw128(sb + kB_R3, 16, 1024);
+    const uint64_t dRR = smem_desc_sw128(sb + kB_R3 + 16384, 16, 1024);
+    const uint64_t dRT = smem_desc_sw128(sb + kB_R3 + 32768, 16, 1024);
+    const uint32_t I64 = idesc_tf32_f32(128, 64);
+    uint32_t ph = 0;
+    bool failed = false;
+
+    if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
+    // phase 1: the Gram [K;Q] K^T and [dO;dB] U^T
+    tile_rows<TI>(sb + kB_R0, kBlk128, 0, kg, t0, len, H, h, dk, One());
+    tile_rows<TI>(sb + kB_R0, kBlk128, 64, qg, t0, len, H, h, dk, One());
+    tile_rows<TI>(sb + kB_R1, kBlk128, 0, og, t0, len, H, h, dv, One());
+    tile_rows<float>(sb + kB_R1, kBlk128, 64, a.rdb, t0, len, H, h, dv, One());
+    tile_rows<float>(sb + kB_R2, kBlk64, 0, a.ru, t0, len, H, h, dv, One());
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        if (elect_one()) {
+            tc_fence_after();
+            for (int kk = 0; kk < dk / 8; ++kk)
+                mma_ss_tf32(tb + tG, f32_desc_kstep(dR0, kk, kBlk128), f32_desc_kstep(dR0, kk, kBlk128), I64, kk > 0);
+            for (int kk = 0; kk < dv / 8; ++kk)
+                mma_ss_tf32(tb + tH, f32_desc_kstep(dR1, kk, kBlk128), f32_desc_kstep(dR2, kk, kBlk64), I64, kk > 0);
+            tc_commit(&sm->bar);
+        }
+        __syncwarp();
+    }
+    do {
+        if (!bt_wait(&sm->bar, ph & 1u, &sm->abort)) { failed = true; break; }
+        ++ph;
+        tc_fence_after();
+        // phase 2: the C x C algebra on CUDA cores, in plain fp32 arrays over R1 / R2
+        float *KK = reinterpret_cast<float *>(smem + kB_R1);
+        float *QK = KK + 64 * kCP, *DM = QK + 64 * kCP, *DA = DM + 64 * kCP;
+        {
+            uint32_t x[32], y[32];
+            tmem_ld32(tl + tG + 32 * half, x);
+            tmem_ld32(tl + tH + 32 * half, y);
+            tmem_wait_ld();
+            const int r = li & 63;
+            float *fa = li < 64 ? KK : QK;
+            float *fb = li < 64 ? DM : DA;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                fa[r * kCP + 32 * half + u] = __uint_as_float(x[u]);
+                fb[r * kCP + 32 * half + u] = __uint_as_float(y[u]);
+            }
+        }
+        __syncthreads();
+        for (int idx = tid; idx < 64 * 64; idx += kBT) {
+            const int r = idx >> 6, m = idx & 63;
+            float P = 0.f, R = 0.f, E = 0.f, dagk = 0.f;
+            if (m <= r) {
+                const float gm = expf(cf->G[r] - cf->G[m]);
+                const float kk = KK[r * kCP + m], qk = QK[r * kCP + m];
+                R = scale * DM[r * kCP + m] * gm;                   // dM ⊙ Gamma
+                if (m < r) {
+                    const float da = -DA[r * kCP + m];
+                    dagk = da * gm * kk;
+                    P = da * gm * cf->beta[r];
+                }
+                E = P * kk + R * qk;
+            }
+            DA[r * kCP + m] = P;
+            DM[r * kCP + m] = R;
+            KK[r * kCP + m] = E;
+            QK[r * kCP + m] = dagk;
+        }
+        __syncthreads();
+        // per-row sums: E by rows and columns, dA Gamma KK, and the value-row dot
+        // products of the stored intermediates
+        for (int r = warp; r < 64; r += kBT / 32) {
+            const float rowE = warp_sum(KK[r * kCP + lane] + KK[r * kCP + 32 + lane]);
+            const float colE = warp_sum(KK[lane * kCP + r] + KK[(32 + lane) * kCP + r]);
+            const float dagk = warp_sum(QK[r * kCP + lane] + QK[r * kCP + 32 + lane]);
+            float s_vdb = 0.f, s_ydb = 0.f, s_oqs = 0.f, s_ukds = 0.f;
+            if (r < len) {
+                const size_t base = ((size_t)(t0 + r) * H + h) * dv;
+                for (int i = lane; i < dv; i += 32) {
+                    const float db = a.rdb[base + i], y = a.ry[base + i];
+                    s_vdb += ld1<TI>(vg + base + i) * db;
+                    s_ydb += y * db;
+                    s_oqs += ld1<TI>(og + base + i) * a.rqs[base + i];
+                    s_ukds += a.ru[base + i] * a.rkds[base + i];
+                }
+            }
+            s_vdb = warp_sum(s_vdb);
+            s_ydb = warp_sum(s_ydb);
+            s_oqs = warp_sum(s_oqs);
+            s_ukds = warp_sum(s_ukds);
+            if (lane == 0) {
+                const float gam = cf->gam[r], beta = cf->beta[r];
+                const float dgam = scale * s_oqs - beta * s_ydb;   // D_gamma in O and X
+                sm->db[r] = s_vdb - gam * s_ydb + dagk;
+                sm->de[r] = s_ukds;
+                sm->dG[r] = rowE - colE + dgam * gam - s_ukds * cf->e[r];
+            }
+        }
+        // B operands of dK and dQ: P + P^T, R, R^T ([row][m], 64 x 64)
+        for (int idx = tid; idx < 64 * 16; idx += kBT) {
+            const int r = idx >> 4, m4 = (idx & 15) * 4;
+            float pp[4], rr[4], rt[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int m = m4 + u;
+                pp[u] = DA[r * kCP + m] + DA[m * kCP + r];
+                rr[u] = DM[r * kCP + m];
+                rt[u] = DM[m * kCP + r];
+            }
+            const uint32_t off = f32_tile_off(r, m4, kBlk64);
+            sts_f4(sb + kB_R3 + off, pp[0], pp[1], pp[2], pp[3]);
+            sts_f4(sb + kB_R3 + 16384 + off, rr[0], rr[1], rr[2], rr[3]);
+            sts_f4(sb + kB_R3 + 32768 + off, rt[0], rt[1], rt[2], rt[3]);
+        }
+        // A operands K^T, Q^T ([key][m], rows past dk zero) over the [K;Q] tile
+        tile_cols<TI>(sb + kB_R0, kBlk128, 128, kg, t0, len, H, h, dk, One());
+        tile_cols<TI>(sb + kB_R0 + 32768, kBlk128, 128, qg, t0, len, H, h, dk, One());
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // phase 3a: dK^T = K^T (P + P^T)^T + Q^T R, dQ^T = K^T R^T
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss_tf32(tb + tDK, f32_desc_kstep(dR0, kk, kBlk128), f32_desc_kstep(dR3, kk, kBlk64), I64, kk > 0);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss_tf32(tb + tDK, f32_desc_kstep(dR0q, kk, kBlk128), f32_desc_kstep(dRT, kk, kBlk64), I64, 1);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss_tf32(tb + tDQ, f32_desc_kstep(dR0, kk, kBlk128), f32_desc_kstep(dRR, kk, kBlk64), I64, kk > 0);
+                tc_commit(&sm->bar);
+            }
+            __syncwarp();
+        }
+        // meanwhile: S0^T ([key][value], rows past dk zero) over R1, -gamma beta dB rows over R2
+        {
+            const float *src = a.s0t + (slot * H + h) * (size_t)dk * dv;
+            const int d4 = dv >> 2;
+            for (int idx = tid; idx < 128 * d4; idx += kBT) {
+                const int j = idx / d4, c4 = idx - j * d4;
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < dk) x = __ldg(reinterpret_cast<const float4 *>(src + (size_t)j * dv + 4 * c4));
+                sts_f4(sb + kB_R1 + f32_tile_off(j, 4 * c4, kBlk128), x.x, x.y, x.z, x.w);
+            }
+        }
+        tile_rows<float>(sb + kB_R2, kBlk64, 0, a.rdb, t0, len, H, h, dv,
+                         [cf](int r) { return -cf->gam[r] * cf->beta[r]; });
+        if (!bt_wait(&sm->bar, ph & 1u, &sm->abort)) { failed = true; break; }
+        ++ph;
+        tc_fence_after();
+        tile_rows<TI>(sb + kB_R3, kBlk64, 0, og, t0, len, H, h, dv, [cf, scale](int r) { return scale * cf->gam[r]; });
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // phase 3b: dK^T += S0^T (D_gamma dX)^T, dQ^T += S0^T (scale D_gamma dO)^T
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < dv / 8; ++kk)
+                    mma_ss_tf32(tb + tDK, f32_desc_kstep(dR1, kk, kBlk128), f32_desc_kstep(dR2, kk, kBlk64), I64, 1);
+                for (int kk = 0; kk < dv / 8; ++kk)
+                    mma_ss_tf32(tb + tDQ, f32_desc_kstep(dR1, kk, kBlk128), f32_desc_kstep(dR3, kk, kBlk64), I64, 1);
+                tc_commit(&sm->bar);
+            }
+            __syncwarp();
+        }
+        if (!bt_wait(&sm->bar, ph & 1u, &sm->abort)) { failed = true; break; }
+        ++ph;
+        tc_fence_after();
+        // phase 3c: dS^T over R0 (with <dS, S0> on the way, S0^T still in R1), e U rows over R2
+        {
+            const float *src = a.dst + (slot * H + h) * (size_t)dk * dv;
+            const int d4 = dv >> 2;
+            float part = 0.f;
+            for (int idx = tid; idx < 128 * d4; idx += kBT) {
+                const int j = idx / d4, c4 = idx - j * d4;
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                const uint32_t off = f32_tile_off(j, 4 * c4, kBlk128);
+                if (j < dk) {
+                    x = __ldg(reinterpret_cast<const float4 *>(src + (size_t)j * dv + 4 * c4));
+                    const float4 s0 = lds_f4(sb + kB_R1 + off);
+                    part += x.x * s0.x + x.y * s0.y + x.z * s0.z + x.w * s0.w;
+                }
+                sts_f4(sb + kB_R0 + off, x.x, x.y, x.z, x.w);
+            }
+            part = warp_sum(part);
+            if (lane == 0) sm->red[warp] = part;
+        }
+        tile_rows<float>(sb + kB_R2, kBlk64, 0, a.ru, t0, len, H, h, dv, [cf](int r) { return cf->e[r]; });
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < dv / 8; ++kk)   // dK^T += dS^T (D_e U)^T
+                    mma_ss_tf32(tb + tDK, f32_desc_kstep(dR0, kk, kBlk128), f32_desc_kstep(dR2, kk, kBlk64), I64, 1);
+                tc_commit(&sm->bar);
+            }
+            __syncwarp();
+            // dg (reverse cumsum of dG, with the terms of gamma_C and of e's
+            // numerator at row len - 1) and dbeta
+            float t = sm->de[lane] * cf->e[lane] + sm->de[32 + lane] * cf->e[32 + lane];
+            t = warp_sum(t);
+            float ss = 0.f;
+            for (int w = 0; w < kBT / 32; ++w) ss += sm->red[w];
+            const float extra = t + cf->gam[len - 1] * ss;
+            float x0 = sm->dG[lane], x1 = sm->dG[32 + lane];
+            if (lane == len - 1) x0 += extra;
+            if (32 + lane == len - 1) x1 += extra;
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y0 = __shfl_down_sync(0xffffffffu, x0, off);
+                const float y1 = __shfl_down_sync(0xffffffffu, x1, off);
+                if (lane + off < 32) { x0 += y0; x1 += y1; }
+            }
+            x0 += __shfl_sync(0xffffffffu, x1, 0);
+            if (lane < len) {
+                a.gg[(size_t)(t0 + lane) * H + h] = x0;
+                a.gbeta[(size_t)(t0 + lane) * H + h] = sm->db[lane];
+            }
+            if (32 + lane < len) {
+                a.gg[(size_t)(t0 + 32 + lane) * H + h] = x1;
+                a.gbeta[(size_t)(t0 + 32 + lane) * H + h] = sm->db[32 + lane];
+            }
+        }
+        if (!bt_wait(&sm->bar, ph & 1u, &sm->abort)) { failed = true; break; }
+        ++ph;
+        tc_fence_after();
+        {   // dK^T, dQ^T: lane = key index, columns = chunk rows
+            uint32_t xk[32], xq[32];
+            tmem_ld32(tl + tDK + 32 * half, xk);
+            tmem_ld32(tl + tDQ + 32 * half, xq);
+            tmem_wait_ld();
+            if (li < dk) {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int r = 32 * half + u;
+                    if (r < len) {
+                        const size_t o = ((size_t)(t0 + r) * H + h) * dk + li;
+                        a.gk[o] = __uint_as_float(xk[u]);
+                        a.gq[o] = __uint_as_float(xq[u]);
+                    }
+                }
+            }
+        }
+    } while (false);
+    if (failed && tid == 0) {
+        report_error(a.err, GDN_ERR_TIMEOUT);
+        sm->abort = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 256);
+    }
+}
+
+template <typename TI>
+cudaError_t launch_bwd_tc_t(const BwdTcArgs &a, int max_chunks, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_tc_chain_kernel<TI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kChainSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_tc_chunk_kernel<TI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChunkSmem);
+    if (e != cudaSuccess) return e;
+    bwd_tc_chain_kernel<TI><<<dim3(a.H, a.N), kBT, kChainSmem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (max_chunks > 0) {
+        bwd_tc_chunk_kernel<TI><<<dim3(max_chunks, a.H), kBT, kChunkSmem, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdTcArgs &a, int max_chunks, cudaStream_t s) {
+    if (a.dtype == GDN_BF16) return launch_bwd_tc_t<__nv_bfloat16>(a, max_chunks, s);
+    return launch_bwd_tc_t<float>(a, max_chunks, s);
+}
+
+}  // namespace gdn

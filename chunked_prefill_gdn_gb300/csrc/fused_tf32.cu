@@ -66,14 +66,12 @@ struct T32Small {
 
 constexpr uint32_t kT32Smem = kOffSmallT + sizeof(T32Small) + 1024;
 
-// byte offset of element k (a multiple of 4 for a 16-byte store) of a row
 __device__ __forceinline__ uint32_t tile_off(uint32_t row, uint32_t k, uint32_t block) {
-    return (k >> 5) * block + sw128_offset(row, (k & 31u) >> 2);
+    return f32_tile_off(row, k, block);
 }
 
-// descriptor of a K-major swizzled tile advanced to MMA K-step kk
 __device__ __forceinline__ uint64_t kstep(uint64_t desc, int kk, uint32_t block) {
-    return desc + ((((uint32_t)kk >> 2) * block + ((uint32_t)kk & 3u) * 32u) >> 4);
+    return f32_desc_kstep(desc, kk, block);
 }
 
 __device__ __forceinline__ float4 ldg_f4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }

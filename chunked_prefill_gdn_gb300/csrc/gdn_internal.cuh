@@ -120,6 +120,26 @@ bool fused_tf32_supported(int dtype, int dk, int dv);
 cudaError_t launch_fused_tf32(const Problem &p, const Workspace &w, int pass, int grid, cudaStream_t s);
 int fused_simt_smem_bytes(int dk, int dv);
 
+// The tensor-core backward (kind::tf32): a chain kernel per (sequence, head)
+// runs the state recurrence forward and the state-gradient recurrence back,
+// storing per-chunk intermediates, then a kernel per (chunk, head) forms the
+// gradients of q, k, g and beta from them.
+struct BwdTcArgs {
+    const void *q, *k, *v, *dout;       // [total_T, H, d], input type
+    const float *g, *beta, *s0, *dsf;   // s0, dsf: [N, H, dk, dv] or NULL
+    const int32_t *cu;                  // device cu_seqlens or NULL
+    const float *tp;                    // [H, total_T, 64]: T' of every chunk, fp32
+    const int4 *chunks;                 // the chunk table (sequence prep)
+    const int *num_chunks;
+    float *s0t, *dst;                   // [slots, H, dk, dv]: chunk start states and end-state gradients
+    float *ry, *rqs, *ru, *rdb, *rkds;  // [total_T, H, dv]: K S0^T, Q S0^T, U, dB, K dS^T rows
+    float *gq, *gk, *gv, *gg, *gbeta, *gs0;
+    int *err;
+    int T, H, dk, dv, N, total_T, varlen, dtype;
+    float scale;
+};
+cudaError_t launch_bwd_tc(const BwdTcArgs &a, int max_chunks, cudaStream_t s);
+
 // Called once per CTA of a persistent pass after it found the queue empty: the
 // last CTA to leave resets the item counter and the exit counter to zero.
 __device__ __forceinline__ void finish_queue(int *item_counter, int *exit_counter) {

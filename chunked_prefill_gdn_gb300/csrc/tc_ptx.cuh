@@ -325,5 +325,18 @@ __device__ __forceinline__ void sts_b16(uint32_t a, uint32_t v) {
 // the 128-byte swizzle (tile base 1024-byte aligned).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
 
+// fp32 K-major operand tiles with the 128-byte swizzle: [K/32 blocks][rows][128 B],
+// `block` bytes apart.  Byte offset of element k of a row (k a multiple of 4
+// for a 16-byte access).
+__device__ __forceinline__ uint32_t f32_tile_off(uint32_t row, uint32_t k, uint32_t block) {
+    return (k >> 5) * block + sw128_offset(row, (k & 31u) >> 2) + (k & 3u) * 4u;
+}
+
+// The descriptor of such a tile advanced to MMA K-step kk (eight fp32 elements,
+// 32 bytes, per kind::tf32 step).
+__device__ __forceinline__ uint64_t f32_desc_kstep(uint64_t desc, int kk, uint32_t block) {
+    return desc + ((((uint32_t)kk >> 2) * block + ((uint32_t)kk & 3u) * 32u) >> 4);
+}
+
 }  // namespace tc
 }  // namespace gdn

@@ -471,9 +471,15 @@ gdn_status gdn_qk_l2norm_bwd(const void *x, const float *dy, float *dx, int64_t 
  *   d_initial_state [N, H, dk, dv]  (may be NULL: not written)
  * All pointers are device pointers, 16-byte aligned.  The workspace must hold
  * gdn_chunk_bwd_workspace_size() bytes (no initialisation needed; it keeps the
- * chunk start states and, for dv > 32, the per-slice partial sums).  Enqueued
- * on `stream`; nothing syncs.  The result does not depend on the launch order
- * of CTAs (partial sums are added in a fixed order).
+ * chunk start states and the per-chunk intermediates).  Enqueued on `stream`;
+ * nothing syncs.  The result does not depend on the launch order of CTAs.
+ *
+ * Kernels (gdn_set_backward_kernel): by default the tensor-core backward, two
+ * tcgen05 kernels with fp32 operands read as tf32 and fp32 accumulation — a
+ * chain kernel per (sequence, head) for the state and state-gradient
+ * recurrences, dv and d_initial_state, then one CTA per (chunk, head) for dq,
+ * dk, dg and dbeta; GDN_KERNEL_SIMT selects the CUDA-core kernel (fp32
+ * products, one CTA per 32 value columns, head and sequence).
  * Errors: GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED / GDN_ERR_WORKSPACE before
  * any launch; GDN_ERR_CUDA on a launch failure; a malformed cu_seqlens is
  * written to the workspace's error word, which gdn_chunk_bwd_check() reads.
@@ -493,8 +499,15 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v,
                          float *d_initial_state,
                          void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/* Selects the kernels of later gdn_chunk_bwd calls in this process:
+ * GDN_KERNEL_AUTO or GDN_KERNEL_TC (the tensor-core backward, the default) or
+ * GDN_KERNEL_SIMT (the CUDA-core backward).  Both fit the same workspace size.
+ * GDN_ERR_INVALID_ARG for another value. */
+gdn_status gdn_set_backward_kernel(gdn_kernel kernel);
+gdn_kernel gdn_get_backward_kernel(void);
+
 /* Synchronises `stream` and reads the error word of a gdn_chunk_bwd
- * workspace: GDN_OK or GDN_ERR_DEVICE_CHECK (bad cu_seqlens). */
+ * workspace: GDN_OK, GDN_ERR_DEVICE_CHECK (bad cu_seqlens) or GDN_ERR_TIMEOUT. */
 gdn_status gdn_chunk_bwd_check(const void *workspace, gdn_stream_t stream);
 
 /* The CUDA error (and, for tensor-map encoding, the driver result) behind the

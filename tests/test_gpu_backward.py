@@ -6,8 +6,9 @@ pinned to the token-level one (test_oracle_backward.py).
 Bar: relative L2 error <= 5e-3 (the forward's) and max-abs error <= 2e-2 times
 max(1, max |reference|) for every gradient — the gradients reach tens, so the
 forward's absolute 2e-2 is applied relative to their scale.  Inputs are
-bf16- or fp32-exact on both sides and the device computes in fp32, so the
-expected error is ~1e-5 relative."""
+bf16- or fp32-exact on both sides.  The tensor-core backward (the default)
+reads its fp32 operands as tf32 (a CPU simulation of that rounding puts every
+gradient near 4e-4 relative); the CUDA-core backward computes in fp32 (~1e-7)."""
 import json
 import os
 
@@ -107,8 +108,17 @@ CASES = {
 }
 
 
+@pytest.fixture
+def bwd_kernel(request):
+    """Selects the backward's kernels for one test, then restores the default."""
+    gdn.gdn_set_backward_kernel(request.param)
+    yield request.param
+    gdn.gdn_set_backward_kernel(gdn.KERNEL_AUTO)
+
+
+@pytest.mark.parametrize("bwd_kernel", [gdn.KERNEL_TC, gdn.KERNEL_SIMT], ids=["tc", "simt"], indirect=True)
 @pytest.mark.parametrize("name", list(CASES))
-def test_backward_matches_oracle(name):
+def test_backward_matches_oracle(name, bwd_kernel):
     inp, grads = CASES[name]()
     ref = reference(inp, grads)
     got = run_bwd(to_device(inp), {k: v.cuda() for k, v in grads.items()})
