@@ -42,7 +42,8 @@ using namespace tc;
 
 namespace {
 
-constexpr int kBT = 256;                      // threads: warps w and w + 4 share TMEM lane quadrant w
+constexpr int kBT = 512;                      // threads: warps w, w + 4, w + 8, w + 12 share TMEM lane quadrant w
+constexpr int kParts = kBT / 128;             // warps per lane quadrant: each takes 16 of 64 columns (32 of 128)
 constexpr uint64_t kBtTimeoutNs = 2000000000ull;
 constexpr uint32_t kBlk128 = 16384;           // block stride of a 128-row fp32 tile
 constexpr uint32_t kBlk64 = 8192;             // block stride of a 64-row fp32 tile
@@ -69,10 +70,10 @@ __device__ __forceinline__ float ld1(const TI *p) {
 }
 
 __device__ __forceinline__ void sts_f4(uint32_t a, float x, float y, float z, float w) {
-    sts_u4(a, make_uint4(__float_as_uint(x), __float_as_uint(y), __float_as_uint(z), __float_as_uint(w)));
+    sts_u4_stage(a, make_uint4(__float_as_uint(x), __float_as_uint(y), __float_as_uint(z), __float_as_uint(w)));
 }
 __device__ __forceinline__ void sts_f32(uint32_t a, float x) {
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(x) : "memory");
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(x));
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -111,67 +112,177 @@ __device__ __forceinline__ void chunk_coef(BtCoef *cf, const float *g, const flo
     cf->beta[32 + lane] = b1;
 }
 
+// The loaders below issue their global loads in batches of kLB per thread
+// (all in flight) before the shared-memory stores: a store is an asm
+// statement the compiler does not move loads across, so a load-store loop
+// would wait one memory round trip per element.
+constexpr int kLB = 4;
+
+__device__ __forceinline__ int log2i(int x) { return 31 - __clz(x); }
+
 // Tile rows row0 + r (r < 64) = f(r) x[t0 + r][0, d); zero past len.
 template <typename TI, typename F>
 __device__ __forceinline__ void tile_rows(uint32_t tile, uint32_t block, int row0, const TI *x, int t0, int len,
                                           int H, int h, int d, F f) {
-    const int d4 = d >> 2;
-    for (int idx = threadIdx.x; idx < 64 * d4; idx += kBT) {
-        const int r = idx / d4, c4 = idx - r * d4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < len) {
-            v = ld4<TI>(x + ((size_t)(t0 + r) * H + h) * d + 4 * c4);
-            const float s = f(r);
-            v.x *= s; v.y *= s; v.z *= s; v.w *= s;
+    const int sh = log2i(d >> 2), total = 64 << sh;
+    const TI *x0 = x + ((size_t)t0 * H + h) * d;     // row r at x0 + r * H * d
+    const int stride = H * d;
+    for (int base = threadIdx.x; base < total; base += kLB * kBT) {
+        float4 v[kLB];
+#pragma unroll
+        for (int b = 0; b < kLB; ++b) {
+            const int idx = base + b * kBT;
+            const int r = idx >> sh, c4 = idx & ((1 << sh) - 1);
+            v[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (idx < total && r < len) {
+                v[b] = ld4<TI>(x0 + r * stride + 4 * c4);
+                const float s = f(r);
+                v[b].x *= s; v[b].y *= s; v[b].z *= s; v[b].w *= s;
+            }
         }
-        sts_f4(tile + f32_tile_off(row0 + r, 4 * c4, block), v.x, v.y, v.z, v.w);
+#pragma unroll
+        for (int b = 0; b < kLB; ++b) {
+            const int idx = base + b * kBT;
+            if (idx < total) {
+                const int r = idx >> sh, c4 = idx & ((1 << sh) - 1);
+                sts_f4(tile + f32_tile_off(row0 + r, 4 * c4, block), v[b].x, v[b].y, v[b].z, v[b].w);
+            }
+        }
     }
 }
 
 // Tile row j < rows, columns r < 64: f(r) x[t0 + r][j] (zero for j >= d or
 // r >= len).  Lanes take consecutive j, so the reads of a token row coalesce.
+// rows is 32, 64 or 128.
 template <typename TI, typename F>
 __device__ __forceinline__ void tile_cols(uint32_t tile, uint32_t block, int rows, const TI *x, int t0, int len,
                                           int H, int h, int d, F f) {
-    for (int idx = threadIdx.x; idx < rows * 16; idx += kBT) {
-        const int r4 = idx / rows, j = idx - r4 * rows;
-        float e[4];
+    const int sh = log2i(rows), total = rows * 16;
+    const TI *x0 = x + ((size_t)t0 * H + h) * d;
+    const int stride = H * d;
+    for (int base = threadIdx.x; base < total; base += kLB * kBT) {
+        float e[kLB][4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int r = 4 * r4 + u;
-            e[u] = (j < d && r < len) ? f(r) * ld1<TI>(x + ((size_t)(t0 + r) * H + h) * d + j) : 0.f;
+        for (int b = 0; b < kLB; ++b) {
+            const int idx = base + b * kBT;
+            const int r4 = idx >> sh, j = idx & (rows - 1);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = 4 * r4 + u;
+                e[b][u] = (idx < total && j < d && r < len) ? f(r) * ld1<TI>(x0 + r * stride + j) : 0.f;
+            }
         }
-        sts_f4(tile + f32_tile_off(j, 4 * r4, block), e[0], e[1], e[2], e[3]);
+#pragma unroll
+        for (int b = 0; b < kLB; ++b) {
+            const int idx = base + b * kBT;
+            if (idx < total) {
+                const int r4 = idx >> sh, j = idx & (rows - 1);
+                sts_f4(tile + f32_tile_off(j, 4 * r4, block), e[b][0], e[b][1], e[b][2], e[b][3]);
+            }
+        }
     }
 }
 
-// T = Gamma ⊙ T' rows [n][m] (fwd) or transposed [r][n] = T[n][r] (rev), from
-// T' rows (row n at tp + 64 n, entries past the chunk not read).
-__device__ __forceinline__ void tile_t(uint32_t tile, const float *tp, int len, const float *G) {
-    for (int idx = threadIdx.x; idx < 64 * 16; idx += kBT) {
-        const int n = idx >> 4, m4 = (idx & 15) * 4;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (n < len && m4 <= n) {
-            const float4 t = __ldg(reinterpret_cast<const float4 *>(tp + (size_t)n * 64 + m4));
-            const float tv[4] = {t.x, t.y, t.z, t.w};
+// Tile row j < 128 = src[j][0, dv) for j < dk (zero past dk), src rows dv
+// apart; with `dot`, also the sum over the tile of this times `dot_tile` at
+// the same place (same block stride).
+__device__ __forceinline__ float tile_state(uint32_t tile, const float *src, int dk, int dv, uint32_t dot_tile) {
+    const int sh = log2i(dv >> 2), total = 128 << sh;
+    float part = 0.f;
+    for (int base = threadIdx.x; base < total; base += kLB * kBT) {
+        float4 v[kLB];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (m4 + u <= n) x[u] = tv[u] * expf(G[n] - G[m4 + u]);
+        for (int b = 0; b < kLB; ++b) {
+            const int idx = base + b * kBT;
+            const int j = idx >> sh, c4 = idx & ((1 << sh) - 1);
+            v[b] = (idx < total && j < dk) ? __ldg(reinterpret_cast<const float4 *>(src + (size_t)j * dv + 4 * c4))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+#pragma unroll
+        for (int b = 0; b < kLB; ++b) {
+            const int idx = base + b * kBT;
+            if (idx < total) {
+                const int j = idx >> sh, c4 = idx & ((1 << sh) - 1);
+                const uint32_t off = f32_tile_off(j, 4 * c4, kBlk128);
+                if (dot_tile) {
+                    const float4 o = lds_f4(dot_tile + off);
+                    part += v[b].x * o.x + v[b].y * o.y + v[b].z * o.z + v[b].w * o.w;
+                }
+                sts_f4(tile + off, v[b].x, v[b].y, v[b].z, v[b].w);
+            }
+        }
+    }
+    return part;
+}
+
+// T = Gamma ⊙ T' rows [n][m] (fwd) or transposed [r][n] = T[n][r] (rev), from
+// T' rows (row n at tp + 64 n, entries past the chunk not read).  1024 items:
+// four per thread, loaded together.
+__device__ __forceinline__ void tile_t(uint32_t tile, const float *tp, int len, const float *G) {
+    constexpr int kN = 1024 / kBT;
+    float4 t[kN];
+#pragma unroll
+    for (int b = 0; b < kN; ++b) {
+        const int idx = threadIdx.x + b * kBT;
+        const int n = idx >> 4, m4 = (idx & 15) * 4;
+        t[b] = (n < len && m4 <= n) ? __ldg(reinterpret_cast<const float4 *>(tp + (size_t)n * 64 + m4))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int b = 0; b < kN; ++b) {
+        const int idx = threadIdx.x + b * kBT;
+        const int n = idx >> 4, m4 = (idx & 15) * 4;
+        const float tv[4] = {t[b].x, t[b].y, t[b].z, t[b].w};
+        float x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = (n < len && m4 + u <= n) ? tv[u] * expf(G[n] - G[m4 + u]) : 0.f;
         sts_f4(tile + f32_tile_off(n, m4, kBlk64), x[0], x[1], x[2], x[3]);
     }
 }
 __device__ __forceinline__ void tile_t_transposed(uint32_t tile, const float *tp, int len, const float *G) {
-    for (int idx = threadIdx.x; idx < 64 * 16; idx += kBT) {
+    constexpr int kN = 1024 / kBT;
+    float x[kN][4];
+#pragma unroll
+    for (int b = 0; b < kN; ++b) {
+        const int idx = threadIdx.x + b * kBT;
         const int n4 = idx >> 6, r = idx & 63;
-        float x[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int n = 4 * n4 + u;
-            x[u] = (n < len && r <= n) ? __ldg(tp + (size_t)n * 64 + r) * expf(G[n] - G[r]) : 0.f;
+            x[b][u] = (n < len && r <= n) ? __ldg(tp + (size_t)n * 64 + r) : 0.f;
         }
-        sts_f4(tile + f32_tile_off(r, 4 * n4, kBlk64), x[0], x[1], x[2], x[3]);
     }
+#pragma unroll
+    for (int b = 0; b < kN; ++b) {
+        const int idx = threadIdx.x + b * kBT;
+        const int n4 = idx >> 6, r = idx & 63;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int n = 4 * n4 + u;
+            if (n < len && r <= n) x[b][u] *= expf(G[n] - G[r]);
+        }
+        sts_f4(tile + f32_tile_off(r, 4 * n4, kBlk64), x[b][0], x[b][1], x[b][2], x[b][3]);
+    }
+}
+
+// L2 prefetch of rows [t0, t0 + len) of a [total_T][H][d] tensor (head h),
+// one row per thread of the given thread range.
+template <typename T>
+__device__ __forceinline__ void prefetch_rows(const T *x, int t0, int len, int H, int h, int d, int thr0) {
+    const int r = (int)threadIdx.x - thr0;
+    if (r >= 0 && r < len) l2_prefetch(x + ((size_t)(t0 + r) * H + h) * d, (uint32_t)(d * sizeof(T)));
+}
+
+// The chain kernel's inputs of one chunk: K, Q and V or dO rows and the T'
+// block, spread over the CTA's threads.
+template <typename TI>
+__device__ __forceinline__ void prefetch_chain_chunk(const BwdTcArgs &a, int t0, int len, int h, bool rev) {
+    const TI *kg = static_cast<const TI *>(a.k), *qg = static_cast<const TI *>(a.q);
+    const TI *xg = static_cast<const TI *>(rev ? a.dout : a.v);
+    prefetch_rows(kg, t0, len, a.H, h, a.dk, 0);
+    prefetch_rows(qg, t0, len, a.H, h, a.dk, 64);
+    prefetch_rows(xg, t0, len, a.H, h, a.dv, 128);
+    if (threadIdx.x == 192) l2_prefetch(a.tp + ((size_t)h * a.total_T + t0) * kChunk, (uint32_t)len * 256u);
 }
 
 struct One {
@@ -236,7 +347,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
     ChainSmall *sm = reinterpret_cast<ChainSmall *>(smem + kA_Small);
     BtCoef *cf = &sm->cf;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
+    const int quad = warp & 3, part = warp >> 2;
     const int li = quad * 32 + lane;
     if (warp == 0) {
         tmem_alloc(&sm->tmem_base, 512);
@@ -270,7 +381,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
     const float scale = a.scale;
 
     // ---------------- forward sweep: the start state of every chunk ----------------
-    for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+    for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
         uint32_t r[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
@@ -284,13 +395,15 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (nc > 0) prefetch_chain_chunk<TI>(a, t_begin, min(kChunk, len_seq), h, false);
     for (int c = 0; c < nc; ++c) {
         const int t0 = t_begin + c * kChunk, len = min(kChunk, t_begin + len_seq - t0);
         const size_t slot = (size_t)(t0 / kChunk + n);
+        if (c + 1 < nc) prefetch_chain_chunk<TI>(a, t0 + kChunk, min(kChunk, t_begin + len_seq - t0 - kChunk), h, false);
         if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
         {   // this chunk's start state, transposed ([key][value]), to the workspace
             float *dst = a.s0t + (slot * H + h) * (size_t)dk * dv;
-            for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+            for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tl + tS + c0, r);
                 tmem_wait_ld();
@@ -318,24 +431,24 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
             }
             __syncwarp();
         }
-        float vv[32];
+        float vv[16];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int r = 32 * half + u;
+        for (int u = 0; u < 16; ++u) {
+            const int r = 16 * part + u;
             vv[u] = (li < dv && r < len) ? ld1<TI>(vg + ((size_t)(t0 + r) * H + h) * dv + li) : 0.f;
         }
         if (!bt_wait(&sm->bar[0], ph[0] & 1u, &sm->abort)) { failed = true; break; }
         ++ph[0];
         tc_fence_after();
         {
-            uint32_t pk[32], pq[32];
-            tmem_ld32(tl + tP + 32 * half, pk);
-            tmem_ld32(tl + tP + 64 + 32 * half, pq);
+            uint32_t pk[16], pq[16];
+            tmem_ld16(tl + tP + 16 * part, pk);
+            tmem_ld16(tl + tP + 64 + 16 * part, pq);
             tmem_wait_ld();
             if (li < dv) {
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int r = 32 * half + u;
+                for (int u = 0; u < 16; ++u) {
+                    const int r = 16 * part + u;
                     if (r < len) {
                         const size_t o = ((size_t)(t0 + r) * H + h) * dv + li;
                         a.ry[o] = __uint_as_float(pk[u]);
@@ -344,19 +457,19 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
                 }
             }
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
+            for (int c4 = 0; c4 < 4; ++c4) {
                 float x[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int r = 32 * half + 4 * c4 + u;
+                    const int r = 16 * part + 4 * c4 + u;
                     x[u] = cf->beta[r] * (vv[4 * c4 + u] - cf->gam[r] * __uint_as_float(pk[4 * c4 + u]));
                 }
-                sts_f4(sb + kA_AV + f32_tile_off(li, 32 * half + 4 * c4, kBlk128), x[0], x[1], x[2], x[3]);
+                sts_f4(sb + kA_AV + f32_tile_off(li, 16 * part + 4 * c4, kBlk128), x[0], x[1], x[2], x[3]);
             }
         }
         {   // S <- gamma_C S (the MMA that read S is complete)
             const float gC = cf->gam[len - 1];
-            for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+            for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tl + tS + c0, r);
                 tmem_wait_ld();
@@ -383,19 +496,19 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
         ++ph[1];
         tc_fence_after();
         {
-            uint32_t u32[32];
-            tmem_ld32(tl + tU + 32 * half, u32);
+            uint32_t u32[16];
+            tmem_ld16(tl + tU + 16 * part, u32);
             tmem_wait_ld();
             if (li < dv) {
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int r = 32 * half + u;
+                for (int u = 0; u < 16; ++u) {
+                    const int r = 16 * part + u;
                     if (r < len) a.ru[((size_t)(t0 + r) * H + h) * dv + li] = __uint_as_float(u32[u]);
                 }
             }
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-                sts_u4(sb + kA_AV + f32_tile_off(li, 32 * half + 4 * c4, kBlk128),
+            for (int c4 = 0; c4 < 4; ++c4)
+                sts_u4_stage(sb + kA_AV + f32_tile_off(li, 16 * part + 4 * c4, kBlk128),
                        make_uint4(u32[4 * c4], u32[4 * c4 + 1], u32[4 * c4 + 2], u32[4 * c4 + 3]));
         }
         fence_proxy_async_smem();
@@ -420,7 +533,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
 
     // ---------------- reverse sweep: the state gradient back to the start ----------------
     if (!failed) {
-        for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+        for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
             uint32_t r[32];
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
@@ -435,13 +548,16 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
         __syncthreads();
         tc_fence_after();
     }
+    if (nc > 0 && !failed)
+        prefetch_chain_chunk<TI>(a, t_begin + (nc - 1) * kChunk, len_seq - (nc - 1) * kChunk, h, true);
     for (int c = nc - 1; c >= 0 && !failed; --c) {
         const int t0 = t_begin + c * kChunk, len = min(kChunk, t_begin + len_seq - t0);
         const size_t slot = (size_t)(t0 / kChunk + n);
+        if (c > 0) prefetch_chain_chunk<TI>(a, t0 - kChunk, kChunk, h, true);
         if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
         {   // this chunk's end-state gradient, transposed, to the workspace
             float *dst = a.dst + (slot * H + h) * (size_t)dk * dv;
-            for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+            for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tl + tS + c0, r);
                 tmem_wait_ld();
@@ -476,33 +592,33 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
         ++ph[0];
         tc_fence_after();
         {
-            uint32_t x[32];
-            tmem_ld32(tl + tU + 32 * half, x);
+            uint32_t x[16];
+            tmem_ld16(tl + tU + 16 * part, x);
             tmem_wait_ld();
             if (li < dv) {
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int r = 32 * half + u;
+                for (int u = 0; u < 16; ++u) {
+                    const int r = 16 * part + u;
                     if (r < len) a.rkds[((size_t)(t0 + r) * H + h) * dv + li] = __uint_as_float(x[u]);
                 }
             }
         }
         if (quad >= 2) {   // M^T [m][r] = Gamma ⊙ tril(Q K^T) [r][m], row r = lane - 64 of Q K^T
-            uint32_t qk[32];
-            tmem_ld32(tl + tQK + 32 * half, qk);
+            uint32_t qk[16];
+            tmem_ld16(tl + tQK + 16 * part, qk);
             tmem_wait_ld();
             const int r = li - 64;
             const float Gr = cf->G[r];
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int m = 32 * half + u;
+            for (int u = 0; u < 16; ++u) {
+                const int m = 16 * part + u;
                 const float x = (r < len && m <= r) ? __uint_as_float(qk[u]) * expf(Gr - cf->G[m]) : 0.f;
                 sts_f32(sb + kA_MT + f32_tile_off(m, r, kBlk64), x);
             }
         }
         {   // dS <- gamma_C dS (the MMA that read it is complete)
             const float gC = cf->gam[len - 1];
-            for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+            for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tl + tS + c0, r);
                 tmem_wait_ld();
@@ -529,19 +645,19 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
         ++ph[1];
         tc_fence_after();
         {   // dU^T = scale dO^T M + (dS K^T) D_e into the A tile
-            uint32_t du[32], x[32];
-            tmem_ld32(tl + tDU + 32 * half, du);
-            tmem_ld32(tl + tU + 32 * half, x);
+            uint32_t du[16], x[16];
+            tmem_ld16(tl + tDU + 16 * part, du);
+            tmem_ld16(tl + tU + 16 * part, x);
             tmem_wait_ld();
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
+            for (int c4 = 0; c4 < 4; ++c4) {
                 float y[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int m = 32 * half + 4 * c4 + u;
+                    const int m = 16 * part + 4 * c4 + u;
                     y[u] = scale * __uint_as_float(du[4 * c4 + u]) + cf->e[m] * __uint_as_float(x[4 * c4 + u]);
                 }
-                sts_f4(sb + kA_AV + f32_tile_off(li, 32 * half + 4 * c4, kBlk128), y[0], y[1], y[2], y[3]);
+                sts_f4(sb + kA_AV + f32_tile_off(li, 16 * part + 4 * c4, kBlk128), y[0], y[1], y[2], y[3]);
             }
         }
         // B operands of the state-gradient update, over the [K;Q] tile (its MMAs are done)
@@ -566,13 +682,13 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
         ++ph[2];
         tc_fence_after();
         {
-            uint32_t db[32];
-            tmem_ld32(tl + tDB + 32 * half, db);
+            uint32_t db[16];
+            tmem_ld16(tl + tDB + 16 * part, db);
             tmem_wait_ld();
             if (li < dv) {
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int r = 32 * half + u;
+                for (int u = 0; u < 16; ++u) {
+                    const int r = 16 * part + u;
                     if (r < len) {
                         const size_t o = ((size_t)(t0 + r) * H + h) * dv + li;
                         a.gv[o] = cf->beta[r] * __uint_as_float(db[u]);
@@ -581,8 +697,8 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
                 }
             }
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-                sts_u4(sb + kA_AV + f32_tile_off(li, 32 * half + 4 * c4, kBlk128),
+            for (int c4 = 0; c4 < 4; ++c4)
+                sts_u4_stage(sb + kA_AV + f32_tile_off(li, 16 * part + 4 * c4, kBlk128),
                        make_uint4(db[4 * c4], db[4 * c4 + 1], db[4 * c4 + 2], db[4 * c4 + 3]));
         }
         fence_proxy_async_smem();
@@ -607,7 +723,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
         tc_fence_after();
     }
     if (!failed && a.gs0) {
-        for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+        for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
             uint32_t r[32];
             tmem_ld32(tl + tS + c0, r);
             tmem_wait_ld();
@@ -640,7 +756,7 @@ constexpr uint32_t kB_Small = 212992;
 struct ChunkSmall {
     BtCoef cf;
     float dG[64], db[64], de[64];
-    float red[8];
+    float red[kBT / 32];
     uint64_t bar;
     uint32_t tmem_base;
     int abort;
@@ -664,7 +780,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
     ChunkSmall *sm = reinterpret_cast<ChunkSmall *>(smem + kB_Small);
     BtCoef *cf = &sm->cf;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
+    const int quad = warp & 3, part = warp >> 2;
     const int li = quad * 32 + lane;
     if (warp == 0) {
         tmem_alloc(&sm->tmem_base, 256);
@@ -700,6 +816,35 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
     uint32_t ph = 0;
     bool failed = false;
 
+    {   // every operand of this chunk into L2 at once; the phases below then
+        // wait on L2, not on one memory round trip after another
+        for (int i = tid; i < 9 * 64; i += kBT) {
+            const int which = i >> 6, r = i & 63;
+            if (r >= len) continue;
+            const size_t row = (size_t)(t0 + r) * H + h;
+            const void *p;
+            uint32_t bytes = (uint32_t)dv * 4u;
+            switch (which) {
+                case 0: p = kg + row * dk; bytes = (uint32_t)(dk * sizeof(TI)); break;
+                case 1: p = qg + row * dk; bytes = (uint32_t)(dk * sizeof(TI)); break;
+                case 2: p = og + row * dv; bytes = (uint32_t)(dv * sizeof(TI)); break;
+                case 3: p = vg + row * dv; bytes = (uint32_t)(dv * sizeof(TI)); break;
+                case 4: p = a.rdb + row * dv; break;
+                case 5: p = a.ru + row * dv; break;
+                case 6: p = a.ry + row * dv; break;
+                case 7: p = a.rqs + row * dv; break;
+                default: p = a.rkds + row * dv; break;
+            }
+            l2_prefetch(p, bytes);
+        }
+        const size_t st = (slot * H + h) * (size_t)dk * dv;
+        const uint32_t sbytes = (uint32_t)(dk * dv * 4), piece = 4096u;
+        for (uint32_t o = (uint32_t)tid * piece; o < 2 * sbytes; o += kBT * piece) {
+            const float *base = o < sbytes ? a.s0t + st : a.dst + st;
+            const uint32_t oo = o < sbytes ? o : o - sbytes;
+            l2_prefetch(reinterpret_cast<const char *>(base) + oo, min(piece, sbytes - oo));
+        }
+    }
     if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
     // phase 1: the Gram [K;Q] K^T and [dO;dB] U^T
     tile_rows<TI>(sb + kB_R0, kBlk128, 0, kg, t0, len, H, h, dk, One());
@@ -729,17 +874,17 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
         float *KK = reinterpret_cast<float *>(smem + kB_R1);
         float *QK = KK + 64 * kCP, *DM = QK + 64 * kCP, *DA = DM + 64 * kCP;
         {
-            uint32_t x[32], y[32];
-            tmem_ld32(tl + tG + 32 * half, x);
-            tmem_ld32(tl + tH + 32 * half, y);
+            uint32_t x[16], y[16];
+            tmem_ld16(tl + tG + 16 * part, x);
+            tmem_ld16(tl + tH + 16 * part, y);
             tmem_wait_ld();
             const int r = li & 63;
             float *fa = li < 64 ? KK : QK;
             float *fb = li < 64 ? DM : DA;
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                fa[r * kCP + 32 * half + u] = __uint_as_float(x[u]);
-                fb[r * kCP + 32 * half + u] = __uint_as_float(y[u]);
+            for (int u = 0; u < 16; ++u) {
+                fa[r * kCP + 16 * part + u] = __uint_as_float(x[u]);
+                fb[r * kCP + 16 * part + u] = __uint_as_float(y[u]);
             }
         }
         __syncthreads();
@@ -770,15 +915,18 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
             const float colE = warp_sum(KK[lane * kCP + r] + KK[(32 + lane) * kCP + r]);
             const float dagk = warp_sum(QK[r * kCP + lane] + QK[r * kCP + 32 + lane]);
             float s_vdb = 0.f, s_ydb = 0.f, s_oqs = 0.f, s_ukds = 0.f;
-            if (r < len) {
-                const size_t base = ((size_t)(t0 + r) * H + h) * dv;
-                for (int i = lane; i < dv; i += 32) {
-                    const float db = a.rdb[base + i], y = a.ry[base + i];
-                    s_vdb += ld1<TI>(vg + base + i) * db;
-                    s_ydb += y * db;
-                    s_oqs += ld1<TI>(og + base + i) * a.rqs[base + i];
-                    s_ukds += a.ru[base + i] * a.rkds[base + i];
-                }
+            if (r < len && 4 * lane < dv) {   // four value columns per lane (dv <= 128)
+                const size_t base = ((size_t)(t0 + r) * H + h) * dv + 4 * lane;
+                const float4 db = __ldg(reinterpret_cast<const float4 *>(a.rdb + base));
+                const float4 y = __ldg(reinterpret_cast<const float4 *>(a.ry + base));
+                const float4 qs = __ldg(reinterpret_cast<const float4 *>(a.rqs + base));
+                const float4 uu = __ldg(reinterpret_cast<const float4 *>(a.ru + base));
+                const float4 kd = __ldg(reinterpret_cast<const float4 *>(a.rkds + base));
+                const float4 vv = ld4<TI>(vg + base), oo = ld4<TI>(og + base);
+                s_vdb = vv.x * db.x + vv.y * db.y + vv.z * db.z + vv.w * db.w;
+                s_ydb = y.x * db.x + y.y * db.y + y.z * db.z + y.w * db.w;
+                s_oqs = oo.x * qs.x + oo.y * qs.y + oo.z * qs.z + oo.w * qs.w;
+                s_ukds = uu.x * kd.x + uu.y * kd.y + uu.z * kd.z + uu.w * kd.w;
             }
             s_vdb = warp_sum(s_vdb);
             s_ydb = warp_sum(s_ydb);
@@ -829,16 +977,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
             __syncwarp();
         }
         // meanwhile: S0^T ([key][value], rows past dk zero) over R1, -gamma beta dB rows over R2
-        {
-            const float *src = a.s0t + (slot * H + h) * (size_t)dk * dv;
-            const int d4 = dv >> 2;
-            for (int idx = tid; idx < 128 * d4; idx += kBT) {
-                const int j = idx / d4, c4 = idx - j * d4;
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (j < dk) x = __ldg(reinterpret_cast<const float4 *>(src + (size_t)j * dv + 4 * c4));
-                sts_f4(sb + kB_R1 + f32_tile_off(j, 4 * c4, kBlk128), x.x, x.y, x.z, x.w);
-            }
-        }
+        tile_state(sb + kB_R1, a.s0t + (slot * H + h) * (size_t)dk * dv, dk, dv, 0u);
         tile_rows<float>(sb + kB_R2, kBlk64, 0, a.rdb, t0, len, H, h, dv,
                          [cf](int r) { return -cf->gam[r] * cf->beta[r]; });
         if (!bt_wait(&sm->bar, ph & 1u, &sm->abort)) { failed = true; break; }
@@ -865,20 +1004,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
         tc_fence_after();
         // phase 3c: dS^T over R0 (with <dS, S0> on the way, S0^T still in R1), e U rows over R2
         {
-            const float *src = a.dst + (slot * H + h) * (size_t)dk * dv;
-            const int d4 = dv >> 2;
-            float part = 0.f;
-            for (int idx = tid; idx < 128 * d4; idx += kBT) {
-                const int j = idx / d4, c4 = idx - j * d4;
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                const uint32_t off = f32_tile_off(j, 4 * c4, kBlk128);
-                if (j < dk) {
-                    x = __ldg(reinterpret_cast<const float4 *>(src + (size_t)j * dv + 4 * c4));
-                    const float4 s0 = lds_f4(sb + kB_R1 + off);
-                    part += x.x * s0.x + x.y * s0.y + x.z * s0.z + x.w * s0.w;
-                }
-                sts_f4(sb + kB_R0 + off, x.x, x.y, x.z, x.w);
-            }
+            float part = tile_state(sb + kB_R0, a.dst + (slot * H + h) * (size_t)dk * dv, dk, dv, sb + kB_R1);
             part = warp_sum(part);
             if (lane == 0) sm->red[warp] = part;
         }
@@ -923,14 +1049,14 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
         ++ph;
         tc_fence_after();
         {   // dK^T, dQ^T: lane = key index, columns = chunk rows
-            uint32_t xk[32], xq[32];
-            tmem_ld32(tl + tDK + 32 * half, xk);
-            tmem_ld32(tl + tDQ + 32 * half, xq);
+            uint32_t xk[16], xq[16];
+            tmem_ld16(tl + tDK + 16 * part, xk);
+            tmem_ld16(tl + tDQ + 16 * part, xq);
             tmem_wait_ld();
             if (li < dk) {
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int r = 32 * half + u;
+                for (int u = 0; u < 16; ++u) {
+                    const int r = 16 * part + u;
                     if (r < len) {
                         const size_t o = ((size_t)(t0 + r) * H + h) * dk + li;
                         a.gk[o] = __uint_as_float(xk[u]);

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kT32Threads, 1)
                 const int row = idx / dk4, c4 = idx - row * dk4, r = row & 63;
                 float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (r < len) x = ldg_f4((row < 64 ? kg : qg) + ((size_t)(t0 + r) * H + h) * dk + 4 * c4);
-                sts_u4(sb + kOffKQ + tile_off(row, 4 * c4, kBlk128), *reinterpret_cast<uint4 *>(&x));
+                sts_u4_stage(sb + kOffKQ + tile_off(row, 4 * c4, kBlk128), *reinterpret_cast<uint4 *>(&x));
             }
             __syncthreads();
             if (tid < kChunk) {
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kT32Threads, 1)
                     const int r = 4 * r4 + u;
                     x[u] = r < len ? sm->dec[r] * __ldg(kg + ((size_t)(t0 + r) * H + h) * dk + j) : 0.f;
                 }
-                sts_u4(sb + kOffKT + tile_off(j, 4 * r4, kBlk128),
+                sts_u4_stage(sb + kOffKT + tile_off(j, 4 * r4, kBlk128),
                        make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
                                   __float_as_uint(x[3])));
             }
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kT32Threads, 1)
                     for (int u = 0; u < 4; ++u)
                         if (m4 + u <= n) x[u] = tv[u] * expf(Gn - sm->G[m4 + u]);
                 }
-                sts_u4(sb + kOffTT + tile_off(n, m4, kBlk64),
+                sts_u4_stage(sb + kOffTT + tile_off(n, m4, kBlk64),
                        make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
                                   __float_as_uint(x[3])));
             }
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kT32Threads, 1)
                         const int r = 32 * half + 4 * c4 + u;
                         x[u] = __float_as_uint(sm->beta[r] * (vv[4 * c4 + u] - sm->gam[r] * __uint_as_float(pk[4 * c4 + u])));
                     }
-                    sts_u4(sb + kOffAV + tile_off(li, 32 * half + 4 * c4, kBlk128), make_uint4(x[0], x[1], x[2], x[3]));
+                    sts_u4_stage(sb + kOffAV + tile_off(li, 32 * half + 4 * c4, kBlk128), make_uint4(x[0], x[1], x[2], x[3]));
                 }
             }
             {
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kT32Threads, 1)
                         x[u] = __float_as_uint((r < len && m <= r) ? __uint_as_float(qk[4 * c4 + u]) * expf(Gr - sm->G[m])
                                                                    : 0.f);
                     }
-                    sts_u4(sb + kOffMQ + tile_off(r, 32 * half + 4 * c4, kBlk64), make_uint4(x[0], x[1], x[2], x[3]));
+                    sts_u4_stage(sb + kOffMQ + tile_off(r, 32 * half + 4 * c4, kBlk64), make_uint4(x[0], x[1], x[2], x[3]));
                 }
             }
             fence_proxy_async_smem();
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kT32Threads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4)
-                    sts_u4(sb + kOffAV + tile_off(li, 32 * half + 4 * c4, kBlk128),
+                    sts_u4_stage(sb + kOffAV + tile_off(li, 32 * half + 4 * c4, kBlk128),
                            make_uint4(u32[4 * c4], u32[4 * c4 + 1], u32[4 * c4 + 2], u32[4 * c4 + 3]));
             }
             fence_proxy_async_smem();

@@ -91,6 +91,12 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Fetch `bytes` (a multiple of 16, 16-byte aligned address) into L2 only.
+__device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
 // Fetch a 3-D box into L2 only (no shared memory, no completion tracking).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
@@ -316,6 +322,13 @@ __device__ __forceinline__ float4 lds_f4(uint32_t a) {
 __device__ __forceinline__ void sts_u4(uint32_t a, uint4 v) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
+}
+// The same store without the memory clobber: still ordered against the other
+// asm statements (fences, barriers), but ordinary loads may move across it, so
+// a loop of global loads feeding such stores keeps its loads in flight
+// together.  The shared tile it writes is read only after a barrier or fence.
+__device__ __forceinline__ void sts_u4_stage(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
 }
 __device__ __forceinline__ void sts_b16(uint32_t a, uint32_t v) {
     asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(static_cast<unsigned short>(v & 0xFFFFu)) : "memory");
