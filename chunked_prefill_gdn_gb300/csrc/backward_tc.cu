@@ -283,6 +283,55 @@ __device__ __forceinline__ void prefetch_chain_chunk(const BwdTcArgs &a, int t0,
     prefetch_rows(qg, t0, len, a.H, h, a.dk, 64);
     prefetch_rows(xg, t0, len, a.H, h, a.dv, 128);
     if (threadIdx.x == 192) l2_prefetch(a.tp + ((size_t)h * a.total_T + t0) * kChunk, (uint32_t)len * 256u);
+    if (threadIdx.x == 193 || threadIdx.x == 194) {   // g, beta rows of the chunk (all heads), inside the tensors
+        const float *x = threadIdx.x == 193 ? a.g : a.beta;
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(x + (size_t)t0 * a.H) & ~uintptr_t(15);
+        const uintptr_t b1 = reinterpret_cast<uintptr_t>(x + (size_t)(t0 + len) * a.H) & ~uintptr_t(15);
+        if (b1 > b0) l2_prefetch(reinterpret_cast<const void *>(b0), (uint32_t)(b1 - b0));
+    }
+}
+
+// Transposed copies out of a [K;Q] row tile in shared memory (K rows 0-63,
+// Q rows 64-127, 128-byte-swizzled fp32, block stride kBlk128):
+//   dst0[j][r] = f0(r) src[q0 + r][j],  dst1[j][r] = f1(r) src[q1 + r][j]
+// for key rows j < rows (zero for j >= dk) and chunk rows r < 64 (n_dst = 1:
+// dst0 only).  With
+// `in_place` the destinations overlap the source, so every value is read
+// into registers before a barrier and written after it.
+template <typename F0, typename F1>
+__device__ __forceinline__ void tile_transpose_kq(uint32_t src, uint32_t dst0, int q0, F0 f0, uint32_t dst1, int q1,
+                                                  F1 f1, int rows, int dk, bool in_place, int n_dst = 2) {
+    const int sh = log2i(rows), per = rows * 16;        // float4 items per destination
+    const int items = n_dst * per;
+    constexpr int kN = 2 * 128 * 16 / kBT;              // items per thread at rows = 128
+    float e[kN][4];
+#pragma unroll
+    for (int b = 0; b < kN; ++b) {
+        const int idx = threadIdx.x + b * kBT;
+        const int which = idx >= per, k = idx - which * per;
+        const int r4 = k >> sh, j = k & (rows - 1);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = 4 * r4 + u;
+            float x = 0.f;
+            if (idx < items && j < dk) {
+                uint32_t a = src + f32_tile_off((which ? q1 : q0) + r, j, kBlk128);
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(x) : "r"(a));
+                x *= which ? f1(r) : f0(r);
+            }
+            e[b][u] = x;
+        }
+    }
+    if (in_place) __syncthreads();
+#pragma unroll
+    for (int b = 0; b < kN; ++b) {
+        const int idx = threadIdx.x + b * kBT;
+        if (idx < items) {
+            const int which = idx >= per, k = idx - which * per;
+            const int r4 = k >> sh, j = k & (rows - 1);
+            sts_f4((which ? dst1 : dst0) + f32_tile_off(j, 4 * r4, kBlk128), e[b][0], e[b][1], e[b][2], e[b][3]);
+        }
+    }
 }
 
 struct One {
@@ -401,7 +450,25 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
         const size_t slot = (size_t)(t0 / kChunk + n);
         if (c + 1 < nc) prefetch_chain_chunk<TI>(a, t0 + kChunk, min(kChunk, t_begin + len_seq - t0 - kChunk), h, false);
         if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
-        {   // this chunk's start state, transposed ([key][value]), to the workspace
+        tile_rows<TI>(sb + kA_KQ, kBlk128, 0, kg, t0, len, H, h, dk, One());
+        tile_rows<TI>(sb + kA_KQ, kBlk128, 64, qg, t0, len, H, h, dk, One());
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();  // the [K;Q] tile and the coefficients
+        if (warp == 0) {
+            if (elect_one()) {
+                tc_fence_after();
+                for (int kk = 0; kk < dk / 8; ++kk)
+                    mma_ts_tf32(tb + tP, tb + tS + 8 * kk, f32_desc_kstep(dKQ, kk, kBlk128), I128, kk > 0);
+                tc_commit(&sm->bar[0]);
+            }
+            __syncwarp();
+        }
+        // while the MMA runs (it only reads S and the [K;Q] tile): this chunk's
+        // start state, transposed ([key][value]), to the workspace; the T and
+        // decay-scaled K^T tiles; the values
+        tc_fence_after();
+        {
             float *dst = a.s0t + (slot * H + h) * (size_t)dk * dv;
             for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
                 uint32_t r[32];
@@ -414,23 +481,9 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
                 }
             }
         }
-        tile_rows<TI>(sb + kA_KQ, kBlk128, 0, kg, t0, len, H, h, dk, One());
-        tile_rows<TI>(sb + kA_KQ, kBlk128, 64, qg, t0, len, H, h, dk, One());
-        __syncthreads();  // coefficients
         tile_t(sb + kA_TT, a.tp + ((size_t)h * a.total_T + t0) * kChunk, len, cf->G);
-        tile_cols<TI>(sb + kA_X, kBlk128, dk, kg, t0, len, H, h, dk, [cf](int r) { return cf->e[r]; });
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) {
-            if (elect_one()) {
-                tc_fence_after();
-                for (int kk = 0; kk < dk / 8; ++kk)
-                    mma_ts_tf32(tb + tP, tb + tS + 8 * kk, f32_desc_kstep(dKQ, kk, kBlk128), I128, kk > 0);
-                tc_commit(&sm->bar[0]);
-            }
-            __syncwarp();
-        }
+        tile_transpose_kq(sb + kA_KQ, sb + kA_X, 0, [cf](int r) { return cf->e[r]; }, sb + kA_X, 0,
+                          [cf](int r) { return cf->e[r]; }, dk, dk, false, 1);   // decay-scaled K^T
         float vv[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
@@ -555,27 +608,11 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
         const size_t slot = (size_t)(t0 / kChunk + n);
         if (c > 0) prefetch_chain_chunk<TI>(a, t0 - kChunk, kChunk, h, true);
         if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
-        {   // this chunk's end-state gradient, transposed, to the workspace
-            float *dst = a.dst + (slot * H + h) * (size_t)dk * dv;
-            for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tl + tS + c0, r);
-                tmem_wait_ld();
-                if (li < dv) {
-#pragma unroll
-                    for (int u = 0; u < 32; ++u)
-                        if (c0 + u < dk) dst[(size_t)(c0 + u) * dv + li] = __uint_as_float(r[u]);
-                }
-            }
-        }
         tile_rows<TI>(sb + kA_KQ, kBlk128, 0, kg, t0, len, H, h, dk, One());
         tile_rows<TI>(sb + kA_KQ, kBlk128, 64, qg, t0, len, H, h, dk, One());
-        tile_cols<TI>(sb + kA_X, kBlk128, 128, og, t0, len, H, h, dv, One());   // dO^T, rows past dv zero
-        __syncthreads();  // coefficients
-        tile_t_transposed(sb + kA_TT, a.tp + ((size_t)h * a.total_T + t0) * kChunk, len, cf->G);
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        __syncthreads();  // the [K;Q] tile and the coefficients
         if (warp == 0) {
             if (elect_one()) {
                 tc_fence_after();
@@ -588,6 +625,24 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
             }
             __syncwarp();
         }
+        // while the MMAs run (they read dS and the [K;Q] tile): this chunk's
+        // end-state gradient, transposed, to the workspace; the dO^T and T^T tiles
+        tc_fence_after();
+        {
+            float *dst = a.dst + (slot * H + h) * (size_t)dk * dv;
+            for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tl + tS + c0, r);
+                tmem_wait_ld();
+                if (li < dv) {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u)
+                        if (c0 + u < dk) dst[(size_t)(c0 + u) * dv + li] = __uint_as_float(r[u]);
+                }
+            }
+        }
+        tile_cols<TI>(sb + kA_X, kBlk128, 128, og, t0, len, H, h, dv, One());   // dO^T, rows past dv zero
+        tile_t_transposed(sb + kA_TT, a.tp + ((size_t)h * a.total_T + t0) * kChunk, len, cf->G);
         if (!bt_wait(&sm->bar[0], ph[0] & 1u, &sm->abort)) { failed = true; break; }
         ++ph[0];
         tc_fence_after();
@@ -661,10 +716,8 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
             }
         }
         // B operands of the state-gradient update, over the [K;Q] tile (its MMAs are done)
-        tile_cols<TI>(sb + kA_KQ, kBlk128, dk, qg, t0, len, H, h, dk,
-                      [cf, scale](int r) { return scale * cf->gam[r]; });
-        tile_cols<TI>(sb + kA_KQ + 32768, kBlk128, dk, kg, t0, len, H, h, dk,
-                      [cf](int r) { return -cf->gam[r] * cf->beta[r]; });
+        tile_transpose_kq(sb + kA_KQ, sb + kA_KQ, 64, [cf, scale](int r) { return scale * cf->gam[r]; },
+                          sb + kA_KQ + 32768, 0, [cf](int r) { return -cf->gam[r] * cf->beta[r]; }, dk, dk, true);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -756,6 +809,7 @@ constexpr uint32_t kB_Small = 212992;
 struct ChunkSmall {
     BtCoef cf;
     float dG[64], db[64], de[64];
+    float s_vdb[64], s_ydb[64], s_oqs[64];   // value-row dot products of each chunk row
     float red[kBT / 32];
     uint64_t bar;
     uint32_t tmem_base;
@@ -866,6 +920,35 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
         }
         __syncwarp();
     }
+    // while the MMAs run: the value-row dot products of each chunk row (dO and
+    // dB from the [dO;dB] tile, U from its tile, the rest from memory)
+    for (int r = warp; r < 64; r += kBT / 32) {
+        float s_vdb = 0.f, s_ydb = 0.f, s_oqs = 0.f, s_ukds = 0.f;
+        if (r < len && 4 * lane < dv) {   // four value columns per lane (dv <= 128)
+            const size_t base = ((size_t)(t0 + r) * H + h) * dv + 4 * lane;
+            const float4 y = __ldg(reinterpret_cast<const float4 *>(a.ry + base));
+            const float4 qs = __ldg(reinterpret_cast<const float4 *>(a.rqs + base));
+            const float4 kd = __ldg(reinterpret_cast<const float4 *>(a.rkds + base));
+            const float4 vv = ld4<TI>(vg + base);
+            const float4 oo = lds_f4(sb + kB_R1 + f32_tile_off(r, 4 * lane, kBlk128));
+            const float4 db = lds_f4(sb + kB_R1 + f32_tile_off(64 + r, 4 * lane, kBlk128));
+            const float4 uu = lds_f4(sb + kB_R2 + f32_tile_off(r, 4 * lane, kBlk64));
+            s_vdb = vv.x * db.x + vv.y * db.y + vv.z * db.z + vv.w * db.w;
+            s_ydb = y.x * db.x + y.y * db.y + y.z * db.z + y.w * db.w;
+            s_oqs = oo.x * qs.x + oo.y * qs.y + oo.z * qs.z + oo.w * qs.w;
+            s_ukds = uu.x * kd.x + uu.y * kd.y + uu.z * kd.z + uu.w * kd.w;
+        }
+        s_vdb = warp_sum(s_vdb);
+        s_ydb = warp_sum(s_ydb);
+        s_oqs = warp_sum(s_oqs);
+        s_ukds = warp_sum(s_ukds);
+        if (lane == 0) {
+            sm->s_vdb[r] = s_vdb;
+            sm->s_ydb[r] = s_ydb;
+            sm->s_oqs[r] = s_oqs;
+            sm->de[r] = s_ukds;
+        }
+    }
     do {
         if (!bt_wait(&sm->bar, ph & 1u, &sm->abort)) { failed = true; break; }
         ++ph;
@@ -908,36 +991,16 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
             QK[r * kCP + m] = dagk;
         }
         __syncthreads();
-        // per-row sums: E by rows and columns, dA Gamma KK, and the value-row dot
-        // products of the stored intermediates
+        // per-row sums: E by rows and columns, dA Gamma KK
         for (int r = warp; r < 64; r += kBT / 32) {
             const float rowE = warp_sum(KK[r * kCP + lane] + KK[r * kCP + 32 + lane]);
             const float colE = warp_sum(KK[lane * kCP + r] + KK[(32 + lane) * kCP + r]);
             const float dagk = warp_sum(QK[r * kCP + lane] + QK[r * kCP + 32 + lane]);
-            float s_vdb = 0.f, s_ydb = 0.f, s_oqs = 0.f, s_ukds = 0.f;
-            if (r < len && 4 * lane < dv) {   // four value columns per lane (dv <= 128)
-                const size_t base = ((size_t)(t0 + r) * H + h) * dv + 4 * lane;
-                const float4 db = __ldg(reinterpret_cast<const float4 *>(a.rdb + base));
-                const float4 y = __ldg(reinterpret_cast<const float4 *>(a.ry + base));
-                const float4 qs = __ldg(reinterpret_cast<const float4 *>(a.rqs + base));
-                const float4 uu = __ldg(reinterpret_cast<const float4 *>(a.ru + base));
-                const float4 kd = __ldg(reinterpret_cast<const float4 *>(a.rkds + base));
-                const float4 vv = ld4<TI>(vg + base), oo = ld4<TI>(og + base);
-                s_vdb = vv.x * db.x + vv.y * db.y + vv.z * db.z + vv.w * db.w;
-                s_ydb = y.x * db.x + y.y * db.y + y.z * db.z + y.w * db.w;
-                s_oqs = oo.x * qs.x + oo.y * qs.y + oo.z * qs.z + oo.w * qs.w;
-                s_ukds = uu.x * kd.x + uu.y * kd.y + uu.z * kd.z + uu.w * kd.w;
-            }
-            s_vdb = warp_sum(s_vdb);
-            s_ydb = warp_sum(s_ydb);
-            s_oqs = warp_sum(s_oqs);
-            s_ukds = warp_sum(s_ukds);
             if (lane == 0) {
                 const float gam = cf->gam[r], beta = cf->beta[r];
-                const float dgam = scale * s_oqs - beta * s_ydb;   // D_gamma in O and X
-                sm->db[r] = s_vdb - gam * s_ydb + dagk;
-                sm->de[r] = s_ukds;
-                sm->dG[r] = rowE - colE + dgam * gam - s_ukds * cf->e[r];
+                const float dgam = scale * sm->s_oqs[r] - beta * sm->s_ydb[r];   // D_gamma in O and X
+                sm->db[r] = sm->s_vdb[r] - gam * sm->s_ydb[r] + dagk;
+                sm->dG[r] = rowE - colE + dgam * gam - sm->de[r] * cf->e[r];
             }
         }
         // B operands of dK and dQ: P + P^T, R, R^T ([row][m], 64 x 64)
@@ -957,8 +1020,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
             sts_f4(sb + kB_R3 + 32768 + off, rt[0], rt[1], rt[2], rt[3]);
         }
         // A operands K^T, Q^T ([key][m], rows past dk zero) over the [K;Q] tile
-        tile_cols<TI>(sb + kB_R0, kBlk128, 128, kg, t0, len, H, h, dk, One());
-        tile_cols<TI>(sb + kB_R0 + 32768, kBlk128, 128, qg, t0, len, H, h, dk, One());
+        tile_transpose_kq(sb + kB_R0, sb + kB_R0, 0, One(), sb + kB_R0 + 32768, 64, One(), 128, dk, true);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
