@@ -442,6 +442,9 @@ def qk_l2norm_measure(gdn, torch, q, k, flush, stream, peaks, peak_src, iters=10
 # FP32 CUDA-core peak of a GB300 at its maximum SM clock: 152 SMs x 128 FP32
 # lanes x 2 flops (FMA) x 2.07 GHz.
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# Dense tf32 tensor peak: the measured bf16 peak times the nominal tf32 / bf16
+# ratio (1.1 / 2.25 PFLOP/s dense).
+TF32_NOMINAL_RATIO = 1.1 / 2.25
 
 
 def backward_flops(dk, dv, chunks, H):
@@ -461,7 +464,8 @@ def backward_measure(gdn, torch, inp, cfg, flush, stream, iters=3):
     """The backward pass (chunk_bwd: gdn_chunk_bwd, with the automatic
     sequence-parallel plan) on this workload with seeded upstream gradients:
     CUDA events around each call, L2 flushed before each.  Reported against the
-    FP32 CUDA-core peak (all but its two Gram products run on CUDA cores)."""
+    dense tf32 tensor peak for the tensor-core backward (the default; every
+    product a kind::tf32 MMA), or the FP32 CUDA-core peak for the CUDA-core one."""
     from chunked_prefill_gdn_gb300.inputs import make_grad_inputs
     grads = make_grad_inputs(cfg, inp["q"].device)
     do, dsf = grads["do"], grads["d_final_state"]
@@ -491,16 +495,30 @@ def backward_measure(gdn, torch, inp, cfg, flush, stream, iters=3):
     flops = backward_flops(dk, dv, chunks, H)
     achieved = flops / (ms * 1e-3) / 1e12
     slices = dv // 32
+    seg_note = ("; with segments > 1 each sequence is cut into that many segments (forward maps and scan, a "
+                "local backward, the reverse gradient scan, the backward per segment: two backward passes); "
+                "not inside the timed step")
+    passes = 1 if segments == 1 else 2
+    extra = 0 if segments == 1 else 7
+    if gdn.gdn_get_backward_kernel() != gdn.KERNEL_SIMT:
+        peak = load_peaks()[0]["bf16_tflops"] * TF32_NOMINAL_RATIO
+        return {"kernel": "bwd_tc_chain_kernel + bwd_tc_chunk_kernel (gdn_chunk_bwd)", "ms": ms,
+                "segments": segments, "tokens_per_s": cfg.total_tokens / (ms * 1e-3), "bound": "tensor",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "alg_flops": flops,
+                "launches": iters * (4 * passes + extra),
+                "peak_source": "measured bf16 peak x nominal tf32/bf16 ratio (1.1/2.25)",
+                "note": "every product a tcgen05 kind::tf32 MMA (fp32 operands, fp32 accumulation): a chain "
+                        "kernel per (sequence, head) for the state and state-gradient recurrences, then one CTA "
+                        "per (chunk, head) for dq, dk, dg, dbeta; plus the sequence prep and the per-chunk "
+                        "inverse" + seg_note}
     return {"kernel": "bwd_kernel + bwd_reduce_kernel (gdn_chunk_bwd)", "ms": ms, "segments": segments,
             "tokens_per_s": cfg.total_tokens / (ms * 1e-3), "bound": "alu", "achieved": achieved,
             "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": achieved / FP32_ALU_TFLOPS,
             "alg_flops": flops,
-            "launches": iters * ((1 + (4 if slices > 1 else 0)) * (1 if segments == 1 else 2) + (0 if segments == 1 else 7)),
+            "launches": iters * ((3 + (4 if slices > 1 else 0)) * passes + extra),
             "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz",
             "note": "Gram products on tcgen05 (bf16, d=128), the other products fp32 on CUDA cores; one CTA per "
-                    "(32 value columns, head, sequence or segment); with segments > 1 each sequence is cut into "
-                    "that many segments (forward maps and scan, a local backward, the reverse gradient scan, the "
-                    "backward per segment: two backward passes); not inside the timed step"}
+                    "(32 value columns, head, sequence or segment)" + seg_note}
 
 
 def e2e_measure(gdn, torch, inp, cfg, opts, dev, args):

@@ -22,7 +22,11 @@
 //             dbeta, dg from every place beta, G enter (then dg is the reverse
 //             cumsum of dG inside the chunk)
 //
-// Design: one CTA per (value-column slice of 32, head, sequence).  The state's
+// This file holds the C entry points (gdn_chunk_bwd and its workspace) and
+// the CUDA-core kernels, selected with gdn_set_backward_kernel; the default
+// kernels, with every product on the tensor cores, are in backward_tc.cu.
+//
+// Design of the CUDA-core kernels: one CTA per (value-column slice of 32, head, sequence).  The state's
 // rows along dv evolve independently, so a slice runs the whole recurrence on
 // its own columns: a forward sweep stores every chunk's start state (slice)
 // in the workspace, then a reverse sweep carries dS from the last chunk to the
