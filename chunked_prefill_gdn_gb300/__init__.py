@@ -34,7 +34,7 @@ __all__ = [
     "gdn_chunk_fwd", "gdn_chunk_fwd_check", "gdn_chunk_fwd_host_buffer_size", "gdn_chunk_fwd_host",
     "gdn_chunk_fwd_static", "gdn_qk_l2norm", "qk_l2norm", "gdn_qk_l2norm_bwd", "qk_l2norm_backward",
     "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd", "gdn_chunk_bwd_check", "chunk_bwd",
-    "gdn_set_backward_kernel", "gdn_get_backward_kernel",
+    "gdn_set_backward_kernel", "gdn_get_backward_kernel", "gdn_chunk_state_grad", "chunk_state_grad",
     "chunk_gated_delta_rule",
     "gdn_status_string", "gdn_version", "gdn_last_error_detail", "chunk_fwd", "chunk_fwd_host", "workspace_for", "GdnError",
     "CP_AUTO", "CP_OFF", "CP_FORCE", "KERNEL_AUTO", "KERNEL_TC", "KERNEL_SIMT", "BF16", "F32",
@@ -141,6 +141,8 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_chunk_bwd.restype = i32
     lib.gdn_chunk_bwd_check.argtypes = [vp, vp]
     lib.gdn_chunk_bwd_check.restype = i32
+    lib.gdn_chunk_state_grad.argtypes = [vp] * 5 + [i32, f32] + [i32] * 6 + [vp] * 4 + [sz, vp]
+    lib.gdn_chunk_state_grad.restype = i32
     lib.gdn_set_backward_kernel.argtypes = [i32]
     lib.gdn_set_backward_kernel.restype = i32
     lib.gdn_get_backward_kernel.argtypes = []
@@ -267,6 +269,10 @@ def gdn_chunk_bwd(*args) -> int:
 
 def gdn_chunk_bwd_check(workspace_ptr, stream_ptr) -> int:
     return int(load_library().gdn_chunk_bwd_check(workspace_ptr, stream_ptr))
+
+
+def gdn_chunk_state_grad(*args) -> int:
+    return int(load_library().gdn_chunk_state_grad(*args))
 
 
 def gdn_set_backward_kernel(kernel) -> None:
@@ -673,6 +679,51 @@ def chunk_bwd(q, k, v, g, beta, do, initial_state=None, cu_seqlens=None, scale=N
             if st != 0:
                 raise GdnError(st, "device check")
     return dq, dk_, dv_, dg, db, ds0
+
+
+def chunk_state_grad(q, k, g, beta, do, cu_seqlens=None, scale=None, d_final_state=None, dv=None,
+                     workspace=None, stream: Optional[torch.cuda.Stream] = None, check: bool = False):
+    """The initial state's gradient alone (gdn_chunk_state_grad): what
+    chunk_bwd returns as d_initial_state, without the other gradients.  dv
+    (the value head size) defaults to do's last dimension."""
+    for name, t in (("q", q), ("k", k), ("g", g), ("beta", beta), ("do", do)):
+        if t is None:
+            raise ValueError("%s is required" % name)
+    B, T, H, dk = q.shape
+    dv = do.shape[-1] if dv is None else dv
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    for name, t, shape in (("k", k, (B, T, H, dk)), ("g", g, (B, T, H)), ("beta", beta, (B, T, H)),
+                           ("do", do, (B, T, H, dv))):
+        _expect(name, t, shape)
+    _expect("d_final_state", d_final_state, (N, H, dk, dv))
+    dt = _dtype_code(q)
+    f32, dev = torch.float32, q.device
+    _check_dtypes(dict(k=k, do=do, g=g, beta=beta, cu_seqlens=cu_seqlens, d_final_state=d_final_state,
+                       workspace=workspace),
+                  dict(k=q.dtype, do=q.dtype, g=f32, beta=f32, cu_seqlens=torch.int32, d_final_state=f32,
+                       workspace=torch.uint8))
+    _check_placement("cuda", None, dict(q=q))
+    _check_placement("cuda", dev, dict(k=k, g=g, beta=beta, do=do, cu_seqlens=cu_seqlens,
+                                       d_final_state=d_final_state, workspace=workspace))
+    with torch.cuda.device(dev):
+        ds0 = torch.empty(N, H, dk, dv, dtype=f32, device=dev)
+        if workspace is None:
+            n = gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, N, cu_seqlens is not None, dt)
+            if n == 0:
+                raise GdnError(1, "gdn_chunk_bwd_workspace_size")
+            workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+        stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        st = gdn_chunk_state_grad(_ptr(q), _ptr(k), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N,
+                                  float(scale) if scale is not None else 0.0, B, T, H, dk, dv, dt, _ptr(do),
+                                  _ptr(d_final_state), _ptr(ds0), _ptr(workspace), workspace.numel(),
+                                  ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise GdnError(st, "gdn_chunk_state_grad")
+        if check:
+            st = gdn_chunk_bwd_check(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream))
+            if st != 0:
+                raise GdnError(st, "device check")
+    return ds0
 
 
 class _ChunkGDN(torch.autograd.Function):

@@ -923,20 +923,31 @@ size_t gdn_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int n_s
     return L.total;
 }
 
-gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
-                         const float *initial_state, const int32_t *cu_seqlens, int n_seqs, float scale,
-                         int B, int T, int H, int dk, int dv, gdn_dtype dtype,
-                         const void *d_o, const float *d_final_state,
-                         float *dq, float *dk_out, float *dv_out, float *dg, float *dbeta,
-                         float *d_initial_state, void *workspace, size_t workspace_bytes, gdn_stream_t stream_in) {
+}  // extern "C"
+
+namespace {
+
+// gdn_chunk_bwd, or with state_grad_only the reverse recurrence alone
+// (gdn_chunk_state_grad: v and the per-token gradients unused).
+gdn_status chunk_bwd_impl(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                          const float *initial_state, const int32_t *cu_seqlens, int n_seqs, float scale,
+                          int B, int T, int H, int dk, int dv, gdn_dtype dtype,
+                          const void *d_o, const float *d_final_state,
+                          float *dq, float *dk_out, float *dv_out, float *dg, float *dbeta,
+                          float *d_initial_state, void *workspace, size_t workspace_bytes, gdn_stream_t stream_in,
+                          int state_grad_only) {
     const int varlen = cu_seqlens != nullptr;
     if (dtype != GDN_BF16 && dtype != GDN_F32) return GDN_ERR_INVALID_ARG;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
     BwdLayout L;
     if (!bwd_layout(B, T, H, dk, dv, n_seqs, varlen, dtype, &L)) return GDN_ERR_INVALID_ARG;
     if (!workspace) return GDN_ERR_INVALID_ARG;
-    if (L.total_T > 0 && (!q || !k || !v || !g || !beta || !d_o || !dq || !dk_out || !dv_out || !dg || !dbeta))
+    if (state_grad_only) {
+        if (!d_initial_state || (L.total_T > 0 && (!q || !k || !g || !beta || !d_o))) return GDN_ERR_INVALID_ARG;
+    } else if (L.total_T > 0 &&
+               (!q || !k || !v || !g || !beta || !d_o || !dq || !dk_out || !dv_out || !dg || !dbeta)) {
         return GDN_ERR_INVALID_ARG;
+    }
     const void *ptrs[] = {q, k, v, g, beta, initial_state, d_o, d_final_state, dq, dk_out, dv_out, dg, dbeta,
                           d_initial_state, workspace};
     for (const void *ptr : ptrs)
@@ -994,7 +1005,7 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
         }
     }
     const bool bf = dtype == GDN_BF16;
-    if (g_bwd_kernel.load() != GDN_KERNEL_SIMT) {
+    if (state_grad_only || g_bwd_kernel.load() != GDN_KERNEL_SIMT) {
         if (L.total_T == 0 && !d_initial_state) return GDN_OK;
         BwdTcArgs t = {};
         t.q = q; t.k = k; t.v = v; t.dout = d_o;
@@ -1013,6 +1024,7 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
         t.err = a.err;
         t.T = T; t.H = H; t.dk = dk; t.dv = dv; t.N = L.N; t.total_T = (int)L.total_T; t.varlen = varlen;
         t.dtype = dtype;
+        t.state_grad_only = state_grad_only;
         t.scale = a.scale;
         if ((e = launch_bwd_tc(t, L.total_T > 0 ? L.max_chunks : 0, s)) != cudaSuccess) {
             set_error_detail("launch tensor-core backward", e);
@@ -1041,6 +1053,31 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
         }
     }
     return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                         const float *initial_state, const int32_t *cu_seqlens, int n_seqs, float scale,
+                         int B, int T, int H, int dk, int dv, gdn_dtype dtype,
+                         const void *d_o, const float *d_final_state,
+                         float *dq, float *dk_out, float *dv_out, float *dg, float *dbeta,
+                         float *d_initial_state, void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+    return chunk_bwd_impl(q, k, v, g, beta, initial_state, cu_seqlens, n_seqs, scale, B, T, H, dk, dv, dtype, d_o,
+                          d_final_state, dq, dk_out, dv_out, dg, dbeta, d_initial_state, workspace, workspace_bytes,
+                          stream, 0);
+}
+
+gdn_status gdn_chunk_state_grad(const void *q, const void *k, const float *g, const float *beta,
+                                const int32_t *cu_seqlens, int n_seqs, float scale, int B, int T, int H, int dk,
+                                int dv, gdn_dtype dtype, const void *d_o, const float *d_final_state,
+                                float *d_initial_state, void *workspace, size_t workspace_bytes,
+                                gdn_stream_t stream) {
+    return chunk_bwd_impl(q, k, nullptr, g, beta, nullptr, cu_seqlens, n_seqs, scale, B, T, H, dk, dv, dtype, d_o,
+                          d_final_state, nullptr, nullptr, nullptr, nullptr, nullptr, d_initial_state, workspace,
+                          workspace_bytes, stream, 1);
 }
 
 gdn_status gdn_set_backward_kernel(gdn_kernel kernel) {

@@ -430,6 +430,9 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
     const float scale = a.scale;
 
     // ---------------- forward sweep: the start state of every chunk ----------------
+    // (not run for the state gradient alone: the reverse recurrence needs no state)
+    const int nc_fwd = a.state_grad_only ? 0 : nc;
+    const bool full = !a.state_grad_only;
     for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
         uint32_t r[32];
 #pragma unroll
@@ -444,11 +447,12 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (nc > 0) prefetch_chain_chunk<TI>(a, t_begin, min(kChunk, len_seq), h, false);
-    for (int c = 0; c < nc; ++c) {
+    if (nc_fwd > 0) prefetch_chain_chunk<TI>(a, t_begin, min(kChunk, len_seq), h, false);
+    for (int c = 0; c < nc_fwd; ++c) {
         const int t0 = t_begin + c * kChunk, len = min(kChunk, t_begin + len_seq - t0);
         const size_t slot = (size_t)(t0 / kChunk + n);
-        if (c + 1 < nc) prefetch_chain_chunk<TI>(a, t0 + kChunk, min(kChunk, t_begin + len_seq - t0 - kChunk), h, false);
+        if (c + 1 < nc_fwd)
+            prefetch_chain_chunk<TI>(a, t0 + kChunk, min(kChunk, t_begin + len_seq - t0 - kChunk), h, false);
         if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
         tile_rows<TI>(sb + kA_KQ, kBlk128, 0, kg, t0, len, H, h, dk, One());
         tile_rows<TI>(sb + kA_KQ, kBlk128, 64, qg, t0, len, H, h, dk, One());
@@ -628,7 +632,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
         // while the MMAs run (they read dS and the [K;Q] tile): this chunk's
         // end-state gradient, transposed, to the workspace; the dO^T and T^T tiles
         tc_fence_after();
-        {
+        if (full) {
             float *dst = a.dst + (slot * H + h) * (size_t)dk * dv;
             for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
                 uint32_t r[32];
@@ -650,7 +654,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
             uint32_t x[16];
             tmem_ld16(tl + tU + 16 * part, x);
             tmem_wait_ld();
-            if (li < dv) {
+            if (full && li < dv) {
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int r = 16 * part + u;
@@ -738,7 +742,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
             uint32_t db[16];
             tmem_ld16(tl + tDB + 16 * part, db);
             tmem_wait_ld();
-            if (li < dv) {
+            if (full && li < dv) {
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int r = 16 * part + u;
@@ -1149,7 +1153,7 @@ cudaError_t launch_bwd_tc_t(const BwdTcArgs &a, int max_chunks, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     bwd_tc_chain_kernel<TI><<<dim3(a.H, a.N), kBT, kChainSmem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (max_chunks > 0) {
+    if (max_chunks > 0 && !a.state_grad_only) {
         bwd_tc_chunk_kernel<TI><<<dim3(max_chunks, a.H), kBT, kChunkSmem, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

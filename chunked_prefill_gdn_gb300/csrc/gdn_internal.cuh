@@ -136,6 +136,7 @@ struct BwdTcArgs {
     float *gq, *gk, *gv, *gg, *gbeta, *gs0;
     int *err;
     int T, H, dk, dv, N, total_T, varlen, dtype;
+    int state_grad_only;                // 1: the reverse recurrence alone, writing only gs0
     float scale;
 };
 cudaError_t launch_bwd_tc(const BwdTcArgs &a, int max_chunks, cudaStream_t s);

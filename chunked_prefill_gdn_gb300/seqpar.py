@@ -122,7 +122,8 @@ def chunk_bwd_segmented(q, k, v, g, beta, do, initial_state, scale, d_final_stat
                         stream=None, check=False):
     """chunk_bwd with every sequence of a batched input cut into `segments`
     segments at chunk boundaries (steps above); returns what chunk_bwd does."""
-    from . import chunk_bwd, chunk_transition, state_grad_scan, state_scan
+    from . import (KERNEL_SIMT, chunk_bwd, chunk_state_grad, chunk_transition, gdn_get_backward_kernel,
+                   state_grad_scan, state_scan)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     nc = -(-T // 64)
@@ -140,8 +141,13 @@ def chunk_bwd_segmented(q, k, v, g, beta, do, initial_state, scale, d_final_stat
     s_star, m = chunk_transition(kp, vp, gp, bp, cu, stream=stream, check=check)
     m_rm = to_rm(m)
     s_start = from_rm(state_scan(to_rm(s_star), m_rm, initial_state, stream=stream))
-    ds_local = chunk_bwd(qp, kp, vp, gp, bp, dop, s_start, cu, scale, None, stream=stream, check=check,
-                         segments=1)[5]
+    # each segment's local map: the state gradient back from a zero end gradient
+    # (the reverse recurrence alone; the CUDA-core backward when it is selected)
+    if gdn_get_backward_kernel() == KERNEL_SIMT:
+        ds_local = chunk_bwd(qp, kp, vp, gp, bp, dop, s_start, cu, scale, None, stream=stream, check=check,
+                             segments=1)[5]
+    else:
+        ds_local = chunk_state_grad(qp, kp, gp, bp, dop, cu, scale, None, dv=dv, stream=stream, check=check)
     ds_end = from_rm(state_grad_scan(to_rm(ds_local), m_rm, d_final_state, stream=stream))
     dq, dk_, dv_, dg, db, ds0 = chunk_bwd(qp, kp, vp, gp, bp, dop, s_start, cu, scale, ds_end, stream=stream,
                                           check=check, segments=1)

@@ -499,6 +499,22 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v,
                          float *d_initial_state,
                          void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/*
+ * The gradient of the initial state alone: d_initial_state of the backward
+ * pass above, from d_o and d_final_state (the state-gradient recurrence run
+ * from the last chunk back to the first; it needs neither v nor the initial
+ * state, and writes nothing else).  The same tensor-core chain kernel as
+ * gdn_chunk_bwd's default, so the result equals its d_initial_state bit for
+ * bit.  The sequence-parallel backward takes each segment's local map from it.
+ * Arguments, workspace (gdn_chunk_bwd_workspace_size) and errors as
+ * gdn_chunk_bwd's; d_initial_state [N, H, dk, dv] fp32 must not be NULL.
+ */
+gdn_status gdn_chunk_state_grad(const void *q, const void *k, const float *g, const float *beta,
+                                const int32_t *cu_seqlens, int n_seqs, float scale,
+                                int B, int T, int H, int dk, int dv, gdn_dtype dtype,
+                                const void *d_o, const float *d_final_state, float *d_initial_state,
+                                void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
 /* Selects the kernels of later gdn_chunk_bwd calls in this process:
  * GDN_KERNEL_AUTO or GDN_KERNEL_TC (the tensor-core backward, the default) or
  * GDN_KERNEL_SIMT (the CUDA-core backward).  Both fit the same workspace size.

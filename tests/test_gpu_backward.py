@@ -126,6 +126,21 @@ def test_backward_matches_oracle(name, bwd_kernel):
         check("%s/%s" % (name, n), x, r)
 
 
+@pytest.mark.parametrize("name", ["layer_ragged_bf16", "varlen_edges_f32", "dk32_dv64_bf16"])
+def test_state_grad_alone_equals_backward(name):
+    """gdn_chunk_state_grad (the reverse recurrence alone, which the
+    sequence-parallel backward uses for each segment's local map) gives the
+    tensor-core backward's d_initial_state bit for bit."""
+    inp, grads = CASES[name]()
+    d_inp, d_grads = to_device(inp), {k: v.cuda() for k, v in grads.items()}
+    gdn.gdn_set_backward_kernel(gdn.KERNEL_TC)
+    full = run_bwd(d_inp, d_grads)[5]
+    alone = gdn.chunk_state_grad(d_inp["q"], d_inp["k"], d_inp["g"], d_inp["beta"], d_grads["do"],
+                                 d_inp.get("cu_seqlens"), d_inp["scale"], d_grads.get("d_final_state"), check=True)
+    torch.cuda.synchronize()
+    assert torch.equal(full, alone)
+
+
 def test_backward_of_zero_upstream_is_zero():
     inp, grads = batched_case(CONFIGS[1].scaled(B=1, T=130, H=2))
     grads = {k: torch.zeros_like(v) for k, v in grads.items()}
