@@ -937,6 +937,8 @@ gdn_status chunk_bwd_impl(const void *q, const void *k, const void *v, const flo
                           float *d_initial_state, void *workspace, size_t workspace_bytes, gdn_stream_t stream_in,
                           int state_grad_only) {
     const int varlen = cu_seqlens != nullptr;
+    // the tensor-core kernels (the default) or the CUDA-core ones, fixed for the call
+    const bool use_tc = state_grad_only || g_bwd_kernel.load() != GDN_KERNEL_SIMT;
     if (dtype != GDN_BF16 && dtype != GDN_F32) return GDN_ERR_INVALID_ARG;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
     BwdLayout L;
@@ -999,13 +1001,13 @@ gdn_status chunk_bwd_impl(const void *q, const void *k, const void *v, const flo
             set_error_detail("launch backward sequence prep", e);
             return GDN_ERR_CUDA;
         }
-        if ((e = launch_inverse_f32(p, w, s)) != cudaSuccess) {
+        if ((e = launch_inverse_f32(p, w, s, use_tc)) != cudaSuccess) {
             set_error_detail("launch backward inverse", e);
             return GDN_ERR_CUDA;
         }
     }
     const bool bf = dtype == GDN_BF16;
-    if (state_grad_only || g_bwd_kernel.load() != GDN_KERNEL_SIMT) {
+    if (use_tc) {
         if (L.total_T == 0 && !d_initial_state) return GDN_OK;
         BwdTcArgs t = {};
         t.q = q; t.k = k; t.v = v; t.dout = d_o;

@@ -36,7 +36,7 @@ using namespace tc;
 
 namespace {
 
-constexpr int kT32Threads = 256;  // warps w and w + 4 share TMEM lane quadrant w and split the columns
+constexpr int kT32Threads = 512;  // warps w, w + 4, w + 8, w + 12 share TMEM lane quadrant w, a quarter of the columns each
 constexpr uint64_t kT32TimeoutNs = 2000000000ull;
 
 // shared memory (offsets from a 1024-byte aligned base): [K/32 blocks][rows][128 B]
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kT32Threads, 1)
     const uint32_t sb = smem_u32(smem);
     T32Small *sm = reinterpret_cast<T32Small *>(smem + kOffSmallT);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
+    const int quad = warp & 3, part = warp >> 2;
     const int li = quad * 32 + lane;  // TMEM lane = state row i
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
 
@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(kT32Threads, 1)
         const int R = ident ? dk : dv;  // state rows of this item
         const int4 si = w.seqinfo[seq];
 
-        // start state: lane li, columns [64 half, 64 half + 64)
-        for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+        // start state: lane li, columns [32 part, 32 part + 32)
+        for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
             uint32_t r[32];
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
@@ -234,35 +234,35 @@ __global__ void __launch_bounds__(kT32Threads, 1)
                 __syncwarp();
             }
             // the values this thread combines with P_K, fetched while the MMAs run
-            float vv[32];
+            float vv[16];
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int r = 32 * half + u;
+            for (int u = 0; u < 16; ++u) {
+                const int r = 16 * part + u;
                 vv[u] = (!ident && li < dv && r < len) ? vg[((size_t)(t0 + r) * H + h) * dv + li] : 0.f;
             }
             bool ok = mbar_wait(&sm->bar_p, ph & 1u, &sm->abort, kT32TimeoutNs);
             if (__syncthreads_or(!ok)) { failed = true; break; }
             tc_fence_after();
             {
-                // V'^T row li, chunk rows [32 half, 32 half + 32)
-                uint32_t pk[32];
-                tmem_ld32(tl + kCP + 32 * half, pk);
+                // V'^T row li, chunk rows [16 part, 16 part + 16)
+                uint32_t pk[16];
+                tmem_ld16(tl + kCP + 16 * part, pk);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
+                for (int c4 = 0; c4 < 4; ++c4) {
                     uint32_t x[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int r = 32 * half + 4 * c4 + u;
+                        const int r = 16 * part + 4 * c4 + u;
                         x[u] = __float_as_uint(sm->beta[r] * (vv[4 * c4 + u] - sm->gam[r] * __uint_as_float(pk[4 * c4 + u])));
                     }
-                    sts_u4_stage(sb + kOffAV + tile_off(li, 32 * half + 4 * c4, kBlk128), make_uint4(x[0], x[1], x[2], x[3]));
+                    sts_u4_stage(sb + kOffAV + tile_off(li, 16 * part + 4 * c4, kBlk128), make_uint4(x[0], x[1], x[2], x[3]));
                 }
             }
             {
                 // S <- gamma_C S (the MMAs that read S are complete)
                 const float gC = sm->gam[len - 1];
-                for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+                for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
                     uint32_t s[32];
                     tmem_ld32(tl + kCS + c0, s);
                     tmem_wait_ld();
@@ -273,22 +273,22 @@ __global__ void __launch_bounds__(kT32Threads, 1)
                 tmem_wait_st();
             }
             if (out && quad >= 2) {
-                // Mq row r = li - 64: Gamma ⊙ tril(Q K^T), columns [32 half, 32 half + 32)
-                uint32_t qk[32];
-                tmem_ld32(tl + kCQK + 32 * half, qk);
+                // Mq row r = li - 64: Gamma ⊙ tril(Q K^T), columns [16 part, 16 part + 16)
+                uint32_t qk[16];
+                tmem_ld16(tl + kCQK + 16 * part, qk);
                 tmem_wait_ld();
                 const int r = li - 64;
                 const float Gr = sm->G[r];
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
+                for (int c4 = 0; c4 < 4; ++c4) {
                     uint32_t x[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int m = 32 * half + 4 * c4 + u;
+                        const int m = 16 * part + 4 * c4 + u;
                         x[u] = __float_as_uint((r < len && m <= r) ? __uint_as_float(qk[4 * c4 + u]) * expf(Gr - sm->G[m])
                                                                    : 0.f);
                     }
-                    sts_u4_stage(sb + kOffMQ + tile_off(r, 32 * half + 4 * c4, kBlk64), make_uint4(x[0], x[1], x[2], x[3]));
+                    sts_u4_stage(sb + kOffMQ + tile_off(r, 16 * part + 4 * c4, kBlk64), make_uint4(x[0], x[1], x[2], x[3]));
                 }
             }
             fence_proxy_async_smem();
@@ -309,12 +309,12 @@ __global__ void __launch_bounds__(kT32Threads, 1)
             tc_fence_after();
             {
                 // U^T row li into the A tile (the MMA that read V'^T is complete)
-                uint32_t u32[32];
-                tmem_ld32(tl + kCU + 32 * half, u32);
+                uint32_t u32[16];
+                tmem_ld16(tl + kCU + 16 * part, u32);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4)
-                    sts_u4_stage(sb + kOffAV + tile_off(li, 32 * half + 4 * c4, kBlk128),
+                for (int c4 = 0; c4 < 4; ++c4)
+                    sts_u4_stage(sb + kOffAV + tile_off(li, 16 * part + 4 * c4, kBlk128),
                            make_uint4(u32[4 * c4], u32[4 * c4 + 1], u32[4 * c4 + 2], u32[4 * c4 + 3]));
             }
             fence_proxy_async_smem();
@@ -340,14 +340,14 @@ __global__ void __launch_bounds__(kT32Threads, 1)
             tc_fence_after();
             ++ph;
             if (out) {
-                uint32_t pq[32], o2[32];
-                tmem_ld32(tl + kCP + 64 + 32 * half, pq);
-                tmem_ld32(tl + kCO + 32 * half, o2);
+                uint32_t pq[16], o2[16];
+                tmem_ld16(tl + kCP + 64 + 16 * part, pq);
+                tmem_ld16(tl + kCO + 16 * part, o2);
                 tmem_wait_ld();
                 if (li < dv) {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const int r = 32 * half + u;
+                    for (int u = 0; u < 16; ++u) {
+                        const int r = 16 * part + u;
                         if (r < len)
                             og[((size_t)(t0 + r) * H + h) * dv + li] =
                                 p.scale * fmaf(sm->gam[r], __uint_as_float(pq[u]), __uint_as_float(o2[u]));
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kT32Threads, 1)
         }
         if (failed) break;
         // end state
-        for (int c0 = 64 * half; c0 < 64 * half + 64 && c0 < dk; c0 += 32) {
+        for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
             uint32_t s[32];
             tmem_ld32(tl + kCS + c0, s);
             tmem_wait_ld();

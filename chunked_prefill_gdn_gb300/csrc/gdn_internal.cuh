@@ -77,14 +77,18 @@ void set_error_text(const char *text);
 cudaError_t launch_seqprep(const Problem &p, const Workspace &w, bool emit_items, cudaStream_t s);
 cudaError_t launch_gate(const Problem &p, const Workspace &w, cudaStream_t s);
 cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &pp, cudaStream_t s);
-// for_tc: the tcgen05 fused kernel consumes the result, which is then T' diag(c1)
-// (the gate-scaled form that kernel multiplies by) instead of T' itself
+// for_tc: a tcgen05 fused kernel consumes the result: for bf16 T' diag(c1)
+// (the gate-scaled form that kernel multiplies by) instead of T' itself; for
+// fp32 keys T' in fp32 from the tcgen05 inverse (kind::tf32 Gram) rather than
+// from the CUDA-core one
 // cols < nc (equal sequences of nc chunks, tcgen05 inverse only): chunk
 // columns [0, cols) only, the fused kernel computing the others
 cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s, int cols = 0, int nc = 0);
 // T' itself (no gate factors) as fp32 rows [H, total_T, 64] into w.tprime (the
 // backward pass's T = Gamma ⊙ T'); needs the chunk table (sequence prep).
-cudaError_t launch_inverse_f32(const Problem &p, const Workspace &w, cudaStream_t s);
+// tc: the tcgen05 inverse for fp32 keys too (kind::tf32 Gram); else those take
+// the CUDA-core inverse (fp32 throughout)
+cudaError_t launch_inverse_f32(const Problem &p, const Workspace &w, cudaStream_t s, bool tc);
 cudaError_t launch_scan(const Problem &p, const Workspace &w, cudaStream_t s);
 // start states of R consecutive slices: out[0] = s0 (or 0), out[r+1] = out[r] M_r + S*_r;
 // grad: end gradients, out[R-1] = s0 (or 0), out[r] = out[r+1] M_{r+1}^T + S*_{r+1}

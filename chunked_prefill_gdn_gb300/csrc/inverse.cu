@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(128) inverse_simt_kernel(const __grid_constant
 namespace gdn {
 namespace {
 
+template <bool F32K>
 __global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid_constant__ InvMaps maps, const __grid_constant__ Problem p,
                                                                      const __grid_constant__ Workspace w, int gate_scaled,
                                                                      const InvSel sel) {
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(kInvThreads, 1) inverse_tc_kernel(const __grid
     InvSel s = sel;
     s.cta = blockIdx.x;
     s.ctas = gridDim.x;
-    inverse_tc_body(&maps.k, p, w, gate_scaled, s, inv_smem_raw);
+    inverse_tc_body<F32K>(&maps.k, p, w, gate_scaled, s, inv_smem_raw);
 }
 
 typedef CUresult (*EncodeTiledFnInv)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -113,18 +114,25 @@ cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, int gate_sca
     }
     InvMaps maps;
     memset(&maps, 0, sizeof(maps));
+    // bf16 keys: boxes of 64 features; fp32 keys (read as tf32): 32 features,
+    // both 128 bytes wide, 64 token rows
+    const bool f32k = p.dtype == GDN_F32;
+    const cuuint64_t es_bytes = f32k ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)p.dk, (cuuint64_t)p.H, (cuuint64_t)p.total_T};
-    cuuint64_t strides[2] = {(cuuint64_t)p.dk * 2, (cuuint64_t)p.H * p.dk * 2};
-    cuuint32_t box[3] = {64, 1, 64};
+    cuuint64_t strides[2] = {(cuuint64_t)p.dk * es_bytes, (cuuint64_t)p.H * p.dk * es_bytes};
+    cuuint32_t box[3] = {f32k ? 32u : 64u, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
-    const int r = fn(&maps.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.k), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const int r = fn(&maps.k, f32k ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                     const_cast<void *>(p.k), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != 0) {
         set_error_detail("encode tensor map (inverse)", cudaErrorInvalidValue, r);
         return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(inverse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kInvSmem);
+    auto kernel = f32k ? inverse_tc_kernel<true> : inverse_tc_kernel<false>;
+    const uint32_t smem = f32k ? InvCfg<true>::kSmem : InvCfg<false>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -139,7 +147,7 @@ cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, int gate_sca
     const long long pairs = (sel.mode ? (long long)p.N * cols : (long long)w.max_chunks) * ((p.H + 1) / 2);
     if (pairs == 0) return cudaSuccess;
     const int grid = (int)std::max(1LL, std::min<long long>(sms, pairs));
-    e = launch_dependent(inverse_tc_kernel, dim3(grid), dim3(kInvThreads), kInvSmem, s, maps, p, w, gate_scaled, sel);
+    e = launch_dependent(kernel, dim3(grid), dim3(kInvThreads), smem, s, maps, p, w, gate_scaled, sel);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -148,8 +156,11 @@ cudaError_t launch_inverse_tc(const Problem &p, const Workspace &w, int gate_sca
 
 cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cudaStream_t s, int cols, int nc) {
     // (the tcgen05 inverse pads head sizes 32 and 64 to 128 with zero features)
-    if (p.dtype == GDN_BF16 && (p.dk == 32 || p.dk == 64 || p.dk == 128) && p.total_T > 0)
-        return launch_inverse_tc(p, w, for_tc ? 1 : 0, cols, nc, 0, s);
+    const bool dk_ok = p.dk == 32 || p.dk == 64 || p.dk == 128;
+    if (p.dtype == GDN_BF16 && dk_ok && p.total_T > 0) return launch_inverse_tc(p, w, for_tc ? 1 : 0, cols, nc, 0, s);
+    // fp32 keys for the tcgen05 fused kernel: the Gram on kind::tf32, T'
+    // itself stored in fp32 (the CUDA-core kernel keeps fp32 throughout below)
+    if (p.dtype == GDN_F32 && for_tc && dk_ok && p.total_T > 0) return launch_inverse_tc(p, w, 0, 0, 0, 1, s);
     const int smem = (kChunk * (p.dk + 1) + 2 * kChunk * 65) * (int)sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(inverse_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -160,11 +171,11 @@ cudaError_t launch_inverse(const Problem &p, const Workspace &w, bool for_tc, cu
 }
 
 // T' itself (no gate factors) as fp32 rows [H, total_T, 64], for the
-// backward pass: the tcgen05 inverse for bf16 keys, the CUDA-core one (whose
-// output follows the input type) for fp32 keys.
-cudaError_t launch_inverse_f32(const Problem &p, const Workspace &w, cudaStream_t s) {
+// backward pass: the tcgen05 inverse for bf16 keys and, with tc, for fp32 keys
+// (Gram on kind::tf32); else the CUDA-core one (fp32 throughout).
+cudaError_t launch_inverse_f32(const Problem &p, const Workspace &w, cudaStream_t s, bool tc) {
     if (p.total_T == 0) return cudaSuccess;
-    if (p.dtype == GDN_BF16 && (p.dk == 32 || p.dk == 64 || p.dk == 128))
+    if ((p.dtype == GDN_BF16 || tc) && (p.dk == 32 || p.dk == 64 || p.dk == 128))
         return launch_inverse_tc(p, w, 0, 0, 0, 1, s);
     if (p.dtype != GDN_F32) return cudaErrorNotSupported;
     return launch_inverse(p, w, false, s);

@@ -10,7 +10,9 @@
 
 namespace gdn {
 // ---------------------------------------------------------------------------
-// tcgen05 variant for bf16 keys with dk = 128: a persistent, pipelined kernel.
+// tcgen05 variant: a persistent, pipelined kernel, for bf16 keys (kind::f16
+// Gram) or fp32 keys (F32K: kind::tf32 Gram, one key pair in flight), head
+// sizes 32, 64 and 128 (features past dk arrive as zeros).
 //
 // Work unit: one chunk of one head; units travel in pairs (two heads of one
 // chunk).  Per CTA (one per SM), in a software pipeline:
@@ -45,12 +47,25 @@ constexpr uint32_t kInvPairBytes = 32768;         // two 64 x 128 bf16 key tiles
 constexpr int kInvSlotFloats = 10 * 256 + 64;     // the 10 lower 16 x 16 blocks of A', then c1[64]
 
 constexpr uint32_t kInvSlotBytes = kInvSlotFloats * 4;
-constexpr uint32_t kInvOffSlots = kInvKStages * kInvPairBytes;
-constexpr uint32_t kInvOffBars = kInvOffSlots + kInvSolvers * kInvSlotBytes;
-constexpr uint32_t kInvSmem = kInvOffBars + 512 + 1024;  // + barriers, + alignment slack
 constexpr uint64_t kInvTimeoutNs = 2000000000ull;
 
-static_assert(kInvSmem <= 227 * 1024, "inverse kernel shared memory");
+// Shared-memory plan for bf16 keys (F32K false: a 3-stage ring of 32 KB
+// pairs) or fp32 keys (F32K true: the keys read as tf32 by the Gram, one
+// 64 KB pair at a time — the eleven A' slots keep the rest).
+template <bool F32K>
+struct InvCfg {
+    static constexpr int kStages = F32K ? 1 : kInvKStages;
+    static constexpr uint32_t kPair = F32K ? 2 * kInvPairBytes : kInvPairBytes;
+    static constexpr uint32_t kOffSlots = kStages * kPair;
+    static constexpr uint32_t kOffBars = kOffSlots + kInvSolvers * kInvSlotBytes;
+    static constexpr uint32_t kSmem = kOffBars + 512 + 1024;   // + barriers, + alignment slack
+};
+constexpr uint32_t kInvOffSlots = InvCfg<false>::kOffSlots;
+constexpr uint32_t kInvOffBars = InvCfg<false>::kOffBars;
+constexpr uint32_t kInvSmem = InvCfg<false>::kSmem;
+
+static_assert(InvCfg<false>::kSmem <= 227 * 1024 && InvCfg<true>::kSmem <= 227 * 1024,
+              "inverse kernel shared memory");
 
 struct InvMaps {
     CUtensorMap k;
@@ -218,13 +233,19 @@ __device__ __forceinline__ PairInfo sel_pair(const Problem &p, const Workspace &
 }
 
 // The whole inverse for the pairs `sel` gives this CTA (kInvThreads threads,
-// kInvSmem bytes of dynamic shared memory at smem_raw; the caller has waited
-// for the previous grid).  `kmap` is the key tensor map ([total_T, H, 128]
-// bf16 rows, boxes of 64 x 64, 128-byte swizzle).
+// InvCfg<F32K>::kSmem bytes of dynamic shared memory at smem_raw; the caller
+// has waited for the previous grid).  `kmap` is the key tensor map ([total_T,
+// H, dk] rows, 128-byte swizzle; bf16 boxes of 64 features x 64 rows, or with
+// F32K fp32 boxes of 32 features x 64 rows), features past dk read as zeros.
+template <bool F32K = false>
 __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const Problem &p, const Workspace &w,
                                                 int gate_scaled, const InvSel &sel, uint8_t *smem_raw) {
+    using Cfg = InvCfg<F32K>;
+    constexpr int kStages = Cfg::kStages;
+    constexpr uint32_t kPair = Cfg::kPair;
+    constexpr uint32_t kOffSlots = Cfg::kOffSlots;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    InvBars &b = *reinterpret_cast<InvBars *>(smem + kInvOffBars);
+    InvBars &b = *reinterpret_cast<InvBars *>(smem + Cfg::kOffBars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_pairs = sel_pairs(p, w, sel);
     // pairs of this CTA: sel.cta, sel.cta + sel.ctas, ...
@@ -232,7 +253,7 @@ __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const P
     if (n_local == 0) return;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kInvKStages; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             tc::mbar_init(&b.kfull[i], 1);
             tc::mbar_init(&b.kempty[i], 1);
         }
@@ -257,45 +278,54 @@ __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const P
         // ---------------- TMA producer + MMA issuer: the whole warp runs the loop
         // (warp-uniform descriptors), one elected lane issues copies and MMAs
         const bool leader = tc::elect_one();
-        constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 128, 0, 0);
+        constexpr uint32_t idesc = F32K ? tc::idesc_tf32_f32(128, 128) : tc::idesc_bf16_f32(128, 128, 0, 0);
         PairInfo pi_next = sel_pair(p, w, sel, sel.cta);   // info of the next pair to load
         auto load = [&](int i) -> bool {
-            const int st = i % kInvKStages;
-            const uint32_t use = i / kInvKStages;
+            const int st = i % kStages;
+            const uint32_t use = i / kStages;
             if (!inv_wait(b, &b.kempty[st], (use & 1) ^ 1, w.err)) return false;
             const PairInfo pi = pi_next;
             if (i + 1 < n_local) pi_next = sel_pair(p, w, sel, sel.cta + (i + 1) * sel.ctas);
-            uint8_t *kt = smem + st * kInvPairBytes;
+            uint8_t *kt = smem + st * kPair;
             if (leader) {
-                tc::mbar_arrive_expect_tx(&b.kfull[st], kInvPairBytes);
-                tc::tma_load_3d(kt + 0, kmap, &b.kfull[st], 0, pi.h0, pi.t0);
-                tc::tma_load_3d(kt + 8192, kmap, &b.kfull[st], 0, pi.h1, pi.t0);
-                tc::tma_load_3d(kt + 16384, kmap, &b.kfull[st], 64, pi.h0, pi.t0);
-                tc::tma_load_3d(kt + 24576, kmap, &b.kfull[st], 64, pi.h1, pi.t0);
+                // [K1;K2] as 128 rows: each 128-byte feature block holds unit 0's
+                // 64 rows, then unit 1's (bf16: 2 blocks of 64 features, fp32:
+                // 4 blocks of 32)
+                tc::mbar_arrive_expect_tx(&b.kfull[st], kPair);
+                constexpr int kBlocks = F32K ? 4 : 2, kFeat = F32K ? 32 : 64;
+#pragma unroll
+                for (int fb = 0; fb < kBlocks; ++fb) {
+                    tc::tma_load_3d(kt + fb * 16384, kmap, &b.kfull[st], fb * kFeat, pi.h0, pi.t0);
+                    tc::tma_load_3d(kt + fb * 16384 + 8192, kmap, &b.kfull[st], fb * kFeat, pi.h1, pi.t0);
+                }
             }
             __syncwarp();
             return true;
         };
         bool ok = true;
         int issued = 0, consumed = 0, mmas = 0;
-        for (; issued < n_local && issued < kInvKStages - 1 && ok; ++issued) ok = load(issued);
+        for (; issued < n_local && issued < kStages - 1 && ok; ++issued) ok = load(issued);
         if (!ok) --issued;
         for (int i = 0; i < n_local && ok; ++i) {
             if (issued < n_local) {
                 if (!load(issued)) break;
                 ++issued;
             }
-            const int st = i % kInvKStages, tb = i & 1;
-            if (!inv_wait(b, &b.kfull[st], (i / kInvKStages) & 1, w.err)) break;
+            const int st = i % kStages, tb = i & 1;
+            if (!inv_wait(b, &b.kfull[st], (i / kStages) & 1, w.err)) break;
             ++consumed;
             if (!inv_wait(b, &b.tempty[tb], ((i >> 1) & 1) ^ 1, w.err)) break;
             tc::tc_fence_after();
-            const uint64_t d0 = tc::smem_desc_sw128(tc::smem_u32(smem + st * kInvPairBytes), 16, 1024);
+            const uint64_t d0 = tc::smem_desc_sw128(tc::smem_u32(smem + st * kPair), 16, 1024);
             if (leader) {
+                // K-steps of 32 bytes: 16 bf16 features, or 8 fp32 ones (kind::tf32)
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < (F32K ? 16 : 8); ++kk) {
                     const uint64_t d = d0 + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    tc::mma_ss(tbase + tb * 128, d, d, idesc, kk > 0);
+                    if constexpr (F32K)
+                        tc::mma_ss_tf32(tbase + tb * 128, d, d, idesc, kk > 0);
+                    else
+                        tc::mma_ss(tbase + tb * 128, d, d, idesc, kk > 0);
                 }
                 tc::tc_commit(&b.tfull[tb]);
                 tc::tc_commit(&b.kempty[st]);
@@ -309,7 +339,7 @@ __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const P
         // current.  (Waits are bounded; the abort flag is not consulted here.)
         int never = 0;
         for (int i = consumed; i < issued; ++i)
-            tc::mbar_wait(&b.kfull[i % kInvKStages], (i / kInvKStages) & 1, &never, kInvTimeoutNs);
+            tc::mbar_wait(&b.kfull[i % kStages], (i / kStages) & 1, &never, kInvTimeoutNs);
         if (mmas > 0) tc::mbar_wait(&b.tfull[(mmas - 1) & 1], ((mmas - 1) >> 1) & 1, &never, kInvTimeoutNs);
     } else if (warp < kInvConv) {
         // ---------------- converters: TMEM Gram rows -> packed A' rows
@@ -345,11 +375,11 @@ __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const P
             if (i + 2 < n_local) pi_next2 = sel_pair(p, w, sel, sel.cta + (i + 2) * sel.ctas);
             if (warp == 0 && lane == 0 && i + kInvL2Ahead < n_local) {
                 const PairInfo pf = sel_pair(p, w, sel, sel.cta + (i + kInvL2Ahead) * sel.ctas);
-                tc::tma_prefetch_l2_3d(kmap, 0, pf.h0, pf.t0);
-                tc::tma_prefetch_l2_3d(kmap, 64, pf.h0, pf.t0);
-                if (pf.h1 != pf.h0) {
-                    tc::tma_prefetch_l2_3d(kmap, 0, pf.h1, pf.t0);
-                    tc::tma_prefetch_l2_3d(kmap, 64, pf.h1, pf.t0);
+                constexpr int kBlocks = F32K ? 4 : 2, kFeat = F32K ? 32 : 64;
+#pragma unroll
+                for (int fb = 0; fb < kBlocks; ++fb) {
+                    tc::tma_prefetch_l2_3d(kmap, fb * kFeat, pf.h0, pf.t0);
+                    if (pf.h1 != pf.h0) tc::tma_prefetch_l2_3d(kmap, fb * kFeat, pf.h1, pf.t0);
                 }
             }
             const int head = half ? pi.h1 : pi.h0;
@@ -366,7 +396,7 @@ __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const P
             tc::tmem_wait_ld();
             tc::tc_fence_before();
             tc::mbar_arrive(&b.tempty[tb]);
-            float *sl = reinterpret_cast<float *>(smem + kInvOffSlots + slot * kInvSlotBytes);
+            float *sl = reinterpret_cast<float *>(smem + kOffSlots + slot * kInvSlotBytes);
             const int rb = r >> 4, ri = r & 15;
 #pragma unroll
             for (int K = 0; K < 4; ++K) {
@@ -402,7 +432,7 @@ __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const P
             const int4 un = b.unit[s];
             const int len = un.y;
             const bool store = un.w & 1;
-            uint8_t *slot_ptr = smem + kInvOffSlots + s * kInvSlotBytes;
+            uint8_t *slot_ptr = smem + kOffSlots + s * kInvSlotBytes;
             const uint32_t A = tc::smem_u32(slot_ptr);
             // The fused kernel consumes T1 = T' diag(c1) with the factored gate
             // c1_m = exp(G* - G_m) beta_m, G* the middle of the chunk's gate
@@ -411,7 +441,7 @@ __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const P
             // the same G values, picks the form in the fused kernel.)
             const bool exact = un.w & 2;
             const float *Gh = w.G + (size_t)un.z * p.total_T + un.x;
-            const float *c1s = reinterpret_cast<const float *>(smem + kInvOffSlots + s * kInvSlotBytes) +
+            const float *c1s = reinterpret_cast<const float *>(smem + kOffSlots + s * kInvSlotBytes) +
                                (kInvSlotFloats - 64);
             const float c1[2] = {c1s[j], c1s[32 + j]};
             float Gc[2] = {0.f, 0.f};
