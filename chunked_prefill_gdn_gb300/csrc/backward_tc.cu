@@ -265,16 +265,21 @@ __device__ __forceinline__ void tile_t_transposed(uint32_t tile, const float *tp
     }
 }
 
-// L2 prefetch of rows [t0, t0 + len) of a [total_T][H][d] tensor (head h),
-// one row per thread of the given thread range.
+// L2 prefetch of the lines of `bytes` bytes at p (this thread's share).
+__device__ __forceinline__ void prefetch_lines(const void *p, uint32_t bytes) {
+    for (uint32_t o = 0; o < bytes; o += 128) l2_prefetch_line(static_cast<const char *>(p) + o);
+}
+
+// L2 prefetch of row r (r < len) of a [total_T][H][d] tensor (head h) by
+// thread thr0 + r: one or two lines each.
 template <typename T>
 __device__ __forceinline__ void prefetch_rows(const T *x, int t0, int len, int H, int h, int d, int thr0) {
     const int r = (int)threadIdx.x - thr0;
-    if (r >= 0 && r < len) l2_prefetch(x + ((size_t)(t0 + r) * H + h) * d, (uint32_t)(d * sizeof(T)));
+    if (r >= 0 && r < len && r < 64) prefetch_lines(x + ((size_t)(t0 + r) * H + h) * d, (uint32_t)(d * sizeof(T)));
 }
 
-// The chain kernel's inputs of one chunk: K, Q and V or dO rows and the T'
-// block, spread over the CTA's threads.
+// The chain kernel's inputs of one chunk — K, Q and V or dO rows, the T'
+// rows, the g and beta rows of all heads — a row or two lines per thread.
 template <typename TI>
 __device__ __forceinline__ void prefetch_chain_chunk(const BwdTcArgs &a, int t0, int len, int h, bool rev) {
     const TI *kg = static_cast<const TI *>(a.k), *qg = static_cast<const TI *>(a.q);
@@ -282,12 +287,11 @@ __device__ __forceinline__ void prefetch_chain_chunk(const BwdTcArgs &a, int t0,
     prefetch_rows(kg, t0, len, a.H, h, a.dk, 0);
     prefetch_rows(qg, t0, len, a.H, h, a.dk, 64);
     prefetch_rows(xg, t0, len, a.H, h, a.dv, 128);
-    if (threadIdx.x == 192) l2_prefetch(a.tp + ((size_t)h * a.total_T + t0) * kChunk, (uint32_t)len * 256u);
-    if (threadIdx.x == 193 || threadIdx.x == 194) {   // g, beta rows of the chunk (all heads), inside the tensors
-        const float *x = threadIdx.x == 193 ? a.g : a.beta;
-        const uintptr_t b0 = reinterpret_cast<uintptr_t>(x + (size_t)t0 * a.H) & ~uintptr_t(15);
-        const uintptr_t b1 = reinterpret_cast<uintptr_t>(x + (size_t)(t0 + len) * a.H) & ~uintptr_t(15);
-        if (b1 > b0) l2_prefetch(reinterpret_cast<const void *>(b0), (uint32_t)(b1 - b0));
+    prefetch_rows(a.tp + (size_t)h * a.total_T * kChunk, t0, len, 1, 0, kChunk, 192);
+    const int r = (int)threadIdx.x - 256;
+    if (r >= 0 && r < 2 * len) {   // g and beta rows of the chunk (all heads)
+        const float *x = (r < len ? a.g : a.beta) + (size_t)(t0 + (r < len ? r : r - len)) * a.H;
+        prefetch_lines(x, (uint32_t)a.H * 4u);
     }
 }
 
@@ -370,7 +374,7 @@ constexpr uint32_t kA_X = 131072;     // decay-scaled K^T [j][r] (forward), dO^T
 constexpr uint32_t kA_Small = 163840;
 
 struct ChainSmall {
-    BtCoef cf;
+    BtCoef cf[2];   // chunk c's coefficients in cf[c & 1]; warp 15 forms the next chunk's during this one
     uint64_t bar[4];
     uint32_t tmem_base;
     int abort;
@@ -394,7 +398,6 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(bt_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
     ChainSmall *sm = reinterpret_cast<ChainSmall *>(smem + kA_Small);
-    BtCoef *cf = &sm->cf;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, part = warp >> 2;
     const int li = quad * 32 + lane;
@@ -448,12 +451,13 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     if (nc_fwd > 0) prefetch_chain_chunk<TI>(a, t_begin, min(kChunk, len_seq), h, false);
+    if (nc_fwd > 0 && warp == 15) chunk_coef(&sm->cf[0], a.g, a.beta, t_begin, min(kChunk, len_seq), H, h);
     for (int c = 0; c < nc_fwd; ++c) {
         const int t0 = t_begin + c * kChunk, len = min(kChunk, t_begin + len_seq - t0);
         const size_t slot = (size_t)(t0 / kChunk + n);
+        BtCoef *cf = &sm->cf[c & 1];
         if (c + 1 < nc_fwd)
             prefetch_chain_chunk<TI>(a, t0 + kChunk, min(kChunk, t_begin + len_seq - t0 - kChunk), h, false);
-        if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
         tile_rows<TI>(sb + kA_KQ, kBlk128, 0, kg, t0, len, H, h, dk, One());
         tile_rows<TI>(sb + kA_KQ, kBlk128, 64, qg, t0, len, H, h, dk, One());
         fence_proxy_async_smem();
@@ -468,10 +472,14 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
             }
             __syncwarp();
         }
-        // while the MMA runs (it only reads S and the [K;Q] tile): this chunk's
-        // start state, transposed ([key][value]), to the workspace; the T and
-        // decay-scaled K^T tiles; the values
+        // while the MMA runs (it only reads S and the [K;Q] tile): the next
+        // chunk's coefficients; this chunk's start state, transposed
+        // ([key][value]), to the workspace; the T and decay-scaled K^T tiles;
+        // the values
         tc_fence_after();
+        if (warp == 15 && c + 1 < nc_fwd)
+            chunk_coef(&sm->cf[(c + 1) & 1], a.g, a.beta, t0 + kChunk, min(kChunk, t_begin + len_seq - t0 - kChunk),
+                       H, h);
         {
             float *dst = a.s0t + (slot * H + h) * (size_t)dk * dv;
             for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
@@ -605,13 +613,17 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
         __syncthreads();
         tc_fence_after();
     }
-    if (nc > 0 && !failed)
+    if (nc > 0 && !failed) {
         prefetch_chain_chunk<TI>(a, t_begin + (nc - 1) * kChunk, len_seq - (nc - 1) * kChunk, h, true);
+        if (warp == 15)
+            chunk_coef(&sm->cf[(nc - 1) & 1], a.g, a.beta, t_begin + (nc - 1) * kChunk, len_seq - (nc - 1) * kChunk,
+                       H, h);
+    }
     for (int c = nc - 1; c >= 0 && !failed; --c) {
         const int t0 = t_begin + c * kChunk, len = min(kChunk, t_begin + len_seq - t0);
         const size_t slot = (size_t)(t0 / kChunk + n);
+        BtCoef *cf = &sm->cf[c & 1];
         if (c > 0) prefetch_chain_chunk<TI>(a, t0 - kChunk, kChunk, h, true);
-        if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
         tile_rows<TI>(sb + kA_KQ, kBlk128, 0, kg, t0, len, H, h, dk, One());
         tile_rows<TI>(sb + kA_KQ, kBlk128, 64, qg, t0, len, H, h, dk, One());
         fence_proxy_async_smem();
@@ -629,9 +641,11 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chain_kernel(const __grid_const
             }
             __syncwarp();
         }
-        // while the MMAs run (they read dS and the [K;Q] tile): this chunk's
-        // end-state gradient, transposed, to the workspace; the dO^T and T^T tiles
+        // while the MMAs run (they read dS and the [K;Q] tile): the previous
+        // chunk's coefficients; this chunk's end-state gradient, transposed, to
+        // the workspace; the dO^T and T^T tiles
         tc_fence_after();
+        if (warp == 15 && c > 0) chunk_coef(&sm->cf[(c - 1) & 1], a.g, a.beta, t0 - kChunk, kChunk, H, h);
         if (full) {
             float *dst = a.dst + (slot * H + h) * (size_t)dk * dv;
             for (int c0 = 32 * part; c0 < 32 * part + 32 && c0 < dk; c0 += 32) {
@@ -874,35 +888,6 @@ __global__ void __launch_bounds__(kBT, 1) bwd_tc_chunk_kernel(const __grid_const
     uint32_t ph = 0;
     bool failed = false;
 
-    {   // every operand of this chunk into L2 at once; the phases below then
-        // wait on L2, not on one memory round trip after another
-        for (int i = tid; i < 9 * 64; i += kBT) {
-            const int which = i >> 6, r = i & 63;
-            if (r >= len) continue;
-            const size_t row = (size_t)(t0 + r) * H + h;
-            const void *p;
-            uint32_t bytes = (uint32_t)dv * 4u;
-            switch (which) {
-                case 0: p = kg + row * dk; bytes = (uint32_t)(dk * sizeof(TI)); break;
-                case 1: p = qg + row * dk; bytes = (uint32_t)(dk * sizeof(TI)); break;
-                case 2: p = og + row * dv; bytes = (uint32_t)(dv * sizeof(TI)); break;
-                case 3: p = vg + row * dv; bytes = (uint32_t)(dv * sizeof(TI)); break;
-                case 4: p = a.rdb + row * dv; break;
-                case 5: p = a.ru + row * dv; break;
-                case 6: p = a.ry + row * dv; break;
-                case 7: p = a.rqs + row * dv; break;
-                default: p = a.rkds + row * dv; break;
-            }
-            l2_prefetch(p, bytes);
-        }
-        const size_t st = (slot * H + h) * (size_t)dk * dv;
-        const uint32_t sbytes = (uint32_t)(dk * dv * 4), piece = 4096u;
-        for (uint32_t o = (uint32_t)tid * piece; o < 2 * sbytes; o += kBT * piece) {
-            const float *base = o < sbytes ? a.s0t + st : a.dst + st;
-            const uint32_t oo = o < sbytes ? o : o - sbytes;
-            l2_prefetch(reinterpret_cast<const char *>(base) + oo, min(piece, sbytes - oo));
-        }
-    }
     if (warp == 0) chunk_coef(cf, a.g, a.beta, t0, len, H, h);
     // phase 1: the Gram [K;Q] K^T and [dO;dB] U^T
     tile_rows<TI>(sb + kB_R0, kBlk128, 0, kg, t0, len, H, h, dk, One());

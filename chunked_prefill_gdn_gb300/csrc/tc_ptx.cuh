@@ -91,10 +91,10 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// Fetch `bytes` (a multiple of 16, 16-byte aligned address) into L2 only.
-__device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
-                 : "memory");
+// Fetch the 128-byte line holding `p` into L2 (an ordinary prefetch: cheap to
+// issue, unlike the bulk form, so many threads can each take a few lines).
+__device__ __forceinline__ void l2_prefetch_line(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }
 
 // Fetch a 3-D box into L2 only (no shared memory, no completion tracking).
