@@ -24,8 +24,9 @@ namespace gdn {
 //                unit's Gram) and writes beta_r (k_r . k_m), m < r, into the
 //                unit's shared-memory slot as the 10 lower-triangular 16 x 16
 //                fp32 blocks of A' (block (I, K), K <= I, at I(I+1)/2 + K,
-//                column-major); warp 0 also prefetches the keys of the pair
-//                six ahead into L2, so the 3-stage TMA ring sees L2 latency.
+//                column-major).  (An L2 tensor prefetch of the keys six pairs
+//                ahead, issued by a converter, measured 6 us slower at the
+//                layer shape: the issuing thread stalls on it.)
 //   warps 4-14   solvers: one unit per warp; lane j forward-substitutes column
 //                j of (I + A') X = I over rows 0..63 and then column 32 + j over
 //                rows 32..63, 16 rows at a time (block rows of A' read as
@@ -42,7 +43,6 @@ constexpr int kInvConv = 4;                       // converter warps
 constexpr int kInvSolvers = 11;                   // solver warps (= A' slots)
 constexpr int kInvThreads = 32 * (kInvConv + kInvSolvers + 1);
 constexpr int kInvKStages = 3;
-constexpr int kInvL2Ahead = 6;                    // pairs between an L2 prefetch and its use
 constexpr uint32_t kInvPairBytes = 32768;         // two 64 x 128 bf16 key tiles
 constexpr int kInvSlotFloats = 10 * 256 + 64;     // the 10 lower 16 x 16 blocks of A', then c1[64]
 
@@ -373,15 +373,6 @@ __device__ __forceinline__ void inverse_tc_body(const CUtensorMap *kmap, const P
                 g_next = gate_of(pi_next);
             }
             if (i + 2 < n_local) pi_next2 = sel_pair(p, w, sel, sel.cta + (i + 2) * sel.ctas);
-            if (warp == 0 && lane == 0 && i + kInvL2Ahead < n_local) {
-                const PairInfo pf = sel_pair(p, w, sel, sel.cta + (i + kInvL2Ahead) * sel.ctas);
-                constexpr int kBlocks = F32K ? 4 : 2, kFeat = F32K ? 32 : 64;
-#pragma unroll
-                for (int fb = 0; fb < kBlocks; ++fb) {
-                    tc::tma_prefetch_l2_3d(kmap, fb * kFeat, pf.h0, pf.t0);
-                    if (pf.h1 != pf.h0) tc::tma_prefetch_l2_3d(kmap, fb * kFeat, pf.h1, pf.t0);
-                }
-            }
             const int head = half ? pi.h1 : pi.h0;
             const int u = 2 * i + half, slot = u % kInvSolvers;
             const uint32_t use = u / kInvSolvers;
