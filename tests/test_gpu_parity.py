@@ -35,6 +35,9 @@ REDUCED = {
     "long_cp": CONFIGS[2].scaled(T=4133, H=4, zero_gate_heads=(0, 1)),
     "varlen": CONFIGS[3].scaled(T=6000, H=4, n_seqs=9),
     "mix_cp": CONFIGS[4].scaled(T=5000, H=5, zero_gate_heads=(0, 1)),
+    # the same mix in fp32 (kind::tf32 kernels): look-back restarts, correction
+    # matrices and the scan through the tf32 state
+    "mix_cp_f32": CONFIGS[4].scaled(T=3000, H=5, zero_gate_heads=(0, 1), dtype="f32"),
 }
 
 
@@ -70,9 +73,13 @@ def test_short_and_ragged_lengths(T):
     assert_close("final_state", oracle.to_f64(sf), sf_ref)
 
 
-def test_varlen_with_empty_and_tiny_sequences():
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_varlen_with_empty_and_tiny_sequences(dtype):
+    """Packed sequences of lengths 0, 1, 64, 200 and 3 with an initial state
+    (bf16: the kind::f16 kernels; fp32: the kind::tf32 fused kernel and the
+    tf32-Gram inverse)."""
     lens = [0, 1, 64, 0, 200, 3, 0]
-    cfg = CONFIGS[1].scaled(B=1, T=sum(lens), H=3, s0_std=0.02)
+    cfg = CONFIGS[1].scaled(B=1, T=sum(lens), H=3, s0_std=0.02, dtype=dtype)
     inp = make_inputs(cfg, "cpu")
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
     inp["cu_seqlens"] = cu
