@@ -495,22 +495,24 @@ def backward_measure(gdn, torch, inp, cfg, flush, stream, iters=3):
     flops = backward_flops(dk, dv, chunks, H)
     achieved = flops / (ms * 1e-3) / 1e12
     slices = dv // 32
-    seg_note = ("; with segments > 1 each sequence is cut into that many segments (forward maps and scan, a "
-                "local backward, the reverse gradient scan, the backward per segment: two backward passes); "
-                "not inside the timed step")
     passes = 1 if segments == 1 else 2
     extra = 0 if segments == 1 else 7
     if gdn.gdn_get_backward_kernel() != gdn.KERNEL_SIMT:
+        seg_note = ("; with segments > 1 each sequence is cut into that many segments (forward maps and scan, "
+                    "each segment's local state-gradient map by the reverse recurrence alone, the reverse "
+                    "gradient scan, then the backward per segment)")
         peak = load_peaks()[0]["bf16_tflops"] * TF32_NOMINAL_RATIO
         return {"kernel": "bwd_tc_chain_kernel + bwd_tc_chunk_kernel (gdn_chunk_bwd)", "ms": ms,
                 "segments": segments, "tokens_per_s": cfg.total_tokens / (ms * 1e-3), "bound": "tensor",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "alg_flops": flops,
-                "launches": iters * (4 * passes + extra),
+                "launches": iters * ((4 if segments == 1 else 3 + 4) + extra),
                 "peak_source": "measured bf16 peak x nominal tf32/bf16 ratio (1.1/2.25)",
                 "note": "every product a tcgen05 kind::tf32 MMA (fp32 operands, fp32 accumulation): a chain "
                         "kernel per (sequence, head) for the state and state-gradient recurrences, then one CTA "
                         "per (chunk, head) for dq, dk, dg, dbeta; plus the sequence prep and the per-chunk "
                         "inverse" + seg_note}
+    seg_note = ("; with segments > 1 each sequence is cut into that many segments (forward maps and scan, a "
+                "local backward, the reverse gradient scan, the backward per segment: two backward passes)")
     return {"kernel": "bwd_kernel + bwd_reduce_kernel (gdn_chunk_bwd)", "ms": ms, "segments": segments,
             "tokens_per_s": cfg.total_tokens / (ms * 1e-3), "bound": "alu", "achieved": achieved,
             "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": achieved / FP32_ALU_TFLOPS,

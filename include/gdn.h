@@ -75,10 +75,12 @@ typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
  * deterministic; FORCE always splits sequences into segments. */
 typedef enum { GDN_CP_AUTO = 0, GDN_CP_OFF = 1, GDN_CP_FORCE = 2 } gdn_cp_mode;
 
-/* Which fused kernel runs: AUTO picks the tcgen05 kernel when it supports the
- * shape (bf16 with dk, dv in {32, 64, 128}; head sizes below 128 run zero-
- * padded to 128 inside the kernels, which is exact) and the CUDA-core kernel
- * otherwise (fp32). */
+/* Which fused kernel runs: AUTO (and TC) pick the tcgen05 kernels for every
+ * supported shape — kind::f16 for bf16 inputs, kind::tf32 for fp32 inputs
+ * (fp32 operands read as tf32, fp32 accumulation), dk, dv in {32, 64, 128},
+ * head sizes below 128 zero-padded to 128 inside the kernels, which is exact;
+ * SIMT selects the CUDA-core kernel (fp32 arithmetic throughout; with fp32
+ * inputs also the CUDA-core per-chunk inverse). */
 typedef enum { GDN_KERNEL_AUTO = 0, GDN_KERNEL_TC = 1, GDN_KERNEL_SIMT = 2 } gdn_kernel;
 
 typedef struct {
@@ -121,7 +123,8 @@ typedef struct {
  * nothing, so every bounded wait of that pass runs out (about 2 s): the pass
  * records GDN_ERR_TIMEOUT, frees what it holds and returns, and the next call
  * on the same workspace runs normally.  It exists to test the timeout path
- * without faulting or hanging the GPU; the CUDA-core pass ignores it. */
+ * without faulting or hanging the GPU; the kind::tf32 and CUDA-core passes
+ * ignore it. */
 enum { GDN_DEBUG_TIMEOUT_PROBE = 1 };
 
 enum {
