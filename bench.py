@@ -500,7 +500,7 @@ def backward_measure(gdn, torch, inp, cfg, flush, stream, iters=3):
     if gdn.gdn_get_backward_kernel() != gdn.KERNEL_SIMT:
         seg_note = ("; with segments > 1 each sequence is cut into that many segments (forward maps and scan, "
                     "each segment's local state-gradient map by the reverse recurrence alone, the reverse "
-                    "gradient scan, then the backward per segment)")
+                    "gradient scan, then the backward per segment); timed on its own, not inside the forward step")
         peak = load_peaks()[0]["bf16_tflops"] * TF32_NOMINAL_RATIO
         return {"kernel": "bwd_tc_chain_kernel + bwd_tc_chunk_kernel (gdn_chunk_bwd)", "ms": ms,
                 "segments": segments, "tokens_per_s": cfg.total_tokens / (ms * 1e-3), "bound": "tensor",
@@ -512,7 +512,8 @@ def backward_measure(gdn, torch, inp, cfg, flush, stream, iters=3):
                         "per (chunk, head) for dq, dk, dg, dbeta; plus the sequence prep and the per-chunk "
                         "inverse" + seg_note}
     seg_note = ("; with segments > 1 each sequence is cut into that many segments (forward maps and scan, a "
-                "local backward, the reverse gradient scan, the backward per segment: two backward passes)")
+                "local backward, the reverse gradient scan, the backward per segment: two backward passes); timed on "
+                "its own, not inside the forward step")
     return {"kernel": "bwd_kernel + bwd_reduce_kernel (gdn_chunk_bwd)", "ms": ms, "segments": segments,
             "tokens_per_s": cfg.total_tokens / (ms * 1e-3), "bound": "alu", "achieved": achieved,
             "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": achieved / FP32_ALU_TFLOPS,
