@@ -239,6 +239,7 @@ __device__ int lookback_window(const Workspace &w, int h, int chunk0, int c_begi
 }
 
 constexpr int kMaxLookbackChunks = 256;
+constexpr int kPlanThreads = 1024;
 
 // Segments per unit for the units that need correction matrices, when every
 // unit has nc chunks and the planner's segment length gives NS0 segments.
@@ -275,7 +276,7 @@ __device__ int correction_segments(int nc, int NS0, int n_m, int n_s, int grid, 
     return (best != NS0 && cb < 0.95 * c0) ? best : 0;
 }
 
-__global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w, const __grid_constant__ PlanParams pp) {
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w, const __grid_constant__ PlanParams pp) {
     grid_dependency_wait();
     __shared__ int s_warp[32];
     __shared__ int s_tot[4];
@@ -350,6 +351,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Prob
     }
     const int ns_m = s_ns_m;
     const int max_walk = min(pp.L, kMaxLookbackChunks);
+    // 3. the work items, kPlanThreads units per round, one thread per unit.
+    //    The look-back windows of the sliding units' segments are walked by
+    //    the whole block, one (unit, segment) pair per thread: each walk is a
+    //    chain of dependent loads of chunk totals, so one thread walking all
+    //    of its unit's segments would leave the round waiting on the longest
+    //    chain of chains.
+    __shared__ int4 s_unit[kPlanThreads];    // (seq, head, chunks, first chunk)
+    __shared__ int4 s_seg[kPlanThreads];     // (segments, chunks per segment, first item, first walk)
+    __shared__ int s_failed[kPlanThreads];   // some window needs more than max_walk chunks
+    __shared__ int s_walks;
     for (int ubase = 0; ubase < units; ubase += blockDim.x) {
         const int u = ubase + tid;
         int seq = 0, h = 0, nc = 0, NS = 0, Lu = 1, chunk0 = 0;
@@ -368,14 +379,47 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Prob
                 Lu = (nc + ns_m - 1) / ns_m;
                 NS = (nc + Lu - 1) / Lu;
             }
-            if (NS > 1) {
-                mpath = !(flagged && pp.sliding);
-                for (int j = 1; j < NS && !mpath; ++j)
-                    if (lookback_window(w, h, chunk0, j * Lu, pp.ln_eps, max_walk) < 0) mpath = true;
+            mpath = NS > 1 && !(flagged && pp.sliding);
+        }
+        // the output pass's items do not depend on the path: NS per unit
+        const int c2 = NS, nwalk = (NS > 1 && !mpath) ? NS - 1 : 0;
+        const int o2 = s_base[0] + block_exclusive_scan(c2, s_warp, &s_tot[0]);
+        const int ow = block_exclusive_scan(nwalk, s_warp, &s_walks);
+        s_unit[tid] = make_int4(seq, h, nc, chunk0);
+        s_seg[tid] = make_int4(NS, Lu, o2, ow);
+        s_failed[tid] = 0;
+        __syncthreads();
+        // segments 1.. of the sliding units: walk, and write the item when the
+        // window fits (a unit with a failed walk is rewritten below)
+        const int walks = s_walks;
+        for (int wi = tid; wi < walks; wi += blockDim.x) {
+            int lo = 0, hi = blockDim.x - 1;   // the last unit whose first walk is <= wi
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_seg[mid].w <= wi) lo = mid; else hi = mid - 1;
+            }
+            const int4 un = s_unit[lo], sg = s_seg[lo];
+            const int j = wi - sg.w + 1;
+            gdn_work_item it;
+            it.seq = un.x;
+            it.head = un.y;
+            it.c_begin = j * sg.y;
+            it.c_end = min(un.z, (j + 1) * sg.y);
+            const int wnd = lookback_window(w, un.y, un.w, it.c_begin, pp.ln_eps, max_walk);
+            if (wnd < 0) {
+                s_failed[lo] = 1;
+            } else if (sg.z + sg.x <= w.max_items) {
+                it.c_start = it.c_begin - wnd;
+                it.slot = -1;
+                it.pad = 0;
+                it.flags = GDN_ITEM_OUTPUT | (j == sg.x - 1 ? GDN_ITEM_WRITE_FINAL : 0) |
+                           (it.c_start == 0 ? GDN_ITEM_FROM_INITIAL : GDN_ITEM_FROM_ZERO);
+                w.items2[sg.z + j] = it;
             }
         }
-        const int c2 = NS, c1 = mpath ? 2 * NS - 3 : 0, cs = mpath ? NS - 1 : 0, cu = mpath ? 1 : 0;
-        const int o2 = s_base[0] + block_exclusive_scan(c2, s_warp, &s_tot[0]);
+        __syncthreads();
+        if (u < units && s_failed[tid]) mpath = true;
+        const int c1 = mpath ? 2 * NS - 3 : 0, cs = mpath ? NS - 1 : 0, cu = mpath ? 1 : 0;
         const int o1 = s_base[1] + block_exclusive_scan(c1, s_warp, &s_tot[1]);
         const int os = s_base[2] + block_exclusive_scan(cs, s_warp, &s_tot[2]);
         const int ou = s_base[3] + block_exclusive_scan(cu, s_warp, &s_tot[3]);
@@ -383,26 +427,19 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Prob
                           os + cs <= w.max_cp_slots && ou + cu <= w.max_cp_slots;
         if (u < units && !fits) report_error(w.err, GDN_ERR_DEVICE_CHECK);
         if (u < units && fits) {
-            for (int j = 0; j < NS; ++j) {
+            // segment 0 always; the others on the correction path, over
+            // whatever the walks above wrote (the barrier orders the writes)
+            const int jend = mpath ? NS : 1;
+            for (int j = 0; j < jend; ++j) {
                 gdn_work_item it;
                 it.seq = seq;
                 it.head = h;
-                it.c_begin = j * Lu;
+                it.c_begin = it.c_start = j * Lu;
                 it.c_end = min(nc, (j + 1) * Lu);
-                it.c_start = it.c_begin;
-                it.slot = -1;
+                it.slot = j == 0 ? -1 : os + j - 1;
                 it.pad = 0;
-                int f = GDN_ITEM_OUTPUT | (j == NS - 1 ? GDN_ITEM_WRITE_FINAL : 0);
-                if (j == 0) {
-                    f |= GDN_ITEM_FROM_INITIAL;
-                } else if (mpath) {
-                    f |= GDN_ITEM_FROM_SLOT;
-                    it.slot = os + j - 1;
-                } else {
-                    it.c_start = it.c_begin - lookback_window(w, h, chunk0, it.c_begin, pp.ln_eps, max_walk);
-                    f |= it.c_start == 0 ? GDN_ITEM_FROM_INITIAL : GDN_ITEM_FROM_ZERO;
-                }
-                it.flags = f;
+                it.flags = GDN_ITEM_OUTPUT | (j == NS - 1 ? GDN_ITEM_WRITE_FINAL : 0) |
+                           (j == 0 ? GDN_ITEM_FROM_INITIAL : GDN_ITEM_FROM_SLOT);
                 w.items2[o2 + j] = it;
             }
             if (mpath) {
@@ -453,7 +490,7 @@ cudaError_t launch_gate(const Problem &p, const Workspace &w, cudaStream_t s) {
 }
 
 cudaError_t launch_plan(const Problem &p, const Workspace &w, const PlanParams &pp, cudaStream_t s) {
-    cudaError_t e = launch_dependent(plan_kernel, dim3(1), dim3(1024), 0, s, p, w, pp);
+    cudaError_t e = launch_dependent(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p, w, pp);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
