@@ -224,22 +224,33 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *s_warp, int *s_t
 // Look-back window for the segment starting at chunk c_begin of a unit: the
 // least number of whole chunks whose summed gate is <= ln_eps, or the whole
 // prefix.  Returns -1 when more than max_walk chunks would be needed (the unit
-// then takes the exact correction-matrix path instead).
-__device__ int lookback_window(const Workspace &w, int h, int chunk0, int c_begin, float ln_eps,
-                               int max_walk) {
+// then takes the exact correction-matrix path instead).  Walked by a group of
+// W lanes (mask: the group's lanes): the group loads W chunk totals at once,
+// then adds them one by one in the walk's order (every lane holds the same
+// sum), so a window of n chunks costs ceil(n / W) memory round trips instead
+// of n, with the sums rounded exactly as a one-thread walk rounds them.
+template <int W>
+__device__ int lookback_window(const Workspace &w, int h, int chunk0, int c_begin, float ln_eps, int max_walk,
+                               unsigned mask) {
+    const int sub = threadIdx.x & (W - 1);
+    const float *tot = w.totals + (size_t)h * w.max_chunks + chunk0;   // chunk c_begin - 1 - i at i
     float acc = 0.f;
-    int wnd = 0;
-    while (wnd < c_begin) {
-        if (wnd >= max_walk) return -1;
-        acc += w.totals[(size_t)h * w.max_chunks + chunk0 + c_begin - 1 - wnd];
-        ++wnd;
-        if (acc <= ln_eps) break;
+    for (int base = 0;; base += W) {
+        const int i = base + sub;
+        const float t = (i < c_begin && i < max_walk) ? tot[c_begin - 1 - i] : 0.f;
+        for (int l = 0; l < W; ++l) {
+            const int wnd = base + l;       // chunks summed so far
+            if (wnd >= c_begin) return wnd;
+            if (wnd >= max_walk) return -1;
+            acc += __shfl_sync(mask, t, l, W);
+            if (acc <= ln_eps) return wnd + 1;
+        }
     }
-    return wnd;
 }
 
 constexpr int kMaxLookbackChunks = 256;
 constexpr int kPlanThreads = 1024;
+constexpr int kWalkLanes = 8;       // lanes per look-back walk
 
 // Segments per unit for the units that need correction matrices, when every
 // unit has nc chunks and the planner's segment length gives NS0 segments.
@@ -251,29 +262,17 @@ constexpr int kPlanThreads = 1024;
 // keep NS0 segments and re-run a look-back of about four chunks), the scan one
 // step per segment; a pass takes as many waves as its items need, each as long
 // as its longest item.  Fewer, longer segments can save a whole wave of pass
-// 1.  Returns 0 to keep NS0 (unless another count is at least 5% cheaper).
-__device__ int correction_segments(int nc, int NS0, int n_m, int n_s, int grid, float state_ratio,
-                                   float scan_ratio) {
-    if (n_m <= 0 || NS0 <= 2 || grid <= 0) return 0;
+// 1.  The planner keeps NS0 unless another count is at least 5% cheaper, and
+// then takes the largest count of least cost; the block evaluates the counts
+// side by side.
+__device__ double correction_cost(int ns, int nc, int NS0, int n_m, int n_s, int grid, float state_ratio,
+                                  float scan_ratio) {
     const int Ls = (nc + NS0 - 1) / NS0 + (n_s > 0 ? 4 : 0);
-    auto cost = [&](int ns) {
-        const int Lm = (nc + ns - 1) / ns;
-        const long long it1 = (long long)n_m * (2 * ns - 3);
-        const long long it2 = (long long)n_m * ns + (long long)n_s * NS0;
-        return (double)((it1 + grid - 1) / grid) * Lm * state_ratio +
-               (double)((it2 + grid - 1) / grid) * max(Lm, n_s > 0 ? Ls : 0) + (double)scan_ratio * ns;
-    };
-    const double c0 = cost(NS0);
-    int best = NS0;
-    double cb = c0;
-    for (int ns = NS0 - 1; ns >= 2; --ns) {
-        const double c = cost(ns);
-        if (c < cb) {
-            cb = c;
-            best = ns;
-        }
-    }
-    return (best != NS0 && cb < 0.95 * c0) ? best : 0;
+    const int Lm = (nc + ns - 1) / ns;
+    const long long it1 = (long long)n_m * (2 * ns - 3);
+    const long long it2 = (long long)n_m * ns + (long long)n_s * NS0;
+    return (double)((it1 + grid - 1) / grid) * Lm * state_ratio +
+           (double)((it2 + grid - 1) / grid) * max(Lm, n_s > 0 ? Ls : 0) + (double)scan_ratio * ns;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ Problem p, const __grid_constant__ Workspace w, const __grid_constant__ PlanParams pp) {
@@ -329,10 +328,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     // 2. segment count of the units that need correction matrices (heads with
     //    alpha identically 1, or every split head without sliding); batched
     //    inputs only, where every sequence has the same chunk count
-    __shared__ int s_nm, s_ns_m;
+    __shared__ int s_nm, s_ns_m, s_best;
+    __shared__ unsigned long long s_cmin;
     if (tid == 0) {
         s_nm = 0;
         s_ns_m = 0;
+        s_best = 0;
+        s_cmin = ~0ull;
     }
     __syncthreads();
     if (pp.cp_enabled && !p.varlen && units > 0) {
@@ -345,7 +347,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
                 if (!(w.flags[u] != 0 && pp.sliding)) ++mine;      // flags are [N, H]: unit u = (u / H, u % H)
             if (mine) atomicAdd(&s_nm, mine);
             __syncthreads();
-            if (tid == 0) s_ns_m = correction_segments(nc, NS0, s_nm, units - s_nm, pp.grid, pp.state_ratio, pp.scan_ratio);
+            const int n_m = s_nm, n_s = units - n_m;
+            if (n_m > 0 && pp.grid > 0) {
+                // least cost over NS0 - 1 .. 2 (non-negative doubles order as their bits)
+                for (int ns = NS0 - 1 - tid; ns >= 2; ns -= blockDim.x)
+                    atomicMin(&s_cmin, (unsigned long long)__double_as_longlong(
+                                           correction_cost(ns, nc, NS0, n_m, n_s, pp.grid, pp.state_ratio, pp.scan_ratio)));
+                __syncthreads();
+                const unsigned long long cmin = s_cmin;
+                for (int ns = NS0 - 1 - tid; ns >= 2; ns -= blockDim.x)
+                    if ((unsigned long long)__double_as_longlong(correction_cost(
+                            ns, nc, NS0, n_m, n_s, pp.grid, pp.state_ratio, pp.scan_ratio)) == cmin)
+                        atomicMax(&s_best, ns);
+                __syncthreads();
+                if (tid == 0) {
+                    const double c0 = correction_cost(NS0, nc, NS0, n_m, n_s, pp.grid, pp.state_ratio, pp.scan_ratio);
+                    s_ns_m = (s_best > 0 && __longlong_as_double((long long)cmin) < 0.95 * c0) ? s_best : 0;
+                }
+            }
             __syncthreads();
         }
     }
@@ -389,10 +408,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         s_seg[tid] = make_int4(NS, Lu, o2, ow);
         s_failed[tid] = 0;
         __syncthreads();
-        // segments 1.. of the sliding units: walk, and write the item when the
-        // window fits (a unit with a failed walk is rewritten below)
+        // segments 1.. of the sliding units: walk (a group of kWalkLanes lanes
+        // per segment), and write the item when the window fits (a unit with
+        // a failed walk is rewritten below)
         const int walks = s_walks;
-        for (int wi = tid; wi < walks; wi += blockDim.x) {
+        const int grp = tid / kWalkLanes, ngrp = blockDim.x / kWalkLanes;
+        const unsigned gmask = ((1u << kWalkLanes) - 1u) << ((tid & 31) & ~(kWalkLanes - 1));
+        for (int wi = grp; wi < walks; wi += ngrp) {
             int lo = 0, hi = blockDim.x - 1;   // the last unit whose first walk is <= wi
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -405,7 +427,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             it.head = un.y;
             it.c_begin = j * sg.y;
             it.c_end = min(un.z, (j + 1) * sg.y);
-            const int wnd = lookback_window(w, un.y, un.w, it.c_begin, pp.ln_eps, max_walk);
+            const int wnd = lookback_window<kWalkLanes>(w, un.y, un.w, it.c_begin, pp.ln_eps, max_walk, gmask);
+            if ((tid & (kWalkLanes - 1)) != 0) continue;
             if (wnd < 0) {
                 s_failed[lo] = 1;
             } else if (sg.z + sg.x <= w.max_items) {
