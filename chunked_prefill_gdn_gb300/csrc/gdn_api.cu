@@ -29,10 +29,10 @@ constexpr double kCorrectionShare = 0.5;
 // Measured step costs of the auto-CP planner (the talk's one-wave model
 // T = lambda1 L + lambda2 N / L, made wave-aware): gdn_plan_costs.  The
 // defaults were measured on a GB300 (152 SMs, 2.07 GHz) with the package's
-// calibrate module: an output chunk step 1.84 us, a state-only chunk step
-// 1.59 us, a scan step 5.98 us, 37.9 us for the two extra launches.
+// calibrate module: an output chunk step 1.79 us, a state-only chunk step
+// 1.51 us, a scan step 3.95 us, 38.3 us for the two extra launches.
 // gdn_set_plan_costs() replaces them.
-constexpr gdn_plan_costs kDefaultCosts = {1.84f, 1.59f, 5.98f, 37.9f};
+constexpr gdn_plan_costs kDefaultCosts = {1.79f, 1.51f, 3.95f, 38.3f};
 std::mutex g_costs_mu;
 gdn_plan_costs g_costs = kDefaultCosts;
 
