@@ -340,7 +340,7 @@ def main():
     roof_ms = max(t_hbm, t_tc) * 1e3
     kname = "tc" if plan.kernel == gdn.KERNEL_TC else "simt"
     traffic = recorded_traffic(kname, workload_label(cfg), bool(plan.cp_enabled))
-    launches_per_step = 5 + (2 if plan.cp_enabled else 0)
+    launches_per_step = plan.launches
 
     result = {
         "metric": metric_for(cfg), "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,

@@ -74,7 +74,8 @@ class GdnPlanInfo(ctypes.Structure):
                 ("chunks_per_segment", ctypes.c_int32), ("max_chunks", ctypes.c_int32),
                 ("max_items", ctypes.c_int32), ("max_cp_slots", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("grid_fused", ctypes.c_int32),
-                ("overlap_columns", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
+                ("overlap_columns", ctypes.c_int32), ("launches", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 class GdnPlanCosts(ctypes.Structure):

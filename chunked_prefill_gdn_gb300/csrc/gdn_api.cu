@@ -77,6 +77,7 @@ struct HostPlan {
     int units;          // (sequence, head) units
     int N;
     long long total_T;
+    int launches;       // library kernels one call launches (whole path)
     Layout lay;
 };
 
@@ -225,6 +226,12 @@ gdn_status make_plan(int B, int T, int H, int dk, int dv, int n_seqs, int varlen
     hp->units = units;
     hp->N = N;
     hp->total_T = total_T;
+    // normalisation, sequence prep, gate, planner (not for equal sequences
+    // without a split: the sequence-prep kernel lists their items), inverse,
+    // correction pass and scan, fused pass
+    const bool direct = !varlen && !cp;
+    hp->launches = (opts.qk_l2norm && max_chunks > 0 ? 1 : 0) + 1 + (max_chunks > 0 ? 2 : 0) + (direct ? 0 : 1) +
+                   (cp ? 2 : 0) + 1;
     return GDN_OK;
 }
 
@@ -309,6 +316,7 @@ gdn_status gdn_plan_query(int B, int T, int H, int dk, int dv, int n_seqs, int v
     out->sm_count = hp.sms;
     out->grid_fused = hp.ov_cols > 0 ? hp.units + hp.ov_ctas : hp.grid;
     out->overlap_columns = hp.ov_cols;
+    out->launches = hp.launches;
     out->workspace_bytes = hp.lay.total;
     return GDN_OK;
 }

@@ -146,6 +146,9 @@ typedef struct {
     int32_t grid_fused;         /* CTAs of the persistent fused kernel */
     int32_t overlap_columns;    /* chunk columns whose inverse runs inside the fused pass
                                    (see gdn_options.inverse_overlap); 0: none */
+    int32_t launches;           /* kernels one gdn_chunk_fwd call launches (the whole path:
+                                   q/k normalisation, sequence prep, gate, planner, inverse,
+                                   correction pass and scan, fused pass, as the plan needs) */
     size_t workspace_bytes;     /* bytes gdn_chunk_fwd needs */
 } gdn_plan_info;
 

@@ -93,6 +93,16 @@ def test_plan_inverse_overlap(lib):
     assert plan(4, 8192, 32, 128, 128, 4, 0, gdn.F32, sm_count=152, inverse_overlap=7).overlap_columns == 0
 
 
+def test_plan_counts_the_launches_of_a_call(lib):
+    """seqprep, gate, inverse, fused pass; a planner launch unless the sequences
+    are equal and unsplit; the correction pass and scan with a split; the
+    normalisation pass when asked for."""
+    assert plan(4, 8192, 32, 128, 128, 4, 0, gdn.BF16, sm_count=152).launches == 4
+    assert plan(4, 8192, 32, 128, 128, 4, 0, gdn.BF16, sm_count=152, qk_l2norm=1).launches == 5
+    assert plan(1, 131072, 8, 128, 128, 1, 0, gdn.BF16, sm_count=152).launches == 7
+    assert plan(1, 4096, 4, 128, 128, 3, 1, gdn.BF16, sm_count=152, cp_mode=gdn.CP_OFF).launches == 5
+
+
 def test_plan_kernel_choice_by_head_size(lib):
     """Head sizes 32, 64 or 128 (any pair) take the tcgen05 kernels: kind::f16
     for bf16, kind::tf32 for fp32; the CUDA-core kernel only when asked."""
