@@ -216,6 +216,7 @@ def _workspace_views(inp, ws, opts=None):
         tprime=view(lay.tprime, H * total_T * 64, q.dtype).view(H, total_T, 64),
         totals=view(lay.chunk_totals, H * info.max_chunks, torch.float32).view(H, info.max_chunks),
         num_chunks=int(view(lay.num_chunks, 1, torch.int32).item()),
+        chunks=view(lay.chunk_table, 4 * info.max_chunks, torch.int32).view(info.max_chunks, 4),
         items=view(lay.items, 8 * info.max_items, torch.int32).view(info.max_items, 8),
         num_items=view(lay.num_items, 4, torch.int32).tolist(),
     )
@@ -284,7 +285,18 @@ def test_gate_and_inverse_intermediates(case):
     G_ref = gate.chunk_local_cumsum(g, cu, 64)
     assert np.abs(oracle.to_f64(views["G"]).T - G_ref).max() < 1e-4
     nck = views["num_chunks"]
-    assert nck == len(gate.chunk_table(cu, 64))
+    table = gate.chunk_table(cu, 64)
+    assert nck == len(table)
+    # the chunk table entry by entry: (sequence, first token, length, chunk index in the sequence)
+    ref_rows = [(n, t0, ln, (t0 - int(cu[n])) // 64) for n, t0, ln in table]
+    assert views["chunks"][:nck].cpu().numpy().tolist() == [list(r) for r in ref_rows]
+    if case == "equal":
+        # the work list the sequence-prep kernel writes: one whole-sequence item per (sequence, head)
+        N = len(cu) - 1
+        nc = [-(-(int(cu[n + 1]) - int(cu[n])) // 64) for n in range(N)]
+        assert views["num_items"][:3] == [N * H, 0, 0]
+        want = [[n, h, 0, nc[n], 0, 1 | 2 | 32, -1, 0] for n in range(N) for h in range(H)]
+        assert views["items"][:N * H].cpu().numpy().tolist() == want
     # chunk totals and head flags
     tot_ref = gate.chunk_totals(g, cu, 64)
     assert np.abs(oracle.to_f64(views["totals"][:, :nck]).T - tot_ref).max() < 1e-4
