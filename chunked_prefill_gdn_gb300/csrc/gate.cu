@@ -13,6 +13,8 @@
 // restart (flagged heads) or correction-matrix work plus a scan (alpha == 1
 // heads).  It runs on the device so no cu_seqlens or gate data crosses to the
 // host.
+#include <limits.h>
+
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -249,6 +251,29 @@ __device__ int lookback_window(const Workspace &w, int h, int chunk0, int c_begi
 }
 
 constexpr int kMaxLookbackChunks = 256;
+constexpr int kLptItems = 2048;     // longest-first dealing: at most this many output-pass items
+constexpr int kLptCtas = 1024;      // and this many CTAs
+
+// Ascending bitonic sort of n (a power of two) 64-bit keys in shared memory by
+// the whole block; every thread calls it, after the keys are in place.
+__device__ void bitonic_sort_u64(unsigned long long *k, int n) {
+    for (int size = 2; size <= n; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int l = i ^ stride;
+                if (l > i) {
+                    const unsigned long long a = k[i], b = k[l];
+                    if ((a > b) == ((i & size) == 0)) {
+                        k[i] = b;
+                        k[l] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
 constexpr int kPlanThreads = 1024;
 constexpr int kWalkLanes = 8;       // lanes per look-back walk
 
@@ -378,7 +403,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     //    chain of chains.
     __shared__ int4 s_unit[kPlanThreads];    // (seq, head, chunks, first chunk)
     __shared__ int4 s_seg[kPlanThreads];     // (segments, chunks per segment, first item, first walk)
-    __shared__ int s_failed[kPlanThreads];   // some window needs more than max_walk chunks
+    __shared__ __align__(16) int s_failed[kPlanThreads];   // some window needs more than max_walk chunks
     __shared__ int s_walks;
     for (int ubase = 0; ubase < units; ubase += blockDim.x) {
         const int u = ubase + tid;
@@ -492,11 +517,91 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         if (tid < 4) s_base[tid] += s_tot[tid];
         __syncthreads();
     }
+    const bool ok = s_base[0] <= w.max_items && s_base[1] <= w.max_items1 && s_base[2] <= w.max_cp_slots;
     if (tid == 0) {
-        bool ok = s_base[0] <= w.max_items && s_base[1] <= w.max_items1 && s_base[2] <= w.max_cp_slots;
         w.num_items[0] = ok ? s_base[0] : 0;
         w.num_items[1] = ok ? s_base[1] : 0;
         w.num_items[2] = ok ? s_base[3] : 0;
+    }
+    // 5. packed sequences of unequal length: the output list reordered so that
+    //    the fused pass's snake order (round r takes item r G + c, or
+    //    r G + G - 1 - c in odd rounds) deals it out longest first.  Items
+    //    sorted by length (chunks walked, look-back included; a bitonic sort)
+    //    go out in rounds of G: the longest item of a round to the group with
+    //    the least work so far, the next to the next, and so on
+    //    (longest-processing-time dealing by rounds; the groups ranked by
+    //    counting, one barrier a round); then each group is
+    //    given the CTA whose snake positions hold its items (groups with an
+    //    item in the last, partial round on its first positions).  Equal
+    //    sequences keep the list as it is: the snake deals their nearly equal
+    //    items as well.
+    const int n2 = s_base[0], G = pp.grid;
+    if (!(ok && p.varlen && w.items_tmp && G > 0 && G <= kLptCtas && n2 > G && n2 <= kLptItems)) return;
+    __syncthreads();   // every item of the list is in memory
+    unsigned long long *key = reinterpret_cast<unsigned long long *>(s_unit);   // [kLptItems]: (length, item)
+    int *cta_at = reinterpret_cast<int *>(s_seg);    // [kLptCtas]: groups by load, then each group's CTA
+    int *group = cta_at + kLptCtas;                  // [kLptItems]: group of the item of rank j
+    int *load = s_failed;                            // [kLptCtas]: chunks dealt to each group (INT_MAX: padding)
+    const int g4 = (G + 3) & ~3;
+    int P = 1;
+    while (P < n2) P <<= 1;
+    for (int i = tid; i < P; i += blockDim.x) {
+        unsigned long long k = ~0ull;
+        if (i < n2) {
+            const gdn_work_item it = w.items2[i];
+            w.items_tmp[i] = it;
+            const unsigned len = (unsigned)max(0, it.c_end - it.c_start);
+            k = ((unsigned long long)(0xFFFFFFFFu - len) << 32) | (unsigned)i;   // longer first, then lower index
+        }
+        key[i] = k;
+    }
+    for (int c = tid; c < g4; c += blockDim.x) load[c] = c < G ? 0 : INT_MAX;
+    __syncthreads();
+    bitonic_sort_u64(key, P);
+    const int rounds = (n2 + G - 1) / G;
+    for (int r = 0; r < rounds; ++r) {
+        for (int c = tid; c < G; c += blockDim.x) {  // less loaded first, then the lower index
+            const int lc = load[c];
+            int rank = 0;
+#pragma unroll 4
+            for (int m = 0; m < g4; m += 4) {
+                const int4 l = *reinterpret_cast<const int4 *>(load + m);
+                rank += (l.x < lc) || (l.x == lc && m < c);
+                rank += (l.y < lc) || (l.y == lc && m + 1 < c);
+                rank += (l.z < lc) || (l.z == lc && m + 2 < c);
+                rank += (l.w < lc) || (l.w == lc && m + 3 < c);
+            }
+            cta_at[rank] = c;
+        }
+        __syncthreads();
+        for (int k = tid; k < G; k += blockDim.x) {
+            const int j = r * G + k;
+            if (j < n2) {
+                const int c = cta_at[k];
+                group[j] = c;
+                load[c] += (int)(0xFFFFFFFFu - (unsigned)(key[j] >> 32));
+            }
+        }
+        __syncthreads();
+    }
+    // each group's CTA: those with an item in the last round first in that
+    // round's snake order
+    const int last = rounds - 1, rem = n2 - last * G;
+    for (int c = tid; c < g4; c += blockDim.x) load[c] = 0;
+    __syncthreads();
+    for (int j = last * G + tid; j < n2; j += blockDim.x) load[group[j]] = 1;
+    __syncthreads();
+    for (int c = tid; c < G; c += blockDim.x) {
+        const int has = load[c];
+        int before = 0;   // groups below c in the same class
+        for (int m = 0; m < c; ++m) before += load[m] == has;
+        const int pos = has ? before : rem + before;
+        cta_at[c] = (last & 1) ? G - 1 - pos : pos;
+    }
+    __syncthreads();
+    for (int j = tid; j < n2; j += blockDim.x) {
+        const int r = j / G, cp = cta_at[group[j]];
+        w.items2[r * G + ((r & 1) ? G - 1 - cp : cp)] = w.items_tmp[(int)(key[j] & 0xFFFFFFFFu)];
     }
 }
 

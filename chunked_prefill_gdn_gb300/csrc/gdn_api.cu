@@ -214,6 +214,8 @@ gdn_status make_plan(int B, int T, int H, int dk, int dv, int n_seqs, int varlen
     lay.qn = take(qk_bytes);
     lay.kn = take(qk_bytes);
     lay.ready = take(ov_cols > 0 ? (size_t)nc_seq * 4 : 0);
+    // the planner's copy of the output list while it deals it out (packed sequences)
+    lay.items_tmp = take(varlen ? (size_t)lay.max_items * sizeof(gdn_work_item) : 0);
     lay.total = off;
     hp->kernel = kernel;
     hp->cp = cp;
@@ -396,6 +398,7 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
     w.seq_order = reinterpret_cast<int *>(base + L.seq_order);
     w.cp_s = reinterpret_cast<float *>(base + L.cp_s);
     w.cp_m = reinterpret_cast<float *>(base + L.cp_m);
+    w.items_tmp = varlen ? reinterpret_cast<gdn_work_item *>(base + L.items_tmp) : nullptr;
     w.max_chunks = L.max_chunks;
     w.max_items = L.max_items;
     w.max_items1 = L.max_items1;

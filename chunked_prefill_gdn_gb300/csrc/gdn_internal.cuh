@@ -38,6 +38,8 @@ struct Workspace {
     void *tprime;           // [H, total_T, C] bf16 (bf16 inputs) or fp32 (fp32 inputs): T', or
                             // T' diag(c1) when the tcgen05 fused kernel runs
     gdn_work_item *items2;  // [max_items]
+    gdn_work_item *items_tmp;  // [max_items] or null (planned packed sequences): the planner's
+                               // copy of the output list while it deals it out longest first
     gdn_work_item *items1;  // [max_items1]
     int4 *scan_units;       // [max_cp_slots]: (seq, head, segments, first slot)
     int *seq_order;         // [N]: sequences, longest first
@@ -62,7 +64,7 @@ struct PlanParams {
 // Host-side layout of the workspace for one problem.
 struct Layout {
     size_t err, counters, num_chunks, num_items, seqinfo, chunks, flags, G, totals, tprime,
-        items2, items1, scan_units, seq_order, cp_s, cp_m, qn, kn, ready, total;
+        items2, items1, scan_units, seq_order, cp_s, cp_m, qn, kn, ready, items_tmp, total;
     int max_chunks, max_items, max_items1, max_cp_slots;
 };
 

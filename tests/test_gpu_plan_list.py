@@ -127,6 +127,44 @@ def model_items(cu, H, flags, totals, L, ln_eps, sliding, varlen, grid):
     return items, walks, (len(items), n1, nscan)
 
 
+def lpt_reorder(items, G):
+    """Packed sequences with more items than CTAs: the list reordered so that
+    the fused pass's snake order (round r: item r G + c, or r G + G - 1 - c in
+    odd rounds) deals it out longest first, by rounds of G, each item to the
+    least-loaded group (ties: lower index), the groups with an item in the last
+    round on that round's first snake positions."""
+    n = len(items)
+    if n <= G:
+        return list(items)
+    ln = [max(0, it[3] - it[4]) for it in items]
+    by_rank = sorted(range(n), key=lambda i: (-ln[i], i))
+    load = [0] * G
+    group = [0] * n
+    rounds = -(-n // G)
+    for r in range(rounds):
+        cta_at = sorted(range(G), key=lambda c: (load[c], c))
+        for k in range(G):
+            j = r * G + k
+            if j < n:
+                group[j] = cta_at[k]
+                load[cta_at[k]] += ln[by_rank[j]]
+    last = rounds - 1
+    rem = n - last * G
+    has = [0] * G
+    for j in range(last * G, n):
+        has[group[j]] = 1
+    phys = [0] * G
+    for c in range(G):
+        before = sum(1 for m in range(c) if has[m] == has[c])
+        pos = before if has[c] else rem + before
+        phys[c] = G - 1 - pos if last & 1 else pos
+    out = [None] * n
+    for j in range(n):
+        r, cp = j // G, phys[group[j]]
+        out[r * G + (G - 1 - cp if r & 1 else cp)] = items[by_rank[j]]
+    return out
+
+
 def near_threshold(sums, ln_eps, w_dev):
     """The device's window differs from the fp64 walk only by where the running
     sum crosses ln(eps): accept it when that sum is within fp32 rounding."""
@@ -146,6 +184,8 @@ CASES = {
     "varlen_L5": (CONFIGS[3].scaled(T=6000, H=4, n_seqs=9), 5, 1),
     # no sliding: every split head through correction matrices
     "mix_nosliding": (CONFIGS[4].scaled(T=5000, H=5, zero_gate_heads=(0, 1)), 7, 0),
+    # more items than CTAs on packed sequences: the list dealt out longest first
+    "varlen_many": (CONFIGS[3].scaled(T=40000, H=4, n_seqs=64), 3, 1),
 }
 
 
@@ -179,6 +219,12 @@ def test_planner_work_list_matches_the_model(name):
     assert info.cp_enabled == 1
     items, walks, counts = model_items(cu, H, flags, totals, info.chunks_per_segment, ln_eps, sliding, varlen,
                                        info.grid_fused)
+    if varlen:
+        # (the look-back allowance below is by list position: map it through the reordering)
+        pos_of = {id(it): j for j, it in enumerate(items)}
+        items = lpt_reorder(items, info.grid_fused)
+        moved = {pos_of[id(it)]: j for j, it in enumerate(items)}
+        walks = [(moved[j], sums) for j, sums in walks]
 
     # every case has correction units; the sliding ones also restart segments from zero
     assert counts[1] > 0 and counts[2] > 0
