@@ -196,7 +196,12 @@ __global__ void __launch_bounds__(256) gate_kernel(const __grid_constant__ Probl
 }
 
 // ---------------------------------------------------------------------------
-// Planner: one CTA builds the work lists.
+// Planner: one CTA builds the work lists, in steps: (1) sequences ordered
+// longest first; (2) the segment count of the units that take correction
+// matrices (a cost search over the counts); (3) per (sequence, head) unit its
+// segments, their look-back windows (walked by lane groups) or correction
+// slots, and the items of the output pass, the correction pass and the scan;
+// (5) for packed sequences, the output list dealt out longest first.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int block_exclusive_scan(int x, int *s_warp, int *s_total) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
