@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(256) gate_kernel(const __grid_constant__ Probl
 // matrices (a cost search over the counts); (3) per (sequence, head) unit its
 // segments, their look-back windows (walked by lane groups) or correction
 // slots, and the items of the output pass, the correction pass and the scan;
-// (5) for packed sequences, the output list dealt out longest first.
+// (4) for packed sequences, the output list dealt out longest first.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int block_exclusive_scan(int x, int *s_warp, int *s_total) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         w.num_items[1] = ok ? s_base[1] : 0;
         w.num_items[2] = ok ? s_base[3] : 0;
     }
-    // 5. packed sequences of unequal length: the output list reordered so that
+    // 4. packed sequences of unequal length: the output list reordered so that
     //    the fused pass's snake order (round r takes item r G + c, or
     //    r G + G - 1 - c in odd rounds) deals it out longest first.  Items
     //    sorted by length (chunks walked, look-back included; a bitonic sort)
